@@ -1,0 +1,246 @@
+"""Seeded synthetic inputs for the packed multi-adapter LoRA layer.
+
+This module draws the numbers both sides of every parity check consume: the
+CUDA path (through the C-ABI binding) and the fp64 CPU oracle.  It holds none
+of the layer's arithmetic: it only samples shapes, ranks, token counts and
+Gaussian tensors, rounds the activation/weight tensors to bfloat16 where the
+workload says so, and hands back plain numpy arrays in the storage layout the
+library uses:
+
+  * ``Wt``  = W transposed, ``[d_out, d_in]`` (the frozen base weight),
+  * ``At[i]`` = A_i transposed, ``[r_i, d_in]`` (fp32 master),
+  * ``Bt[i]`` = B_i transposed, ``[d_out, r_i]`` (fp32 master),
+  * ``X`` ``[N, d_in]`` and ``dY`` ``[N, d_out]``, the packed token rows, job i
+    owning rows ``[offset_i, offset_i + n_i)``.
+
+bf16 tensors are returned as ``uint16`` bit patterns (round-to-nearest-even
+from the fp32 draw); fp32 tensors as ``float32``.
+
+Randomness: every tensor has its own counter-based Philox stream keyed by
+``(config_id, tensor_id, chunk)``, drawn in fixed chunks of ``CHUNK`` elements,
+so a tensor's values do not depend on how many threads draw it nor on which
+other tensors were drawn before it.  Init distributions follow the workload
+descriptions (PLoRA, §2.1 for the LoRA shapes; §4.1/§11.2.1 for the model
+dimensions): ``N(0, 1/d_in)`` is a variance, ``N(0, 0.02)`` a standard deviation.
+"""
+from __future__ import annotations
+
+import concurrent.futures as _cf
+import os
+from dataclasses import dataclass, field
+
+import numpy as np
+
+CHUNK = 1 << 22
+
+# tensor ids inside one config's key space
+T_RANKS, T_TOKENS, T_W, T_X, T_DY, T_MISC = 0, 1, 2, 3, 4, 5
+T_ADAPTER_BASE = 100          # A_i -> 100 + 4 i, B_i -> 101 + 4 i, extras 102/103 + 4 i
+
+
+def _key(cfg_id: int, tensor_id: int, chunk: int) -> np.ndarray:
+    return np.array([cfg_id & 0xFFFFFFFFFFFFFFFF, ((tensor_id & 0xFFFFFFFF) << 32) | (chunk & 0xFFFFFFFF)],
+                    dtype=np.uint64)
+
+
+def rng(cfg_id: int, tensor_id: int, chunk: int = 0) -> np.random.Generator:
+    """Counter-based generator for one chunk of one tensor."""
+    return np.random.Generator(np.random.Philox(key=_key(cfg_id, tensor_id, chunk)))
+
+
+def _threads() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def normal_f32(cfg_id: int, tensor_id: int, n: int, std: float) -> np.ndarray:
+    """``n`` fp32 draws of N(0, std^2), chunked so the values are thread-count independent."""
+    out = np.empty(n, dtype=np.float32)
+    nchunks = (n + CHUNK - 1) // CHUNK
+
+    def work(c: int) -> None:
+        lo, hi = c * CHUNK, min(n, (c + 1) * CHUNK)
+        seg = out[lo:hi]
+        rng(cfg_id, tensor_id, c).standard_normal(out=seg, dtype=np.float32)
+        if std != 1.0:
+            seg *= np.float32(std)
+
+    if nchunks <= 1:
+        for c in range(nchunks):
+            work(c)
+    else:
+        with _cf.ThreadPoolExecutor(min(_threads(), nchunks)) as ex:
+            list(ex.map(work, range(nchunks)))
+    return out
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 to bfloat16 (round to nearest, ties to even); returns uint16 bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounded = u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))
+    return (rounded >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns to fp32."""
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclass
+class Workload:
+    """Sizes and seeds of one packed LoRA layer problem (no tensors)."""
+    name: str
+    cfg_id: int
+    d_in: int
+    d_out: int
+    dtype: str                       # "f32" or "bf16": dtype of X, W, dY, Y, dX
+    ranks: list
+    n_tokens: list
+    alphas: list
+    w_std: float
+    a_std: float
+    b_std: float
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.999
+    eps: float = 1e-8
+    weight_decay: float = 0.01
+
+    @property
+    def n_adapters(self) -> int:
+        return len(self.ranks)
+
+    @property
+    def offsets(self) -> list:
+        off, out = 0, []
+        for n in self.n_tokens:
+            out.append(off)
+            off += n
+        return out
+
+    @property
+    def N(self) -> int:
+        return int(sum(self.n_tokens))
+
+
+@dataclass
+class Tensors:
+    """Materialised inputs of a :class:`Workload` (numpy, storage layout)."""
+    wl: Workload
+    Wt: np.ndarray
+    X: np.ndarray
+    dY: np.ndarray
+    At: list = field(default_factory=list)
+    Bt: list = field(default_factory=list)
+
+
+# --------------------------------------------------------------------------
+# The five workloads (sizes from the packed-LoRA pages' model shapes; see
+# PLoRA §4.1 for the Llama-3/Qwen dimensions and §11.2.1 for the microbench
+# ranges).  Unstated alphas follow the tiny config (alpha = 2 r).
+# --------------------------------------------------------------------------
+
+def tiny_f32() -> Workload:
+    """d=256, ranks {4,8,16}, segments {64,32,96}, alpha=2r, fp32."""
+    d = 256
+    return Workload("tiny_f32_d256_r4-8-16", 1, d, d, "f32", [4, 8, 16], [64, 32, 96],
+                    [8.0, 16.0, 32.0], w_std=(1.0 / d) ** 0.5, a_std=(1.0 / d) ** 0.5, b_std=0.02)
+
+
+def llama8b_qproj() -> Workload:
+    """q_proj 4096x4096 bf16, 8 adapters ranks {8,8,16,16,32,32,64,64}, 2048 tokens each."""
+    ranks = [8, 8, 16, 16, 32, 32, 64, 64]
+    return Workload("llama3_8b_q_proj_4096x4096_8ad_16384tok", 2, 4096, 4096, "bf16", ranks, [2048] * 8,
+                    [2.0 * r for r in ranks], w_std=0.02, a_std=(1.0 / 4096) ** 0.5, b_std=0.02)
+
+
+def mlp_up_lognormal() -> Workload:
+    """4096->14336 bf16, 16 adapters, ranks U{4..128}, tokens lognormal(7,1) rounded to 16, clipped [64,8192], alpha=16."""
+    cfg = 3
+    g = rng(cfg, T_RANKS)
+    ranks = [int(r) for r in g.choice(np.array([4, 8, 16, 32, 64, 128]), size=16)]
+    g = rng(cfg, T_TOKENS)
+    raw = g.lognormal(mean=7.0, sigma=1.0, size=16)
+    toks = [int(min(8192, max(64, int(np.rint(v / 16.0)) * 16))) for v in raw]
+    return Workload("mlp_up_4096x14336_16ad_lognormal", cfg, 4096, 14336, "bf16", ranks, toks,
+                    [16.0] * 16, w_std=0.02, a_std=(1.0 / 4096) ** 0.5, b_std=0.02)
+
+
+LLAMA8B_PROJ = [("q", 4096, 4096), ("k", 4096, 1024), ("v", 4096, 1024), ("o", 4096, 4096),
+                ("gate", 4096, 14336), ("up", 4096, 14336), ("down", 14336, 4096)]
+
+
+def llama8b_layer(proj: int) -> Workload:
+    """One of the 7 projections of a Llama-3-8B decoder layer, 32 adapters, seq 1024, 1..8 seqs per job."""
+    cfg = 4
+    g = rng(cfg, T_RANKS)
+    ranks = [int(r) for r in g.choice(np.array([8, 16, 32, 64, 128]), size=32)]
+    g = rng(cfg, T_TOKENS)
+    toks = [int(b) * 1024 for b in g.integers(1, 9, size=32)]
+    name, din, dout = LLAMA8B_PROJ[proj]
+    return Workload(f"llama3_8b_layer_{name}_{din}x{dout}_32ad", 40 + proj, din, dout, "bf16", ranks, toks,
+                    [2.0 * r for r in ranks], w_std=0.02, a_std=(1.0 / 4096) ** 0.5, b_std=0.02)
+
+
+def llama70b_down_many_small() -> Workload:
+    """down_proj 28672->8192 bf16, 128 adapters, ranks {1..256} powers of two, segments 16..256 step 16, alpha=r."""
+    cfg = 5
+    g = rng(cfg, T_RANKS)
+    ranks = [int(r) for r in g.choice(np.array([1 << k for k in range(9)]), size=128)]
+    g = rng(cfg, T_TOKENS)
+    toks = [int(v) * 16 for v in g.integers(1, 17, size=128)]
+    return Workload("llama70b_down_28672x8192_128ad_small", cfg, 28672, 8192, "bf16", ranks, toks,
+                    [float(r) for r in ranks], w_std=0.02, a_std=(1.0 / 4096) ** 0.5, b_std=0.02)
+
+
+def custom(name: str, cfg_id: int, d_in: int, d_out: int, ranks, n_tokens, alphas=None, dtype="bf16",
+           w_std=0.02, a_std=None, b_std=0.02) -> Workload:
+    """Ad-hoc workload for edge-case tests (ragged tails, rank 1, straddling segments...)."""
+    ranks = [int(r) for r in ranks]
+    alphas = [2.0 * r for r in ranks] if alphas is None else [float(a) for a in alphas]
+    a_std = (1.0 / d_in) ** 0.5 if a_std is None else a_std
+    return Workload(name, cfg_id, d_in, d_out, dtype, ranks, [int(n) for n in n_tokens], alphas,
+                    w_std=w_std, a_std=a_std, b_std=b_std)
+
+
+CONFIGS = {
+    "tiny": tiny_f32,
+    "qproj": llama8b_qproj,
+    "mlp_up": mlp_up_lognormal,
+    "many_small": llama70b_down_many_small,
+}
+
+
+def _act(wl: Workload, tid: int, n: int, std: float) -> np.ndarray:
+    x = normal_f32(wl.cfg_id, tid, n, std)
+    return to_bf16_bits(x) if wl.dtype == "bf16" else x
+
+
+def materialise(wl: Workload, with_dY: bool = True) -> Tensors:
+    """Draw every tensor of the workload (storage layout, see module doc)."""
+    N = wl.N
+    Wt = _act(wl, T_W, wl.d_out * wl.d_in, wl.w_std).reshape(wl.d_out, wl.d_in)
+    X = _act(wl, T_X, N * wl.d_in, 1.0).reshape(N, wl.d_in)
+    dY = _act(wl, T_DY, N * wl.d_out, 1.0).reshape(N, wl.d_out) if with_dY else None
+    At, Bt = [], []
+    for i, r in enumerate(wl.ranks):
+        At.append(normal_f32(wl.cfg_id, T_ADAPTER_BASE + 4 * i, r * wl.d_in, wl.a_std).reshape(r, wl.d_in))
+        Bt.append(normal_f32(wl.cfg_id, T_ADAPTER_BASE + 4 * i + 1, wl.d_out * r, wl.b_std).reshape(wl.d_out, r))
+    return Tensors(wl, Wt, X, dY, At, Bt)
+
+
+def optimizer_state(wl: Workload, which: str, i: int, shape, kind: str) -> np.ndarray:
+    """Seeded fp32 stand-ins for a gradient (``kind='g'``), a first moment (``'m'``) or a
+    second moment (``'v'``, non-negative) of adapter ``i``'s ``which`` in {'A','B'}."""
+    n = int(np.prod(shape))
+    tid = 10_000 + 8 * i + (0 if which == "A" else 4) + {"g": 0, "m": 1, "v": 2}[kind]
+    x = normal_f32(wl.cfg_id, tid, n, 1e-2 if kind != "v" else 1e-2)
+    if kind == "v":
+        x = x * x
+    return x.reshape(shape)
+
+
+def rows_as_f64(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact fp64 view of stored values (bf16 bit patterns or fp32)."""
+    if dtype == "bf16":
+        return bf16_bits_to_f32(a).astype(np.float64)
+    return np.asarray(a, dtype=np.float64)
