@@ -1,0 +1,142 @@
+"""ctypes binding of ``libmlora.so`` (the C ABI declared in ``include/mlora.h``).
+
+The functions here carry the C names and only marshal arguments: every step of the layer runs
+in the library's CUDA kernels.  PyTorch is used for device memory and streams only.  If the
+library has not been built, :func:`lib` raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmlora.so")
+
+MLORA_OK, MLORA_ERR_INVALID, MLORA_ERR_UNSUPPORTED, MLORA_ERR_CUDA, MLORA_ERR_TIMEOUT, MLORA_ERR_OOM = range(6)
+MLORA_F32, MLORA_BF16 = 0, 1
+MLORA_PLAN_HOST_ONLY = 1
+MLORA_DEBUG_SHORT_TIMEOUT = 2
+MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD_B, MLORA_Q_WINDOW = range(6)
+
+# every symbol include/mlora.h declares
+EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward", "mlora_adamw",
+           "mlora_sync_status", "mlora_h_elems", "mlora_plan_describe", "mlora_status_string",
+           "mlora_last_error", "mlora_version"]
+
+
+class mlora_segment(C.Structure):
+    _fields_ = [("tok_offset", C.c_int64), ("n_tokens", C.c_int32), ("rank", C.c_int32), ("scale", C.c_float),
+                ("At", C.c_void_p), ("Bt", C.c_void_p), ("dAt", C.c_void_p), ("dBt", C.c_void_p),
+                ("mA", C.c_void_p), ("vA", C.c_void_p), ("mB", C.c_void_p), ("vB", C.c_void_p)]
+
+
+class mlora_problem(C.Structure):
+    _fields_ = [("n_tokens", C.c_int64), ("d_in", C.c_int32), ("d_out", C.c_int32), ("dtype", C.c_int32),
+                ("flags", C.c_uint32)]
+
+
+class MloraError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: {detail} (status {status})")
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded library; raises if it was not built (run ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, i64, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_float
+        L.mlora_plan.argtypes = [C.POINTER(mlora_problem), C.POINTER(mlora_segment), i32, C.POINTER(C.c_size_t),
+                                 C.POINTER(vp)]
+        L.mlora_plan.restype = i32
+        L.mlora_plan_destroy.argtypes = [vp]
+        L.mlora_plan_destroy.restype = None
+        L.mlora_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+        L.mlora_forward.restype = i32
+        L.mlora_backward.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.mlora_backward.restype = i32
+        L.mlora_adamw.argtypes = [vp, f32, f32, f32, f32, f32, i32, vp]
+        L.mlora_adamw.restype = i32
+        L.mlora_sync_status.argtypes = [vp, vp]
+        L.mlora_sync_status.restype = i32
+        L.mlora_h_elems.argtypes = [vp]
+        L.mlora_h_elems.restype = i64
+        L.mlora_plan_describe.argtypes = [vp, i32, C.POINTER(i64), i64, C.POINTER(i64)]
+        L.mlora_plan_describe.restype = i32
+        L.mlora_status_string.argtypes = [i32]
+        L.mlora_status_string.restype = C.c_char_p
+        L.mlora_last_error.argtypes = []
+        L.mlora_last_error.restype = C.c_char_p
+        L.mlora_version.argtypes = []
+        L.mlora_version.restype = i32
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != MLORA_OK:
+        L = lib()
+        raise MloraError(status, where, (L.mlora_last_error() or b"").decode() or
+                         L.mlora_status_string(status).decode())
+
+
+# ------------------------------------------------------------------ thin wrappers, C names
+
+def mlora_plan(problem: mlora_problem, segs) -> tuple[int, int]:
+    """Returns (plan handle, workspace bytes)."""
+    arr = (mlora_segment * len(segs))(*segs)
+    ws = C.c_size_t(0)
+    h = C.c_void_p(0)
+    _check(lib().mlora_plan(C.byref(problem), arr, len(segs), C.byref(ws), C.byref(h)), "mlora_plan")
+    return h.value, ws.value
+
+
+def mlora_plan_destroy(plan: int) -> None:
+    lib().mlora_plan_destroy(plan)
+
+
+def mlora_forward(plan, X, Wt, Y, H, workspace, stream) -> None:
+    _check(lib().mlora_forward(plan, X, Wt, Y, H, workspace, stream), "mlora_forward")
+
+
+def mlora_backward(plan, X, Wt, dY, H, dX, dH, workspace, stream) -> None:
+    _check(lib().mlora_backward(plan, X, Wt, dY, H, dX, dH, workspace, stream), "mlora_backward")
+
+
+def mlora_adamw(plan, lr, beta1, beta2, eps, weight_decay, step, stream) -> None:
+    _check(lib().mlora_adamw(plan, lr, beta1, beta2, eps, weight_decay, step, stream), "mlora_adamw")
+
+
+def mlora_sync_status(plan, stream) -> int:
+    """Returns the status code (does not raise on MLORA_ERR_TIMEOUT)."""
+    st = lib().mlora_sync_status(plan, stream)
+    if st not in (MLORA_OK, MLORA_ERR_TIMEOUT):
+        _check(st, "mlora_sync_status")
+    return st
+
+
+def mlora_h_elems(plan) -> int:
+    return int(lib().mlora_h_elems(plan))
+
+
+def mlora_plan_describe(plan, what: int) -> list[int]:
+    L = lib()
+    n = C.c_int64(0)
+    _check(L.mlora_plan_describe(plan, what, None, 0, C.byref(n)), "mlora_plan_describe")
+    buf = (C.c_int64 * max(1, n.value))()
+    _check(L.mlora_plan_describe(plan, what, buf, n.value, C.byref(n)), "mlora_plan_describe")
+    return list(buf[:n.value])
+
+
+def mlora_status_string(status: int) -> str:
+    return lib().mlora_status_string(status).decode()
+
+
+def mlora_version() -> int:
+    return int(lib().mlora_version())

@@ -1,0 +1,634 @@
+// C ABI of the packed multi-adapter LoRA layer: planner, workspace layout, tensor maps and the
+// launch sequences of forward / backward / AdamW.  See include/mlora.h for the contract.
+//
+// The planner is the host half of the rank-aware nano-batch scheduler ("tLoRA: Efficient
+// Multi-LoRA Training with Elastic Shared Super-Models", abstract: rank-aware nano-batches;
+// "PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §9.2: tile along
+// tokens / hidden dims, never along the rank).  It lays every job's rank window side by side in
+// one packed rank space (windows padded to 16 columns, cut into 64-column chunks), maps each
+// 128-token tile to the jobs and chunks it covers, and builds one static work list per kernel:
+//   * base GEMMs: (token tile x 256 output columns), rastered in groups of M tiles for L2 reuse;
+//   * shrink / dH: (token tile, <= 4 chunks of its window);
+//   * dA / dB: (128-row block of d_in / d_out, job, <= 4 chunks), sorted longest-first so the
+//     persistent grid's round-robin assignment balances uneven jobs.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "mlora.h"
+
+namespace mlora {
+template <int MODE>
+cudaError_t launch_seg_gemm(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int,
+                            cudaStream_t);
+cudaError_t launch_pack_fwd(const DevSeg*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, int,
+                            cudaStream_t);
+cudaError_t launch_pack_bwd(const DevSeg*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, cudaStream_t);
+cudaError_t launch_h_images(const DevSeg*, const MTile*, const int*, int, long long, const float*, uint8_t*,
+                            cudaStream_t);
+cudaError_t launch_adamw(const AdamItem*, int, float, float, float, float, float, int, int, cudaStream_t);
+cudaError_t launch_f32_forward(const DevSeg*, int, long long, int, int, long long, const float*, const float*, float*,
+                               float*, cudaStream_t);
+cudaError_t launch_f32_backward(const DevSeg*, int, long long, int, int, long long, int, const float*, const float*,
+                                const float*, const float*, float*, float*, cudaStream_t);
+}  // namespace mlora
+
+using namespace mlora;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+mlora_status fail(mlora_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+mlora_status cuda_fail(cudaError_t e, const char* where) {
+  g_last_error = std::string(where) + ": " + cudaGetErrorString(e);
+  return MLORA_ERR_CUDA;
+}
+
+constexpr int ADAM_CHUNK = 16384;
+constexpr int MAX_RANK = 256;
+constexpr unsigned long long DEFAULT_TIMEOUT_NS = 4000000000ull;   // 4 s
+constexpr unsigned long long SHORT_TIMEOUT_NS = 1000000ull;        // 1 ms
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix with a (box_inner x box_outer) box,
+// 128-byte swizzle, zero fill outside the matrix.
+mlora_status make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_elems,
+                      uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_elems * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] box %ux%u", static_cast<int>(r),
+             static_cast<unsigned long long>(outer), static_cast<unsigned long long>(inner), box_inner, box_outer);
+    return fail(MLORA_ERR_CUDA, buf);
+  }
+  return MLORA_OK;
+}
+
+}  // namespace
+
+struct mlora_plan_s {
+  mlora_problem prob{};
+  int n_segs = 0;
+  std::vector<mlora_segment> user;
+  std::vector<DevSeg> segs;
+  int C_total = 0, n_chunks = 0, n_mtiles = 0, max_rank = 0;
+  long long n_images = 0, h_elems = 0;
+  std::vector<MTile> mtiles;
+  std::vector<int> img_tile;
+  std::vector<int> col_seg;
+  std::vector<WinItem> win;
+  std::vector<WItem> da, db;
+  std::vector<AdamItem> adam;
+  bool can_backward = false, can_adamw = false;
+  size_t off_shadow = 0, off_himg = 0, off_dhimg = 0, ws_bytes = 0;
+  int group_m = 8;
+  // device
+  bool on_device = false;
+  int device = 0, num_sms = 148;
+  void* dev_block = nullptr;
+  DevSeg* d_segs = nullptr;
+  MTile* d_mtiles = nullptr;
+  int* d_img_tile = nullptr;
+  int* d_col_seg = nullptr;
+  WinItem* d_win = nullptr;
+  WItem* d_da = nullptr;
+  WItem* d_db = nullptr;
+  AdamItem* d_adam = nullptr;
+  int* d_err = nullptr;
+  unsigned long long timeout_ns = DEFAULT_TIMEOUT_NS;
+};
+
+namespace {
+
+mlora_status validate(const mlora_problem* p, const mlora_segment* s, int32_t n) {
+  if (!p || !s) return fail(MLORA_ERR_INVALID, "null problem or segment table");
+  if (n < 1) return fail(MLORA_ERR_INVALID, "n_segs must be >= 1");
+  if (p->dtype != MLORA_F32 && p->dtype != MLORA_BF16) return fail(MLORA_ERR_INVALID, "unknown dtype");
+  if (p->d_in < 1 || p->d_out < 1) return fail(MLORA_ERR_INVALID, "d_in and d_out must be >= 1");
+  const int q = p->dtype == MLORA_BF16 ? 8 : 4;
+  if (p->d_in % q || p->d_out % q)
+    return fail(MLORA_ERR_UNSUPPORTED, "d_in and d_out must be multiples of 8 (bf16) or 4 (fp32)");
+  if (p->n_tokens < 1 || p->n_tokens > 0x7fffffffLL) return fail(MLORA_ERR_INVALID, "n_tokens out of range");
+  long long expect = 0;
+  for (int i = 0; i < n; ++i) {
+    const mlora_segment& g = s[i];
+    char buf[160];
+    if (g.tok_offset != expect) {
+      snprintf(buf, sizeof buf, "segment %d starts at row %lld, expected %lld (segments must tile [0, N) in order)", i,
+               static_cast<long long>(g.tok_offset), expect);
+      return fail(MLORA_ERR_INVALID, buf);
+    }
+    if (g.n_tokens < 1) {
+      snprintf(buf, sizeof buf, "segment %d has n_tokens < 1", i);
+      return fail(MLORA_ERR_INVALID, buf);
+    }
+    if (g.rank < 1) {
+      snprintf(buf, sizeof buf, "segment %d has rank < 1", i);
+      return fail(MLORA_ERR_INVALID, buf);
+    }
+    if (g.rank > MAX_RANK) {
+      snprintf(buf, sizeof buf, "segment %d has rank %d > %d", i, g.rank, MAX_RANK);
+      return fail(MLORA_ERR_UNSUPPORTED, buf);
+    }
+    if (!std::isfinite(g.scale)) {
+      snprintf(buf, sizeof buf, "segment %d has a non-finite scale", i);
+      return fail(MLORA_ERR_INVALID, buf);
+    }
+    if (!g.At || !g.Bt) {
+      snprintf(buf, sizeof buf, "segment %d: At and Bt are required", i);
+      return fail(MLORA_ERR_INVALID, buf);
+    }
+    const float* ptrs[8] = {g.At, g.Bt, g.dAt, g.dBt, g.mA, g.vA, g.mB, g.vB};
+    for (const float* ptr : ptrs)
+      if (ptr && !aligned16(ptr)) {
+        snprintf(buf, sizeof buf, "segment %d: adapter buffers must be 16-byte aligned", i);
+        return fail(MLORA_ERR_INVALID, buf);
+      }
+    expect += g.n_tokens;
+  }
+  if (expect != p->n_tokens) {
+    char buf[160];
+    snprintf(buf, sizeof buf, "segments cover %lld rows but n_tokens is %lld", expect,
+             static_cast<long long>(p->n_tokens));
+    return fail(MLORA_ERR_INVALID, buf);
+  }
+  return MLORA_OK;
+}
+
+void build_tables(mlora_plan_t* P) {
+  const mlora_problem& pr = P->prob;
+  const long long N = pr.n_tokens;
+  // jobs and the packed rank space
+  int c = 0;
+  long long h = 0;
+  P->segs.resize(P->n_segs);
+  P->can_backward = P->can_adamw = true;
+  for (int i = 0; i < P->n_segs; ++i) {
+    const mlora_segment& u = P->user[i];
+    DevSeg& d = P->segs[i];
+    d.off = u.tok_offset;
+    d.n = u.n_tokens;
+    d.r = u.rank;
+    d.rp = static_cast<int>(round_up(u.rank, RANK_PAD));
+    d.c = c;
+    d.s = u.scale;
+    d.pad0 = 0;
+    d.h_off = h;
+    d.At = u.At;
+    d.Bt = u.Bt;
+    d.dAt = u.dAt;
+    d.dBt = u.dBt;
+    c += d.rp;
+    h += static_cast<long long>(u.n_tokens) * u.rank;
+    P->max_rank = std::max(P->max_rank, u.rank);
+    if (!u.dAt || !u.dBt) P->can_backward = false;
+    if (!u.dAt || !u.dBt || !u.mA || !u.vA || !u.mB || !u.vB) P->can_adamw = false;
+  }
+  P->C_total = c;
+  P->h_elems = h;
+  P->n_chunks = (c + CHUNK_COLS - 1) / CHUNK_COLS;
+  P->col_seg.resize(c);
+  for (int i = 0; i < P->n_segs; ++i)
+    for (int t = 0; t < P->segs[i].rp; ++t) P->col_seg[P->segs[i].c + t] = i;
+
+  // token tiles -> jobs -> chunks -> staged images
+  P->n_mtiles = static_cast<int>((N + BM - 1) / BM);
+  P->mtiles.resize(P->n_mtiles);
+  int j = 0;
+  long long img = 0;
+  for (int t = 0; t < P->n_mtiles; ++t) {
+    const long long r0 = static_cast<long long>(t) * BM, r1 = std::min(N, r0 + BM) - 1;
+    while (P->segs[j].off + P->segs[j].n <= r0) ++j;
+    int k = j;
+    while (P->segs[k].off + P->segs[k].n <= r1) ++k;
+    MTile& m = P->mtiles[t];
+    m.seg_first = j;
+    m.seg_last = k;
+    const int c_lo = P->segs[j].c, c_hi = P->segs[k].c + P->segs[k].rp;
+    m.q_lo = c_lo / CHUNK_COLS;
+    m.nch = (c_hi + CHUNK_COLS - 1) / CHUNK_COLS - m.q_lo;
+    m.img_off = static_cast<int>(img);
+    m.pad0 = m.pad1 = m.pad2 = 0;
+    img += m.nch;
+  }
+  P->n_images = img;
+  P->img_tile.resize(img);
+  for (int t = 0; t < P->n_mtiles; ++t)
+    for (int e = 0; e < P->mtiles[t].nch; ++e) P->img_tile[P->mtiles[t].img_off + e] = t;
+
+  // shrink / dH work: one item per (tile, <= 4 chunks)
+  P->win.clear();
+  for (int t = 0; t < P->n_mtiles; ++t) {
+    const MTile& m = P->mtiles[t];
+    for (int q = 0; q < m.nch; q += 4) P->win.push_back(WinItem{t, m.q_lo + q, std::min(4, m.nch - q), 0});
+  }
+
+  // dA / dB work: (row block, job, <= 4 chunks), longest first
+  auto wgrad = [&](int rows) {
+    std::vector<WItem> v;
+    for (int i = 0; i < P->n_segs; ++i) {
+      const DevSeg& d = P->segs[i];
+      const int ga = static_cast<int>(d.off / 64);
+      const int gb = static_cast<int>((d.off + d.n + 63) / 64);
+      const int qa = d.c / CHUNK_COLS, qb = (d.c + d.rp + CHUNK_COLS - 1) / CHUNK_COLS;
+      for (int q = qa; q < qb; q += 4)
+        for (int r0 = 0; r0 < rows; r0 += BM) v.push_back(WItem{r0, i, ga, gb, q, std::min(4, qb - q), 0, 0});
+    }
+    std::stable_sort(v.begin(), v.end(), [](const WItem& a, const WItem& b) {
+      return static_cast<long long>(a.gb - a.ga) * (16 + a.nq) > static_cast<long long>(b.gb - b.ga) * (16 + b.nq);
+    });
+    return v;
+  };
+  P->da = wgrad(pr.d_in);
+  P->db = wgrad(pr.d_out);
+
+  // AdamW pieces
+  P->adam.clear();
+  if (P->can_adamw) {
+    for (int i = 0; i < P->n_segs; ++i) {
+      const mlora_segment& u = P->user[i];
+      struct T { float *p, *g, *m, *v; long long n; } ts[2] = {
+          {u.At, u.dAt, u.mA, u.vA, static_cast<long long>(u.rank) * pr.d_in},
+          {u.Bt, u.dBt, u.mB, u.vB, static_cast<long long>(u.rank) * pr.d_out}};
+      for (const T& tt : ts)
+        for (long long s0 = 0; s0 < tt.n; s0 += ADAM_CHUNK) {
+          AdamItem a{};
+          a.p = tt.p + s0;
+          a.g = tt.g + s0;
+          a.m = tt.m + s0;
+          a.v = tt.v + s0;
+          a.count = static_cast<int>(std::min<long long>(ADAM_CHUNK, tt.n - s0));
+          P->adam.push_back(a);
+        }
+    }
+  }
+
+  // workspace: bf16 shadows (forward and backward use the same region), then the two image sets
+  if (pr.dtype == MLORA_BF16) {
+    const size_t shadow = round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024) +
+                          round_up(static_cast<size_t>(P->C_total) * pr.d_out * 2, 1024);
+    P->off_shadow = 0;
+    P->off_himg = round_up(shadow, 1024);
+    P->off_dhimg = P->off_himg + static_cast<size_t>(P->n_images) * IMG_BYTES;
+    P->ws_bytes = P->off_dhimg + static_cast<size_t>(P->n_images) * IMG_BYTES;
+  } else {
+    P->ws_bytes = 0;
+  }
+  // raster group for the base GEMMs: enough M tiles that one wave of CTAs shares W tiles
+  P->group_m = 16;
+}
+
+template <typename T>
+size_t table_bytes(const std::vector<T>& v) {
+  return round_up(std::max<size_t>(1, v.size()) * sizeof(T), 256);
+}
+
+mlora_status upload(mlora_plan_t* P) {
+  cudaError_t e = cudaGetDevice(&P->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  const size_t b_segs = table_bytes(P->segs), b_mt = table_bytes(P->mtiles), b_it = table_bytes(P->img_tile),
+               b_cs = table_bytes(P->col_seg), b_win = table_bytes(P->win), b_da = table_bytes(P->da),
+               b_db = table_bytes(P->db), b_adam = table_bytes(P->adam), b_err = 256;
+  const size_t total = b_segs + b_mt + b_it + b_cs + b_win + b_da + b_db + b_adam + b_err;
+  e = cudaMalloc(&P->dev_block, total);
+  if (e != cudaSuccess) {
+    P->dev_block = nullptr;
+    cudaGetLastError();
+    return fail(MLORA_ERR_OOM, std::string("cudaMalloc of the plan tables failed: ") + cudaGetErrorString(e));
+  }
+  uint8_t* b = static_cast<uint8_t*>(P->dev_block);
+  size_t o = 0;
+  auto place = [&](auto*& dst, const auto& vec, size_t bytes) -> cudaError_t {
+    using TT = std::remove_reference_t<decltype(*dst)>;
+    dst = reinterpret_cast<TT*>(b + o);
+    o += bytes;
+    if (vec.empty()) return cudaSuccess;
+    return cudaMemcpy(dst, vec.data(), vec.size() * sizeof(vec[0]), cudaMemcpyHostToDevice);
+  };
+  if ((e = place(P->d_segs, P->segs, b_segs)) != cudaSuccess ||
+      (e = place(P->d_mtiles, P->mtiles, b_mt)) != cudaSuccess ||
+      (e = place(P->d_img_tile, P->img_tile, b_it)) != cudaSuccess ||
+      (e = place(P->d_col_seg, P->col_seg, b_cs)) != cudaSuccess ||
+      (e = place(P->d_win, P->win, b_win)) != cudaSuccess || (e = place(P->d_da, P->da, b_da)) != cudaSuccess ||
+      (e = place(P->d_db, P->db, b_db)) != cudaSuccess || (e = place(P->d_adam, P->adam, b_adam)) != cudaSuccess)
+    return cuda_fail(e, "uploading the plan tables");
+  P->d_err = reinterpret_cast<int*>(b + o);
+  e = cudaMemset(P->d_err, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  P->on_device = true;
+  return MLORA_OK;
+}
+
+GemmArgs base_args(const mlora_plan_t* P) {
+  GemmArgs g{};
+  g.N = static_cast<int>(P->prob.n_tokens);
+  g.d_in = P->prob.d_in;
+  g.d_out = P->prob.d_out;
+  g.n_mtiles = P->n_mtiles;
+  g.group_m = P->group_m;
+  g.mtiles = P->d_mtiles;
+  g.win = P->d_win;
+  g.segs = P->d_segs;
+  g.err = P->d_err;
+  g.timeout_ns = P->timeout_ns;
+  return g;
+}
+
+int grid_of(const mlora_plan_t* P, int items) { return std::max(1, std::min(items, P->num_sms)); }
+
+mlora_status check_exec(const mlora_plan_t* P) {
+  if (!P) return fail(MLORA_ERR_INVALID, "null plan");
+  if (!P->on_device) return fail(MLORA_ERR_INVALID, "plan was built with MLORA_PLAN_HOST_ONLY");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != P->device)
+    return fail(MLORA_ERR_INVALID, "the current device is not the one the plan was built on");
+  return MLORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
+                        size_t* workspace_bytes, mlora_plan_t** out) {
+  g_last_error.clear();
+  if (!out || !workspace_bytes) return fail(MLORA_ERR_INVALID, "null output pointer");
+  *out = nullptr;
+  mlora_status st = validate(problem, segs, n_segs);
+  if (st != MLORA_OK) return st;
+  mlora_plan_t* P = new (std::nothrow) mlora_plan_s();
+  if (!P) return fail(MLORA_ERR_OOM, "host allocation failed");
+  P->prob = *problem;
+  P->n_segs = n_segs;
+  P->user.assign(segs, segs + n_segs);
+  if (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT) P->timeout_ns = SHORT_TIMEOUT_NS;
+  build_tables(P);
+  if (!(problem->flags & MLORA_PLAN_HOST_ONLY)) {
+    st = upload(P);
+    if (st != MLORA_OK) {
+      mlora_plan_destroy(P);
+      return st;
+    }
+  }
+  *workspace_bytes = P->ws_bytes;
+  *out = P;
+  return MLORA_OK;
+}
+
+void mlora_plan_destroy(mlora_plan_t* plan) {
+  if (!plan) return;
+  if (plan->dev_block) cudaFree(plan->dev_block);
+  delete plan;
+}
+
+int64_t mlora_h_elems(const mlora_plan_t* plan) { return plan ? plan->h_elems : -1; }
+
+mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt, void* Y, float* H, void* workspace,
+                           void* stream) {
+  g_last_error.clear();
+  mlora_status st = check_exec(P);
+  if (st != MLORA_OK) return st;
+  if (!X || !Wt || !Y || (!H && P->h_elems > 0)) return fail(MLORA_ERR_INVALID, "null tensor argument");
+  if (!aligned16(X) || !aligned16(Wt) || !aligned16(Y) || !aligned16(H))
+    return fail(MLORA_ERR_INVALID, "X, Wt, Y and H must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const mlora_problem& pr = P->prob;
+  cudaError_t e;
+  if (pr.dtype == MLORA_F32) {
+    e = launch_f32_forward(P->d_segs, P->n_segs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems,
+                           static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<float*>(Y), H, s);
+    return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 forward launch");
+  }
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(MLORA_ERR_INVALID, "workspace must be a 256-byte aligned device buffer");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* at_all = reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow);
+  __nv_bfloat16* bt_all =
+      reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow + round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024));
+  uint8_t* himg = ws + P->off_himg;
+
+  e = launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+
+  CUtensorMap mX, mAt, mW, mBt;
+  if ((st = make_map(&mX, X, pr.d_in, pr.n_tokens, pr.d_in, 64, 128)) != MLORA_OK) return st;
+  if ((st = make_map(&mAt, at_all, pr.d_in, P->C_total, pr.d_in, 64, 64)) != MLORA_OK) return st;
+  if ((st = make_map(&mW, Wt, pr.d_in, pr.d_out, pr.d_in, 64, 256)) != MLORA_OK) return st;
+  if ((st = make_map(&mBt, bt_all, P->C_total, pr.d_out, P->C_total, 64, 256)) != MLORA_OK) return st;
+
+  GemmArgs g = base_args(P);
+  g.kmain = (pr.d_in + BK - 1) / BK;
+  g.n_items = static_cast<int>(P->win.size());
+  g.img_out = himg;
+  g.hout = H;
+  e = launch_seg_gemm<MODE_SHRINK>(mX, mAt, mAt, g, grid_of(P, g.n_items), s);
+  if (e != cudaSuccess) return cuda_fail(e, "shrink launch");
+
+  g = base_args(P);
+  g.kmain = (pr.d_in + BK - 1) / BK;
+  g.n_tiles_n = (pr.d_out + BN - 1) / BN;
+  g.n_items = P->n_mtiles * g.n_tiles_n;
+  g.img_in = himg;
+  g.out = Y;
+  g.ld_out = pr.d_out;
+  e = launch_seg_gemm<MODE_FWD>(mX, mW, mBt, g, grid_of(P, g.n_items), s);
+  if (e != cudaSuccess) return cuda_fail(e, "forward GEMM launch");
+  return MLORA_OK;
+}
+
+mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt, const void* dY, const float* H,
+                            void* dX, float* dH, void* workspace, void* stream) {
+  g_last_error.clear();
+  mlora_status st = check_exec(P);
+  if (st != MLORA_OK) return st;
+  if (!P->can_backward) return fail(MLORA_ERR_INVALID, "the plan's segments have no dAt/dBt buffers");
+  if (!X || !Wt || !dY || !dX || ((!H || !dH) && P->h_elems > 0)) return fail(MLORA_ERR_INVALID, "null tensor argument");
+  if (!aligned16(X) || !aligned16(Wt) || !aligned16(dY) || !aligned16(dX) || !aligned16(H) || !aligned16(dH))
+    return fail(MLORA_ERR_INVALID, "X, Wt, dY, dX, H and dH must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const mlora_problem& pr = P->prob;
+  cudaError_t e;
+  if (pr.dtype == MLORA_F32) {
+    e = launch_f32_backward(P->d_segs, P->n_segs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems, P->max_rank,
+                            static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<const float*>(dY),
+                            H, static_cast<float*>(dX), dH, s);
+    return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 backward launch");
+  }
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(MLORA_ERR_INVALID, "workspace must be a 256-byte aligned device buffer");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __nv_bfloat16* a_all = reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow);
+  __nv_bfloat16* b_all =
+      reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow + round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024));
+  uint8_t* himg = ws + P->off_himg;
+  uint8_t* dhimg = ws + P->off_dhimg;
+
+  e = launch_pack_bwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, a_all, b_all, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+  e = launch_h_images(P->d_segs, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s);
+  if (e != cudaSuccess) return cuda_fail(e, "image launch");
+
+  CUtensorMap mdY, mdYt, mB, mWmn, mA, mXt;
+  if ((st = make_map(&mdY, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 128)) != MLORA_OK) return st;
+  if ((st = make_map(&mdYt, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 64)) != MLORA_OK) return st;
+  if ((st = make_map(&mB, b_all, pr.d_out, P->C_total, pr.d_out, 64, 64)) != MLORA_OK) return st;
+  if ((st = make_map(&mWmn, Wt, pr.d_in, pr.d_out, pr.d_in, 64, 64)) != MLORA_OK) return st;
+  if ((st = make_map(&mA, a_all, P->C_total, pr.d_in, P->C_total, 64, 256)) != MLORA_OK) return st;
+  if ((st = make_map(&mXt, X, pr.d_in, pr.n_tokens, pr.d_in, 64, 64)) != MLORA_OK) return st;
+
+  // dH = s dY B^T  (+ staged dHtilde images)
+  GemmArgs g = base_args(P);
+  g.kmain = (pr.d_out + BK - 1) / BK;
+  g.n_items = static_cast<int>(P->win.size());
+  g.img_out = dhimg;
+  g.hout = dH;
+  e = launch_seg_gemm<MODE_DH>(mdY, mB, mB, g, grid_of(P, g.n_items), s);
+  if (e != cudaSuccess) return cuda_fail(e, "dH launch");
+
+  // dB = Htilde^T dY
+  g = base_args(P);
+  g.witems = P->d_db;
+  g.n_items = static_cast<int>(P->db.size());
+  g.img_in = himg;
+  e = launch_seg_gemm<MODE_DB>(mdYt, mdYt, mdYt, g, grid_of(P, g.n_items), s);
+  if (e != cudaSuccess) return cuda_fail(e, "dB launch");
+
+  // dX = dY W^T + dHtilde A^T
+  g = base_args(P);
+  g.kmain = (pr.d_out + BK - 1) / BK;
+  g.n_tiles_n = (pr.d_in + BN - 1) / BN;
+  g.n_items = P->n_mtiles * g.n_tiles_n;
+  g.img_in = dhimg;
+  g.out = dX;
+  g.ld_out = pr.d_in;
+  e = launch_seg_gemm<MODE_BWD>(mdY, mWmn, mA, g, grid_of(P, g.n_items), s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward GEMM launch");
+
+  // dA = X^T dHtilde
+  g = base_args(P);
+  g.witems = P->d_da;
+  g.n_items = static_cast<int>(P->da.size());
+  g.img_in = dhimg;
+  e = launch_seg_gemm<MODE_DA>(mXt, mXt, mXt, g, grid_of(P, g.n_items), s);
+  if (e != cudaSuccess) return cuda_fail(e, "dA launch");
+  return MLORA_OK;
+}
+
+mlora_status mlora_adamw(const mlora_plan_t* P, float lr, float beta1, float beta2, float eps, float weight_decay,
+                         int32_t step, void* stream) {
+  g_last_error.clear();
+  mlora_status st = check_exec(P);
+  if (st != MLORA_OK) return st;
+  if (!P->can_adamw) return fail(MLORA_ERR_INVALID, "the plan's segments lack gradient or moment buffers");
+  if (step < 1) return fail(MLORA_ERR_INVALID, "step must be >= 1");
+  if (!(beta1 >= 0.f && beta1 < 1.f && beta2 >= 0.f && beta2 < 1.f) || !std::isfinite(lr) || !std::isfinite(eps) ||
+      !std::isfinite(weight_decay))
+    return fail(MLORA_ERR_INVALID, "bad AdamW hyper-parameters");
+  cudaError_t e = launch_adamw(P->d_adam, static_cast<int>(P->adam.size()), lr, beta1, beta2, eps, weight_decay, step,
+                               P->num_sms, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "AdamW launch");
+}
+
+mlora_status mlora_sync_status(const mlora_plan_t* P, void* stream) {
+  g_last_error.clear();
+  mlora_status st = check_exec(P);
+  if (st != MLORA_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, P->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (v != 0) {
+    e = cudaMemset(P->d_err, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    char buf[96];
+    snprintf(buf, sizeof buf, "a device-side wait gave up (code 0x%x)", v);
+    return fail(MLORA_ERR_TIMEOUT, buf);
+  }
+  return MLORA_OK;
+}
+
+mlora_status mlora_plan_describe(const mlora_plan_t* P, int32_t what, int64_t* out, int64_t cap, int64_t* count) {
+  if (!P || !count) return fail(MLORA_ERR_INVALID, "null plan or count");
+  std::vector<int64_t> v;
+  switch (what) {
+    case MLORA_Q_SUMMARY:
+      v = {P->prob.n_tokens, P->prob.d_in, P->prob.d_out, P->n_segs, P->n_mtiles, P->C_total, P->n_chunks,
+           P->n_images, static_cast<int64_t>(P->win.size()), static_cast<int64_t>(P->da.size()),
+           static_cast<int64_t>(P->db.size()), static_cast<int64_t>(P->ws_bytes)};
+      break;
+    case MLORA_Q_MTILES:
+      for (const MTile& m : P->mtiles) v.insert(v.end(), {m.seg_first, m.seg_last, m.q_lo, m.nch, m.img_off});
+      break;
+    case MLORA_Q_COLUMNS:
+      for (const DevSeg& d : P->segs) v.insert(v.end(), {d.c, d.rp});
+      break;
+    case MLORA_Q_WGRAD_A:
+    case MLORA_Q_WGRAD_B:
+      for (const WItem& w : (what == MLORA_Q_WGRAD_A ? P->da : P->db))
+        v.insert(v.end(), {w.row0, w.seg, w.ga, w.gb, w.q0, w.nq});
+      break;
+    case MLORA_Q_WINDOW:
+      for (const WinItem& w : P->win) v.insert(v.end(), {w.tile, w.q0, w.nq});
+      break;
+    default:
+      return fail(MLORA_ERR_INVALID, "unknown table");
+  }
+  *count = static_cast<int64_t>(v.size());
+  if (out) std::copy(v.begin(), v.begin() + std::min<int64_t>(cap, *count), out);
+  return MLORA_OK;
+}
+
+const char* mlora_status_string(mlora_status s) {
+  switch (s) {
+    case MLORA_OK: return "ok";
+    case MLORA_ERR_INVALID: return "invalid argument";
+    case MLORA_ERR_UNSUPPORTED: return "unsupported";
+    case MLORA_ERR_CUDA: return "CUDA error";
+    case MLORA_ERR_TIMEOUT: return "device wait timed out";
+    case MLORA_ERR_OOM: return "out of memory";
+  }
+  return "unknown status";
+}
+
+const char* mlora_last_error(void) { return g_last_error.c_str(); }
+
+int32_t mlora_version(void) { return 100; }
+
+}  // extern "C"

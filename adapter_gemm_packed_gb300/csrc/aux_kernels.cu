@@ -1,0 +1,244 @@
+// Memory-bound helper kernels of the packed LoRA layer:
+//  * bf16 shadows of the fp32 adapter masters in the packed rank space (the operands the
+//    tensor-core engine reads through TMA), in the two orientations forward and backward need;
+//  * rebuild of the staged Htilde images from the saved activation H (backward);
+//  * the per-adapter AdamW step over every A_i and B_i ("PLoRA: Efficient Concurrent LoRA
+//    Training for Large Language Models", §8: moment, velocity and gradient per parameter;
+//    the step order is PyTorch's decoupled-weight-decay AdamW).
+#include "common.cuh"
+
+namespace mlora {
+
+namespace {
+
+// At_all [C_total, d_in] bf16: row c = At_i[c - c_i] for c in job i's window, zero in padding.
+__global__ void k_pack_at(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_in,
+                          __nv_bfloat16* __restrict__ at_all) {
+  const int d8 = d_in / 8;
+  const long long total = static_cast<long long>(C_total) * d8;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(i / d8);
+    const int k = static_cast<int>(i - static_cast<long long>(c) * d8) * 8;
+    const DevSeg& sg = segs[col_seg[c]];
+    const int t = c - sg.c;
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (t < sg.r) {
+      const float4* src = reinterpret_cast<const float4*>(sg.At + static_cast<size_t>(t) * d_in + k);
+      const float4 a = src[0], b = src[1];
+      o.x = pack_bf16x2(a.x, a.y);
+      o.y = pack_bf16x2(a.z, a.w);
+      o.z = pack_bf16x2(b.x, b.y);
+      o.w = pack_bf16x2(b.z, b.w);
+    }
+    *reinterpret_cast<uint4*>(at_all + static_cast<size_t>(c) * d_in + k) = o;
+  }
+}
+
+// Bt_all [d_out, C_total] bf16: Bt_all[o][c] = Bt_i[o][c - c_i] (zero in padding).
+__global__ void k_pack_bt(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_out,
+                          __nv_bfloat16* __restrict__ bt_all) {
+  const int c8 = C_total / 8;
+  const long long total = static_cast<long long>(d_out) * c8;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int o = static_cast<int>(i / c8);
+    const int c = static_cast<int>(i - static_cast<long long>(o) * c8) * 8;
+    const DevSeg& sg = segs[col_seg[c]];   // 8 columns never straddle two windows (windows are 16-aligned)
+    const float* src = sg.Bt + static_cast<size_t>(o) * sg.r;
+    float f[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = c - sg.c + u;
+      f[u] = t < sg.r ? src[t] : 0.f;
+    }
+    uint4 v;
+    v.x = pack_bf16x2(f[0], f[1]);
+    v.y = pack_bf16x2(f[2], f[3]);
+    v.z = pack_bf16x2(f[4], f[5]);
+    v.w = pack_bf16x2(f[6], f[7]);
+    *reinterpret_cast<uint4*>(bt_all + static_cast<size_t>(o) * C_total + c) = v;
+  }
+}
+
+// Transposing packs through shared memory, 32x32 tiles.
+// A_all [d_in, C_total] bf16: A_all[k][c] = At_i[c - c_i][k].
+__global__ void k_pack_a_t(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_in,
+                           __nv_bfloat16* __restrict__ a_all) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.y * 32, k0 = blockIdx.x * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
+  for (int yy = ty; yy < 32; yy += 8) {
+    const int c = c0 + yy, k = k0 + tx;
+    float v = 0.f;
+    if (c < C_total && k < d_in) {
+      const DevSeg& sg = segs[col_seg[c]];
+      const int t = c - sg.c;
+      if (t < sg.r) v = sg.At[static_cast<size_t>(t) * d_in + k];
+    }
+    tile[yy][tx] = v;
+  }
+  __syncthreads();
+  for (int yy = ty; yy < 32; yy += 8) {
+    const int k = k0 + yy, c = c0 + tx;
+    if (k < d_in && c < C_total) a_all[static_cast<size_t>(k) * C_total + c] = __float2bfloat16_rn(tile[tx][yy]);
+  }
+}
+
+// B_all [C_total, d_out] bf16: B_all[c][o] = Bt_i[o][c - c_i].
+__global__ void k_pack_b_t(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_out,
+                           __nv_bfloat16* __restrict__ b_all) {
+  __shared__ float tile[32][33];
+  const int o0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int yy = ty; yy < 32; yy += 8) {
+    const int o = o0 + yy, c = c0 + tx;
+    float v = 0.f;
+    if (o < d_out && c < C_total) {
+      const DevSeg& sg = segs[col_seg[c]];
+      const int t = c - sg.c;
+      if (t < sg.r) v = sg.Bt[static_cast<size_t>(o) * sg.r + t];
+    }
+    tile[yy][tx] = v;
+  }
+  __syncthreads();
+  for (int yy = ty; yy < 32; yy += 8) {
+    const int c = c0 + yy, o = o0 + tx;
+    if (c < C_total && o < d_out) b_all[static_cast<size_t>(c) * d_out + o] = __float2bfloat16_rn(tile[tx][yy]);
+  }
+}
+
+// Staged Htilde images from H: image (tile t, chunk q) row r col u = s_j H_j[row - off_j][64q + u - c_j]
+// when token row (128 t + r) belongs to job j and column 64q+u lies in job j's rank window, else 0.
+__global__ void k_h_images(const DevSeg* __restrict__ segs, const MTile* __restrict__ mtiles,
+                           const int* __restrict__ img_tile, long long N, const float* __restrict__ H,
+                           uint8_t* __restrict__ img_out) {
+  const int img = blockIdx.x;
+  const int t = img_tile[img];
+  const MTile mt = mtiles[t];
+  const int q = mt.q_lo + (img - mt.img_off);
+  const int rit = threadIdx.x;   // 128 threads: one row each
+  const long long row = static_cast<long long>(t) * BM + rit;
+  int c_lo = 0, c_hi = 0;
+  float s = 0.f;
+  const float* hrow = nullptr;
+  if (row < N) {
+    int j = mt.seg_first;
+    while (j < mt.seg_last && row >= segs[j + 1].off) ++j;
+    const DevSeg& sg = segs[j];
+    c_lo = sg.c;
+    c_hi = sg.c + sg.r;
+    s = sg.s;
+    hrow = H + sg.h_off + (row - sg.off) * sg.r - sg.c;
+  }
+  uint8_t* base = img_out + static_cast<size_t>(img) * IMG_BYTES;
+#pragma unroll
+  for (int k8 = 0; k8 < 8; ++k8) {
+    uint32_t pk[4];
+#pragma unroll
+    for (int u = 0; u < 8; u += 2) {
+      const int c0 = q * CHUNK_COLS + k8 * 8 + u, c1 = c0 + 1;
+      const float a0 = (c0 >= c_lo && c0 < c_hi) ? s * hrow[c0] : 0.f;
+      const float a1 = (c1 >= c_lo && c1 < c_hi) ? s * hrow[c1] : 0.f;
+      pk[u / 2] = pack_bf16x2(a0, a1);
+    }
+    *reinterpret_cast<uint4*>(base + swz128_offset(rit, k8 * 8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  }
+}
+
+// AdamW over a list of <= ADAM_CHUNK-element pieces of every adapter's A and B.
+__global__ void k_adamw(const AdamItem* __restrict__ items, int n_items, float lr, float beta1, float beta2,
+                        float eps, float decay, float bc1, float bc2) {
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const AdamItem w = items[it];
+    const int n4 = w.count >> 2;
+    float4* p4 = reinterpret_cast<float4*>(w.p);
+    const float4* g4 = reinterpret_cast<const float4*>(w.g);
+    float4* m4 = reinterpret_cast<float4*>(w.m);
+    float4* v4 = reinterpret_cast<float4*>(w.v);
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+      float4 p = p4[i];
+      const float4 g = g4[i];
+      float4 m = m4[i], v = v4[i];
+      float* pp = &p.x;
+      const float* gg = &g.x;
+      float* mm = &m.x;
+      float* vv = &v.x;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float gu = gg[u];
+        const float pd = pp[u] * decay;
+        const float mu = beta1 * mm[u] + (1.f - beta1) * gu;
+        const float vu = beta2 * vv[u] + (1.f - beta2) * gu * gu;
+        const float mhat = mu / bc1;
+        const float vhat = vu / bc2;
+        pp[u] = pd - lr * mhat / (sqrtf(vhat) + eps);
+        mm[u] = mu;
+        vv[u] = vu;
+      }
+      p4[i] = p;
+      m4[i] = m;
+      v4[i] = v;
+    }
+    for (int i = (n4 << 2) + threadIdx.x; i < w.count; i += blockDim.x) {
+      const float gu = w.g[i];
+      const float pd = w.p[i] * decay;
+      const float mu = beta1 * w.m[i] + (1.f - beta1) * gu;
+      const float vu = beta2 * w.v[i] + (1.f - beta2) * gu * gu;
+      w.p[i] = pd - lr * (mu / bc1) / (sqrtf(vu / bc2) + eps);
+      w.m[i] = mu;
+      w.v[i] = vu;
+    }
+  }
+}
+
+inline int grid_for(long long work, int threads, int num_sms) {
+  long long b = (work + threads - 1) / threads;
+  long long cap = static_cast<long long>(num_sms) * 8;
+  if (b > cap) b = cap;
+  if (b < 1) b = 1;
+  return static_cast<int>(b);
+}
+
+}  // namespace
+
+cudaError_t launch_pack_fwd(const DevSeg* segs, const int* col_seg, int C_total, int d_in, int d_out,
+                            __nv_bfloat16* at_all, __nv_bfloat16* bt_all, int num_sms, cudaStream_t st) {
+  const long long w1 = static_cast<long long>(C_total) * (d_in / 8);
+  k_pack_at<<<grid_for(w1, 256, num_sms), 256, 0, st>>>(segs, col_seg, C_total, d_in, at_all);
+  const long long w2 = static_cast<long long>(d_out) * (C_total / 8);
+  k_pack_bt<<<grid_for(w2, 256, num_sms), 256, 0, st>>>(segs, col_seg, C_total, d_out, bt_all);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_bwd(const DevSeg* segs, const int* col_seg, int C_total, int d_in, int d_out,
+                            __nv_bfloat16* a_all, __nv_bfloat16* b_all, cudaStream_t st) {
+  dim3 blk(32, 8);
+  dim3 g1((d_in + 31) / 32, (C_total + 31) / 32);
+  k_pack_a_t<<<g1, blk, 0, st>>>(segs, col_seg, C_total, d_in, a_all);
+  dim3 g2((d_out + 31) / 32, (C_total + 31) / 32);
+  k_pack_b_t<<<g2, blk, 0, st>>>(segs, col_seg, C_total, d_out, b_all);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_h_images(const DevSeg* segs, const MTile* mtiles, const int* img_tile, int n_images, long long N,
+                            const float* H, uint8_t* img_out, cudaStream_t st) {
+  if (n_images <= 0) return cudaSuccess;
+  k_h_images<<<n_images, BM, 0, st>>>(segs, mtiles, img_tile, N, H, img_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_adamw(const AdamItem* items, int n_items, float lr, float beta1, float beta2, float eps,
+                         float weight_decay, int step, int num_sms, cudaStream_t st) {
+  if (n_items <= 0) return cudaSuccess;
+  const double bc1 = 1.0 - pow(static_cast<double>(beta1), step);
+  const double bc2 = 1.0 - pow(static_cast<double>(beta2), step);
+  const float decay = 1.0f - lr * weight_decay;
+  int grid = n_items;
+  if (grid > num_sms * 16) grid = num_sms * 16;
+  k_adamw<<<grid, 512, 0, st>>>(items, n_items, lr, beta1, beta2, eps, decay, static_cast<float>(bc1),
+                                static_cast<float>(bc2));
+  return cudaGetLastError();
+}
+
+}  // namespace mlora

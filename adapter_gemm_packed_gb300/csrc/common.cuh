@@ -1,0 +1,289 @@
+// Internal definitions shared by the CUDA translation units of the packed LoRA library:
+// device-side tables built by the planner, kernel argument blocks, and thin inline-PTX
+// wrappers for the sm_103a features the kernels use (tcgen05 MMA/TMEM, TMA bulk tensor
+// copies, mbarriers).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mlora {
+
+// ---------------------------------------------------------------------------------------
+// Tiling constants of the segmented tensor-core GEMM engine.
+// A 128-row tile of tokens (or of d_in/d_out rows for the weight-gradient products) is the
+// M side of every tcgen05 MMA; operands move in 64-element (128-byte) K slices, so every
+// smem operand tile is a stack of 128B-swizzled 8-row atoms (1024 bytes each).
+// ---------------------------------------------------------------------------------------
+constexpr int BM = 128;              // MMA M (rows of the accumulator = TMEM lanes)
+constexpr int BN = 256;              // max MMA N (accumulator columns per buffer)
+constexpr int BK = 64;               // K slice per pipeline stage (64 bf16 = 128 bytes)
+constexpr int STAGES = 4;            // smem pipeline depth
+constexpr int A_STAGE_BYTES = BM * BK * 2;       // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK * 2;       // 32 KB
+constexpr int CHUNK_COLS = 64;       // rank-window chunk: 64 packed rank columns
+constexpr int IMG_BYTES = BM * CHUNK_COLS * 2;   // one staged [128 x 64] bf16 image (16 KB)
+constexpr int RANK_PAD = 16;         // each job's rank window is padded to a multiple of 16
+constexpr int GEMM_THREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int TMEM_COLS = 512;       // two 256-column fp32 accumulators
+constexpr int GEMM_SMEM_BYTES = STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
+
+enum GemmMode : int {
+  MODE_FWD = 0,     // Y  = X  Wt^T + Htilde  Bt_all^T          (rank term as extra K slices)
+  MODE_BWD = 1,     // dX = dY W    + dHtilde A_all^T           (W read MN-major from Wt)
+  MODE_SHRINK = 2,  // H  = X  At_all^T over the tile's rank window -> H (fp32) + Htilde images
+  MODE_DH = 3,      // dH = s dY B_all^T over the tile's rank window -> dH (fp32) + dHtilde images
+  MODE_DA = 4,      // dA = X^T dHtilde  (token reduction, both operands MN-major)
+  MODE_DB = 5       // dB = dY^T Htilde  (token reduction, both operands MN-major)
+};
+
+// Per-job record on the device.
+struct DevSeg {
+  long long off;       // first token row
+  int n;               // tokens
+  int r;               // rank
+  int c;               // first column of the job's window in the packed rank space
+  int rp;              // padded window width (multiple of RANK_PAD)
+  float s;             // scale alpha / r
+  int pad0;
+  long long h_off;     // element offset of the job's [n, r] block in H / dH
+  float* At;
+  float* Bt;
+  float* dAt;
+  float* dBt;
+};
+
+// Per 128-token tile: which jobs it covers and where its staged rank images live.
+struct MTile {
+  int seg_first, seg_last;   // jobs overlapping the tile (inclusive)
+  int q_lo, nch;             // 64-column chunks [q_lo, q_lo + nch) of the packed rank space
+  int img_off;               // index of the tile's first staged image
+  int pad0, pad1, pad2;
+};
+
+// Rank-window work item (shrink / dH): one tile, up to 4 chunks (N <= 256).
+struct WinItem {
+  int tile, q0, nq, pad0;
+};
+
+// Weight-gradient work item (dA / dB): one 128-row block of d_in (dA) or d_out (dB), one
+// job, its 64-token half-tiles [ga, gb), chunks [q0, q0 + nq) of its rank window.
+struct WItem {
+  int row0, seg, ga, gb, q0, nq, pad0, pad1;
+};
+
+struct AdamItem {
+  float* p;
+  const float* g;
+  float* m;
+  float* v;
+  int count;
+  int pad0;
+  long long pad1;
+};
+
+struct GemmArgs {
+  int N;               // tokens
+  int d_in, d_out;
+  int kmain;           // 64-wide K slices of the main product (FWD/BWD/SHRINK/DH)
+  int n_items;
+  int n_tiles_n;       // FWD/BWD: output column tiles of 256
+  int group_m;         // FWD/BWD raster: M tiles per group
+  int n_mtiles;
+  const MTile* mtiles;
+  const WinItem* win;
+  const WItem* witems;
+  const DevSeg* segs;
+  const uint8_t* img_in;   // staged images read as an operand (FWD/BWD ext, DA/DB)
+  uint8_t* img_out;        // staged images written by the epilogue (SHRINK/DH)
+  void* out;               // Y / dX (bf16)
+  float* hout;             // H / dH (fp32)
+  int ld_out;              // row stride (elements) of `out`
+  int* err;                // device status word
+  unsigned long long timeout_ns;
+};
+
+// Status codes written to the device status word (first one wins).
+constexpr int DEV_ERR_TIMEOUT_PRODUCER = 0x101;
+constexpr int DEV_ERR_TIMEOUT_MMA = 0x102;
+constexpr int DEV_ERR_TIMEOUT_EPILOGUE = 0x103;
+constexpr int DEV_ERR_TIMEOUT_TEARDOWN = 0x104;
+
+// ---------------------------------------------------------------------------------------
+// inline PTX wrappers
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after `timeout_ns` or when another
+// role of the CTA has already given up (`abort_flag`).  On giving up it records `code` in the
+// device status word (first error wins) and returns false; it never traps.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          int code, unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1;
+        atomicCAS(err, 0, code);
+        return false;
+      }
+    }
+  }
+}
+
+// 2-D TMA tile load into shared memory, completing `bytes` on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Contiguous bulk copy global -> shared (16-byte aligned, size multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// --- tcgen05 -----------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 inputs, fp32 accumulate; issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns of TMEM -> 32 registers per thread.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading/stride byte
+// offsets, descriptor version 1, 128-byte swizzle.  For K-major operands the stride byte
+// offset is the distance between 8-row atoms (1024 B) and the leading offset is unused; for
+// MN-major operands the leading offset is the distance between 64-element MN blocks and the
+// stride offset the distance between 8-deep K groups.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;   // descriptor version (tcgen05)
+  d |= static_cast<uint64_t>(2) << 61;   // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4)                                  // D format: fp32
+         | (1u << 7)                                // A format: bf16
+         | (1u << 10)                               // B format: bf16
+         | ((a_mn_major ? 1u : 0u) << 15)           // A major-ness
+         | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Byte offset of element (row, col) in a [rows x 64] bf16 tile stored as 128B-swizzled
+// 8-row atoms (the layout TMA SWIZZLE_128B produces and the MMA descriptors expect).
+__host__ __device__ __forceinline__ uint32_t swz128_offset(uint32_t row, uint32_t col) {
+  const uint32_t chunk = (col >> 3) & 7u;
+  return row * 128u + (((chunk ^ (row & 7u)) << 4) | ((col & 7u) << 1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+}  // namespace mlora

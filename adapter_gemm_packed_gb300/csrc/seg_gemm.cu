@@ -1,0 +1,447 @@
+// Segmented tensor-core GEMM engine for the packed LoRA layer (sm_103a: tcgen05 + TMEM + TMA).
+//
+// One persistent, warp-specialised kernel template computes every product of the layer
+// ("PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §9.2: tiles run
+// along the token and hidden dimensions, never along the rank):
+//
+//   MODE_FWD    Y  = X W + s_i H_i B_i        base GEMM; the rank term is appended as extra
+//                                              K slices of the same TMEM accumulator
+//                                              ([X | Htilde] x [Wt | Bt_all]^T)
+//   MODE_BWD    dX = dY W^T + dH_i A_i^T      same, W read MN-major straight from Wt
+//   MODE_SHRINK H_i = X_i A_i                  per tile, N = the tile's rank window
+//   MODE_DH     dH_i = s_i dY_i B_i^T          per tile, N = the tile's rank window (Case 2)
+//   MODE_DA     dA_i = X_i^T dH_i              token reduction (Case 3)
+//   MODE_DB     dB_i = s_i H_i^T dY_i          token reduction (Case 1)
+//
+// The packed rank space: job i owns columns [c_i, c_i + rp_i) (rp_i = r_i rounded up to 16),
+// cut into 64-column chunks.  A 128-token tile that covers jobs i1..im needs only the chunks
+// spanning their windows.  Htilde / dHtilde are kept as "staged images": for each (tile,
+// chunk) a [128 x 64] bf16 block already in the 128B-swizzled smem layout, holding s_j H_j
+// (resp. dH_j) in the rows of job j and the columns of job j, and zero everywhere else.  The
+// zeros make the rank-term K extension of FWD/BWD and the token reductions of DA/DB exact
+// per job without masks in the main loop (tLoRA's "adaptively reconstructed low-rank tiles",
+// read as tiles assembled from the jobs a token tile happens to cover).
+//
+// Roles (192 threads, one CTA per SM, persistent over a static work list):
+//   warp 0     TMA / bulk-copy producer (one lane) into a STAGES-deep smem ring
+//   warp 1     TMEM allocator and MMA issuer (one lane), two 256-column accumulators
+//   warps 2-5  epilogue: TMEM -> registers -> global (lane quarter = warp id % 4)
+// Every wait is bounded (see mbar_wait): on expiry the CTA records a status code, drains
+// what it issued, frees TMEM and returns.
+#include "common.cuh"
+
+namespace mlora {
+
+namespace {
+
+__device__ __forceinline__ void decode_mn(const GemmArgs& g, int item, int& m, int& n) {
+  const int per_group = g.group_m * g.n_tiles_n;
+  const int group = item / per_group;
+  const int first_m = group * g.group_m;
+  const int gm = min(g.group_m, g.n_mtiles - first_m);
+  const int in_group = item - group * per_group;
+  m = first_m + in_group % gm;
+  n = in_group / gm;
+}
+
+template <int MODE>
+__device__ __forceinline__ int item_kblocks(const GemmArgs& g, int item) {
+  if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
+    int m, n;
+    decode_mn(g, item, m, n);
+    return g.kmain + g.mtiles[m].nch;
+  } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
+    return g.kmain;
+  } else {
+    const WItem w = g.witems[item];
+    return w.gb - w.ga;
+  }
+}
+
+// Number of accumulator columns (MMA N) of an item.
+template <int MODE>
+__device__ __forceinline__ int item_ncols(const GemmArgs& g, int item) {
+  if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
+    return BN;
+  } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
+    return CHUNK_COLS * g.win[item].nq;
+  } else {
+    return CHUNK_COLS * g.witems[item].nq;
+  }
+}
+
+// ------------------------------------------------------------------- producer (one thread)
+template <int MODE>
+__device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                               const CUtensorMap* tmE, int item, int kb, uint8_t* sA,
+                                               uint8_t* sB, uint64_t* full) {
+  if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
+    int m, n;
+    decode_mn(g, item, m, n);
+    const int m0 = m * BM, n0 = n * BN;
+    mbar_arrive_expect_tx(full, A_STAGE_BYTES + B_STAGE_BYTES);
+    if (kb < g.kmain) {
+      tma_load_2d(sA, tmA, full, kb * BK, m0);
+      if constexpr (MODE == MODE_FWD) {
+        tma_load_2d(sB, tmB, full, kb * BK, n0);
+      } else {
+        // W as the B operand of dX = dY W^T: element (n = d_in index, k = d_out index) is
+        // Wt[k][n], contiguous along n -> four 64-wide MN-major boxes.
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * (BK * 64 * 2), tmB, full, n0 + 64 * j, kb * BK);
+      }
+    } else {
+      const MTile mt = g.mtiles[m];
+      const int e = kb - g.kmain;
+      bulk_load(sA, g.img_in + static_cast<size_t>(mt.img_off + e) * IMG_BYTES, IMG_BYTES, full);
+      tma_load_2d(sB, tmE, full, (mt.q_lo + e) * CHUNK_COLS, n0);
+    }
+  } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
+    const WinItem w = g.win[item];
+    const int m0 = w.tile * BM;
+    mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (CHUNK_COLS * BK * 2));
+    tma_load_2d(sA, tmA, full, kb * BK, m0);
+    for (int j = 0; j < w.nq; ++j)
+      tma_load_2d(sB + j * (CHUNK_COLS * BK * 2), tmB, full, kb * BK, (w.q0 + j) * CHUNK_COLS);
+  } else {
+    const WItem w = g.witems[item];
+    const int gh = w.ga + kb;            // 64-token half tile
+    const int t = gh >> 1, h = gh & 1;
+    const MTile mt = g.mtiles[t];
+    mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (IMG_BYTES / 2));
+    // X (dA) or dY (dB) as an MN-major operand: 64 hidden columns x 64 tokens per box.
+    tma_load_2d(sA, tmA, full, w.row0, gh * 64);
+    tma_load_2d(sA + 64 * 64 * 2, tmA, full, w.row0 + 64, gh * 64);
+    for (int j = 0; j < w.nq; ++j) {
+      const uint8_t* src = g.img_in + static_cast<size_t>(mt.img_off + w.q0 + j - mt.q_lo) * IMG_BYTES +
+                           h * (IMG_BYTES / 2);
+      bulk_load(sB + j * (IMG_BYTES / 2), src, IMG_BYTES / 2, full);
+    }
+  }
+}
+
+// ------------------------------------------------------------------- MMA (one thread)
+template <int MODE>
+__device__ __forceinline__ void mma_kblock(const GemmArgs& g, int item, int kb, uint32_t sA, uint32_t sB,
+                                           uint32_t d_tmem, int ncols) {
+  if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
+    const bool main_part = kb < g.kmain;
+    const bool b_mn = (MODE == MODE_BWD) && main_part;
+    const uint32_t idesc = idesc_bf16(BM, BN, false, b_mn);
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k) {
+      const uint64_t a = smem_desc(sA + k * 32, 16, 1024);
+      const uint64_t b = b_mn ? smem_desc(sB + k * 2048, 64 * 64 * 2, 1024) : smem_desc(sB + k * 32, 16, 1024);
+      umma_bf16(d_tmem, a, b, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+    }
+  } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
+    const uint32_t idesc = idesc_bf16(BM, ncols, false, false);
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k) {
+      umma_bf16(d_tmem, smem_desc(sA + k * 32, 16, 1024), smem_desc(sB + k * 32, 16, 1024), idesc,
+                (kb > 0 || k > 0) ? 1u : 0u);
+    }
+  } else {
+    const uint32_t idesc = idesc_bf16(BM, ncols, true, true);
+#pragma unroll
+    for (int k = 0; k < BK / 16; ++k) {
+      umma_bf16(d_tmem, smem_desc(sA + k * 2048, 64 * 64 * 2, 1024), smem_desc(sB + k * 2048, IMG_BYTES / 2, 1024),
+                idesc, (kb > 0 || k > 0) ? 1u : 0u);
+    }
+  }
+}
+
+// ------------------------------------------------------------------- epilogues (128 threads)
+__device__ __forceinline__ int find_seg(const DevSeg* segs, int first, int last, long long row) {
+  int j = first;
+  while (j < last && row >= segs[j + 1].off) ++j;
+  return j;
+}
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint32_t t_acc, int quarter, int lane) {
+  const int rit = quarter * 32 + lane;   // accumulator row owned by this thread
+  if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
+    int m, n;
+    decode_mn(g, item, m, n);
+    const long long row = static_cast<long long>(m) * BM + rit;
+    const int col0 = n * BN;
+    const int ld = g.ld_out;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
+#pragma unroll 1
+    for (int cb = 0; cb < BN; cb += 32) {
+      uint32_t v[32];
+      tmem_ld32(t_acc + cb, v);
+      tmem_ld_wait();
+      const int col = col0 + cb;
+      if (row < g.N && col < ld) {
+        __nv_bfloat16* dst = out + row * ld + col;
+        if (col + 32 <= ld) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+            u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+            u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+            u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+            d4[q] = u;
+          }
+        } else {
+          for (int u = 0; u < 32 && col + u < ld; ++u) dst[u] = __float2bfloat16_rn(__uint_as_float(v[u]));
+        }
+      }
+    }
+  } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
+    const WinItem w = g.win[item];
+    const MTile mt = g.mtiles[w.tile];
+    const long long row = static_cast<long long>(w.tile) * BM + rit;
+    int j = -1;
+    if (row < g.N) j = find_seg(g.segs, mt.seg_first, mt.seg_last, row);
+    long long hbase = 0;
+    int c_lo = 0, c_hi = 0, r = 1;
+    float s = 0.f;
+    if (j >= 0) {
+      const DevSeg sg = g.segs[j];
+      r = sg.r;
+      c_lo = sg.c;
+      c_hi = sg.c + sg.r;
+      s = sg.s;
+      hbase = sg.h_off + (row - sg.off) * sg.r - sg.c;
+    }
+    // SHRINK: H = acc, image = s*acc.  DH: dH = s*acc, image = s*acc.
+#pragma unroll 1
+    for (int jq = 0; jq < w.nq; ++jq) {
+      const int q = w.q0 + jq;
+      uint8_t* img = g.img_out + static_cast<size_t>(mt.img_off + q - mt.q_lo) * IMG_BYTES;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+        tmem_ld32(t_acc + jq * CHUNK_COLS + half * 32, v);
+        tmem_ld_wait();
+        const int cbase = q * CHUNK_COLS + half * 32;
+        uint32_t pk[16];
+#pragma unroll
+        for (int u = 0; u < 32; u += 2) {
+          const int c0 = cbase + u, c1 = c0 + 1;
+          const float a0 = __uint_as_float(v[u]), a1 = __uint_as_float(v[u + 1]);
+          const bool in0 = c0 >= c_lo && c0 < c_hi, in1 = c1 >= c_lo && c1 < c_hi;
+          if (in0) g.hout[hbase + c0] = (MODE == MODE_SHRINK) ? a0 : s * a0;
+          if (in1) g.hout[hbase + c1] = (MODE == MODE_SHRINK) ? a1 : s * a1;
+          pk[u / 2] = pack_bf16x2(in0 ? s * a0 : 0.f, in1 ? s * a1 : 0.f);
+        }
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16) {
+          const uint32_t off = swz128_offset(static_cast<uint32_t>(rit), static_cast<uint32_t>(half * 32 + k16 * 8));
+          *reinterpret_cast<uint4*>(img + off) = make_uint4(pk[4 * k16], pk[4 * k16 + 1], pk[4 * k16 + 2], pk[4 * k16 + 3]);
+        }
+      }
+    }
+  } else {
+    const WItem w = g.witems[item];
+    const DevSeg sg = g.segs[w.seg];
+    const int row = w.row0 + rit;                       // d_in (DA) or d_out (DB) index
+    const int bound = (MODE == MODE_DA) ? g.d_in : g.d_out;
+#pragma unroll 1
+    for (int jq = 0; jq < w.nq; ++jq) {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+        tmem_ld32(t_acc + jq * CHUNK_COLS + half * 32, v);
+        tmem_ld_wait();
+        if (row < bound) {
+          const int cbase = (w.q0 + jq) * CHUNK_COLS + half * 32 - sg.c;   // rank index of v[0]
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const int t = cbase + u;
+            if (t >= 0 && t < sg.r) {
+              if constexpr (MODE == MODE_DA)
+                sg.dAt[static_cast<size_t>(t) * g.d_in + row] = __uint_as_float(v[u]);
+              else
+                sg.dBt[static_cast<size_t>(row) * sg.r + t] = __uint_as_float(v[u]);
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+template <int MODE>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_seg_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmE, const __grid_constant__ GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE_BYTES);
+  uint64_t* full = bars;                 // [STAGES]  TMA -> MMA
+  uint64_t* empty = bars + STAGES;       // [STAGES]  MMA -> TMA
+  uint64_t* tfull = bars + 2 * STAGES;   // [2]       MMA -> epilogue
+  uint64_t* tempty = tfull + 2;          // [2]       epilogue -> MMA
+  uint64_t* done = tempty + 2;           // [1]       MMA drain at teardown
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmE);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const unsigned long long tmo = g.timeout_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < g.n_items; item += gridDim.x) {
+        const int nkb = item_kblocks<MODE>(g, item);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
+            ok = false;
+            break;
+          }
+          produce_kblock<MODE>(g, &tmA, &tmB, &tmE, item, kb, sA + stage * A_STAGE_BYTES,
+                               sB + stage * B_STAGE_BYTES, &full[stage]);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok || *abort_flag) {
+        // Drain: wait (bounded) for the copies of the last STAGES issued slots to land so
+        // no bulk copy is still writing this CTA's shared memory when it exits.
+        volatile int no_abort = 0;
+        for (int k = 0; k < STAGES && k < issued; ++k) {
+          if (--stage < 0) {
+            stage = STAGES - 1;
+            phase ^= 1u;
+          }
+          mbar_wait(&full[stage], phase, &no_abort, g.err, DEV_ERR_TIMEOUT_TEARDOWN, tmo);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < g.n_items; item += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        const int nkb = item_kblocks<MODE>(g, item);
+        const int ncols = item_ncols<MODE>(g, item);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_kblock<MODE>(g, item, kb, smem_u32(sA + stage * A_STAGE_BYTES), smem_u32(sB + stage * B_STAGE_BYTES),
+                           d_tmem, ncols);
+          umma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Every MMA issued by this thread has completed once `done` flips.
+      umma_commit(done);
+      volatile int no_abort = 0;
+      mbar_wait(done, 0, &no_abort, g.err, DEV_ERR_TIMEOUT_TEARDOWN, tmo);
+    }
+  } else {
+    const int quarter = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int item = blockIdx.x; item < g.n_items; item += gridDim.x) {
+      // One lane waits; the warp follows its decision so the .sync.aligned TMEM loads below
+      // are always executed by all 32 lanes together.
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, g.err, DEV_ERR_TIMEOUT_EPILOGUE, tmo);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      epilogue_item<MODE>(g, item, t_acc, quarter, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// Host-side launch helper (one per mode).
+template <int MODE>
+cudaError_t launch_seg_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmE,
+                            const GemmArgs& g, int grid, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_seg_gemm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (g.n_items <= 0) return cudaSuccess;
+  k_seg_gemm<MODE><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(tmA, tmB, tmE, g);
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_seg_gemm<MODE_FWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                               const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_seg_gemm<MODE_BWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                               const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_seg_gemm<MODE_SHRINK>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                                  const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_seg_gemm<MODE_DH>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                              const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_seg_gemm<MODE_DA>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                              const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_seg_gemm<MODE_DB>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                              const GemmArgs&, int, cudaStream_t);
+
+}  // namespace mlora

@@ -1,0 +1,175 @@
+/*
+ * mlora.h — C ABI of the packed multi-adapter LoRA layer (forward, backward, AdamW).
+ *
+ * Many LoRA jobs share one frozen base weight W (d_in x d_out).  Job i owns a
+ * contiguous run of token rows X_i (rows [tok_offset_i, tok_offset_i + n_i) of
+ * the packed activation X, N x d_in), a rank r_i, a scale s_i = alpha_i / r_i and
+ * trainable A_i (d_in x r_i), B_i (r_i x d_out).  The layer computes
+ *
+ *     Y_i  = X_i W + s_i (X_i A_i) B_i                              (forward)
+ *     H_i  = X_i A_i                                                (saved activation)
+ *     dH_i = s_i dY_i B_i^T,   dB_i = s_i H_i^T dY_i                (B-side gradients)
+ *     dA_i = X_i^T dH_i,       dX_i = dY_i W^T + dH_i A_i^T         (A-side gradients)
+ *
+ * followed by one decoupled-weight-decay AdamW step on every A_i and B_i.
+ *
+ * Sources: "PLoRA: Efficient Concurrent LoRA Training for Large Language
+ * Models" (full text), §2.1 (the LoRA layer: A is d x r, B is r x k), §2.4
+ * (packing: every job applies its own adapter to its own inputs), §9.2
+ * "Packed LoRA Kernels" (the four backward products, Cases 1-4, and the rule
+ * that tiles run along the token or hidden dimensions, never along the rank),
+ * §8 (AdamW keeps gradient, first and second moment per parameter).  "tLoRA:
+ * Efficient Multi-LoRA Training with Elastic Shared Super-Models" (abstract)
+ * for the rank-aware grouping of uneven jobs into one launch.
+ *
+ * Storage (all row-major, all device pointers unless stated):
+ *   X   [N, d_in]      bf16 (MLORA_BF16) or fp32 (MLORA_F32)
+ *   Wt  [d_out, d_in]  W transposed, same dtype as X (the nn.Linear weight layout)
+ *   Y   [N, d_out], dY [N, d_out], dX [N, d_in]: same dtype as X
+ *   At_i [r_i, d_in], Bt_i [d_out, r_i]: fp32 masters (A_i, B_i transposed);
+ *   dAt_i, dBt_i, mA_i, vA_i, mB_i, vB_i: fp32, same shapes as At_i / Bt_i.
+ *   H, dH: fp32, job i's [n_i, r_i] block stored row-major at element offset
+ *          sum_{j<i} n_j r_j (mlora_h_elems() gives the total).
+ * Ownership: the caller allocates and frees every buffer named above, the
+ * workspace and the stream.  A plan owns only its own small device tables
+ * (segment table, tile lists, status word) and a copy of the segment table.
+ * Every call is asynchronous on the given stream (a cudaStream_t passed as
+ * void*; NULL = legacy default stream) and returns an error code at once for
+ * anything detectable on the host; nothing crosses the ABI as an exception.
+ * A device-side wait that gives up (see MLORA_ERR_TIMEOUT) records its code in
+ * the plan's status word, read back by mlora_sync_status().
+ */
+#ifndef MLORA_H
+#define MLORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mlora_status {
+    MLORA_OK = 0,
+    MLORA_ERR_INVALID = 1,      /* bad argument: null pointer, bad segment table, misaligned buffer */
+    MLORA_ERR_UNSUPPORTED = 2,  /* valid but outside what this library implements (e.g. rank > 256) */
+    MLORA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed; mlora_last_error() has the text */
+    MLORA_ERR_TIMEOUT = 4,      /* a device-side wait gave up (reported by mlora_sync_status) */
+    MLORA_ERR_OOM = 5           /* the plan's small device tables could not be allocated */
+} mlora_status;
+
+typedef enum mlora_dtype {
+    MLORA_F32 = 0,   /* X, W, dY, Y, dX in fp32; true fp32 FFMA arithmetic */
+    MLORA_BF16 = 1   /* X, W, dY, Y, dX in bf16; tensor-core products with fp32 accumulation */
+} mlora_dtype;
+
+/* mlora_problem.flags */
+#define MLORA_PLAN_HOST_ONLY 1u        /* build and validate the tables on the host only: no CUDA call,
+                                          the plan can be inspected but not executed */
+#define MLORA_DEBUG_SHORT_TIMEOUT 2u   /* device waits give up after ~1 ms instead of ~4 s */
+
+/* One job of the pack.  Pointers are device pointers to fp32 buffers of the
+ * shapes given above, each 16-byte aligned.  dAt/dBt are overwritten (not
+ * accumulated) by mlora_backward; At/Bt/mA/vA/mB/vB are updated in place by
+ * mlora_adamw.  Pointers unused by a call may be NULL for that call only if
+ * the plan was built with them NULL (e.g. a forward-only plan). */
+typedef struct mlora_segment {
+    int64_t tok_offset;   /* first row of this job in X / dY / Y / dX */
+    int32_t n_tokens;     /* n_i >= 1 */
+    int32_t rank;         /* 1 <= r_i <= 256 */
+    float scale;          /* s_i = alpha_i / r_i */
+    float* At;
+    float* Bt;
+    float* dAt;
+    float* dBt;
+    float* mA;
+    float* vA;
+    float* mB;
+    float* vB;
+} mlora_segment;
+
+typedef struct mlora_problem {
+    int64_t n_tokens;     /* N: rows of X; the segments must tile [0, N) in order, without gaps */
+    int32_t d_in;         /* multiple of 8 (bf16) or 4 (fp32) */
+    int32_t d_out;        /* multiple of 8 (bf16) or 4 (fp32) */
+    int32_t dtype;        /* mlora_dtype */
+    uint32_t flags;       /* MLORA_PLAN_* / MLORA_DEBUG_* bits */
+} mlora_problem;
+
+typedef struct mlora_plan_s mlora_plan_t;
+
+/* Validate the segment table and build the tile schedule (the M-tile to job
+ * map, the per-tile rank windows and the rank-aware work lists of every
+ * kernel), then upload it to the current device.  On success *out is a plan
+ * that stays valid, immutable and reusable for any number of steps while the
+ * shapes and the segment table's pointers stay the same, and
+ * *workspace_bytes is the size of the scratch buffer that forward/backward
+ * need (caller-allocated device memory, 256-byte aligned, contents need not
+ * be initialised).  Errors: MLORA_ERR_INVALID (null/misaligned pointers,
+ * segments out of order, overlapping, leaving gaps, n_i < 1, bad dims),
+ * MLORA_ERR_UNSUPPORTED (rank > 256, d not a multiple of 8/4),
+ * MLORA_ERR_OOM / MLORA_ERR_CUDA (device tables). */
+mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
+                        size_t* workspace_bytes, mlora_plan_t** out);
+
+/* Free the plan's device tables (after work using it has finished). NULL is a no-op. */
+void mlora_plan_destroy(mlora_plan_t* plan);
+
+/* Forward pass: Y = X W + s_i (X_i A_i) B_i per job, and the saved activation
+ * H (fp32, packed as described above).  Reads At_i/Bt_i of every segment. */
+mlora_status mlora_forward(const mlora_plan_t* plan, const void* X, const void* Wt, void* Y, float* H,
+                           void* workspace, void* stream);
+
+/* Backward pass given the upstream gradient dY and the forward's H:
+ * writes dX, dH (fp32, packed like H) and every segment's dAt/dBt. */
+mlora_status mlora_backward(const mlora_plan_t* plan, const void* X, const void* Wt, const void* dY,
+                            const float* H, void* dX, float* dH, void* workspace, void* stream);
+
+/* One AdamW step on every job's A and B (PyTorch's order: decay p by
+ * (1 - lr*weight_decay), update the moments, bias-correct with step t >= 1,
+ * then p -= lr * m_hat / (sqrt(v_hat) + eps)).  Reads dAt/dBt; updates
+ * At/Bt/mA/vA/mB/vB in place.  Moments start at zero at t = 1 (caller-zeroed). */
+mlora_status mlora_adamw(const mlora_plan_t* plan, float lr, float beta1, float beta2, float eps,
+                         float weight_decay, int32_t step, void* stream);
+
+/* Synchronise the stream, then read and clear the plan's device status word:
+ * MLORA_OK, or MLORA_ERR_TIMEOUT if a device-side wait gave up since the last
+ * call (the outputs of that launch are then undefined). */
+mlora_status mlora_sync_status(const mlora_plan_t* plan, void* stream);
+
+/* Number of fp32 elements of H / dH: sum_i n_i r_i. */
+int64_t mlora_h_elems(const mlora_plan_t* plan);
+
+/* Inspect the plan's host tables (for tests and tooling).  `what` selects a
+ * table (MLORA_Q_*); up to `cap` int64 values are copied to `out` and the
+ * table's full length is stored in *count.  Tables:
+ *   MLORA_Q_SUMMARY : N, d_in, d_out, n_segs, n_mtiles, C_total, n_chunks, n_images,
+ *                     n_items(shrink), n_items(dA), n_items(dB), workspace_bytes
+ *   MLORA_Q_MTILES  : per 128-row tile: first job, last job, first chunk, chunk count, image offset
+ *   MLORA_Q_COLUMNS : per job: first column of its rank window, padded width
+ *   MLORA_Q_WGRAD_A : per dA work item: row block, job, first and end half-tile, first chunk, chunks
+ *   MLORA_Q_WGRAD_B : per dB work item: same fields
+ *   MLORA_Q_WINDOW  : per shrink / dH work item: tile, first chunk, chunks */
+#define MLORA_Q_SUMMARY 0
+#define MLORA_Q_MTILES 1
+#define MLORA_Q_COLUMNS 2
+#define MLORA_Q_WGRAD_A 3
+#define MLORA_Q_WGRAD_B 4
+#define MLORA_Q_WINDOW 5
+mlora_status mlora_plan_describe(const mlora_plan_t* plan, int32_t what, int64_t* out, int64_t cap,
+                                 int64_t* count);
+
+/* Human-readable name of a status code (static storage). */
+const char* mlora_status_string(mlora_status s);
+
+/* Text of the last error raised on this host thread ("" if none). */
+const char* mlora_last_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t mlora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLORA_H */

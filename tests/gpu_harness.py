@@ -1,0 +1,127 @@
+"""Runs one workload through the CUDA path (C ABI) and through the fp64 oracle on the same
+seeded inputs, and compares them tensor by tensor.
+
+Tolerances (relative Frobenius error per output tensor): 1e-4 for fp32 workloads, 2e-2 for
+bf16 workloads (bf16 inputs, fp32 accumulation, bf16 Y/dX).  An all-zero reference tensor
+uses an absolute bound instead (1e-6 times the largest input magnitude, see ``rel_err``).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from adapter_gemm_packed_gb300 import workloads as W
+from adapter_gemm_packed_gb300.layer import PackedLoRA
+from oracle import lora_oracle as orc
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def rel_err(got, want) -> float:
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    nw = np.linalg.norm(want)
+    d = np.linalg.norm(got - want)
+    if nw == 0:
+        return d / 1e-6
+    return d / nw
+
+
+def to_dev(a: np.ndarray, dtype: str):
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def from_dev(t, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return W.bf16_bits_to_f32(t.view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def scales_of(wl):
+    # the segment table's scale s_i = alpha_i / r_i (exact in fp32 for every workload here)
+    return [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
+
+
+def oracle_segs(wl, T):
+    return [orc.Seg(o, n, T.At[i].astype(np.float64).T, T.Bt[i].astype(np.float64).T, wl.alphas[i])
+            for i, (o, n) in enumerate(zip(wl.offsets, wl.n_tokens))]
+
+
+class GpuRun:
+    """Forward, backward and one AdamW step of a workload on the GPU; results as float64 numpy."""
+
+    def __init__(self, wl, T, step=True, flags=0, Wt_override=None):
+        self.wl = wl
+        torch.cuda.synchronize()
+        self.layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales_of(wl), dtype=wl.dtype,
+                                At=T.At, Bt=T.Bt, flags=flags)
+        self.X = to_dev(T.X, wl.dtype)
+        self.Wt = to_dev(T.Wt if Wt_override is None else Wt_override, wl.dtype)
+        self.dY = to_dev(T.dY, wl.dtype)
+        self.Y = self.layer.forward(self.X, self.Wt)
+        self.dX = self.layer.backward(self.X, self.Wt, self.dY)
+        torch.cuda.synchronize()
+        self.status_after_backward = self.layer.sync_status()
+        self.res = dict(
+            Y=from_dev(self.Y, wl.dtype), dX=from_dev(self.dX, wl.dtype),
+            H=[h.cpu().numpy().astype(np.float64) for h in self.layer.h_blocks()],
+            dH=[h.cpu().numpy().astype(np.float64) for h in self.layer.h_blocks(self.layer.dH)],
+            dAt=[a.cpu().numpy().astype(np.float64) for a in self.layer.dAt],
+            dBt=[b.cpu().numpy().astype(np.float64) for b in self.layer.dBt])
+        if step:
+            self.layer.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, 1)
+            torch.cuda.synchronize()
+            self.res.update(
+                At=[a.cpu().numpy().astype(np.float64) for a in self.layer.At],
+                Bt=[b.cpu().numpy().astype(np.float64) for b in self.layer.Bt],
+                mA=[a.cpu().numpy().astype(np.float64) for a in self.layer.mA],
+                vA=[a.cpu().numpy().astype(np.float64) for a in self.layer.vA],
+                mB=[b.cpu().numpy().astype(np.float64) for b in self.layer.mB],
+                vB=[b.cpu().numpy().astype(np.float64) for b in self.layer.vB])
+
+    def close(self):
+        self.layer.close()
+
+
+def oracle_full(wl, T, Wt_override=None):
+    """Every output of the layer (and the AdamW step at t=1 from zero moments), fp64."""
+    X = W.rows_as_f64(T.X, wl.dtype)
+    Wm = W.rows_as_f64(T.Wt if Wt_override is None else Wt_override, wl.dtype).T
+    dY = W.rows_as_f64(T.dY, wl.dtype)
+    segs = oracle_segs(wl, T)
+    Y, H = orc.forward(X, Wm, segs)
+    dX, dA, dB, dH = orc.backward(X, Wm, dY, segs)
+    out = dict(Y=Y, dX=dX, H=H, dH=dH, dAt=[a.T for a in dA], dBt=[b.T for b in dB])
+    out.update(adamw_expect(wl, T, out["dAt"], out["dBt"]))
+    return out
+
+
+def adamw_expect(wl, T, dAt, dBt):
+    At, Bt, mA, vA, mB, vB = [], [], [], [], [], []
+    for i in range(wl.n_adapters):
+        for p, g, P, Mm, V in ((T.At[i], dAt[i], At, mA, vA), (T.Bt[i], dBt[i], Bt, mB, vB)):
+            p2, m2, v2 = orc.adamw(p.astype(np.float64), g, np.zeros_like(g), np.zeros_like(g), wl.lr, wl.beta1,
+                                   wl.beta2, wl.eps, wl.weight_decay, 1)
+            P.append(p2)
+            Mm.append(m2)
+            V.append(v2)
+    return dict(At=At, Bt=Bt, mA=mA, vA=vA, mB=mB, vB=vB)
+
+
+def compare(got: dict, want: dict, tol: float, keys=None) -> dict:
+    """Max relative Frobenius error per key (lists: per job, reporting the worst)."""
+    errs = {}
+    for k in (keys or want.keys()):
+        if k not in got or k not in want:
+            continue
+        g, w = got[k], want[k]
+        if isinstance(w, list):
+            errs[k] = max(rel_err(a, b) for a, b in zip(g, w))
+        else:
+            errs[k] = rel_err(g, w)
+    bad = {k: v for k, v in errs.items() if not v <= tol}
+    assert not bad, f"tolerance {tol} exceeded: {bad} (all: {errs})"
+    return errs

@@ -1,0 +1,122 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI (needs a GB300).
+
+Small and medium cases run the whole oracle; they span several 128-token tiles, ragged token
+and column tails, ranks 1..256 and jobs that straddle tiles."""
+import numpy as np
+import pytest
+import torch
+
+from adapter_gemm_packed_gb300 import _mlora as M
+from adapter_gemm_packed_gb300 import workloads as W
+from oracle import lora_oracle as orc
+import gpu_harness as G
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from adapter_gemm_packed_gb300 import build
+    build.build()
+
+
+def _run(wl, keys=None, **kw):
+    T = W.materialise(wl)
+    run = G.GpuRun(wl, T, **kw)
+    try:
+        assert run.status_after_backward == M.MLORA_OK
+        want = G.oracle_full(wl, T, kw.get("Wt_override"))
+        return G.compare(run.res, want, G.TOL[wl.dtype], keys), run.res, want
+    finally:
+        run.close()
+
+
+def test_tiny_f32_all_outputs():
+    errs, _, _ = _run(W.tiny_f32())
+    assert errs["Y"] < 1e-5
+
+
+SMALL_BF16 = {
+    "ragged_tail": dict(d_in=512, d_out=640, ranks=[1, 7, 64, 256], n_tokens=[200, 56, 300, 17]),
+    "jobs_straddle_tiles": dict(d_in=256, d_out=384, ranks=[1, 2, 4, 8, 16, 32, 64, 128, 256, 3],
+                                n_tokens=[16, 16, 32, 16, 48, 16, 16, 64, 16, 5]),
+    "single_token_job": dict(d_in=128, d_out=136, ranks=[5], n_tokens=[1]),
+    "one_job_many_tiles": dict(d_in=1024, d_out=512, ranks=[32], n_tokens=[1000]),
+    "wide_hidden": dict(d_in=2048, d_out=1536, ranks=[16, 128, 8], n_tokens=[256, 384, 130]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL_BF16))
+def test_bf16_small(name):
+    cfg = SMALL_BF16[name]
+    wl = W.custom(f"small_{name}", 900 + sorted(SMALL_BF16).index(name), cfg["d_in"], cfg["d_out"], cfg["ranks"],
+                  cfg["n_tokens"], dtype="bf16", w_std=0.05, b_std=0.05)
+    _run(wl)
+
+
+def test_bf16_zero_base_weight_isolates_rank_term():
+    wl = W.custom("zero_W", 950, 512, 384, [4, 64, 17], [130, 200, 70], dtype="bf16", b_std=0.05)
+    zero = np.zeros((wl.d_out, wl.d_in), np.uint16)
+    errs, got, want = _run(wl, Wt_override=zero)
+    assert np.linalg.norm(want["Y"]) > 0
+
+
+def test_bf16_zero_B_gives_base_product():
+    wl = W.custom("zero_B", 951, 384, 256, [8, 3], [100, 90], dtype="bf16", b_std=0.0)
+    errs, got, want = _run(wl)
+    X = W.rows_as_f64(W.materialise(wl).X, "bf16")
+    # dA must vanish when B = 0 (Case 3 of the backward has B as a factor)
+    assert all(np.max(np.abs(a)) == 0 for a in got["dAt"])
+
+
+def test_repeat_calls_are_deterministic():
+    wl = W.custom("repeat", 952, 256, 256, [8, 24], [150, 170], dtype="bf16")
+    T = W.materialise(wl)
+    r1 = G.GpuRun(wl, T, step=False)
+    r2 = G.GpuRun(wl, T, step=False)
+    try:
+        for k in ("Y", "dX"):
+            assert np.array_equal(r1.res[k], r2.res[k])
+        for k in ("H", "dH", "dAt", "dBt"):
+            assert all(np.array_equal(a, b) for a, b in zip(r1.res[k], r2.res[k]))
+    finally:
+        r1.close()
+        r2.close()
+
+
+def test_adamw_isolated_t3():
+    """The AdamW kernel alone on seeded gradients and moments (t = 3), so the update
+    p' - p itself can be checked: at small t it is close to -lr * sign(g), which would
+    amplify rounding differences in a gradient computed upstream."""
+    wl = W.custom("adamw", 953, 264, 136, [3, 16, 40], [7, 9, 4], dtype="bf16")
+    T = W.materialise(wl, with_dY=True)
+    layer = G.PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, G.scales_of(wl), dtype="bf16", At=T.At, Bt=T.Bt)
+    try:
+        want = {}
+        for i in range(wl.n_adapters):
+            for which, p, g_t, m_t, v_t in (("A", layer.At[i], layer.dAt[i], layer.mA[i], layer.vA[i]),
+                                            ("B", layer.Bt[i], layer.dBt[i], layer.mB[i], layer.vB[i])):
+                shape = tuple(p.shape)
+                g = W.optimizer_state(wl, which, i, shape, "g")
+                m = W.optimizer_state(wl, which, i, shape, "m")
+                v = W.optimizer_state(wl, which, i, shape, "v")
+                g_t.copy_(torch.from_numpy(g))
+                m_t.copy_(torch.from_numpy(m))
+                v_t.copy_(torch.from_numpy(v))
+                p0 = p.cpu().numpy().astype(np.float64)
+                want[(which, i)] = (p0,) + orc.adamw(p0, g, m, v, 2e-3, 0.9, 0.95, 1e-8, 0.05, 3)
+        layer.adamw(2e-3, 0.9, 0.95, 1e-8, 0.05, 3)
+        torch.cuda.synchronize()
+        for i in range(wl.n_adapters):
+            for which, p, m_t, v_t in (("A", layer.At[i], layer.mA[i], layer.vA[i]),
+                                       ("B", layer.Bt[i], layer.mB[i], layer.vB[i])):
+                p0, pw, mw, vw = want[(which, i)]
+                pg = p.cpu().numpy().astype(np.float64)
+                assert G.rel_err(pg - p0, pw - p0) < 1e-4
+                assert G.rel_err(pg, pw) < 1e-6
+                assert G.rel_err(m_t.cpu().numpy(), mw) < 1e-6
+                assert G.rel_err(v_t.cpu().numpy(), vw) < 1e-6
+    finally:
+        layer.close()

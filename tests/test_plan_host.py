@@ -1,0 +1,178 @@
+"""Host-side checks of the C library: it loads, exports every declared symbol, and the planner's
+tables (tile -> job map, packed rank windows, work lists) are complete and consistent.  No GPU:
+plans are built with MLORA_PLAN_HOST_ONLY, which makes no CUDA call."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from adapter_gemm_packed_gb300 import _mlora as M
+from adapter_gemm_packed_gb300 import workloads as W
+from adapter_gemm_packed_gb300.layer import host_plan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from adapter_gemm_packed_gb300 import build
+    build.build()
+
+
+def test_header_symbols_exported():
+    hdr = open(os.path.join(ROOT, "include", "mlora.h")).read()
+    declared = set(re.findall(r"\b(mlora_[a-z_]+)\s*\(", hdr))
+    assert declared == set(M.EXPORTS)
+    L = M.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+    assert M.mlora_version() >= 100
+    assert M.mlora_status_string(M.MLORA_ERR_TIMEOUT) == "device wait timed out"
+
+
+def _tables(plan):
+    s = M.mlora_plan_describe(plan, M.MLORA_Q_SUMMARY)
+    keys = ["N", "d_in", "d_out", "n_segs", "n_mtiles", "C_total", "n_chunks", "n_images", "n_win", "n_da", "n_db",
+            "ws"]
+    summ = dict(zip(keys, s))
+    mt = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_MTILES)).reshape(-1, 5)
+    cols = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_COLUMNS)).reshape(-1, 2)
+    win = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WINDOW)).reshape(-1, 3)
+    da = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WGRAD_A)).reshape(-1, 6)
+    db = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WGRAD_B)).reshape(-1, 6)
+    return summ, mt, cols, win, da, db
+
+
+CASES = {
+    "qproj": (4096, 4096, [8, 8, 16, 16, 32, 32, 64, 64], [2048] * 8),
+    "ragged": (512, 640, [1, 7, 64, 256], [200, 56, 300, 17]),
+    "tiny_segments": (256, 256, [1, 2, 4, 8, 16, 32, 64, 128, 256, 3], [16, 16, 32, 16, 48, 16, 16, 64, 16, 5]),
+    "one_token": (64, 64, [5], [1]),
+    "many_small": None,
+    "mlp_up": None,
+}
+
+
+def _case(name):
+    if name == "many_small":
+        wl = W.llama70b_down_many_small()
+        return wl.d_in, wl.d_out, wl.ranks, wl.n_tokens
+    if name == "mlp_up":
+        wl = W.mlp_up_lognormal()
+        return wl.d_in, wl.d_out, wl.ranks, wl.n_tokens
+    return CASES[name]
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_planner_tables(name):
+    d_in, d_out, ranks, ns = _case(name)
+    plan, ws = host_plan(d_in, d_out, ranks, ns)
+    try:
+        summ, mt, cols, win, da, db = _tables(plan)
+    finally:
+        M.mlora_plan_destroy(plan)
+    N = sum(ns)
+    offs = np.cumsum([0] + ns)[:-1]
+    assert summ["N"] == N and summ["n_segs"] == len(ranks)
+    # packed rank space: windows in job order, 16-aligned, wide enough, no overlap
+    c = 0
+    for i, r in enumerate(ranks):
+        assert cols[i, 0] == c and cols[i, 1] % 16 == 0 and r <= cols[i, 1] < r + 16
+        c += cols[i, 1]
+    assert summ["C_total"] == c and summ["n_chunks"] == -(-c // 64)
+    # token tiles: every row covered once, and the tile's job range is exactly the jobs it touches
+    assert summ["n_mtiles"] == -(-N // 128) == len(mt)
+    seg_of = np.repeat(np.arange(len(ns)), ns)
+    img = 0
+    for t in range(len(mt)):
+        rows = np.arange(128 * t, min(N, 128 * t + 128))
+        jobs = np.unique(seg_of[rows])
+        f, l, q_lo, nch, img_off = mt[t]
+        assert (f, l) == (jobs[0], jobs[-1])
+        lo, hi = cols[f, 0], cols[l, 0] + cols[l, 1]
+        assert q_lo == lo // 64 and q_lo + nch == -(-hi // 64)
+        assert img_off == img
+        img += nch
+    assert summ["n_images"] == img
+    # window work: each tile's chunks exactly once, <= 4 per item
+    seen = {}
+    for t, q0, nq in win:
+        assert 1 <= nq <= 4
+        for q in range(q0, q0 + nq):
+            assert (t, q) not in seen
+            seen[(t, q)] = 1
+    want = {(t, q) for t in range(len(mt)) for q in range(mt[t, 2], mt[t, 2] + mt[t, 3])}
+    assert set(seen) == want
+    # weight-gradient work: per job, its chunk span x row blocks exactly once, tokens covered
+    for items, rows_total in ((da, d_in), (db, d_out)):
+        cover = {}
+        for row0, j, ga, gb, q0, nq in items:
+            assert row0 % 128 == 0 and 0 <= row0 < rows_total and 1 <= nq <= 4
+            assert ga * 64 <= offs[j] and (offs[j] + ns[j]) <= gb * 64 and gb - ga <= -(-ns[j] // 64) + 1
+            for q in range(q0, q0 + nq):
+                key = (row0, j, q)
+                assert key not in cover
+                cover[key] = 1
+        want = set()
+        for j in range(len(ns)):
+            qa, qb = cols[j, 0] // 64, -(-(cols[j, 0] + cols[j, 1]) // 64)
+            want |= {(r0, j, q) for r0 in range(0, rows_total, 128) for q in range(qa, qb)}
+        assert set(cover) == want
+        lens = [(gb - ga) * (16 + nq) for _, _, ga, gb, _, nq in items]
+        assert lens == sorted(lens, reverse=True)       # longest first
+    # workspace = bf16 shadows + two image sets
+    shadow = -(-c * d_in * 2 // 1024) * 1024 + -(-c * d_out * 2 // 1024) * 1024
+    assert ws == shadow + 2 * img * 16384
+
+
+def _status_of(fn):
+    try:
+        fn()
+    except M.MloraError as e:
+        return e.status
+    return M.MLORA_OK
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(offsets=[0, 5]), M.MLORA_ERR_INVALID),            # overlap (second job should start at 10)
+    (dict(offsets=[0, 12]), M.MLORA_ERR_INVALID),           # gap
+    (dict(n_total=25), M.MLORA_ERR_INVALID),                # rows not covered
+    (dict(ranks=[0, 4]), M.MLORA_ERR_INVALID),
+    (dict(ranks=[257, 4]), M.MLORA_ERR_UNSUPPORTED),
+    (dict(d_in=100), M.MLORA_ERR_UNSUPPORTED),              # not a multiple of 8 (bf16)
+    (dict(n_tokens=[0, 10]), M.MLORA_ERR_INVALID),
+])
+def test_plan_rejects_bad_tables(bad, status):
+    args = dict(d_in=128, d_out=64, ranks=[4, 8], n_tokens=[10, 10])
+    args.update(bad)
+    assert _status_of(lambda: M.mlora_plan_destroy(host_plan(**args)[0])) == status
+
+
+def test_plan_rejects_null_and_misaligned_adapters():
+    ok = M.mlora_segment(0, 4, 2, 1.0, 0x1000, 0x2000, 0, 0, 0, 0, 0, 0)
+    prob = M.mlora_problem(4, 64, 64, M.MLORA_BF16, M.MLORA_PLAN_HOST_ONLY)
+    h, _ = M.mlora_plan(prob, [ok])
+    M.mlora_plan_destroy(h)
+    for field, val in (("At", 0), ("Bt", 0), ("At", 0x1004), ("dBt", 0x2008)):
+        s = M.mlora_segment(0, 4, 2, 1.0, 0x1000, 0x2000, 0, 0, 0, 0, 0, 0)
+        setattr(s, field, val)
+        assert _status_of(lambda: M.mlora_plan(prob, [s])) == M.MLORA_ERR_INVALID
+
+
+def test_host_only_plan_refuses_execution():
+    plan, _ = host_plan(128, 64, [4], [10])
+    try:
+        st = M.lib().mlora_forward(plan, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, None)
+        assert st == M.MLORA_ERR_INVALID
+        assert "HOST_ONLY" in M.lib().mlora_last_error().decode()
+    finally:
+        M.mlora_plan_destroy(plan)
+
+
+def test_h_elems_is_sum_n_r():
+    plan, _ = host_plan(128, 64, [4, 8, 3], [10, 7, 5])
+    try:
+        assert M.mlora_h_elems(plan) == 4 * 10 + 8 * 7 + 3 * 5
+    finally:
+        M.mlora_plan_destroy(plan)
