@@ -21,7 +21,8 @@ MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD
 # every symbol include/mlora.h declares
 EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward", "mlora_adamw",
            "mlora_sync_status", "mlora_h_elems", "mlora_plan_describe", "mlora_status_string",
-           "mlora_last_error", "mlora_version"]
+           "mlora_last_error", "mlora_version", "mlora_profile_enable", "mlora_profile_read",
+           "mlora_kernel_name", "mlora_launch_count"]
 
 
 class mlora_segment(C.Structure):
@@ -75,6 +76,14 @@ def lib() -> C.CDLL:
         L.mlora_last_error.restype = C.c_char_p
         L.mlora_version.argtypes = []
         L.mlora_version.restype = i32
+        L.mlora_profile_enable.argtypes = [vp, i32]
+        L.mlora_profile_enable.restype = i32
+        L.mlora_profile_read.argtypes = [vp, C.POINTER(C.c_double), C.POINTER(i64), i32, C.POINTER(i32)]
+        L.mlora_profile_read.restype = i32
+        L.mlora_kernel_name.argtypes = [i32]
+        L.mlora_kernel_name.restype = C.c_char_p
+        L.mlora_launch_count.argtypes = []
+        L.mlora_launch_count.restype = i64
         _lib = L
     return _lib
 
@@ -140,3 +149,21 @@ def mlora_status_string(status: int) -> str:
 
 def mlora_version() -> int:
     return int(lib().mlora_version())
+
+
+def mlora_profile_enable(plan, enable: bool) -> None:
+    _check(lib().mlora_profile_enable(plan, 1 if enable else 0), "mlora_profile_enable")
+
+
+def mlora_profile_read(plan) -> dict:
+    """{kernel name: (summed ms, timed launches)} since the last read."""
+    L = lib()
+    n = C.c_int32(0)
+    ms = (C.c_double * 64)()
+    cnt = (C.c_int64 * 64)()
+    _check(L.mlora_profile_read(plan, ms, cnt, 64, C.byref(n)), "mlora_profile_read")
+    return {L.mlora_kernel_name(i).decode(): (ms[i], int(cnt[i])) for i in range(n.value)}
+
+
+def mlora_launch_count() -> int:
+    return int(lib().mlora_launch_count())

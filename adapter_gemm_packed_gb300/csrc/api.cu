@@ -130,6 +130,11 @@ struct mlora_plan_s {
   AdamItem* d_adam = nullptr;
   int* d_err = nullptr;
   unsigned long long timeout_ns = DEFAULT_TIMEOUT_NS;
+  // optional per-kernel timing with CUDA events recorded on the launching stream
+  bool profiling = false;
+  std::vector<cudaEvent_t> ev_pool;
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> ev_pending;
+  size_t ev_next = 0;
 };
 
 namespace {
@@ -355,6 +360,46 @@ mlora_status upload(mlora_plan_t* P) {
   return MLORA_OK;
 }
 
+enum KernelId {
+  K_PACK_FWD = 0, K_SHRINK, K_FWD_GEMM, K_PACK_BWD, K_H_IMAGES, K_DH, K_DB, K_BWD_GEMM, K_DA, K_ADAMW,
+  K_F32_FWD, K_F32_BWD, K_COUNT
+};
+const char* const kKernelNames[K_COUNT] = {
+    "pack_fwd", "shrink", "fwd_gemm", "pack_bwd", "h_images", "dH", "dB", "bwd_gemm", "dA", "adamw",
+    "f32_forward", "f32_backward"};
+// kernels launched by each id (a pack step is two kernels, the fp32 passes several)
+const int kKernelLaunches[K_COUNT] = {2, 1, 1, 2, 1, 1, 1, 1, 1, 1, 2, 4};
+
+long long g_launches = 0;
+
+cudaEvent_t next_event(mlora_plan_t* P) {
+  if (P->ev_next == P->ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    P->ev_pool.push_back(e);
+  }
+  return P->ev_pool[P->ev_next++];
+}
+
+// Run one launch step; with profiling on, bracket it by events on the same stream.
+template <typename F>
+cudaError_t timed(const mlora_plan_t* Pc, int id, cudaStream_t s, F&& launch) {
+  mlora_plan_t* P = const_cast<mlora_plan_t*>(Pc);
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (P->profiling) {
+    a = next_event(P);
+    b = next_event(P);
+    if (a && b) cudaEventRecord(a, s);
+  }
+  cudaError_t e = launch();
+  if (e == cudaSuccess) g_launches += kKernelLaunches[id];
+  if (a && b) {
+    cudaEventRecord(b, s);
+    P->ev_pending.push_back({id, {a, b}});
+  }
+  return e;
+}
+
 GemmArgs base_args(const mlora_plan_t* P) {
   GemmArgs g{};
   g.N = static_cast<int>(P->prob.n_tokens);
@@ -413,6 +458,7 @@ mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs,
 
 void mlora_plan_destroy(mlora_plan_t* plan) {
   if (!plan) return;
+  for (cudaEvent_t e : plan->ev_pool) cudaEventDestroy(e);
   if (plan->dev_block) cudaFree(plan->dev_block);
   delete plan;
 }
@@ -431,8 +477,8 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
   const mlora_problem& pr = P->prob;
   cudaError_t e;
   if (pr.dtype == MLORA_F32) {
-    e = launch_f32_forward(P->d_segs, P->n_segs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems,
-                           static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<float*>(Y), H, s);
+    e = timed(P, K_F32_FWD, s, [&] { return launch_f32_forward(P->d_segs, P->n_segs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems,
+                           static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<float*>(Y), H, s); });
     return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 forward launch");
   }
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -443,7 +489,7 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
       reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow + round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024));
   uint8_t* himg = ws + P->off_himg;
 
-  e = launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s);
+  e = timed(P, K_PACK_FWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s); });
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
 
   CUtensorMap mX, mAt, mW, mBt;
@@ -457,7 +503,7 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
   g.n_items = static_cast<int>(P->win.size());
   g.img_out = himg;
   g.hout = H;
-  e = launch_seg_gemm<MODE_SHRINK>(mX, mAt, mAt, g, grid_of(P, g.n_items), s);
+  e = timed(P, K_SHRINK, s, [&] { return launch_seg_gemm<MODE_SHRINK>(mX, mAt, mAt, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "shrink launch");
 
   g = base_args(P);
@@ -467,7 +513,7 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
   g.img_in = himg;
   g.out = Y;
   g.ld_out = pr.d_out;
-  e = launch_seg_gemm<MODE_FWD>(mX, mW, mBt, g, grid_of(P, g.n_items), s);
+  e = timed(P, K_FWD_GEMM, s, [&] { return launch_seg_gemm<MODE_FWD>(mX, mW, mBt, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "forward GEMM launch");
   return MLORA_OK;
 }
@@ -485,9 +531,9 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   const mlora_problem& pr = P->prob;
   cudaError_t e;
   if (pr.dtype == MLORA_F32) {
-    e = launch_f32_backward(P->d_segs, P->n_segs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems, P->max_rank,
+    e = timed(P, K_F32_BWD, s, [&] { return launch_f32_backward(P->d_segs, P->n_segs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems, P->max_rank,
                             static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<const float*>(dY),
-                            H, static_cast<float*>(dX), dH, s);
+                            H, static_cast<float*>(dX), dH, s); });
     return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 backward launch");
   }
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -499,9 +545,9 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   uint8_t* himg = ws + P->off_himg;
   uint8_t* dhimg = ws + P->off_dhimg;
 
-  e = launch_pack_bwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, a_all, b_all, s);
+  e = timed(P, K_PACK_BWD, s, [&] { return launch_pack_bwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, a_all, b_all, s); });
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
-  e = launch_h_images(P->d_segs, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s);
+  e = timed(P, K_H_IMAGES, s, [&] { return launch_h_images(P->d_segs, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s); });
   if (e != cudaSuccess) return cuda_fail(e, "image launch");
 
   CUtensorMap mdY, mdYt, mB, mWmn, mA, mXt;
@@ -518,7 +564,7 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   g.n_items = static_cast<int>(P->win.size());
   g.img_out = dhimg;
   g.hout = dH;
-  e = launch_seg_gemm<MODE_DH>(mdY, mB, mB, g, grid_of(P, g.n_items), s);
+  e = timed(P, K_DH, s, [&] { return launch_seg_gemm<MODE_DH>(mdY, mB, mB, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "dH launch");
 
   // dB = Htilde^T dY
@@ -526,7 +572,7 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   g.witems = P->d_db;
   g.n_items = static_cast<int>(P->db.size());
   g.img_in = himg;
-  e = launch_seg_gemm<MODE_DB>(mdYt, mdYt, mdYt, g, grid_of(P, g.n_items), s);
+  e = timed(P, K_DB, s, [&] { return launch_seg_gemm<MODE_DB>(mdYt, mdYt, mdYt, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "dB launch");
 
   // dX = dY W^T + dHtilde A^T
@@ -537,7 +583,7 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   g.img_in = dhimg;
   g.out = dX;
   g.ld_out = pr.d_in;
-  e = launch_seg_gemm<MODE_BWD>(mdY, mWmn, mA, g, grid_of(P, g.n_items), s);
+  e = timed(P, K_BWD_GEMM, s, [&] { return launch_seg_gemm<MODE_BWD>(mdY, mWmn, mA, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "backward GEMM launch");
 
   // dA = X^T dHtilde
@@ -545,7 +591,7 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   g.witems = P->d_da;
   g.n_items = static_cast<int>(P->da.size());
   g.img_in = dhimg;
-  e = launch_seg_gemm<MODE_DA>(mXt, mXt, mXt, g, grid_of(P, g.n_items), s);
+  e = timed(P, K_DA, s, [&] { return launch_seg_gemm<MODE_DA>(mXt, mXt, mXt, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "dA launch");
   return MLORA_OK;
 }
@@ -560,8 +606,11 @@ mlora_status mlora_adamw(const mlora_plan_t* P, float lr, float beta1, float bet
   if (!(beta1 >= 0.f && beta1 < 1.f && beta2 >= 0.f && beta2 < 1.f) || !std::isfinite(lr) || !std::isfinite(eps) ||
       !std::isfinite(weight_decay))
     return fail(MLORA_ERR_INVALID, "bad AdamW hyper-parameters");
-  cudaError_t e = launch_adamw(P->d_adam, static_cast<int>(P->adam.size()), lr, beta1, beta2, eps, weight_decay, step,
-                               P->num_sms, static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed(P, K_ADAMW, s, [&] {
+    return launch_adamw(P->d_adam, static_cast<int>(P->adam.size()), lr, beta1, beta2, eps, weight_decay, step,
+                        P->num_sms, s);
+  });
   return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "AdamW launch");
 }
 
@@ -614,6 +663,39 @@ mlora_status mlora_plan_describe(const mlora_plan_t* P, int32_t what, int64_t* o
   if (out) std::copy(v.begin(), v.begin() + std::min<int64_t>(cap, *count), out);
   return MLORA_OK;
 }
+
+mlora_status mlora_profile_enable(mlora_plan_t* P, int32_t enable) {
+  if (!P) return fail(MLORA_ERR_INVALID, "null plan");
+  P->profiling = enable != 0;
+  return MLORA_OK;
+}
+
+mlora_status mlora_profile_read(mlora_plan_t* P, double* ms, int64_t* launches, int32_t cap, int32_t* n_kernels) {
+  if (!P || !n_kernels) return fail(MLORA_ERR_INVALID, "null plan or count");
+  *n_kernels = K_COUNT;
+  std::vector<double> acc(K_COUNT, 0.0);
+  std::vector<int64_t> cnt(K_COUNT, 0);
+  for (auto& pe : P->ev_pending) {
+    cudaError_t e = cudaEventSynchronize(pe.second.second);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float t = 0.f;
+    e = cudaEventElapsedTime(&t, pe.second.first, pe.second.second);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    acc[pe.first] += t;
+    cnt[pe.first] += 1;
+  }
+  P->ev_pending.clear();
+  P->ev_next = 0;
+  for (int i = 0; i < K_COUNT && i < cap; ++i) {
+    if (ms) ms[i] = acc[i];
+    if (launches) launches[i] = cnt[i];
+  }
+  return MLORA_OK;
+}
+
+const char* mlora_kernel_name(int32_t id) { return (id >= 0 && id < K_COUNT) ? kKernelNames[id] : ""; }
+
+int64_t mlora_launch_count(void) { return g_launches; }
 
 const char* mlora_status_string(mlora_status s) {
   switch (s) {

@@ -159,6 +159,22 @@ int64_t mlora_h_elems(const mlora_plan_t* plan);
 mlora_status mlora_plan_describe(const mlora_plan_t* plan, int32_t what, int64_t* out, int64_t cap,
                                  int64_t* count);
 
+/* Per-kernel timing, for tooling.  While enabled, every launch the plan makes is bracketed by
+ * two CUDA events recorded on the launching stream (so the measured time is the kernels' own,
+ * in stream order).  mlora_profile_read() waits for the recorded events, stores for each kernel
+ * id the summed milliseconds (ms[id]) and the number of timed launches (launches[id]) for ids
+ * below cap, sets *n_kernels to the number of ids, and clears the record.  Either array may be
+ * NULL.  The plan is not thread-safe while profiling. */
+mlora_status mlora_profile_enable(mlora_plan_t* plan, int32_t enable);
+mlora_status mlora_profile_read(mlora_plan_t* plan, double* ms, int64_t* launches, int32_t cap,
+                                int32_t* n_kernels);
+
+/* Name of a kernel id of mlora_profile_read ("fwd_gemm", "adamw", ...; "" if out of range). */
+const char* mlora_kernel_name(int32_t id);
+
+/* Number of CUDA kernels this library has launched in this process so far. */
+int64_t mlora_launch_count(void);
+
 /* Human-readable name of a status code (static storage). */
 const char* mlora_status_string(mlora_status s);
 
