@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Throughput of the packed multi-adapter LoRA layer: forward + backward + AdamW per step.
+
+Default workload: Llama-3-8B-shaped q_proj (d_in = d_out = 4096, bf16 activations and weight,
+fp32 adapter masters), 8 jobs with ranks {8,8,16,16,32,32,64,64}, 2048 tokens each (16384
+tokens per step).  One step = mlora_forward + mlora_backward + mlora_adamw over the whole pack
+with inputs resident in HBM.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+
+--impl reference times the fp64 CPU oracle (the reference arm of this metric) on a bounded
+sample of the same workload.  Under torchrun (N > 1) every rank runs its own replica of the
+workload (weak scaling, no collective on the data path); the barrier and max-over-ranks
+timing bracket the timed region.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "packed multi-LoRA fwd+bwd tokens/s and TFLOP/s per layer; % of bf16/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return FALLBACK_PEAKS, "fallback"
+
+
+def workload(name):
+    from adapter_gemm_packed_gb300 import workloads as W
+    if name in W.CONFIGS:
+        return W.CONFIGS[name]()
+    if name.startswith("llama8b_layer_"):
+        return W.llama8b_layer(int(name.rsplit("_", 1)[1]))
+    raise SystemExit(f"unknown workload {name}")
+
+
+def flops_per_step(wl):
+    lora = sum(n * r for n, r in zip(wl.n_tokens, wl.ranks))
+    return 4.0 * wl.N * wl.d_in * wl.d_out + 6.0 * lora * (wl.d_in + wl.d_out)
+
+
+def kernel_flops(wl, kernel):
+    """Algorithmic FLOPs of one launch of a tensor-core kernel."""
+    lora = sum(n * r for n, r in zip(wl.n_tokens, wl.ranks))
+    if kernel == "fwd_gemm":
+        return 2.0 * wl.N * wl.d_in * wl.d_out + 2.0 * lora * wl.d_out
+    if kernel == "bwd_gemm":
+        return 2.0 * wl.N * wl.d_in * wl.d_out + 2.0 * lora * wl.d_in
+    return None
+
+
+def kernel_bytes(wl, kernel):
+    """Algorithmic HBM bytes of one launch of a memory-bound kernel (bf16 activations)."""
+    e = 2
+    lora = sum(n * r for n, r in zip(wl.n_tokens, wl.ranks))
+    sr = sum(wl.ranks)
+    params = sr * (wl.d_in + wl.d_out)
+    if kernel == "shrink":
+        return wl.N * wl.d_in * e + sr * wl.d_in * 2 + lora * 4
+    if kernel == "dH":
+        return wl.N * wl.d_out * e + sr * wl.d_out * 2 + lora * 4
+    if kernel == "dA":
+        return wl.N * wl.d_in * e + lora * 2 + wl.d_in * sr * 4
+    if kernel == "dB":
+        return wl.N * wl.d_out * e + lora * 2 + wl.d_out * sr * 4
+    if kernel == "adamw":
+        return params * 28
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+                except ValueError:
+                    continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[3][1:]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+def oracle_sample(wl, T, per_job):
+    """A bounded sample of the workload for the CPU oracle: the first `per_job` tokens of every job."""
+    import numpy as np
+    from adapter_gemm_packed_gb300 import workloads as W
+    from oracle import lora_oracle as orc
+    rows = np.concatenate([np.arange(o, o + min(per_job, n)) for o, n in zip(wl.offsets, wl.n_tokens)])
+    X = W.rows_as_f64(T.X[rows], wl.dtype)
+    dY = W.rows_as_f64(T.dY[rows], wl.dtype)
+    Wm = W.rows_as_f64(T.Wt, wl.dtype).T.copy()
+    segs, off = [], 0
+    for i, n in enumerate(wl.n_tokens):
+        k = min(per_job, n)
+        segs.append(orc.Seg(off, k, T.At[i].astype(np.float64).T.copy(), T.Bt[i].astype(np.float64).T.copy(),
+                            wl.alphas[i]))
+        off += k
+    return X, Wm, dY, segs, len(rows)
+
+
+def oracle_step(wl, X, Wm, dY, segs, state, t):
+    from oracle import lora_oracle as orc
+    Y, H = orc.forward(X, Wm, segs)
+    dX, dA, dB, dH = orc.backward(X, Wm, dY, segs)
+    for i, sg in enumerate(segs):
+        for name, p, g in (("A", sg.A, dA[i]), ("B", sg.B, dB[i])):
+            m, v = state.get((name, i), (0.0, 0.0))
+            p2, m, v = orc.adamw(p, g, m, v, wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, t)
+            state[(name, i)] = (m, v)
+    return Y, dX
+
+
+def cores_used():
+    return os.cpu_count() or 1
+
+
+def run_reference(args, wl, rank):
+    """The reference arm of this metric: the fp64 CPU oracle on the host cores."""
+    if rank != 0:
+        return
+    from adapter_gemm_packed_gb300 import workloads as W
+    T = W.materialise(wl)
+    per_job = args.ref_tokens_per_job
+    X, Wm, dY, segs, ntok = oracle_sample(wl, T, per_job)
+    state = {}
+    for t in range(1, args.warmup + 1):
+        oracle_step(wl, X, Wm, dY, segs, state, t)
+    t0 = time.perf_counter()
+    for t in range(args.warmup + 1, args.warmup + args.steps + 1):
+        oracle_step(wl, X, Wm, dY, segs, state, t)
+    dt = time.perf_counter() - t0
+    value = ntok * args.steps / dt
+    sample = f"first {per_job} tokens of each of the {wl.n_adapters} jobs ({ntok} tokens), full d_in x d_out"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded Philox)", "config": config_of(wl, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, ngpus):
+    return {"workload": wl.name, "d_in": wl.d_in, "d_out": wl.d_out, "adapters": wl.n_adapters,
+            "ranks": wl.ranks, "tokens_per_step": wl.N, "dtype_io": wl.dtype, "parallelism": f"replicas x{ngpus}",
+            "l2": "inputs larger than L2 (X and dY are N x d bf16, each above the 129 MB L2)"
+            if wl.N * min(wl.d_in, wl.d_out) * 2 > 129e6 else "inputs smaller than L2"}
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path))
+    except Exception:
+        return None
+    src = open(os.path.join(ROOT, "adapter_gemm_packed_gb300", "csrc", "seg_gemm.cu"), "rb").read()
+    h = hashlib.sha256(src).hexdigest()[:16]
+    r = rec.get(kernel)
+    if not r or r.get("source_sha") != h:
+        return None
+    return r.get("bytes_per_launch")
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import numpy as np
+    import torch
+    from adapter_gemm_packed_gb300 import _mlora as M
+    from adapter_gemm_packed_gb300 import workloads as W
+    from adapter_gemm_packed_gb300.layer import PackedLoRA
+
+    dist = world > 1
+    torch.cuda.set_device(local_rank)
+    T = W.materialise(wl)
+    scales = [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
+    layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At, Bt=T.Bt)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+
+    def host(a):
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if wl.dtype == "bf16" else torch.from_numpy(a)
+        return t.pin_memory()
+
+    X_h, Wt_h, dY_h = host(T.X), host(T.Wt), host(T.dY)
+    X, Wt, dY = X_h.cuda(), Wt_h.cuda(), dY_h.cuda()
+    Y = torch.empty((wl.N, wl.d_out), dtype=tdt, device="cuda")
+    dX = torch.empty((wl.N, wl.d_in), dtype=tdt, device="cuda")
+    stream = torch.cuda.current_stream()
+    step_no = [0]
+
+    def step():
+        step_no[0] += 1
+        layer.forward(X, Wt, Y)
+        layer.backward(X, Wt, dY, dX)
+        layer.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, step_no[0])
+
+    def barrier():
+        if dist:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if layer.sync_status() != M.MLORA_OK:
+        raise SystemExit("device status error during warm-up")
+
+    # ---- timed region (device): K steps, per-kernel events recorded by the library
+    M.mlora_profile_enable(layer.plan, True)
+    M.mlora_profile_read(layer.plan)
+    launches0 = M.mlora_launch_count()
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    launches = M.mlora_launch_count() - launches0
+    prof = M.mlora_profile_read(layer.plan)
+    M.mlora_profile_enable(layer.plan, False)
+    if layer.sync_status() != M.MLORA_OK:
+        raise SystemExit("device status error in the timed region")
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through the public API: pinned host inputs in, results out, every step
+    e2e = None
+    if not args.no_e2e:
+        Y_h = torch.empty_like(Y, device="cpu").pin_memory()
+        dX_h = torch.empty_like(dX, device="cpu").pin_memory()
+
+        def e2e_step():
+            X.copy_(X_h, non_blocking=True)
+            dY.copy_(dY_h, non_blocking=True)
+            step()
+            Y_h.copy_(Y, non_blocking=True)
+            dX_h.copy_(dX, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ems = e0.elapsed_time(e1)
+        if dist:
+            t = torch.tensor([ems], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        b_in = X.numel() * X.element_size() + dY.numel() * dY.element_size()
+        b_out = Y.numel() * Y.element_size() + dX.numel() * dX.element_size()
+        e2e = {"value": wl.N * world * args.steps / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": b_in, "d2h_bytes_per_step": b_out, "ms_per_step": ems / args.steps}
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    kernels = {k: {"ms_per_launch": v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1] > 0}
+    step_ms = ms / args.steps
+    for k, v in kernels.items():
+        v["share_of_step"] = v["ms_per_launch"] * (v["launches"] / args.steps) / step_ms
+        f = kernel_flops(wl, k)
+        b = kernel_bytes(wl, k)
+        if f:
+            v["tflops"] = f / (v["ms_per_launch"] * 1e-3) / 1e12
+        if b:
+            v["gbs"] = b / (v["ms_per_launch"] * 1e-3) / 1e9
+    dom = max(("fwd_gemm", "bwd_gemm"), key=lambda k: kernels.get(k, {}).get("ms_per_launch", 0))
+    dk = kernels[dom]
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    roof = {"kernel": dom, "bound": "tensor", "achieved": dk["tflops"], "peak": peak, "unit": "TFLOP/s",
+            "frac": dk["tflops"] / peak, "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
+            "traffic": traffic_record(dom)}
+    value = wl.N * world * args.steps / (ms / 1e3)
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic (seeded Philox; shapes of the named workload, random-init adapters)",
+            "config": config_of(wl, world),
+            "tflops": flops_per_step(wl) * world * args.steps / (ms / 1e3) / 1e12,
+            "roofline": roof, "kernels": kernels, "gpu_launches": launches, "e2e": e2e,
+            "clocks": clk.summary()}
+    if not args.no_cpu_baseline and world == 1:
+        X_, Wm, dY_, segs, ntok = oracle_sample(wl, T, args.ref_tokens_per_job)
+        state, t, dt, reps = {}, 0, 0.0, 0
+        t0 = time.perf_counter()
+        while reps < 1 or (time.perf_counter() - t0 < args.cpu_seconds and reps < 50):
+            t += 1
+            oracle_step(wl, X_, Wm, dY_, segs, state, t)
+            reps += 1
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": ntok * reps / dt, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+                                "sample": f"first {args.ref_tokens_per_job} tokens of each job ({ntok} tokens) x {reps} "
+                                          f"steps, fp64 numpy (BLAS threads = cores)"}
+    print(json.dumps(line), flush=True)
+    layer.close()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qproj")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-tokens-per-job", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl, rank)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0:
+        import __graft_entry__
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    run_ours(args, wl, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -64,9 +64,11 @@ def test_bf16_zero_base_weight_isolates_rank_term():
 
 
 def test_bf16_zero_B_gives_base_product():
+    # B starts at 0, so the updated B equals the AdamW update itself, which at t = 1 is about
+    # -lr * sign(g): the sign of near-zero gradient entries decides it.  The update is checked
+    # on identical gradients in test_adamw_isolated_t3; here the layer outputs and moments.
     wl = W.custom("zero_B", 951, 384, 256, [8, 3], [100, 90], dtype="bf16", b_std=0.0)
-    errs, got, want = _run(wl)
-    X = W.rows_as_f64(W.materialise(wl).X, "bf16")
+    errs, got, want = _run(wl, keys=["Y", "dX", "H", "dH", "dAt", "dBt", "At", "mA", "vA", "mB", "vB"])
     # dA must vanish when B = 0 (Case 3 of the backward has B as a factor)
     assert all(np.max(np.abs(a)) == 0 for a in got["dAt"])
 
