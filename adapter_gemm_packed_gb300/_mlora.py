@@ -16,6 +16,7 @@ MLORA_OK, MLORA_ERR_INVALID, MLORA_ERR_UNSUPPORTED, MLORA_ERR_CUDA, MLORA_ERR_TI
 MLORA_F32, MLORA_BF16 = 0, 1
 MLORA_PLAN_HOST_ONLY = 1
 MLORA_DEBUG_SHORT_TIMEOUT = 2
+MLORA_GEMM_SINGLE_CTA = 4
 MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD_B, MLORA_Q_WINDOW = range(6)
 
 # every symbol include/mlora.h declares

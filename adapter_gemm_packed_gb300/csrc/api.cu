@@ -26,8 +26,11 @@
 
 namespace mlora {
 template <int MODE>
-cudaError_t launch_seg_gemm(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int,
-                            cudaStream_t);
+cudaError_t launch_seg_gemm(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                            const GemmArgs&, int, cudaStream_t);
+template <int MODE>
+cudaError_t launch_gemm_2sm(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                            const GemmArgs&, int, cudaStream_t);
 cudaError_t launch_pack_fwd(const DevSeg*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, int,
                             cudaStream_t);
 cudaError_t launch_pack_bwd(const DevSeg*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, cudaStream_t);
@@ -249,6 +252,22 @@ void build_tables(mlora_plan_t* P) {
     m.img_off = static_cast<int>(img);
     m.pad0 = m.pad1 = m.pad2 = 0;
     img += m.nch;
+  }
+  // The 2-CTA base GEMMs run 256-token tiles whose rank-term K extension is one MMA over both
+  // 128-token halves, so both halves of a pair stage the union of their chunk ranges.
+  img = 0;
+  for (int t = 0; t < P->n_mtiles; t += 2) {
+    MTile& a = P->mtiles[t];
+    if (t + 1 < P->n_mtiles) {
+      MTile& b = P->mtiles[t + 1];
+      const int lo = std::min(a.q_lo, b.q_lo), hi = std::max(a.q_lo + a.nch, b.q_lo + b.nch);
+      a.q_lo = b.q_lo = lo;
+      a.nch = b.nch = hi - lo;
+    }
+    for (int u = t; u < std::min(t + 2, P->n_mtiles); ++u) {
+      P->mtiles[u].img_off = static_cast<int>(img);
+      img += P->mtiles[u].nch;
+    }
   }
   P->n_images = img;
   P->img_tile.resize(img);
@@ -492,28 +511,36 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
   e = timed(P, K_PACK_FWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s); });
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
 
-  CUtensorMap mX, mAt, mW, mBt;
+  const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
+  CUtensorMap mX, mAt, mW, mBt, mI;
   if ((st = make_map(&mX, X, pr.d_in, pr.n_tokens, pr.d_in, 64, 128)) != MLORA_OK) return st;
   if ((st = make_map(&mAt, at_all, pr.d_in, P->C_total, pr.d_in, 64, 64)) != MLORA_OK) return st;
-  if ((st = make_map(&mW, Wt, pr.d_in, pr.d_out, pr.d_in, 64, 256)) != MLORA_OK) return st;
-  if ((st = make_map(&mBt, bt_all, P->C_total, pr.d_out, P->C_total, 64, 256)) != MLORA_OK) return st;
+  if ((st = make_map(&mW, Wt, pr.d_in, pr.d_out, pr.d_in, 64, pairs ? 128 : 256)) != MLORA_OK) return st;
+  if ((st = make_map(&mBt, bt_all, P->C_total, pr.d_out, P->C_total, 64, pairs ? 128 : 256)) != MLORA_OK) return st;
+  if ((st = make_map(&mI, himg, CHUNK_COLS, P->n_images * BM, CHUNK_COLS, 64, 128)) != MLORA_OK) return st;
 
   GemmArgs g = base_args(P);
   g.kmain = (pr.d_in + BK - 1) / BK;
   g.n_items = static_cast<int>(P->win.size());
   g.img_out = himg;
   g.hout = H;
-  e = timed(P, K_SHRINK, s, [&] { return launch_seg_gemm<MODE_SHRINK>(mX, mAt, mAt, g, grid_of(P, g.n_items), s); });
+  e = timed(P, K_SHRINK, s, [&] { return launch_seg_gemm<MODE_SHRINK>(mX, mAt, mAt, mX, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "shrink launch");
 
   g = base_args(P);
   g.kmain = (pr.d_in + BK - 1) / BK;
   g.n_tiles_n = (pr.d_out + BN - 1) / BN;
-  g.n_items = P->n_mtiles * g.n_tiles_n;
-  g.img_in = himg;
   g.out = Y;
   g.ld_out = pr.d_out;
-  e = timed(P, K_FWD_GEMM, s, [&] { return launch_seg_gemm<MODE_FWD>(mX, mW, mBt, g, grid_of(P, g.n_items), s); });
+  if (pairs) {
+    g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
+    e = timed(P, K_FWD_GEMM, s, [&] {
+      return launch_gemm_2sm<MODE_FWD>(mX, mW, mBt, mI, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
+    });
+  } else {
+    g.n_items = P->n_mtiles * g.n_tiles_n;
+    e = timed(P, K_FWD_GEMM, s, [&] { return launch_seg_gemm<MODE_FWD>(mX, mW, mBt, mI, g, grid_of(P, g.n_items), s); });
+  }
   if (e != cudaSuccess) return cuda_fail(e, "forward GEMM launch");
   return MLORA_OK;
 }
@@ -550,13 +577,17 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   e = timed(P, K_H_IMAGES, s, [&] { return launch_h_images(P->d_segs, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s); });
   if (e != cudaSuccess) return cuda_fail(e, "image launch");
 
-  CUtensorMap mdY, mdYt, mB, mWmn, mA, mXt;
+  const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
+  CUtensorMap mdY, mdYt, mB, mWmn, mA, mXt, mHi, mdHi, mdHi64;
   if ((st = make_map(&mdY, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 128)) != MLORA_OK) return st;
   if ((st = make_map(&mdYt, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mB, b_all, pr.d_out, P->C_total, pr.d_out, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mWmn, Wt, pr.d_in, pr.d_out, pr.d_in, 64, 64)) != MLORA_OK) return st;
-  if ((st = make_map(&mA, a_all, P->C_total, pr.d_in, P->C_total, 64, 256)) != MLORA_OK) return st;
+  if ((st = make_map(&mA, a_all, P->C_total, pr.d_in, P->C_total, 64, pairs ? 128 : 256)) != MLORA_OK) return st;
   if ((st = make_map(&mXt, X, pr.d_in, pr.n_tokens, pr.d_in, 64, 64)) != MLORA_OK) return st;
+  if ((st = make_map(&mHi, himg, CHUNK_COLS, P->n_images * BM, CHUNK_COLS, 64, 64)) != MLORA_OK) return st;
+  if ((st = make_map(&mdHi, dhimg, CHUNK_COLS, P->n_images * BM, CHUNK_COLS, 64, 128)) != MLORA_OK) return st;
+  if ((st = make_map(&mdHi64, dhimg, CHUNK_COLS, P->n_images * BM, CHUNK_COLS, 64, 64)) != MLORA_OK) return st;
 
   // dH = s dY B^T  (+ staged dHtilde images)
   GemmArgs g = base_args(P);
@@ -564,34 +595,38 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   g.n_items = static_cast<int>(P->win.size());
   g.img_out = dhimg;
   g.hout = dH;
-  e = timed(P, K_DH, s, [&] { return launch_seg_gemm<MODE_DH>(mdY, mB, mB, g, grid_of(P, g.n_items), s); });
+  e = timed(P, K_DH, s, [&] { return launch_seg_gemm<MODE_DH>(mdY, mB, mB, mdY, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "dH launch");
 
   // dB = Htilde^T dY
   g = base_args(P);
   g.witems = P->d_db;
   g.n_items = static_cast<int>(P->db.size());
-  g.img_in = himg;
-  e = timed(P, K_DB, s, [&] { return launch_seg_gemm<MODE_DB>(mdYt, mdYt, mdYt, g, grid_of(P, g.n_items), s); });
+  e = timed(P, K_DB, s, [&] { return launch_seg_gemm<MODE_DB>(mdYt, mdYt, mdYt, mHi, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "dB launch");
 
   // dX = dY W^T + dHtilde A^T
   g = base_args(P);
   g.kmain = (pr.d_out + BK - 1) / BK;
   g.n_tiles_n = (pr.d_in + BN - 1) / BN;
-  g.n_items = P->n_mtiles * g.n_tiles_n;
-  g.img_in = dhimg;
   g.out = dX;
   g.ld_out = pr.d_in;
-  e = timed(P, K_BWD_GEMM, s, [&] { return launch_seg_gemm<MODE_BWD>(mdY, mWmn, mA, g, grid_of(P, g.n_items), s); });
+  if (pairs) {
+    g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
+    e = timed(P, K_BWD_GEMM, s, [&] {
+      return launch_gemm_2sm<MODE_BWD>(mdY, mWmn, mA, mdHi, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
+    });
+  } else {
+    g.n_items = P->n_mtiles * g.n_tiles_n;
+    e = timed(P, K_BWD_GEMM, s, [&] { return launch_seg_gemm<MODE_BWD>(mdY, mWmn, mA, mdHi, g, grid_of(P, g.n_items), s); });
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward GEMM launch");
 
   // dA = X^T dHtilde
   g = base_args(P);
   g.witems = P->d_da;
   g.n_items = static_cast<int>(P->da.size());
-  g.img_in = dhimg;
-  e = timed(P, K_DA, s, [&] { return launch_seg_gemm<MODE_DA>(mXt, mXt, mXt, g, grid_of(P, g.n_items), s); });
+  e = timed(P, K_DA, s, [&] { return launch_seg_gemm<MODE_DA>(mXt, mXt, mXt, mdHi64, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "dA launch");
   return MLORA_OK;
 }

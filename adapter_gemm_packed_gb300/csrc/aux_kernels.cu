@@ -108,7 +108,8 @@ __global__ void k_pack_b_t(const DevSeg* __restrict__ segs, const int* __restric
   }
 }
 
-// Staged Htilde images from H: image (tile t, chunk q) row r col u = s_j H_j[row - off_j][64q + u - c_j]
+// Staged Htilde images from H (row-major [128 x 64] bf16 blocks):
+// image (tile t, chunk q) row r col u = s_j H_j[row - off_j][64q + u - c_j]
 // when token row (128 t + r) belongs to job j and column 64q+u lies in job j's rank window, else 0.
 __global__ void k_h_images(const DevSeg* __restrict__ segs, const MTile* __restrict__ mtiles,
                            const int* __restrict__ img_tile, long long N, const float* __restrict__ H,
@@ -142,7 +143,7 @@ __global__ void k_h_images(const DevSeg* __restrict__ segs, const MTile* __restr
       const float a1 = (c1 >= c_lo && c1 < c_hi) ? s * hrow[c1] : 0.f;
       pk[u / 2] = pack_bf16x2(a0, a1);
     }
-    *reinterpret_cast<uint4*>(base + swz128_offset(rit, k8 * 8)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    *reinterpret_cast<uint4*>(base + rit * (CHUNK_COLS * 2) + k8 * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 

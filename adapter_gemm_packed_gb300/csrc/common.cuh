@@ -96,7 +96,6 @@ struct GemmArgs {
   const WinItem* win;
   const WItem* witems;
   const DevSeg* segs;
-  const uint8_t* img_in;   // staged images read as an operand (FWD/BWD ext, DA/DB)
   uint8_t* img_out;        // staged images written by the epilogue (SHRINK/DH)
   void* out;               // Y / dX (bf16)
   float* hout;             // H / dH (fp32)

@@ -1,0 +1,330 @@
+// Base GEMMs of the packed LoRA layer on CTA pairs (tcgen05 cta_group::2, cluster of 2).
+//
+//   MODE_FWD  Y  = X W + s_i H_i B_i      ([X | Htilde] x [Wt | Bt_all]^T, one accumulator)
+//   MODE_BWD  dX = dY W^T + dH_i A_i^T    ([dY | dHtilde] x [W | A_all]^T, W MN-major from Wt)
+//
+// A pair of CTAs on the two SMs of a TPC computes one 256-token x 256-column tile: each CTA
+// stages its own 128 rows of A and its own 128-row half of B per 64-wide K slice (32 KB) in a
+// 6-deep ring, and the even CTA issues one M=256, N=256 tcgen05.mma per 16-wide K step that
+// reads both CTAs' shared memory and writes each CTA's 128 accumulator lanes.  Against the
+// single-CTA 128x256 tile this halves the B bytes each SM pulls from L2 per FLOP and buys two
+// more pipeline stages (the single-CTA kernel's profile showed the tensor pipe waiting on
+// operands at ~60 % activity with L2 and DRAM far from saturated).
+//
+// Synchronisation: the even CTA's full[s] barrier collects the TMA bytes of both CTAs (the odd
+// CTA's copies signal it through .cta_group::2); the MMA warp's commits are multicast to both
+// CTAs' empty[s] / tfull[a]; both CTAs' epilogue warps arrive on the even CTA's tempty[a].
+// The rank term's K extension is identical for both halves because the planner gives both
+// 128-token tiles of a pair the union of their rank-chunk ranges.
+// Every wait is bounded (mbar_wait); on expiry the CTA records a status code and unwinds.
+#include "common.cuh"
+
+namespace mlora {
+
+namespace {
+
+constexpr int S2 = 6;                         // pipeline stages
+constexpr int A2_BYTES = 128 * BK * 2;        // this CTA's 128 rows of A per stage
+constexpr int B2_BYTES = 128 * BK * 2;        // this CTA's 128-row half of B per stage
+constexpr int SMEM_2SM = S2 * (A2_BYTES + B2_BYTES) + 1024 + 256;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+  return d;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// TMA tile load into this CTA's shared memory whose completion is counted on an mbarrier that
+// may live in the peer CTA (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void umma_pair_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once each) on the barrier at this offset in every CTA of `mask` when all MMAs issued
+// so far by this thread have completed.
+__device__ __forceinline__ void umma_pair_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
+__device__ __forceinline__ void decode_pair(const GemmArgs& g, int item, int& mp, int& n) {
+  const int n_pairs = (g.n_mtiles + 1) >> 1;
+  const int per_group = g.group_m * g.n_tiles_n;
+  const int group = item / per_group;
+  const int first = group * g.group_m;
+  const int gm = min(g.group_m, n_pairs - first);
+  const int in_group = item - group * per_group;
+  mp = first + in_group % gm;
+  n = in_group / gm;
+}
+
+}  // namespace
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+    k_gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmI,
+               const __grid_constant__ GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + S2 * A2_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S2 * B2_BYTES);
+  uint64_t* full = bars;               // [S2]  (even CTA) TMA bytes of both CTAs -> MMA
+  uint64_t* empty = bars + S2;         // [S2]  MMA -> each CTA's producer
+  uint64_t* tfull = bars + 2 * S2;     // [2]   MMA -> each CTA's epilogue
+  uint64_t* tempty = tfull + 2;        // [2]   (even CTA) both epilogues -> MMA
+  uint64_t* done = tempty + 2;         // [1]   (even CTA) MMA drain at teardown
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, n_pairs_grid = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S2; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmE);
+    prefetch_tmap(&tmI);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const unsigned long long tmo = g.timeout_ns;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int item = pair; ok && item < g.n_items; item += n_pairs_grid) {
+        int mp, n;
+        decode_pair(g, item, mp, n);
+        const int tile = 2 * mp + static_cast<int>(rank);
+        const MTile mt = g.mtiles[min(tile, g.n_mtiles - 1)];   // a missing odd tile borrows its partner's
+        const int m0 = tile * BM;
+        const int nh0 = n * BN + static_cast<int>(rank) * 128;   // this CTA's half of the N tile
+        const int nkb = g.kmain + mt.nch;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A2_BYTES + B2_BYTES));
+          const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+          uint8_t* a = sA + stage * A2_BYTES;
+          uint8_t* b = sB + stage * B2_BYTES;
+          if (kb < g.kmain) {
+            tma_load_2d_pair(a, &tmA, bar, kb * BK, m0);
+            if constexpr (MODE == MODE_FWD) {
+              tma_load_2d_pair(b, &tmB, bar, kb * BK, nh0);
+            } else {
+              tma_load_2d_pair(b, &tmB, bar, nh0, kb * BK);
+              tma_load_2d_pair(b + 64 * 64 * 2, &tmB, bar, nh0 + 64, kb * BK);
+            }
+          } else {
+            const int e = kb - g.kmain;
+            tma_load_2d_pair(a, &tmI, bar, 0, (mt.img_off + e) * BM);
+            tma_load_2d_pair(b, &tmE, bar, (mt.q_lo + e) * CHUNK_COLS, nh0);
+          }
+          if (++stage == S2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      const uint32_t idesc_k = idesc_bf16(2 * BM, BN, false, false);
+      const uint32_t idesc_main = idesc_bf16(2 * BM, BN, false, MODE == MODE_BWD);
+      for (int item = pair; ok && item < g.n_items; item += n_pairs_grid) {
+        int mp, n;
+        decode_pair(g, item, mp, n);
+        const int nkb = g.kmain + g.mtiles[min(2 * mp, g.n_mtiles - 1)].nch;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_u32(sA + stage * A2_BYTES);
+          const uint32_t b = smem_u32(sB + stage * B2_BYTES);
+          const bool b_mn = (MODE == MODE_BWD) && kb < g.kmain;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = smem_desc(a + k * 32, 16, 1024);
+            const uint64_t bd = b_mn ? smem_desc(b + k * 2048, 64 * 64 * 2, 1024) : smem_desc(b + k * 32, 16, 1024);
+            umma_pair_bf16(d_tmem, ad, bd, b_mn ? idesc_main : idesc_k, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_pair_commit_mc(&empty[stage], 0x3);
+          if (++stage == S2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_pair_commit_mc(&tfull[acc], 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_pair_commit_mc(done, 0x1);
+      volatile int no_abort = 0;
+      mbar_wait(done, 0, &no_abort, g.err, DEV_ERR_TIMEOUT_TEARDOWN, tmo);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int rit = quarter * 32 + lane;
+    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
+    const int ld = g.ld_out;
+    for (int item = pair; item < g.n_items; item += n_pairs_grid) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, g.err, DEV_ERR_TIMEOUT_EPILOGUE, tmo);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      int mp, n;
+      decode_pair(g, item, mp, n);
+      const long long row = static_cast<long long>(2 * mp + static_cast<int>(rank)) * BM + rit;
+      const int col0 = n * BN;
+      const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+#pragma unroll 1
+      for (int cb = 0; cb < BN; cb += 32) {
+        uint32_t v[32];
+        tmem_ld32(t_acc + cb, v);
+        tmem_ld_wait();
+        const int col = col0 + cb;
+        if (row < g.N && col < ld) {
+          __nv_bfloat16* dst = out + row * ld + col;
+          if (col + 32 <= ld) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+              u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+              u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+              u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+              d4[q] = u;
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+              if (col + u < ld) dst[u] = __float2bfloat16_rn(__uint_as_float(v[u]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(acc ? tempty_leader1 : tempty_leader0);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  if (*abort_flag) {
+    // Give copies already issued by this CTA time to land before its shared memory goes away.
+    const unsigned long long t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 50000ull) {
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_gemm_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmE,
+                            const CUtensorMap& tmI, const GemmArgs& g, int n_pairs, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_2sm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_2SM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (g.n_items <= 0) return cudaSuccess;
+  k_gemm_2sm<MODE><<<2 * n_pairs, GEMM_THREADS, SMEM_2SM, stream>>>(tmA, tmB, tmE, tmI, g);
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_gemm_2sm<MODE_FWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                               const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+template cudaError_t launch_gemm_2sm<MODE_BWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                               const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+
+}  // namespace mlora

@@ -16,14 +16,15 @@
 // The packed rank space: job i owns columns [c_i, c_i + rp_i) (rp_i = r_i rounded up to 16),
 // cut into 64-column chunks.  A 128-token tile that covers jobs i1..im needs only the chunks
 // spanning their windows.  Htilde / dHtilde are kept as "staged images": for each (tile,
-// chunk) a [128 x 64] bf16 block already in the 128B-swizzled smem layout, holding s_j H_j
-// (resp. dH_j) in the rows of job j and the columns of job j, and zero everywhere else.  The
+// chunk) a row-major [128 x 64] bf16 block (TMA applies the 128B swizzle on the way into shared
+// memory), holding s_j H_j (resp. dH_j) in the rows of job j and the columns of job j, and zero
+// everywhere else.  The
 // zeros make the rank-term K extension of FWD/BWD and the token reductions of DA/DB exact
 // per job without masks in the main loop (tLoRA's "adaptively reconstructed low-rank tiles",
 // read as tiles assembled from the jobs a token tile happens to cover).
 //
 // Roles (192 threads, one CTA per SM, persistent over a static work list):
-//   warp 0     TMA / bulk-copy producer (one lane) into a STAGES-deep smem ring
+//   warp 0     TMA producer (one lane) into a STAGES-deep smem ring
 //   warp 1     TMEM allocator and MMA issuer (one lane), two 256-column accumulators
 //   warps 2-5  epilogue: TMEM -> registers -> global (lane quarter = warp id % 4)
 // Every wait is bounded (see mbar_wait): on expiry the CTA records a status code, drains
@@ -73,8 +74,8 @@ __device__ __forceinline__ int item_ncols(const GemmArgs& g, int item) {
 // ------------------------------------------------------------------- producer (one thread)
 template <int MODE>
 __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                               const CUtensorMap* tmE, int item, int kb, uint8_t* sA,
-                                               uint8_t* sB, uint64_t* full) {
+                                               const CUtensorMap* tmE, const CUtensorMap* tmI, int item, int kb,
+                                               uint8_t* sA, uint8_t* sB, uint64_t* full) {
   if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
     int m, n;
     decode_mn(g, item, m, n);
@@ -93,7 +94,7 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
     } else {
       const MTile mt = g.mtiles[m];
       const int e = kb - g.kmain;
-      bulk_load(sA, g.img_in + static_cast<size_t>(mt.img_off + e) * IMG_BYTES, IMG_BYTES, full);
+      tma_load_2d(sA, tmI, full, 0, (mt.img_off + e) * BM);          // staged image, [128 x 64]
       tma_load_2d(sB, tmE, full, (mt.q_lo + e) * CHUNK_COLS, n0);
     }
   } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
@@ -112,11 +113,9 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
     // X (dA) or dY (dB) as an MN-major operand: 64 hidden columns x 64 tokens per box.
     tma_load_2d(sA, tmA, full, w.row0, gh * 64);
     tma_load_2d(sA + 64 * 64 * 2, tmA, full, w.row0 + 64, gh * 64);
-    for (int j = 0; j < w.nq; ++j) {
-      const uint8_t* src = g.img_in + static_cast<size_t>(mt.img_off + w.q0 + j - mt.q_lo) * IMG_BYTES +
-                           h * (IMG_BYTES / 2);
-      bulk_load(sB + j * (IMG_BYTES / 2), src, IMG_BYTES / 2, full);
-    }
+    // staged images as an MN-major operand: 64 rank columns x 64 tokens per box
+    for (int j = 0; j < w.nq; ++j)
+      tma_load_2d(sB + j * (IMG_BYTES / 2), tmI, full, 0, (mt.img_off + w.q0 + j - mt.q_lo) * BM + h * 64);
   }
 }
 
@@ -188,7 +187,9 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
             d4[q] = u;
           }
         } else {
-          for (int u = 0; u < 32 && col + u < ld; ++u) dst[u] = __float2bfloat16_rn(__uint_as_float(v[u]));
+#pragma unroll
+          for (int u = 0; u < 32; ++u)
+            if (col + u < ld) dst[u] = __float2bfloat16_rn(__uint_as_float(v[u]));
         }
       }
     }
@@ -230,11 +231,10 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
           if (in1) g.hout[hbase + c1] = (MODE == MODE_SHRINK) ? a1 : s * a1;
           pk[u / 2] = pack_bf16x2(in0 ? s * a0 : 0.f, in1 ? s * a1 : 0.f);
         }
+        uint4* dst = reinterpret_cast<uint4*>(img + rit * (CHUNK_COLS * 2) + half * 64);
 #pragma unroll
-        for (int k16 = 0; k16 < 4; ++k16) {
-          const uint32_t off = swz128_offset(static_cast<uint32_t>(rit), static_cast<uint32_t>(half * 32 + k16 * 8));
-          *reinterpret_cast<uint4*>(img + off) = make_uint4(pk[4 * k16], pk[4 * k16 + 1], pk[4 * k16 + 2], pk[4 * k16 + 3]);
-        }
+        for (int k16 = 0; k16 < 4; ++k16)
+          dst[k16] = make_uint4(pk[4 * k16], pk[4 * k16 + 1], pk[4 * k16 + 2], pk[4 * k16 + 3]);
       }
     }
   } else {
@@ -272,7 +272,8 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
 template <int MODE>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_seg_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmE, const __grid_constant__ GemmArgs g) {
+               const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmI,
+               const __grid_constant__ GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -303,6 +304,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmE);
+    prefetch_tmap(&tmI);
   }
   if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
@@ -324,7 +326,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
-          produce_kblock<MODE>(g, &tmA, &tmB, &tmE, item, kb, sA + stage * A_STAGE_BYTES,
+          produce_kblock<MODE>(g, &tmA, &tmB, &tmE, &tmI, item, kb, sA + stage * A_STAGE_BYTES,
                                sB + stage * B_STAGE_BYTES, &full[stage]);
           ++issued;
           if (++stage == STAGES) {
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 // Host-side launch helper (one per mode).
 template <int MODE>
 cudaError_t launch_seg_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmE,
-                            const GemmArgs& g, int grid, cudaStream_t stream) {
+                            const CUtensorMap& tmI, const GemmArgs& g, int grid, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(k_seg_gemm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
@@ -427,21 +429,21 @@ cudaError_t launch_seg_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
     attr_set = true;
   }
   if (g.n_items <= 0) return cudaSuccess;
-  k_seg_gemm<MODE><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(tmA, tmB, tmE, g);
+  k_seg_gemm<MODE><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(tmA, tmB, tmE, tmI, g);
   return cudaGetLastError();
 }
 
 template cudaError_t launch_seg_gemm<MODE_FWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                               const GemmArgs&, int, cudaStream_t);
+                                               const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_seg_gemm<MODE_BWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                               const GemmArgs&, int, cudaStream_t);
+                                               const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_seg_gemm<MODE_SHRINK>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                                  const GemmArgs&, int, cudaStream_t);
+                                                const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_seg_gemm<MODE_DH>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                              const GemmArgs&, int, cudaStream_t);
+                                                const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_seg_gemm<MODE_DA>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                              const GemmArgs&, int, cudaStream_t);
+                                                const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_seg_gemm<MODE_DB>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                              const GemmArgs&, int, cudaStream_t);
+                                                const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 
 }  // namespace mlora

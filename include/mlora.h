@@ -67,6 +67,8 @@ typedef enum mlora_dtype {
 #define MLORA_PLAN_HOST_ONLY 1u        /* build and validate the tables on the host only: no CUDA call,
                                           the plan can be inspected but not executed */
 #define MLORA_DEBUG_SHORT_TIMEOUT 2u   /* device waits give up after ~1 ms instead of ~4 s */
+#define MLORA_GEMM_SINGLE_CTA 4u       /* run the two base GEMMs on single-CTA 128x256 tiles instead of
+                                          CTA pairs (256x256 tiles); same results up to rounding order */
 
 /* One job of the pack.  Pointers are device pointers to fp32 buffers of the
  * shapes given above, each 16-byte aligned.  dAt/dBt are overwritten (not

@@ -48,12 +48,16 @@ SMALL_BF16 = {
 }
 
 
+ENGINES = {"cta_pairs": 0, "single_cta": M.MLORA_GEMM_SINGLE_CTA}
+
+
+@pytest.mark.parametrize("engine", sorted(ENGINES))
 @pytest.mark.parametrize("name", sorted(SMALL_BF16))
-def test_bf16_small(name):
+def test_bf16_small(name, engine):
     cfg = SMALL_BF16[name]
     wl = W.custom(f"small_{name}", 900 + sorted(SMALL_BF16).index(name), cfg["d_in"], cfg["d_out"], cfg["ranks"],
                   cfg["n_tokens"], dtype="bf16", w_std=0.05, b_std=0.05)
-    _run(wl)
+    _run(wl, flags=ENGINES[engine])
 
 
 def test_bf16_zero_base_weight_isolates_rank_term():

@@ -81,7 +81,8 @@ def test_planner_tables(name):
         assert cols[i, 0] == c and cols[i, 1] % 16 == 0 and r <= cols[i, 1] < r + 16
         c += cols[i, 1]
     assert summ["C_total"] == c and summ["n_chunks"] == -(-c // 64)
-    # token tiles: every row covered once, and the tile's job range is exactly the jobs it touches
+    # token tiles: every row covered once, and the tile's job range is exactly the jobs it touches;
+    # its staged chunk range is the union over its 256-token pair (the CTA-pair GEMM tile)
     assert summ["n_mtiles"] == -(-N // 128) == len(mt)
     seg_of = np.repeat(np.arange(len(ns)), ns)
     img = 0
@@ -90,8 +91,11 @@ def test_planner_tables(name):
         jobs = np.unique(seg_of[rows])
         f, l, q_lo, nch, img_off = mt[t]
         assert (f, l) == (jobs[0], jobs[-1])
-        lo, hi = cols[f, 0], cols[l, 0] + cols[l, 1]
+        prow = np.arange(256 * (t // 2), min(N, 256 * (t // 2) + 256))
+        pj = np.unique(seg_of[prow])
+        lo, hi = cols[pj[0], 0], cols[pj[-1], 0] + cols[pj[-1], 1]
         assert q_lo == lo // 64 and q_lo + nch == -(-hi // 64)
+        assert q_lo <= cols[f, 0] // 64 and -(-(cols[l, 0] + cols[l, 1]) // 64) <= q_lo + nch
         assert img_off == img
         img += nch
     assert summ["n_images"] == img
