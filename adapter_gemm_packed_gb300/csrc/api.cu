@@ -8,8 +8,8 @@
 // one packed rank space (windows padded to 16 columns, cut into 64-column chunks), maps each
 // 128-token tile to the jobs and chunks it covers, and builds one static work list per kernel:
 //   * base GEMMs: (token tile x 256 output columns), rastered in groups of M tiles for L2 reuse;
-//   * shrink / dH: (token tile, <= 4 chunks of its window);
-//   * dA / dB: (128-row block of d_in / d_out, job, <= 4 chunks), sorted longest-first so the
+//   * shrink / dH: (token tile, <= 2 chunks of its window);
+//   * dA / dB: (128-row block of d_in / d_out, job, <= 2 chunks), sorted longest-first so the
 //     persistent grid's round-robin assignment balances uneven jobs.
 #include <algorithm>
 #include <cmath>
@@ -278,7 +278,8 @@ void build_tables(mlora_plan_t* P) {
   P->win.clear();
   for (int t = 0; t < P->n_mtiles; ++t) {
     const MTile& m = P->mtiles[t];
-    for (int q = 0; q < m.nch; q += 4) P->win.push_back(WinItem{t, m.q_lo + q, std::min(4, m.nch - q), 0});
+    for (int q = 0; q < m.nch; q += MAX_ITEM_CHUNKS)
+      P->win.push_back(WinItem{t, m.q_lo + q, std::min(MAX_ITEM_CHUNKS, m.nch - q), 0});
   }
 
   // dA / dB work: (row block, job, <= 4 chunks), longest first
@@ -289,8 +290,9 @@ void build_tables(mlora_plan_t* P) {
       const int ga = static_cast<int>(d.off / 64);
       const int gb = static_cast<int>((d.off + d.n + 63) / 64);
       const int qa = d.c / CHUNK_COLS, qb = (d.c + d.rp + CHUNK_COLS - 1) / CHUNK_COLS;
-      for (int q = qa; q < qb; q += 4)
-        for (int r0 = 0; r0 < rows; r0 += BM) v.push_back(WItem{r0, i, ga, gb, q, std::min(4, qb - q), 0, 0});
+      for (int q = qa; q < qb; q += MAX_ITEM_CHUNKS)
+        for (int r0 = 0; r0 < rows; r0 += BM)
+          v.push_back(WItem{r0, i, ga, gb, q, std::min(MAX_ITEM_CHUNKS, qb - q), 0, 0});
     }
     std::stable_sort(v.begin(), v.end(), [](const WItem& a, const WItem& b) {
       return static_cast<long long>(a.gb - a.ga) * (16 + a.nq) > static_cast<long long>(b.gb - b.ga) * (16 + b.nq);

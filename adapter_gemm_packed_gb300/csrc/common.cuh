@@ -20,7 +20,6 @@ namespace mlora {
 constexpr int BM = 128;              // MMA M (rows of the accumulator = TMEM lanes)
 constexpr int BN = 256;              // max MMA N (accumulator columns per buffer)
 constexpr int BK = 64;               // K slice per pipeline stage (64 bf16 = 128 bytes)
-constexpr int STAGES = 4;            // smem pipeline depth
 constexpr int A_STAGE_BYTES = BM * BK * 2;       // 16 KB
 constexpr int B_STAGE_BYTES = BN * BK * 2;       // 32 KB
 constexpr int CHUNK_COLS = 64;       // rank-window chunk: 64 packed rank columns
@@ -28,7 +27,7 @@ constexpr int IMG_BYTES = BM * CHUNK_COLS * 2;   // one staged [128 x 64] bf16 i
 constexpr int RANK_PAD = 16;         // each job's rank window is padded to a multiple of 16
 constexpr int GEMM_THREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int TMEM_COLS = 512;       // two 256-column fp32 accumulators
-constexpr int GEMM_SMEM_BYTES = STAGES * (A_STAGE_BYTES + B_STAGE_BYTES) + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int MAX_ITEM_CHUNKS = 2;  // rank chunks per shrink / dH / dA / dB work item (N <= 128)
 
 enum GemmMode : int {
   MODE_FWD = 0,     // Y  = X  Wt^T + Htilde  Bt_all^T          (rank term as extra K slices)
@@ -63,13 +62,13 @@ struct MTile {
   int pad0, pad1, pad2;
 };
 
-// Rank-window work item (shrink / dH): one tile, up to 4 chunks (N <= 256).
+// Rank-window work item (shrink / dH): one tile, up to MAX_ITEM_CHUNKS chunks.
 struct WinItem {
   int tile, q0, nq, pad0;
 };
 
 // Weight-gradient work item (dA / dB): one 128-row block of d_in (dA) or d_out (dB), one
-// job, its 64-token half-tiles [ga, gb), chunks [q0, q0 + nq) of its rank window.
+// job, its 64-token half-tiles [ga, gb), chunks [q0, q0 + nq) of its rank window (nq <= MAX_ITEM_CHUNKS).
 struct WItem {
   int row0, seg, ga, gb, q0, nq, pad0, pad1;
 };

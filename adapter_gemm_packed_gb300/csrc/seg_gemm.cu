@@ -35,6 +35,19 @@ namespace mlora {
 
 namespace {
 
+// Shared-memory ring geometry per mode.  The tensor-bound single-CTA base GEMMs stage 16 KB of
+// A and 32 KB of B per K slice (4 stages); the memory-bound modes stage 16 KB of A and at most
+// 16 KB of B (work items carry at most two rank chunks), so six stages keep ~192 KB of loads
+// in flight per SM.
+template <int MODE>
+struct Ring {
+  static constexpr bool kBase = MODE == MODE_FWD || MODE == MODE_BWD;
+  static constexpr int kStages = kBase ? 4 : 6;
+  static constexpr int kABytes = A_STAGE_BYTES;
+  static constexpr int kBBytes = kBase ? B_STAGE_BYTES : 2 * CHUNK_COLS * BK * 2;
+  static constexpr int kSmem = kStages * (kABytes + kBBytes) + 1024 + 256;
+};
+
 __device__ __forceinline__ void decode_mn(const GemmArgs& g, int item, int& m, int& n) {
   const int per_group = g.group_m * g.n_tiles_n;
   const int group = item / per_group;
@@ -274,11 +287,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_seg_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmI,
                const __grid_constant__ GemmArgs g) {
+  constexpr int STAGES = Ring<MODE>::kStages;
+  constexpr int A_BYTES = Ring<MODE>::kABytes;
+  constexpr int B_BYTES = Ring<MODE>::kBBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_STAGE_BYTES);
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
   uint64_t* full = bars;                 // [STAGES]  TMA -> MMA
   uint64_t* empty = bars + STAGES;       // [STAGES]  MMA -> TMA
   uint64_t* tfull = bars + 2 * STAGES;   // [2]       MMA -> epilogue
@@ -326,8 +342,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
-          produce_kblock<MODE>(g, &tmA, &tmB, &tmE, &tmI, item, kb, sA + stage * A_STAGE_BYTES,
-                               sB + stage * B_STAGE_BYTES, &full[stage]);
+          produce_kblock<MODE>(g, &tmA, &tmB, &tmE, &tmI, item, kb, sA + stage * A_BYTES, sB + stage * B_BYTES,
+                               &full[stage]);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -370,8 +386,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          mma_kblock<MODE>(g, item, kb, smem_u32(sA + stage * A_STAGE_BYTES), smem_u32(sB + stage * B_STAGE_BYTES),
-                           d_tmem, ncols);
+          mma_kblock<MODE>(g, item, kb, smem_u32(sA + stage * A_BYTES), smem_u32(sB + stage * B_BYTES), d_tmem,
+                           ncols);
           umma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
@@ -424,12 +440,13 @@ cudaError_t launch_seg_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
                             const CUtensorMap& tmI, const GemmArgs& g, int grid, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_seg_gemm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM_BYTES);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_seg_gemm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<MODE>::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (g.n_items <= 0) return cudaSuccess;
-  k_seg_gemm<MODE><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, stream>>>(tmA, tmB, tmE, tmI, g);
+  k_seg_gemm<MODE><<<grid, GEMM_THREADS, Ring<MODE>::kSmem, stream>>>(tmA, tmB, tmE, tmI, g);
   return cudaGetLastError();
 }
 

@@ -84,7 +84,7 @@ def kernel_bytes(wl, kernel):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while running."""
+    """nvidia-smi clock / throttle samples every 50 ms while running."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
@@ -99,7 +99,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -175,7 +175,13 @@ def run_reference(args, wl, rank):
         return
     from adapter_gemm_packed_gb300 import workloads as W
     T = W.materialise(wl)
-    per_job = args.ref_tokens_per_job
+    # size each step's sample so the whole run stays near --ref-budget-s seconds
+    X, Wm, dY, segs, ntok = oracle_sample(wl, T, 8)
+    t0 = time.perf_counter()
+    oracle_step(wl, X, Wm, dY, segs, {}, 1)
+    per_tok = (time.perf_counter() - t0) / ntok
+    budget = args.ref_budget_s / max(1, args.steps + args.warmup)
+    per_job = int(max(1, min(args.ref_tokens_per_job, budget / per_tok / wl.n_adapters)))
     X, Wm, dY, segs, ntok = oracle_sample(wl, T, per_job)
     state = {}
     for t in range(1, args.warmup + 1):
@@ -335,10 +341,18 @@ def run_ours(args, wl, rank, world, local_rank):
             v["gbs"] = b / (v["ms_per_launch"] * 1e-3) / 1e9
     dom = max(("fwd_gemm", "bwd_gemm"), key=lambda k: kernels.get(k, {}).get("ms_per_launch", 0))
     dk = kernels[dom]
-    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    # The burst figure is the larger (stricter) denominator; the sustained one is what a
+    # seconds-long power-capped loop reaches and is reported beside it.
+    peak = peaks.get("bf16_tflops")
+    sust = peaks.get("bf16_tflops_sustained")
     roof = {"kernel": dom, "bound": "tensor", "achieved": dk["tflops"], "peak": peak, "unit": "TFLOP/s",
-            "frac": dk["tflops"] / peak, "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step loop)",
+            "frac": dk["tflops"] / peak, "peak_source": f"{peak_src} bf16_tflops (burst cuBLAS GEMM)",
+            "frac_of_sustained": (dk["tflops"] / sust) if sust else None,
             "traffic": traffic_record(dom)}
+    hbm = peaks.get("hbm_gbs")
+    for k in ("shrink", "dH", "dA", "dB", "adamw"):
+        if k in kernels and "gbs" in kernels[k]:
+            kernels[k]["frac_of_hbm"] = kernels[k]["gbs"] / hbm
     value = wl.N * world * args.steps / (ms / 1e3)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -367,14 +381,15 @@ def run_ours(args, wl, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qproj")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens-per-job", type=int, default=64)
+    ap.add_argument("--ref-budget-s", type=float, default=90.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
