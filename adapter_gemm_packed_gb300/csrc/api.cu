@@ -32,11 +32,10 @@ template <int MODE>
 cudaError_t launch_gemm_2sm(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                             const GemmArgs&, int, cudaStream_t);
 cudaError_t launch_pack_fwd(const DevSeg*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, int,
-                            cudaStream_t);
-cudaError_t launch_pack_bwd(const DevSeg*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, cudaStream_t);
+                            cudaStream_t, bool);
 cudaError_t launch_h_images(const DevSeg*, const MTile*, const int*, int, long long, const float*, uint8_t*,
-                            cudaStream_t);
-cudaError_t launch_adamw(const AdamItem*, int, float, float, float, float, float, int, int, cudaStream_t);
+                            cudaStream_t, bool);
+cudaError_t launch_adamw(const AdamItem*, int, float, float, float, float, float, int, int, cudaStream_t, bool);
 cudaError_t launch_f32_forward(const DevSeg*, int, long long, int, int, long long, const float*, const float*, float*,
                                float*, cudaStream_t);
 cudaError_t launch_f32_backward(const DevSeg*, int, long long, int, int, long long, int, const float*, const float*,
@@ -133,6 +132,7 @@ struct mlora_plan_s {
   AdamItem* d_adam = nullptr;
   int* d_err = nullptr;
   unsigned long long timeout_ns = DEFAULT_TIMEOUT_NS;
+  bool pdl = true;
   // optional per-kernel timing with CUDA events recorded on the launching stream
   bool profiling = false;
   std::vector<cudaEvent_t> ev_pool;
@@ -323,7 +323,8 @@ void build_tables(mlora_plan_t* P) {
     }
   }
 
-  // workspace: bf16 shadows (forward and backward use the same region), then the two image sets
+  // workspace: the two bf16 shadows At_all, Bt_all (rebuilt by every forward and backward call),
+  // then the two image sets
   if (pr.dtype == MLORA_BF16) {
     const size_t shadow = round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024) +
                           round_up(static_cast<size_t>(P->C_total) * pr.d_out * 2, 1024);
@@ -389,7 +390,7 @@ const char* const kKernelNames[K_COUNT] = {
     "pack_fwd", "shrink", "fwd_gemm", "pack_bwd", "h_images", "dH", "dB", "bwd_gemm", "dA", "adamw",
     "f32_forward", "f32_backward"};
 // kernels launched by each id (a pack step is two kernels, the fp32 passes several)
-const int kKernelLaunches[K_COUNT] = {2, 1, 1, 2, 1, 1, 1, 1, 1, 1, 2, 4};
+const int kKernelLaunches[K_COUNT] = {2, 1, 1, 2, 1, 1, 1, 1, 1, 1, 2, 4};   // pack steps are two kernels
 
 long long g_launches = 0;
 
@@ -433,6 +434,7 @@ GemmArgs base_args(const mlora_plan_t* P) {
   g.segs = P->d_segs;
   g.err = P->d_err;
   g.timeout_ns = P->timeout_ns;
+  g.pdl = P->pdl ? 1 : 0;
   return g;
 }
 
@@ -464,6 +466,7 @@ mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs,
   P->n_segs = n_segs;
   P->user.assign(segs, segs + n_segs);
   if (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT) P->timeout_ns = SHORT_TIMEOUT_NS;
+  if (problem->flags & MLORA_NO_OVERLAP) P->pdl = false;
   build_tables(P);
   if (!(problem->flags & MLORA_PLAN_HOST_ONLY)) {
     st = upload(P);
@@ -510,7 +513,7 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
       reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow + round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024));
   uint8_t* himg = ws + P->off_himg;
 
-  e = timed(P, K_PACK_FWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s); });
+  e = timed(P, K_PACK_FWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
 
   const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
@@ -568,24 +571,26 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return fail(MLORA_ERR_INVALID, "workspace must be a 256-byte aligned device buffer");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  __nv_bfloat16* a_all = reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow);
-  __nv_bfloat16* b_all =
+  __nv_bfloat16* at_all = reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow);
+  __nv_bfloat16* bt_all =
       reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow + round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024));
   uint8_t* himg = ws + P->off_himg;
   uint8_t* dhimg = ws + P->off_dhimg;
 
-  e = timed(P, K_PACK_BWD, s, [&] { return launch_pack_bwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, a_all, b_all, s); });
+  // The backward reads the same two bf16 shadows as the forward, At_all [C, d_in] and
+  // Bt_all [d_out, C], as MN-major operands.
+  e = timed(P, K_PACK_BWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
-  e = timed(P, K_H_IMAGES, s, [&] { return launch_h_images(P->d_segs, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s); });
+  e = timed(P, K_H_IMAGES, s, [&] { return launch_h_images(P->d_segs, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s, P->pdl); });
   if (e != cudaSuccess) return cuda_fail(e, "image launch");
 
   const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
-  CUtensorMap mdY, mdYt, mB, mWmn, mA, mXt, mHi, mdHi, mdHi64;
+  CUtensorMap mdY, mdYt, mBt64, mWmn, mAt64, mXt, mHi, mdHi, mdHi64;
   if ((st = make_map(&mdY, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 128)) != MLORA_OK) return st;
   if ((st = make_map(&mdYt, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 64)) != MLORA_OK) return st;
-  if ((st = make_map(&mB, b_all, pr.d_out, P->C_total, pr.d_out, 64, 64)) != MLORA_OK) return st;
+  if ((st = make_map(&mBt64, bt_all, P->C_total, pr.d_out, P->C_total, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mWmn, Wt, pr.d_in, pr.d_out, pr.d_in, 64, 64)) != MLORA_OK) return st;
-  if ((st = make_map(&mA, a_all, P->C_total, pr.d_in, P->C_total, 64, pairs ? 128 : 256)) != MLORA_OK) return st;
+  if ((st = make_map(&mAt64, at_all, pr.d_in, P->C_total, pr.d_in, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mXt, X, pr.d_in, pr.n_tokens, pr.d_in, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mHi, himg, CHUNK_COLS, P->n_images * BM, CHUNK_COLS, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mdHi, dhimg, CHUNK_COLS, P->n_images * BM, CHUNK_COLS, 64, 128)) != MLORA_OK) return st;
@@ -597,7 +602,7 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   g.n_items = static_cast<int>(P->win.size());
   g.img_out = dhimg;
   g.hout = dH;
-  e = timed(P, K_DH, s, [&] { return launch_seg_gemm<MODE_DH>(mdY, mB, mB, mdY, g, grid_of(P, g.n_items), s); });
+  e = timed(P, K_DH, s, [&] { return launch_seg_gemm<MODE_DH>(mdY, mBt64, mBt64, mdY, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "dH launch");
 
   // dB = Htilde^T dY
@@ -616,11 +621,11 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   if (pairs) {
     g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
     e = timed(P, K_BWD_GEMM, s, [&] {
-      return launch_gemm_2sm<MODE_BWD>(mdY, mWmn, mA, mdHi, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
+      return launch_gemm_2sm<MODE_BWD>(mdY, mWmn, mAt64, mdHi, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
     });
   } else {
     g.n_items = P->n_mtiles * g.n_tiles_n;
-    e = timed(P, K_BWD_GEMM, s, [&] { return launch_seg_gemm<MODE_BWD>(mdY, mWmn, mA, mdHi, g, grid_of(P, g.n_items), s); });
+    e = timed(P, K_BWD_GEMM, s, [&] { return launch_seg_gemm<MODE_BWD>(mdY, mWmn, mAt64, mdHi, g, grid_of(P, g.n_items), s); });
   }
   if (e != cudaSuccess) return cuda_fail(e, "backward GEMM launch");
 
@@ -646,7 +651,7 @@ mlora_status mlora_adamw(const mlora_plan_t* P, float lr, float beta1, float bet
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = timed(P, K_ADAMW, s, [&] {
     return launch_adamw(P->d_adam, static_cast<int>(P->adam.size()), lr, beta1, beta2, eps, weight_decay, step,
-                        P->num_sms, s);
+                        P->num_sms, s, P->pdl);
   });
   return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "AdamW launch");
 }

@@ -1,6 +1,6 @@
 // Memory-bound helper kernels of the packed LoRA layer:
 //  * bf16 shadows of the fp32 adapter masters in the packed rank space (the operands the
-//    tensor-core engine reads through TMA), in the two orientations forward and backward need;
+//    tensor-core engine reads through TMA; the backward reads them MN-major);
 //  * rebuild of the staged Htilde images from the saved activation H (backward);
 //  * the per-adapter AdamW step over every A_i and B_i ("PLoRA: Efficient Concurrent LoRA
 //    Training for Large Language Models", §8: moment, velocity and gradient per parameter;
@@ -14,6 +14,8 @@ namespace {
 // At_all [C_total, d_in] bf16: row c = At_i[c - c_i] for c in job i's window, zero in padding.
 __global__ void k_pack_at(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_in,
                           __nv_bfloat16* __restrict__ at_all) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int d8 = d_in / 8;
   const long long total = static_cast<long long>(C_total) * d8;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -38,6 +40,8 @@ __global__ void k_pack_at(const DevSeg* __restrict__ segs, const int* __restrict
 // Bt_all [d_out, C_total] bf16: Bt_all[o][c] = Bt_i[o][c - c_i] (zero in padding).
 __global__ void k_pack_bt(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_out,
                           __nv_bfloat16* __restrict__ bt_all) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int c8 = C_total / 8;
   const long long total = static_cast<long long>(d_out) * c8;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -61,59 +65,14 @@ __global__ void k_pack_bt(const DevSeg* __restrict__ segs, const int* __restrict
   }
 }
 
-// Transposing packs through shared memory, 32x32 tiles.
-// A_all [d_in, C_total] bf16: A_all[k][c] = At_i[c - c_i][k].
-__global__ void k_pack_a_t(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_in,
-                           __nv_bfloat16* __restrict__ a_all) {
-  __shared__ float tile[32][33];
-  const int c0 = blockIdx.y * 32, k0 = blockIdx.x * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;   // 32 x 8
-  for (int yy = ty; yy < 32; yy += 8) {
-    const int c = c0 + yy, k = k0 + tx;
-    float v = 0.f;
-    if (c < C_total && k < d_in) {
-      const DevSeg& sg = segs[col_seg[c]];
-      const int t = c - sg.c;
-      if (t < sg.r) v = sg.At[static_cast<size_t>(t) * d_in + k];
-    }
-    tile[yy][tx] = v;
-  }
-  __syncthreads();
-  for (int yy = ty; yy < 32; yy += 8) {
-    const int k = k0 + yy, c = c0 + tx;
-    if (k < d_in && c < C_total) a_all[static_cast<size_t>(k) * C_total + c] = __float2bfloat16_rn(tile[tx][yy]);
-  }
-}
-
-// B_all [C_total, d_out] bf16: B_all[c][o] = Bt_i[o][c - c_i].
-__global__ void k_pack_b_t(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_out,
-                           __nv_bfloat16* __restrict__ b_all) {
-  __shared__ float tile[32][33];
-  const int o0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  for (int yy = ty; yy < 32; yy += 8) {
-    const int o = o0 + yy, c = c0 + tx;
-    float v = 0.f;
-    if (o < d_out && c < C_total) {
-      const DevSeg& sg = segs[col_seg[c]];
-      const int t = c - sg.c;
-      if (t < sg.r) v = sg.Bt[static_cast<size_t>(o) * sg.r + t];
-    }
-    tile[yy][tx] = v;
-  }
-  __syncthreads();
-  for (int yy = ty; yy < 32; yy += 8) {
-    const int c = c0 + yy, o = o0 + tx;
-    if (c < C_total && o < d_out) b_all[static_cast<size_t>(c) * d_out + o] = __float2bfloat16_rn(tile[tx][yy]);
-  }
-}
-
 // Staged Htilde images from H (row-major [128 x 64] bf16 blocks):
 // image (tile t, chunk q) row r col u = s_j H_j[row - off_j][64q + u - c_j]
 // when token row (128 t + r) belongs to job j and column 64q+u lies in job j's rank window, else 0.
 __global__ void k_h_images(const DevSeg* __restrict__ segs, const MTile* __restrict__ mtiles,
                            const int* __restrict__ img_tile, long long N, const float* __restrict__ H,
                            uint8_t* __restrict__ img_out) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int img = blockIdx.x;
   const int t = img_tile[img];
   const MTile mt = mtiles[t];
@@ -150,6 +109,8 @@ __global__ void k_h_images(const DevSeg* __restrict__ segs, const MTile* __restr
 // AdamW over a list of <= ADAM_CHUNK-element pieces of every adapter's A and B.
 __global__ void k_adamw(const AdamItem* __restrict__ items, int n_items, float lr, float beta1, float beta2,
                         float eps, float decay, float bc1, float bc2) {
+  griddep_wait();
+  griddep_launch_dependents();
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const AdamItem w = items[it];
     const int n4 = w.count >> 2;
@@ -204,42 +165,32 @@ inline int grid_for(long long work, int threads, int num_sms) {
 }  // namespace
 
 cudaError_t launch_pack_fwd(const DevSeg* segs, const int* col_seg, int C_total, int d_in, int d_out,
-                            __nv_bfloat16* at_all, __nv_bfloat16* bt_all, int num_sms, cudaStream_t st) {
+                            __nv_bfloat16* at_all, __nv_bfloat16* bt_all, int num_sms, cudaStream_t st, bool pdl) {
   const long long w1 = static_cast<long long>(C_total) * (d_in / 8);
-  k_pack_at<<<grid_for(w1, 256, num_sms), 256, 0, st>>>(segs, col_seg, C_total, d_in, at_all);
+  cudaError_t e = launch_k(k_pack_at, dim3(grid_for(w1, 256, num_sms)), dim3(256), 0, st, pdl, segs, col_seg, C_total,
+                           d_in, at_all);
+  if (e != cudaSuccess) return e;
   const long long w2 = static_cast<long long>(d_out) * (C_total / 8);
-  k_pack_bt<<<grid_for(w2, 256, num_sms), 256, 0, st>>>(segs, col_seg, C_total, d_out, bt_all);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_pack_bwd(const DevSeg* segs, const int* col_seg, int C_total, int d_in, int d_out,
-                            __nv_bfloat16* a_all, __nv_bfloat16* b_all, cudaStream_t st) {
-  dim3 blk(32, 8);
-  dim3 g1((d_in + 31) / 32, (C_total + 31) / 32);
-  k_pack_a_t<<<g1, blk, 0, st>>>(segs, col_seg, C_total, d_in, a_all);
-  dim3 g2((d_out + 31) / 32, (C_total + 31) / 32);
-  k_pack_b_t<<<g2, blk, 0, st>>>(segs, col_seg, C_total, d_out, b_all);
-  return cudaGetLastError();
+  return launch_k(k_pack_bt, dim3(grid_for(w2, 256, num_sms)), dim3(256), 0, st, pdl, segs, col_seg, C_total, d_out,
+                  bt_all);
 }
 
 cudaError_t launch_h_images(const DevSeg* segs, const MTile* mtiles, const int* img_tile, int n_images, long long N,
-                            const float* H, uint8_t* img_out, cudaStream_t st) {
+                            const float* H, uint8_t* img_out, cudaStream_t st, bool pdl) {
   if (n_images <= 0) return cudaSuccess;
-  k_h_images<<<n_images, BM, 0, st>>>(segs, mtiles, img_tile, N, H, img_out);
-  return cudaGetLastError();
+  return launch_k(k_h_images, dim3(n_images), dim3(BM), 0, st, pdl, segs, mtiles, img_tile, N, H, img_out);
 }
 
 cudaError_t launch_adamw(const AdamItem* items, int n_items, float lr, float beta1, float beta2, float eps,
-                         float weight_decay, int step, int num_sms, cudaStream_t st) {
+                         float weight_decay, int step, int num_sms, cudaStream_t st, bool pdl) {
   if (n_items <= 0) return cudaSuccess;
   const double bc1 = 1.0 - pow(static_cast<double>(beta1), step);
   const double bc2 = 1.0 - pow(static_cast<double>(beta2), step);
   const float decay = 1.0f - lr * weight_decay;
   int grid = n_items;
   if (grid > num_sms * 16) grid = num_sms * 16;
-  k_adamw<<<grid, 512, 0, st>>>(items, n_items, lr, beta1, beta2, eps, decay, static_cast<float>(bc1),
-                                static_cast<float>(bc2));
-  return cudaGetLastError();
+  return launch_k(k_adamw, dim3(grid), dim3(512), 0, st, pdl, items, n_items, lr, beta1, beta2, eps, decay,
+                  static_cast<float>(bc1), static_cast<float>(bc2));
 }
 
 }  // namespace mlora

@@ -1,7 +1,8 @@
 // Base GEMMs of the packed LoRA layer on CTA pairs (tcgen05 cta_group::2, cluster of 2).
 //
 //   MODE_FWD  Y  = X W + s_i H_i B_i      ([X | Htilde] x [Wt | Bt_all]^T, one accumulator)
-//   MODE_BWD  dX = dY W^T + dH_i A_i^T    ([dY | dHtilde] x [W | A_all]^T, W MN-major from Wt)
+//   MODE_BWD  dX = dY W^T + dH_i A_i^T    ([dY | dHtilde] x [W | A]^T, W and A read MN-major from
+//                                         Wt and At_all)
 //
 // A pair of CTAs on the two SMs of a TPC computes one 256-token x 256-column tile: each CTA
 // stages its own 128 rows of A and its own 128-row half of B per 64-wide K slice (32 KB) in a
@@ -148,6 +149,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const unsigned long long tmo = g.timeout_ns;
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -182,7 +185,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           } else {
             const int e = kb - g.kmain;
             tma_load_2d_pair(a, &tmI, bar, 0, (mt.img_off + e) * BM);
-            tma_load_2d_pair(b, &tmE, bar, (mt.q_lo + e) * CHUNK_COLS, nh0);
+            if constexpr (MODE == MODE_FWD) {
+              tma_load_2d_pair(b, &tmE, bar, (mt.q_lo + e) * CHUNK_COLS, nh0);   // Bt_all rows, K-major
+            } else {   // At_all [C, d_in] as MN-major B (n = d_in index, k = rank column)
+              tma_load_2d_pair(b, &tmE, bar, nh0, (mt.q_lo + e) * CHUNK_COLS);
+              tma_load_2d_pair(b + 64 * 64 * 2, &tmE, bar, nh0 + 64, (mt.q_lo + e) * CHUNK_COLS);
+            }
           }
           if (++stage == S2) {
             stage = 0;
@@ -218,7 +226,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           tc_fence_after();
           const uint32_t a = smem_u32(sA + stage * A2_BYTES);
           const uint32_t b = smem_u32(sB + stage * B2_BYTES);
-          const bool b_mn = (MODE == MODE_BWD) && kb < g.kmain;
+          constexpr bool b_mn = MODE == MODE_BWD;   // W and At_all are both read MN-major
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = smem_desc(a + k * 32, 16, 1024);
@@ -318,8 +326,8 @@ cudaError_t launch_gemm_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
     attr_set = true;
   }
   if (g.n_items <= 0) return cudaSuccess;
-  k_gemm_2sm<MODE><<<2 * n_pairs, GEMM_THREADS, SMEM_2SM, stream>>>(tmA, tmB, tmE, tmI, g);
-  return cudaGetLastError();
+  return launch_k(k_gemm_2sm<MODE>, dim3(2 * n_pairs), dim3(GEMM_THREADS), SMEM_2SM, stream, g.pdl != 0, tmA, tmB,
+                  tmE, tmI, g);
 }
 
 template cudaError_t launch_gemm_2sm<MODE_FWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,

@@ -7,9 +7,10 @@
 //   MODE_FWD    Y  = X W + s_i H_i B_i        base GEMM; the rank term is appended as extra
 //                                              K slices of the same TMEM accumulator
 //                                              ([X | Htilde] x [Wt | Bt_all]^T)
-//   MODE_BWD    dX = dY W^T + dH_i A_i^T      same, W read MN-major straight from Wt
+//   MODE_BWD    dX = dY W^T + dH_i A_i^T      same, W (from Wt) and A (from At_all) read MN-major
 //   MODE_SHRINK H_i = X_i A_i                  per tile, N = the tile's rank window
-//   MODE_DH     dH_i = s_i dY_i B_i^T          per tile, N = the tile's rank window (Case 2)
+//   MODE_DH     dH_i = s_i dY_i B_i^T          per tile, N = the tile's rank window (Case 2),
+//                                              B read MN-major from Bt_all
 //   MODE_DA     dA_i = X_i^T dH_i              token reduction (Case 3)
 //   MODE_DB     dB_i = s_i H_i^T dY_i          token reduction (Case 1)
 //
@@ -108,20 +109,35 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
       const MTile mt = g.mtiles[m];
       const int e = kb - g.kmain;
       tma_load_2d(sA, tmI, full, 0, (mt.img_off + e) * BM);          // staged image, [128 x 64]
-      tma_load_2d(sB, tmE, full, (mt.q_lo + e) * CHUNK_COLS, n0);
+      if constexpr (MODE == MODE_FWD) {
+        tma_load_2d(sB, tmE, full, (mt.q_lo + e) * CHUNK_COLS, n0);  // Bt_all rows, K-major
+      } else {
+        // At_all [C, d_in] as the MN-major B operand (n = d_in index, k = rank column)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tma_load_2d(sB + j * (BK * 64 * 2), tmE, full, n0 + 64 * j, (mt.q_lo + e) * CHUNK_COLS);
+      }
     }
   } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
     const WinItem w = g.win[item];
     const int m0 = w.tile * BM;
+    if (kb + PREFETCH_KB < g.kmain) prefetch_l2_2d(tmA, (kb + PREFETCH_KB) * BK, m0);
     mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (CHUNK_COLS * BK * 2));
     tma_load_2d(sA, tmA, full, kb * BK, m0);
-    for (int j = 0; j < w.nq; ++j)
-      tma_load_2d(sB + j * (CHUNK_COLS * BK * 2), tmB, full, kb * BK, (w.q0 + j) * CHUNK_COLS);
+    for (int j = 0; j < w.nq; ++j) {
+      if constexpr (MODE == MODE_SHRINK)   // At_all rows (K-major, k = d_in)
+        tma_load_2d(sB + j * (CHUNK_COLS * BK * 2), tmB, full, kb * BK, (w.q0 + j) * CHUNK_COLS);
+      else                                 // Bt_all [d_out, C] as MN-major (n = rank column, k = d_out)
+        tma_load_2d(sB + j * (CHUNK_COLS * BK * 2), tmB, full, (w.q0 + j) * CHUNK_COLS, kb * BK);
+    }
   } else {
     const WItem w = g.witems[item];
     const int gh = w.ga + kb;            // 64-token half tile
     const int t = gh >> 1, h = gh & 1;
     const MTile mt = g.mtiles[t];
+    if (gh + PREFETCH_KB < w.gb) {
+      prefetch_l2_2d(tmA, w.row0, (gh + PREFETCH_KB) * 64);
+      prefetch_l2_2d(tmA, w.row0 + 64, (gh + PREFETCH_KB) * 64);
+    }
     mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (IMG_BYTES / 2));
     // X (dA) or dY (dB) as an MN-major operand: 64 hidden columns x 64 tokens per box.
     tma_load_2d(sA, tmA, full, w.row0, gh * 64);
@@ -137,8 +153,7 @@ template <int MODE>
 __device__ __forceinline__ void mma_kblock(const GemmArgs& g, int item, int kb, uint32_t sA, uint32_t sB,
                                            uint32_t d_tmem, int ncols) {
   if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
-    const bool main_part = kb < g.kmain;
-    const bool b_mn = (MODE == MODE_BWD) && main_part;
+    const bool b_mn = MODE == MODE_BWD;   // W and At_all are both read MN-major by the backward
     const uint32_t idesc = idesc_bf16(BM, BN, false, b_mn);
 #pragma unroll
     for (int k = 0; k < BK / 16; ++k) {
@@ -147,11 +162,12 @@ __device__ __forceinline__ void mma_kblock(const GemmArgs& g, int item, int kb, 
       umma_bf16(d_tmem, a, b, idesc, (kb > 0 || k > 0) ? 1u : 0u);
     }
   } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
-    const uint32_t idesc = idesc_bf16(BM, ncols, false, false);
+    constexpr bool b_mn = MODE == MODE_DH;
+    const uint32_t idesc = idesc_bf16(BM, ncols, false, b_mn);
 #pragma unroll
     for (int k = 0; k < BK / 16; ++k) {
-      umma_bf16(d_tmem, smem_desc(sA + k * 32, 16, 1024), smem_desc(sB + k * 32, 16, 1024), idesc,
-                (kb > 0 || k > 0) ? 1u : 0u);
+      const uint64_t b = b_mn ? smem_desc(sB + k * 2048, CHUNK_COLS * BK * 2, 1024) : smem_desc(sB + k * 32, 16, 1024);
+      umma_bf16(d_tmem, smem_desc(sA + k * 32, 16, 1024), b, idesc, (kb > 0 || k > 0) ? 1u : 0u);
     }
   } else {
     const uint32_t idesc = idesc_bf16(BM, ncols, true, true);
@@ -328,6 +344,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const unsigned long long tmo = g.timeout_ns;
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -446,8 +464,8 @@ cudaError_t launch_seg_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
     attr_set = true;
   }
   if (g.n_items <= 0) return cudaSuccess;
-  k_seg_gemm<MODE><<<grid, GEMM_THREADS, Ring<MODE>::kSmem, stream>>>(tmA, tmB, tmE, tmI, g);
-  return cudaGetLastError();
+  return launch_k(k_seg_gemm<MODE>, dim3(grid), dim3(GEMM_THREADS), Ring<MODE>::kSmem, stream, g.pdl != 0, tmA, tmB,
+                  tmE, tmI, g);
 }
 
 template cudaError_t launch_seg_gemm<MODE_FWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,

@@ -67,6 +67,9 @@ typedef enum mlora_dtype {
 #define MLORA_PLAN_HOST_ONLY 1u        /* build and validate the tables on the host only: no CUDA call,
                                           the plan can be inspected but not executed */
 #define MLORA_DEBUG_SHORT_TIMEOUT 2u   /* device waits give up after ~1 ms instead of ~4 s */
+#define MLORA_NO_OVERLAP 8u            /* launch every kernel strictly after the previous one (no programmatic
+                                          dependent launch overlapping a kernel's prologue with the tail of
+                                          the one before); results are identical either way */
 #define MLORA_GEMM_SINGLE_CTA 4u       /* run the two base GEMMs on single-CTA 128x256 tiles instead of
                                           CTA pairs (256x256 tiles); same results up to rounding order */
 

@@ -92,6 +92,23 @@ def test_repeat_calls_are_deterministic():
         r2.close()
 
 
+def test_launch_overlap_does_not_change_results():
+    """Programmatic dependent launch (the default) and strictly serial launches give bitwise
+    identical outputs: every kernel waits for its predecessor before touching memory."""
+    wl = W.custom("overlap", 954, 512, 384, [4, 64, 130], [300, 100, 150], dtype="bf16")
+    T = W.materialise(wl)
+    r1 = G.GpuRun(wl, T, step=True)
+    r2 = G.GpuRun(wl, T, step=True, flags=M.MLORA_NO_OVERLAP)
+    try:
+        for k in ("Y", "dX"):
+            assert np.array_equal(r1.res[k], r2.res[k])
+        for k in ("H", "dH", "dAt", "dBt", "At", "Bt", "mA", "vA", "mB", "vB"):
+            assert all(np.array_equal(a, b) for a, b in zip(r1.res[k], r2.res[k])), k
+    finally:
+        r1.close()
+        r2.close()
+
+
 def test_adamw_isolated_t3():
     """The AdamW kernel alone on seeded gradients and moments (t = 3), so the update
     p' - p itself can be checked: at small t it is close to -lr * sign(g), which would
