@@ -8,8 +8,8 @@
 // one packed rank space (windows padded to 16 columns, cut into 64-column chunks), maps each
 // 128-token tile to the jobs and chunks it covers, and builds one static work list per kernel:
 //   * base GEMMs: (token tile x 256 output columns), rastered in groups of M tiles for L2 reuse;
-//   * shrink / dH: (token tile, <= 2 chunks of its window);
-//   * dA / dB: (128-row block of d_in / d_out, job, <= 2 chunks), sorted longest-first so the
+//   * shrink / dH: (token tile, one 64-column chunk of its window);
+//   * dA / dB: (128-row block of d_in / d_out, job, one chunk), sorted longest-first so the
 //     persistent grid's round-robin assignment balances uneven jobs.
 #include <algorithm>
 #include <cmath>
@@ -290,8 +290,10 @@ void build_tables(mlora_plan_t* P) {
       const int ga = static_cast<int>(d.off / 64);
       const int gb = static_cast<int>((d.off + d.n + 63) / 64);
       const int qa = d.c / CHUNK_COLS, qb = (d.c + d.rp + CHUNK_COLS - 1) / CHUNK_COLS;
-      for (int q = qa; q < qb; q += MAX_ITEM_CHUNKS)
-        for (int r0 = 0; r0 < rows; r0 += BM)
+      // chunks innermost: the items that read the same X / dY block sit side by side in the
+      // list, so the persistent grid runs them concurrently and the block is read from HBM once
+      for (int r0 = 0; r0 < rows; r0 += BM)
+        for (int q = qa; q < qb; q += MAX_ITEM_CHUNKS)
           v.push_back(WItem{r0, i, ga, gb, q, std::min(MAX_ITEM_CHUNKS, qb - q), 0, 0});
     }
     std::stable_sort(v.begin(), v.end(), [](const WItem& a, const WItem& b) {

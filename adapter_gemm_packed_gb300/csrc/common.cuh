@@ -29,8 +29,7 @@ constexpr int IMG_BYTES = BM * CHUNK_COLS * 2;   // one staged [128 x 64] bf16 i
 constexpr int RANK_PAD = 16;         // each job's rank window is padded to a multiple of 16
 constexpr int GEMM_THREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int TMEM_COLS = 512;       // two 256-column fp32 accumulators
-constexpr int PREFETCH_KB = 8;       // memory-bound modes: L2 prefetch distance, in K slices
-constexpr int MAX_ITEM_CHUNKS = 2;  // rank chunks per shrink / dH / dA / dB work item (N <= 128)
+constexpr int MAX_ITEM_CHUNKS = 1;  // rank chunks per shrink / dH / dA / dB work item (N = 64)
 
 enum GemmMode : int {
   MODE_FWD = 0,     // Y  = X  Wt^T + Htilde  Bt_all^T          (rank term as extra K slices)

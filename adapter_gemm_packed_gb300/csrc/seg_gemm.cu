@@ -37,16 +37,20 @@ namespace mlora {
 namespace {
 
 // Shared-memory ring geometry per mode.  The tensor-bound single-CTA base GEMMs stage 16 KB of
-// A and 32 KB of B per K slice (4 stages); the memory-bound modes stage 16 KB of A and at most
-// 16 KB of B (work items carry at most two rank chunks), so six stages keep ~192 KB of loads
-// in flight per SM.
+// A and 32 KB of B per K slice (4 stages).  The memory-bound modes stream one operand from HBM
+// (X or dY, 16 KB per slice) against a small L2-resident one (one 64-column rank chunk, 8 KB):
+// eight stages keep 128 KB of the streamed operand in flight per SM, which is what a GB300
+// needs to keep HBM busy at its loaded latency (a bare TMA streaming loop reaches ~6.9 TB/s
+// with 8 x 16 KB per SM and ~4.4 TB/s with 6 x 16 KB).  dB also gets a 32x33 fp32 transpose
+// tile per epilogue warp for coalesced stores.
 template <int MODE>
 struct Ring {
   static constexpr bool kBase = MODE == MODE_FWD || MODE == MODE_BWD;
-  static constexpr int kStages = kBase ? 4 : 6;
+  static constexpr int kStages = kBase ? 4 : 8;
   static constexpr int kABytes = A_STAGE_BYTES;
-  static constexpr int kBBytes = kBase ? B_STAGE_BYTES : 2 * CHUNK_COLS * BK * 2;
-  static constexpr int kSmem = kStages * (kABytes + kBBytes) + 1024 + 256;
+  static constexpr int kBBytes = kBase ? B_STAGE_BYTES : MAX_ITEM_CHUNKS * CHUNK_COLS * BK * 2;
+  static constexpr int kXpose = MODE == MODE_DB ? 4 * 32 * 33 * 4 : 0;
+  static constexpr int kSmem = kStages * (kABytes + kBBytes) + kXpose + 1024 + 256;
 };
 
 __device__ __forceinline__ void decode_mn(const GemmArgs& g, int item, int& m, int& n) {
@@ -120,7 +124,6 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
   } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
     const WinItem w = g.win[item];
     const int m0 = w.tile * BM;
-    if (kb + PREFETCH_KB < g.kmain) prefetch_l2_2d(tmA, (kb + PREFETCH_KB) * BK, m0);
     mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (CHUNK_COLS * BK * 2));
     tma_load_2d(sA, tmA, full, kb * BK, m0);
     for (int j = 0; j < w.nq; ++j) {
@@ -134,10 +137,6 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
     const int gh = w.ga + kb;            // 64-token half tile
     const int t = gh >> 1, h = gh & 1;
     const MTile mt = g.mtiles[t];
-    if (gh + PREFETCH_KB < w.gb) {
-      prefetch_l2_2d(tmA, w.row0, (gh + PREFETCH_KB) * 64);
-      prefetch_l2_2d(tmA, w.row0 + 64, (gh + PREFETCH_KB) * 64);
-    }
     mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (IMG_BYTES / 2));
     // X (dA) or dY (dB) as an MN-major operand: 64 hidden columns x 64 tokens per box.
     tma_load_2d(sA, tmA, full, w.row0, gh * 64);
@@ -187,7 +186,8 @@ __device__ __forceinline__ int find_seg(const DevSeg* segs, int first, int last,
 }
 
 template <int MODE>
-__device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint32_t t_acc, int quarter, int lane) {
+__device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint32_t t_acc, int quarter, int lane,
+                                              float* xpose) {
   const int rit = quarter * 32 + lane;   // accumulator row owned by this thread
   if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
     int m, n;
@@ -278,17 +278,32 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
         uint32_t v[32];
         tmem_ld32(t_acc + jq * CHUNK_COLS + half * 32, v);
         tmem_ld_wait();
-        if (row < bound) {
-          const int cbase = (w.q0 + jq) * CHUNK_COLS + half * 32 - sg.c;   // rank index of v[0]
+        const int cbase = (w.q0 + jq) * CHUNK_COLS + half * 32 - sg.c;   // rank index of v[0]
+        if constexpr (MODE == MODE_DA) {
+          // dAt_i[t][row]: for a fixed t the 32 lanes write 32 consecutive rows (coalesced)
+          if (row < bound) {
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const int t = cbase + u;
-            if (t >= 0 && t < sg.r) {
-              if constexpr (MODE == MODE_DA)
-                sg.dAt[static_cast<size_t>(t) * g.d_in + row] = __uint_as_float(v[u]);
-              else
-                sg.dBt[static_cast<size_t>(row) * sg.r + t] = __uint_as_float(v[u]);
+            for (int u = 0; u < 32; ++u) {
+              const int t = cbase + u;
+              if (t >= 0 && t < sg.r) sg.dAt[static_cast<size_t>(t) * g.d_in + row] = __uint_as_float(v[u]);
             }
+          }
+        } else {
+          // dBt_i[row][t] is rank-contiguous per row: transpose the warp's 32x32 block through
+          // shared memory so each store instruction covers consecutive addresses.
+          const int ulo = max(0, -cbase), uhi = min(32, sg.r - cbase);
+          if (uhi > ulo) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) xpose[lane * 33 + u] = __uint_as_float(v[u]);
+            __syncwarp();
+            const int wdt = uhi - ulo;
+            const int row_base = w.row0 + quarter * 32;
+            for (int e = lane; e < 32 * wdt; e += 32) {
+              const int rr = e / wdt, u = ulo + e % wdt;
+              if (row_base + rr < bound)
+                sg.dBt[static_cast<size_t>(row_base + rr) * sg.r + cbase + u] = xpose[rr * 33 + u];
+            }
+            __syncwarp();
           }
         }
       }
@@ -310,7 +325,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  float* xpose_all = reinterpret_cast<float*>(sB + STAGES * B_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES + Ring<MODE>::kXpose);
   uint64_t* full = bars;                 // [STAGES]  TMA -> MMA
   uint64_t* empty = bars + STAGES;       // [STAGES]  MMA -> TMA
   uint64_t* tfull = bars + 2 * STAGES;   // [2]       MMA -> epilogue
@@ -435,7 +451,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      epilogue_item<MODE>(g, item, t_acc, quarter, lane);
+      epilogue_item<MODE>(g, item, t_acc, quarter, lane, xpose_all + quarter * 32 * 33);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
