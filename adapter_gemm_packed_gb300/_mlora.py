@@ -24,7 +24,7 @@ MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD
 EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward", "mlora_adamw",
            "mlora_sync_status", "mlora_h_elems", "mlora_plan_describe", "mlora_status_string",
            "mlora_last_error", "mlora_version", "mlora_profile_enable", "mlora_profile_read",
-           "mlora_kernel_name", "mlora_launch_count"]
+           "mlora_kernel_name", "mlora_launch_count", "mlora_forward_static_ws"]
 
 
 class mlora_segment(C.Structure):
@@ -86,6 +86,8 @@ def lib() -> C.CDLL:
         L.mlora_kernel_name.restype = C.c_char_p
         L.mlora_launch_count.argtypes = []
         L.mlora_launch_count.restype = i64
+        L.mlora_forward_static_ws.argtypes = [vp, vp, vp, vp, vp, vp]
+        L.mlora_forward_static_ws.restype = i32
         _lib = L
     return _lib
 
@@ -169,3 +171,8 @@ def mlora_profile_read(plan) -> dict:
 
 def mlora_launch_count() -> int:
     return int(lib().mlora_launch_count())
+
+
+def mlora_forward_static_ws(plan, X, Wt, Y, H, stream) -> None:
+    """Forward pass using the library's static device scratch instead of a caller workspace."""
+    _check(lib().mlora_forward_static_ws(plan, X, Wt, Y, H, stream), "mlora_forward_static_ws")

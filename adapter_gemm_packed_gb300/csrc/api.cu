@@ -48,6 +48,15 @@ namespace {
 
 thread_local std::string g_last_error;
 
+}  // namespace
+
+namespace mlora {
+// Lets other translation units of the library report a message through mlora_last_error().
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace mlora
+
+namespace {
+
 mlora_status fail(mlora_status s, const std::string& msg) {
   g_last_error = msg;
   return s;

@@ -180,6 +180,24 @@ const char* mlora_kernel_name(int32_t id);
 /* Number of CUDA kernels this library has launched in this process so far. */
 int64_t mlora_launch_count(void);
 
+/* Forward pass without a caller workspace, for callers that cannot allocate device memory
+ * when they run the layer (a runtime that forbids cudaMalloc after start-up, a framework whose
+ * memory comes only from its own pools, code running while another thread captures a graph).
+ * The paper has no counterpart; this is a deployment convenience.
+ *
+ * Same arguments and results as mlora_forward, minus `workspace`: the scratch is one static
+ * device array of 64 MiB that the library holds on every GPU it is loaded on until the
+ * process exits.  This call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).  Its first call on a device looks up that array's device address on the current
+ * device (a one-time set-up per device); make that first call before any stream capture.
+ * Plans whose forward needs more scratch than 64 MiB are rejected with MLORA_ERR_UNSUPPORTED
+ * and a message in mlora_last_error(); use mlora_forward for them.  All calls on a device
+ * share the one array and it keeps the last call's contents (nothing in it needs to start at
+ * zero): calls that overlap on the GPU (different streams without ordering between them)
+ * race on it, so order them on one stream or with events. */
+mlora_status mlora_forward_static_ws(const mlora_plan_t* plan, const void* X, const void* Wt, void* Y, float* H,
+                                     void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* mlora_status_string(mlora_status s);
 
