@@ -142,6 +142,7 @@ struct mlora_plan_s {
   int* d_err = nullptr;
   unsigned long long timeout_ns = DEFAULT_TIMEOUT_NS;
   bool pdl = true;
+  bool debug_drop = false;
   // optional per-kernel timing with CUDA events recorded on the launching stream
   bool profiling = false;
   std::vector<cudaEvent_t> ev_pool;
@@ -478,6 +479,8 @@ mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs,
   P->user.assign(segs, segs + n_segs);
   if (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT) P->timeout_ns = SHORT_TIMEOUT_NS;
   if (problem->flags & MLORA_NO_OVERLAP) P->pdl = false;
+  // the copy-withholding test hook is honoured only with the 1 ms wait limit
+  if ((problem->flags & MLORA_DEBUG_DROP_COPY) && (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT)) P->debug_drop = true;
   build_tables(P);
   if (!(problem->flags & MLORA_PLAN_HOST_ONLY)) {
     st = upload(P);
@@ -540,6 +543,7 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
   g.n_items = static_cast<int>(P->win.size());
   g.img_out = himg;
   g.hout = H;
+  g.debug_drop = P->debug_drop ? 1 : 0;
   e = timed(P, K_SHRINK, s, [&] { return launch_seg_gemm<MODE_SHRINK>(mX, mAt, mAt, mX, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "shrink launch");
 

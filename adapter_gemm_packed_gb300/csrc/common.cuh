@@ -104,6 +104,7 @@ struct GemmArgs {
   int* err;                // device status word
   unsigned long long timeout_ns;
   int pdl;                 // launched with programmatic dependent launch
+  int debug_drop;          // test hook: CTA 0 arms its first slot but issues no copy into it
 };
 
 // Status codes written to the device status word (first one wins).

@@ -376,8 +376,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             ok = false;
             break;
           }
-          produce_kblock<MODE>(g, &tmA, &tmB, &tmE, &tmI, item, kb, sA + stage * A_BYTES, sB + stage * B_BYTES,
-                               &full[stage]);
+          if (g.debug_drop && blockIdx.x == 0 && issued == 0) {
+            // Test hook for the timeout path: arm the slot, issue nothing.  The MMA warp's
+            // bounded wait on it runs out and records a status code; nothing faults or hangs.
+            mbar_arrive_expect_tx(&full[stage], A_BYTES);
+          } else {
+            produce_kblock<MODE>(g, &tmA, &tmB, &tmE, &tmI, item, kb, sA + stage * A_BYTES, sB + stage * B_BYTES,
+                                 &full[stage]);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;

@@ -67,6 +67,11 @@ typedef enum mlora_dtype {
 #define MLORA_PLAN_HOST_ONLY 1u        /* build and validate the tables on the host only: no CUDA call,
                                           the plan can be inspected but not executed */
 #define MLORA_DEBUG_SHORT_TIMEOUT 2u   /* device waits give up after ~1 ms instead of ~4 s */
+#define MLORA_DEBUG_DROP_COPY 16u      /* test hook, honoured only with MLORA_DEBUG_SHORT_TIMEOUT: in the
+                                          forward's first tensor-core launch one CTA arms a pipeline slot
+                                          but copies nothing into it, so a device wait runs out (~1 ms),
+                                          the status word records it and mlora_sync_status() returns
+                                          MLORA_ERR_TIMEOUT; that call's outputs are undefined */
 #define MLORA_NO_OVERLAP 8u            /* launch every kernel strictly after the previous one (no programmatic
                                           dependent launch overlapping a kernel's prologue with the tail of
                                           the one before); results are identical either way */

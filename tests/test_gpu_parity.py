@@ -143,3 +143,20 @@ def test_adamw_isolated_t3():
                 assert G.rel_err(v_t.cpu().numpy(), vw) < 1e-6
     finally:
         layer.close()
+
+
+def test_device_wait_timeout_is_reported_and_context_survives():
+    """A bounded device wait that runs out (test hook: a pipeline slot that no copy fills)
+    surfaces as MLORA_ERR_TIMEOUT from mlora_sync_status, and the same process keeps working:
+    a normal plan afterwards computes correct results."""
+    wl = W.custom("timeout", 955, 256, 256, [8, 16], [200, 90], dtype="bf16")
+    T = W.materialise(wl)
+    bad = G.PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, G.scales_of(wl), dtype="bf16", At=T.At, Bt=T.Bt,
+                       flags=M.MLORA_DEBUG_SHORT_TIMEOUT | M.MLORA_DEBUG_DROP_COPY)
+    try:
+        bad.forward(G.to_dev(T.X, "bf16"), G.to_dev(T.Wt, "bf16"))
+        assert bad.sync_status() == M.MLORA_ERR_TIMEOUT
+        assert bad.sync_status() == M.MLORA_OK          # the status word was read and cleared
+    finally:
+        bad.close()
+    _run(wl)                                           # the context is still usable
