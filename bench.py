@@ -216,10 +216,11 @@ def traffic_record(kernel):
         rec = json.load(open(path))
     except Exception:
         return None
-    src = open(os.path.join(ROOT, "adapter_gemm_packed_gb300", "csrc", "seg_gemm.cu"), "rb").read()
-    h = hashlib.sha256(src).hexdigest()[:16]
     r = rec.get(kernel)
-    if not r or r.get("source_sha") != h:
+    if not r:
+        return None
+    src = open(os.path.join(ROOT, r["source"]), "rb").read()
+    if hashlib.sha256(src).hexdigest()[:16] != r.get("source_sha"):
         return None
     return r.get("bytes_per_launch")
 
