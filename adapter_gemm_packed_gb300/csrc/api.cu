@@ -8,8 +8,8 @@
 // one packed rank space (windows padded to 16 columns, cut into 64-column chunks), maps each
 // 128-token tile to the jobs and chunks it covers, and builds one static work list per kernel:
 //   * base GEMMs: (token tile x 256 output columns), rastered in groups of M tiles for L2 reuse;
-//   * shrink / dH: (token tile, one 64-column chunk of its window);
-//   * dA / dB: (128-row block of d_in / d_out, job, one chunk), sorted longest-first so the
+//   * shrink / dH: (token tile, <= 2 64-column chunks of its window);
+//   * dA / dB: (128-row block of d_in / d_out, job, <= 2 chunks), sorted longest-first so the
 //     persistent grid's round-robin assignment balances uneven jobs.
 #include <algorithm>
 #include <cmath>

@@ -29,7 +29,7 @@ constexpr int IMG_BYTES = BM * CHUNK_COLS * 2;   // one staged [128 x 64] bf16 i
 constexpr int RANK_PAD = 16;         // each job's rank window is padded to a multiple of 16
 constexpr int GEMM_THREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int TMEM_COLS = 512;       // two 256-column fp32 accumulators
-constexpr int MAX_ITEM_CHUNKS = 1;  // rank chunks per shrink / dH / dA / dB work item (N = 64)
+constexpr int MAX_ITEM_CHUNKS = 2;  // rank chunks per shrink / dH / dA / dB work item (N <= 128)
 
 enum GemmMode : int {
   MODE_FWD = 0,     // Y  = X  Wt^T + Htilde  Bt_all^T          (rank term as extra K slices)
@@ -182,6 +182,28 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Same, with an L2 cache policy (see l2_policy_*).
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policies: data streamed once (evict first) and small operands re-read by many CTAs (evict last).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // Contiguous bulk copy global -> shared (16-byte aligned, size multiple of 16).

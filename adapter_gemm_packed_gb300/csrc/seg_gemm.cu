@@ -38,15 +38,15 @@ namespace {
 
 // Shared-memory ring geometry per mode.  The tensor-bound single-CTA base GEMMs stage 16 KB of
 // A and 32 KB of B per K slice (4 stages).  The memory-bound modes stream one operand from HBM
-// (X or dY, 16 KB per slice) against a small L2-resident one (one 64-column rank chunk, 8 KB):
-// eight stages keep 128 KB of the streamed operand in flight per SM, which is what a GB300
-// needs to keep HBM busy at its loaded latency (a bare TMA streaming loop reaches ~6.9 TB/s
-// with 8 x 16 KB per SM and ~4.4 TB/s with 6 x 16 KB).  dB also gets a 32x33 fp32 transpose
-// tile per epilogue warp for coalesced stores.
+// (X or dY, 16 KB per slice, loaded with an evict-first L2 policy) against a small operand that
+// many CTAs re-read from L2 (up to two 64-column rank chunks, <= 16 KB, evict-last): six stages
+// keep 96 KB of the streamed operand in flight per SM (a bare TMA streaming loop on a GB300
+// reaches 6.6 TB/s with 4 x 16 KB per SM).  dB also gets a 32x33 fp32 transpose tile per
+// epilogue warp for coalesced stores.
 template <int MODE>
 struct Ring {
   static constexpr bool kBase = MODE == MODE_FWD || MODE == MODE_BWD;
-  static constexpr int kStages = kBase ? 4 : 8;
+  static constexpr int kStages = kBase ? 4 : 6;
   static constexpr int kABytes = A_STAGE_BYTES;
   static constexpr int kBBytes = kBase ? B_STAGE_BYTES : MAX_ITEM_CHUNKS * CHUNK_COLS * BK * 2;
   static constexpr int kXpose = MODE == MODE_DB ? 4 * 32 * 33 * 4 : 0;
@@ -93,7 +93,8 @@ __device__ __forceinline__ int item_ncols(const GemmArgs& g, int item) {
 template <int MODE>
 __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensorMap* tmA, const CUtensorMap* tmB,
                                                const CUtensorMap* tmE, const CUtensorMap* tmI, int item, int kb,
-                                               uint8_t* sA, uint8_t* sB, uint64_t* full) {
+                                               uint8_t* sA, uint8_t* sB, uint64_t* full, uint64_t pol_stream,
+                                               uint64_t pol_keep) {
   if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
     int m, n;
     decode_mn(g, item, m, n);
@@ -125,12 +126,12 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
     const WinItem w = g.win[item];
     const int m0 = w.tile * BM;
     mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (CHUNK_COLS * BK * 2));
-    tma_load_2d(sA, tmA, full, kb * BK, m0);
+    tma_load_2d_hint(sA, tmA, full, kb * BK, m0, pol_stream);
     for (int j = 0; j < w.nq; ++j) {
       if constexpr (MODE == MODE_SHRINK)   // At_all rows (K-major, k = d_in)
-        tma_load_2d(sB + j * (CHUNK_COLS * BK * 2), tmB, full, kb * BK, (w.q0 + j) * CHUNK_COLS);
+        tma_load_2d_hint(sB + j * (CHUNK_COLS * BK * 2), tmB, full, kb * BK, (w.q0 + j) * CHUNK_COLS, pol_keep);
       else                                 // Bt_all [d_out, C] as MN-major (n = rank column, k = d_out)
-        tma_load_2d(sB + j * (CHUNK_COLS * BK * 2), tmB, full, (w.q0 + j) * CHUNK_COLS, kb * BK);
+        tma_load_2d_hint(sB + j * (CHUNK_COLS * BK * 2), tmB, full, (w.q0 + j) * CHUNK_COLS, kb * BK, pol_keep);
     }
   } else {
     const WItem w = g.witems[item];
@@ -139,11 +140,12 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
     const MTile mt = g.mtiles[t];
     mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (IMG_BYTES / 2));
     // X (dA) or dY (dB) as an MN-major operand: 64 hidden columns x 64 tokens per box.
-    tma_load_2d(sA, tmA, full, w.row0, gh * 64);
-    tma_load_2d(sA + 64 * 64 * 2, tmA, full, w.row0 + 64, gh * 64);
+    tma_load_2d_hint(sA, tmA, full, w.row0, gh * 64, pol_stream);
+    tma_load_2d_hint(sA + 64 * 64 * 2, tmA, full, w.row0 + 64, gh * 64, pol_stream);
     // staged images as an MN-major operand: 64 rank columns x 64 tokens per box
     for (int j = 0; j < w.nq; ++j)
-      tma_load_2d(sB + j * (IMG_BYTES / 2), tmI, full, 0, (mt.img_off + w.q0 + j - mt.q_lo) * BM + h * 64);
+      tma_load_2d_hint(sB + j * (IMG_BYTES / 2), tmI, full, 0, (mt.img_off + w.q0 + j - mt.q_lo) * BM + h * 64,
+                       pol_keep);
   }
 }
 
@@ -252,13 +254,29 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
         const int cbase = q * CHUNK_COLS + half * 32;
         uint32_t pk[16];
 #pragma unroll
-        for (int u = 0; u < 32; u += 2) {
-          const int c0 = cbase + u, c1 = c0 + 1;
-          const float a0 = __uint_as_float(v[u]), a1 = __uint_as_float(v[u + 1]);
-          const bool in0 = c0 >= c_lo && c0 < c_hi, in1 = c1 >= c_lo && c1 < c_hi;
-          if (in0) g.hout[hbase + c0] = (MODE == MODE_SHRINK) ? a0 : s * a0;
-          if (in1) g.hout[hbase + c1] = (MODE == MODE_SHRINK) ? a1 : s * a1;
-          pk[u / 2] = pack_bf16x2(in0 ? s * a0 : 0.f, in1 ? s * a1 : 0.f);
+        for (int u = 0; u < 32; u += 4) {
+          const int c0 = cbase + u;
+          float a[4];
+          bool in[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            a[k] = __uint_as_float(v[u + k]);
+            in[k] = c0 + k >= c_lo && c0 + k < c_hi;
+          }
+          float hv[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) hv[k] = (MODE == MODE_SHRINK) ? a[k] : s * a[k];
+          // H / dH row segment: one 16-byte store when the four columns are in the window and aligned
+          float* hp = g.hout + hbase + c0;
+          if (in[0] && in[3] && ((reinterpret_cast<uintptr_t>(hp) & 15u) == 0)) {
+            *reinterpret_cast<float4*>(hp) = make_float4(hv[0], hv[1], hv[2], hv[3]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (in[k]) hp[k] = hv[k];
+          }
+          pk[u / 2] = pack_bf16x2(in[0] ? s * a[0] : 0.f, in[1] ? s * a[1] : 0.f);
+          pk[u / 2 + 1] = pack_bf16x2(in[2] ? s * a[2] : 0.f, in[3] ? s * a[3] : 0.f);
         }
         uint4* dst = reinterpret_cast<uint4*>(img + rit * (CHUNK_COLS * 2) + half * 64);
 #pragma unroll
@@ -365,6 +383,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      const uint64_t pol_stream = l2_policy_evict_first();
+      const uint64_t pol_keep = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
@@ -382,7 +402,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mbar_arrive_expect_tx(&full[stage], A_BYTES);
           } else {
             produce_kblock<MODE>(g, &tmA, &tmB, &tmE, &tmI, item, kb, sA + stage * A_BYTES, sB + stage * B_BYTES,
-                                 &full[stage]);
+                                 &full[stage], pol_stream, pol_keep);
           }
           ++issued;
           if (++stage == STAGES) {
