@@ -143,6 +143,11 @@ struct mlora_plan_s {
   unsigned long long timeout_ns = DEFAULT_TIMEOUT_NS;
   bool pdl = true;
   bool debug_drop = false;
+  // what the last forward left in a workspace (used with MLORA_REUSE_STAGING)
+  bool reuse_staging = false;
+  bool staged_valid = false;
+  const void* staged_ws = nullptr;
+  const float* staged_H = nullptr;
   // optional per-kernel timing with CUDA events recorded on the launching stream
   bool profiling = false;
   std::vector<cudaEvent_t> ev_pool;
@@ -479,6 +484,7 @@ mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs,
   P->user.assign(segs, segs + n_segs);
   if (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT) P->timeout_ns = SHORT_TIMEOUT_NS;
   if (problem->flags & MLORA_NO_OVERLAP) P->pdl = false;
+  if (problem->flags & MLORA_REUSE_STAGING) P->reuse_staging = true;
   // the copy-withholding test hook is honoured only with the 1 ms wait limit
   if ((problem->flags & MLORA_DEBUG_DROP_COPY) && (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT)) P->debug_drop = true;
   build_tables(P);
@@ -562,6 +568,12 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
     e = timed(P, K_FWD_GEMM, s, [&] { return launch_seg_gemm<MODE_FWD>(mX, mW, mBt, mI, g, grid_of(P, g.n_items), s); });
   }
   if (e != cudaSuccess) return cuda_fail(e, "forward GEMM launch");
+  {
+    mlora_plan_t* Pm = const_cast<mlora_plan_t*>(P);
+    Pm->staged_valid = true;
+    Pm->staged_ws = workspace;
+    Pm->staged_H = H;
+  }
   return MLORA_OK;
 }
 
@@ -593,11 +605,16 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   uint8_t* dhimg = ws + P->off_dhimg;
 
   // The backward reads the same two bf16 shadows as the forward, At_all [C, d_in] and
-  // Bt_all [d_out, C], as MN-major operands.
-  e = timed(P, K_PACK_BWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
-  if (e != cudaSuccess) return cuda_fail(e, "pack launch");
-  e = timed(P, K_H_IMAGES, s, [&] { return launch_h_images(P->d_segs, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s, P->pdl); });
-  if (e != cudaSuccess) return cuda_fail(e, "image launch");
+  // Bt_all [d_out, C], as MN-major operands, and the staged s*H images.  With
+  // MLORA_REUSE_STAGING, when this workspace and H are the ones the last forward used (and no
+  // AdamW step ran since), they are still in place and are not rebuilt.
+  const bool reuse = P->reuse_staging && P->staged_valid && P->staged_ws == workspace && P->staged_H == H;
+  if (!reuse) {
+    e = timed(P, K_PACK_BWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+    e = timed(P, K_H_IMAGES, s, [&] { return launch_h_images(P->d_segs, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s, P->pdl); });
+    if (e != cudaSuccess) return cuda_fail(e, "image launch");
+  }
 
   const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
   CUtensorMap mdY, mdYt, mBt64, mWmn, mAt64, mXt, mHi, mdHi, mdHi64;
@@ -660,6 +677,7 @@ mlora_status mlora_adamw(const mlora_plan_t* P, float lr, float beta1, float bet
   if (st != MLORA_OK) return st;
   if (!P->can_adamw) return fail(MLORA_ERR_INVALID, "the plan's segments lack gradient or moment buffers");
   if (step < 1) return fail(MLORA_ERR_INVALID, "step must be >= 1");
+  const_cast<mlora_plan_t*>(P)->staged_valid = false;   // the masters change: shadows are stale
   if (!(beta1 >= 0.f && beta1 < 1.f && beta2 >= 0.f && beta2 < 1.f) || !std::isfinite(lr) || !std::isfinite(eps) ||
       !std::isfinite(weight_decay))
     return fail(MLORA_ERR_INVALID, "bad AdamW hyper-parameters");

@@ -202,11 +202,14 @@ def run_reference(args, wl, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(wl, ngpus):
-    return {"workload": wl.name, "d_in": wl.d_in, "d_out": wl.d_out, "adapters": wl.n_adapters,
-            "ranks": wl.ranks, "tokens_per_step": wl.N, "dtype_io": wl.dtype, "parallelism": f"replicas x{ngpus}",
-            "l2": "inputs larger than L2 (X and dY are N x d bf16, each above the 129 MB L2)"
-            if wl.N * min(wl.d_in, wl.d_out) * 2 > 129e6 else "inputs smaller than L2"}
+def config_of(wl, ngpus, options=None):
+    c = {"workload": wl.name, "d_in": wl.d_in, "d_out": wl.d_out, "adapters": wl.n_adapters,
+         "ranks": wl.ranks, "tokens_per_step": wl.N, "dtype_io": wl.dtype, "parallelism": f"replicas x{ngpus}",
+         "l2": "inputs larger than L2 (X and dY are N x d bf16, each above the 129 MB L2)"
+         if wl.N * min(wl.d_in, wl.d_out) * 2 > 129e6 else "inputs smaller than L2"}
+    if options:
+        c["options"] = options
+    return c
 
 
 def traffic_record(kernel):
@@ -236,7 +239,8 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     T = W.materialise(wl)
     scales = [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
-    layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At, Bt=T.Bt)
+    layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At, Bt=T.Bt,
+                       flags=0 if args.no_reuse else M.MLORA_REUSE_STAGING)
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
 
     def host(a):
@@ -406,7 +410,8 @@ def run_ours(args, wl, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
             "data": "synthetic (seeded Philox; shapes of the named workload, random-init adapters)",
-            "config": config_of(wl, world),
+            "config": config_of(wl, world, None if args.no_reuse else
+                                "MLORA_REUSE_STAGING (backward reuses the forward's bf16 shadows and staged H)"),
             "tflops": flops_per_step(wl) * world * args.steps / (ms / 1e3) / 1e12,
             "roofline": roof, "kernels": kernels, "kernel_timing_ms_per_step": prof_step_ms,
             "gpu_launches": launches, "e2e": e2e,
@@ -435,6 +440,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qproj")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-reuse", action="store_true", help="rebuild the backward's staging (no MLORA_REUSE_STAGING)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens-per-job", type=int, default=64)

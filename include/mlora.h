@@ -72,6 +72,11 @@ typedef enum mlora_dtype {
                                           but copies nothing into it, so a device wait runs out (~1 ms),
                                           the status word records it and mlora_sync_status() returns
                                           MLORA_ERR_TIMEOUT; that call's outputs are undefined */
+#define MLORA_REUSE_STAGING 32u       /* mlora_backward skips rebuilding the bf16 adapter shadows and the
+                                          staged s*H images when its workspace and H are the ones the last
+                                          mlora_forward of this plan used and no mlora_adamw ran since; the
+                                          caller guarantees that neither At/Bt, H nor that workspace changed
+                                          in between (results are then identical to the full backward) */
 #define MLORA_NO_OVERLAP 8u            /* launch every kernel strictly after the previous one (no programmatic
                                           dependent launch overlapping a kernel's prologue with the tail of
                                           the one before); results are identical either way */

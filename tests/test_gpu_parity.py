@@ -109,6 +109,32 @@ def test_launch_overlap_does_not_change_results():
         r2.close()
 
 
+def test_reuse_staging_gives_identical_results():
+    """With MLORA_REUSE_STAGING the backward reuses the forward's shadows and images from the
+    shared workspace; over two full steps (AdamW in between invalidates the reuse once) every
+    output matches the plain path bitwise."""
+    wl = W.custom("reuse", 956, 384, 512, [4, 64, 130], [300, 100, 150], dtype="bf16", b_std=0.05)
+    T = W.materialise(wl)
+    outs = []
+    for flags in (0, M.MLORA_REUSE_STAGING):
+        L = G.PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, G.scales_of(wl), dtype="bf16", At=T.At, Bt=T.Bt,
+                         flags=flags)
+        X, Wt, dY = G.to_dev(T.X, "bf16"), G.to_dev(T.Wt, "bf16"), G.to_dev(T.dY, "bf16")
+        res = []
+        for step in (1, 2):
+            Y = L.forward(X, Wt)
+            dX = L.backward(X, Wt, dY)
+            L.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, step)
+            torch.cuda.synchronize()
+            res.append([G.from_dev(Y, "bf16"), G.from_dev(dX, "bf16")] + [a.cpu().numpy() for a in L.dAt + L.dBt + L.At])
+        assert L.sync_status() == M.MLORA_OK
+        outs.append(res)
+        L.close()
+    for a, b in zip(outs[0], outs[1]):
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y)
+
+
 def test_adamw_isolated_t3():
     """The AdamW kernel alone on seeded gradients and moments (t = 3), so the update
     p' - p itself can be checked: at small t it is close to -lr * sign(g), which would
