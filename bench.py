@@ -391,16 +391,27 @@ def run_ours(args, wl, rank, world, local_rank):
             v["tflops"] = f / (v["ms_per_launch"] * 1e-3) / 1e12
         if b:
             v["gbs"] = b / (v["ms_per_launch"] * 1e-3) / 1e9
-    dom = max(("fwd_gemm", "bwd_gemm"), key=lambda k: kernels.get(k, {}).get("ms_per_launch", 0))
-    dk = kernels[dom]
-    # The burst figure is the larger (stricter) denominator; the sustained one is what a
-    # seconds-long power-capped loop reaches and is reported beside it.
-    peak = peaks.get("bf16_tflops")
-    sust = peaks.get("bf16_tflops_sustained")
-    roof = {"kernel": dom, "bound": "tensor", "achieved": dk["tflops"], "peak": peak, "unit": "TFLOP/s",
-            "frac": dk["tflops"] / peak, "peak_source": f"{peak_src} bf16_tflops (burst cuBLAS GEMM)",
-            "frac_of_sustained": (dk["tflops"] / sust) if sust else None,
-            "traffic": traffic_record(dom)}
+    if wl.dtype == "bf16":
+        dom = max(("fwd_gemm", "bwd_gemm"), key=lambda k: kernels.get(k, {}).get("ms_per_launch", 0))
+        dk = kernels[dom]
+        # The burst figure is the larger (stricter) denominator; the sustained one is what a
+        # seconds-long power-capped loop reaches and is reported beside it.
+        peak = peaks.get("bf16_tflops")
+        sust = peaks.get("bf16_tflops_sustained")
+        roof = {"kernel": dom, "bound": "tensor", "achieved": dk["tflops"], "peak": peak, "unit": "TFLOP/s",
+                "frac": dk["tflops"] / peak, "peak_source": f"{peak_src} bf16_tflops (burst cuBLAS GEMM)",
+                "frac_of_sustained": (dk["tflops"] / sust) if sust else None,
+                "traffic": traffic_record(dom)}
+    else:
+        # fp32 path: plain FFMA.  Peak = SMs x 128 FFMA lanes x 2 FLOP x max SM clock.
+        dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"])
+        f = {"f32_forward": 2.0 * wl.N * wl.d_in * wl.d_out + 4.0 * sum(n * r for n, r in zip(wl.n_tokens, wl.ranks)) * (wl.d_in + wl.d_out) / 2,
+             "f32_backward": 2.0 * wl.N * wl.d_in * wl.d_out + 4.0 * sum(n * r for n, r in zip(wl.n_tokens, wl.ranks)) * (wl.d_in + wl.d_out)}
+        sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
+        peak = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        ach = f.get(dom, 0.0) / (kernels[dom]["ms_per_launch"] * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                "peak_source": "derived: SMs x 128 FP32 lanes x 2 FLOP x max SM clock", "traffic": None}
     hbm = peaks.get("hbm_gbs")
     for k in ("shrink", "dH", "dA", "dB", "adamw"):
         if k in kernels and "gbs" in kernels[k]:
