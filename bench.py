@@ -405,8 +405,9 @@ def run_ours(args, wl, rank, world, local_rank):
     else:
         # fp32 path: plain FFMA.  Peak = SMs x 128 FFMA lanes x 2 FLOP x max SM clock.
         dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"])
-        f = {"f32_forward": 2.0 * wl.N * wl.d_in * wl.d_out + 4.0 * sum(n * r for n, r in zip(wl.n_tokens, wl.ranks)) * (wl.d_in + wl.d_out) / 2,
-             "f32_backward": 2.0 * wl.N * wl.d_in * wl.d_out + 4.0 * sum(n * r for n, r in zip(wl.n_tokens, wl.ranks)) * (wl.d_in + wl.d_out)}
+        nr = sum(n * r for n, r in zip(wl.n_tokens, wl.ranks))
+        f = {"f32_forward": 2.0 * wl.N * wl.d_in * wl.d_out + 2.0 * nr * (wl.d_in + wl.d_out),     # XW, XA, HB
+             "f32_backward": 2.0 * wl.N * wl.d_in * wl.d_out + 4.0 * nr * (wl.d_in + wl.d_out)}    # dYW^T, dH, dX_lora, dA, dB
         sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
         peak = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         ach = f.get(dom, 0.0) / (kernels[dom]["ms_per_launch"] * 1e-3) / 1e12
