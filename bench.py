@@ -135,6 +135,21 @@ class ClockSampler:
                 "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of a per-rank float over all ranks (the rank itself when not distributed)."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_rate(units_per_rank: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world * steps / (max_ms / 1e3)
+
+
 def oracle_sample(wl, T, per_job):
     """A bounded sample of the workload for the CPU oracle: the first `per_job` tokens of every job."""
     import numpy as np
@@ -287,10 +302,7 @@ def run_ours(args, wl, rank, world, local_rank):
     launches = M.mlora_launch_count() - launches0
     if layer.sync_status() != M.MLORA_OK:
         raise SystemExit("device status error in the timed region")
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, device="cuda")
 
     # ---- per-kernel times: the same K steps again with the library recording a CUDA event pair
     # around every launch on the launching stream (events between launches serialise them, so
@@ -364,14 +376,10 @@ def run_ours(args, wl, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ems = e0.elapsed_time(e1)
-        if dist:
-            t = torch.tensor([ems], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(e0.elapsed_time(e1), device="cuda")
         b_in = X.numel() * X.element_size() + dY.numel() * dY.element_size()
         b_out = Y.numel() * Y.element_size() + dX.numel() * dX.element_size()
-        e2e = {"value": wl.N * world * args.steps / (ems / 1e3), "unit": "tokens/s",
+        e2e = {"value": weak_scaling_rate(wl.N, world, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": b_in, "d2h_bytes_per_step": b_out, "ms_per_step": ems / args.steps,
                "pipelined": "H2D and D2H copies on their own streams, double-buffered device buffers"}
         if layer.sync_status() != M.MLORA_OK:
@@ -417,7 +425,7 @@ def run_ours(args, wl, rank, world, local_rank):
     for k in ("shrink", "dH", "dA", "dB", "adamw"):
         if k in kernels and "gbs" in kernels[k]:
             kernels[k]["frac_of_hbm"] = kernels[k]["gbs"] / hbm
-    value = wl.N * world * args.steps / (ms / 1e3)
+    value = weak_scaling_rate(wl.N, world, args.steps, ms)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
