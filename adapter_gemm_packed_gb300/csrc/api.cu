@@ -67,7 +67,7 @@ mlora_status cuda_fail(cudaError_t e, const char* where) {
   return MLORA_ERR_CUDA;
 }
 
-constexpr int ADAM_CHUNK = 16384;
+constexpr int ADAM_CHUNK = 4096;
 constexpr int MAX_RANK = 256;
 constexpr unsigned long long DEFAULT_TIMEOUT_NS = 4000000000ull;   // 4 s
 constexpr unsigned long long SHORT_TIMEOUT_NS = 1000000ull;        // 1 ms

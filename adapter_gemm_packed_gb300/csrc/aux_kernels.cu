@@ -189,7 +189,7 @@ cudaError_t launch_adamw(const AdamItem* items, int n_items, float lr, float bet
   const float decay = 1.0f - lr * weight_decay;
   int grid = n_items;
   if (grid > num_sms * 16) grid = num_sms * 16;
-  return launch_k(k_adamw, dim3(grid), dim3(512), 0, st, pdl, items, n_items, lr, beta1, beta2, eps, decay,
+  return launch_k(k_adamw, dim3(grid), dim3(256), 0, st, pdl, items, n_items, lr, beta1, beta2, eps, decay,
                   static_cast<float>(bc1), static_cast<float>(bc2));
 }
 
