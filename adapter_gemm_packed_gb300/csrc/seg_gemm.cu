@@ -41,16 +41,14 @@ namespace {
 // (X or dY, 16 KB per slice, loaded with an evict-first L2 policy) against a small operand that
 // many CTAs re-read from L2 (up to two 64-column rank chunks, <= 16 KB, evict-last): six stages
 // keep 96 KB of the streamed operand in flight per SM (a bare TMA streaming loop on a GB300
-// reaches 6.6 TB/s with 4 x 16 KB per SM).  dB also gets a 32x33 fp32 transpose tile per
-// epilogue warp for coalesced stores.
+// reaches 6.6 TB/s with 4 x 16 KB per SM).
 template <int MODE>
 struct Ring {
   static constexpr bool kBase = MODE == MODE_FWD || MODE == MODE_BWD;
   static constexpr int kStages = kBase ? 4 : 6;
   static constexpr int kABytes = A_STAGE_BYTES;
   static constexpr int kBBytes = kBase ? B_STAGE_BYTES : MAX_ITEM_CHUNKS * CHUNK_COLS * BK * 2;
-  static constexpr int kXpose = MODE == MODE_DB ? 4 * 32 * 33 * 4 : 0;
-  static constexpr int kSmem = kStages * (kABytes + kBBytes) + kXpose + 1024 + 256;
+  static constexpr int kSmem = kStages * (kABytes + kBBytes) + 1024 + 256;
 };
 
 __device__ __forceinline__ void decode_mn(const GemmArgs& g, int item, int& m, int& n) {
@@ -188,8 +186,7 @@ __device__ __forceinline__ int find_seg(const DevSeg* segs, int first, int last,
 }
 
 template <int MODE>
-__device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint32_t t_acc, int quarter, int lane,
-                                              float* xpose) {
+__device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint32_t t_acc, int quarter, int lane) {
   const int rit = quarter * 32 + lane;   // accumulator row owned by this thread
   if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
     int m, n;
@@ -246,11 +243,13 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
     for (int jq = 0; jq < w.nq; ++jq) {
       const int q = w.q0 + jq;
       uint8_t* img = g.img_out + static_cast<size_t>(mt.img_off + q - mt.q_lo) * IMG_BYTES;
-#pragma unroll 1
+      uint32_t vv[64];
+      tmem_ld32(t_acc + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&vv[0]));
+      tmem_ld32(t_acc + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&vv[32]));
+      tmem_ld_wait();
+#pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        tmem_ld32(t_acc + jq * CHUNK_COLS + half * 32, v);
-        tmem_ld_wait();
+        const uint32_t* v = vv + half * 32;
         const int cbase = q * CHUNK_COLS + half * 32;
         uint32_t pk[16];
 #pragma unroll
@@ -291,37 +290,35 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
     const int bound = (MODE == MODE_DA) ? g.d_in : g.d_out;
 #pragma unroll 1
     for (int jq = 0; jq < w.nq; ++jq) {
-#pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        uint32_t v[32];
-        tmem_ld32(t_acc + jq * CHUNK_COLS + half * 32, v);
-        tmem_ld_wait();
-        const int cbase = (w.q0 + jq) * CHUNK_COLS + half * 32 - sg.c;   // rank index of v[0]
-        if constexpr (MODE == MODE_DA) {
-          // dAt_i[t][row]: for a fixed t the 32 lanes write 32 consecutive rows (coalesced)
-          if (row < bound) {
+      // both 32-column halves of the chunk in flight before one wait
+      uint32_t v[64];
+      tmem_ld32(t_acc + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(t_acc + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld_wait();
+      const int cbase = (w.q0 + jq) * CHUNK_COLS - sg.c;   // rank index of v[0]
+      if (row >= bound) continue;
+      if constexpr (MODE == MODE_DA) {
+        // dAt_i[t][row]: for a fixed t the 32 lanes write 32 consecutive rows (coalesced)
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-              const int t = cbase + u;
-              if (t >= 0 && t < sg.r) sg.dAt[static_cast<size_t>(t) * g.d_in + row] = __uint_as_float(v[u]);
-            }
-          }
-        } else {
-          // dBt_i[row][t] is rank-contiguous per row: transpose the warp's 32x32 block through
-          // shared memory so each store instruction covers consecutive addresses.
-          const int ulo = max(0, -cbase), uhi = min(32, sg.r - cbase);
-          if (uhi > ulo) {
+        for (int u = 0; u < 64; ++u) {
+          const int t = cbase + u;
+          if (t >= 0 && t < sg.r) sg.dAt[static_cast<size_t>(t) * g.d_in + row] = __uint_as_float(v[u]);
+        }
+      } else {
+        // dBt_i[row][t]: this thread's row segment is contiguous; 16-byte stores where aligned
+        // (the L2 merges the lanes' partial sectors).
+        float* dst = sg.dBt + static_cast<size_t>(row) * sg.r + cbase;   // + u
+        const bool al = ((static_cast<long long>(row) * sg.r + cbase) & 3) == 0;
 #pragma unroll
-            for (int u = 0; u < 32; ++u) xpose[lane * 33 + u] = __uint_as_float(v[u]);
-            __syncwarp();
-            const int wdt = uhi - ulo;
-            const int row_base = w.row0 + quarter * 32;
-            for (int e = lane; e < 32 * wdt; e += 32) {
-              const int rr = e / wdt, u = ulo + e % wdt;
-              if (row_base + rr < bound)
-                sg.dBt[static_cast<size_t>(row_base + rr) * sg.r + cbase + u] = xpose[rr * 33 + u];
-            }
-            __syncwarp();
+        for (int u = 0; u < 64; u += 4) {
+          const int t = cbase + u;
+          if (al && t >= 0 && t + 3 < sg.r) {
+            *reinterpret_cast<float4*>(dst + u) = make_float4(__uint_as_float(v[u]), __uint_as_float(v[u + 1]),
+                                                              __uint_as_float(v[u + 2]), __uint_as_float(v[u + 3]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (t + k >= 0 && t + k < sg.r) dst[u + k] = __uint_as_float(v[u + k]);
           }
         }
       }
@@ -343,8 +340,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  float* xpose_all = reinterpret_cast<float*>(sB + STAGES * B_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES + Ring<MODE>::kXpose);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
   uint64_t* full = bars;                 // [STAGES]  TMA -> MMA
   uint64_t* empty = bars + STAGES;       // [STAGES]  MMA -> TMA
   uint64_t* tfull = bars + 2 * STAGES;   // [2]       MMA -> epilogue
@@ -477,7 +473,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      epilogue_item<MODE>(g, item, t_acc, quarter, lane, xpose_all + quarter * 32 * 33);
+      epilogue_item<MODE>(g, item, t_acc, quarter, lane);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
