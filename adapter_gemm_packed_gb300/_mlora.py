@@ -26,7 +26,8 @@ MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD
 EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward", "mlora_adamw",
            "mlora_sync_status", "mlora_h_elems", "mlora_plan_describe", "mlora_status_string",
            "mlora_last_error", "mlora_version", "mlora_profile_enable", "mlora_profile_read",
-           "mlora_kernel_name", "mlora_launch_count", "mlora_forward_static_ws"]
+           "mlora_kernel_name", "mlora_launch_count", "mlora_forward_static_ws", "mlora_memory_estimate",
+           "mlora_shard_jobs"]
 
 
 class mlora_segment(C.Structure):
@@ -38,6 +39,11 @@ class mlora_segment(C.Structure):
 class mlora_problem(C.Structure):
     _fields_ = [("n_tokens", C.c_int64), ("d_in", C.c_int32), ("d_out", C.c_int32), ("dtype", C.c_int32),
                 ("flags", C.c_uint32)]
+
+
+class mlora_memory(C.Structure):
+    _fields_ = [(k, C.c_int64) for k in ("base_weight", "activations", "lora_params", "lora_grad_state", "lora_act",
+                                          "workspace", "plan_tables", "total")]
 
 
 class MloraError(RuntimeError):
@@ -90,6 +96,11 @@ def lib() -> C.CDLL:
         L.mlora_launch_count.restype = i64
         L.mlora_forward_static_ws.argtypes = [vp, vp, vp, vp, vp, vp]
         L.mlora_forward_static_ws.restype = i32
+        L.mlora_memory_estimate.argtypes = [vp, C.POINTER(mlora_memory)]
+        L.mlora_memory_estimate.restype = i32
+        L.mlora_shard_jobs.argtypes = [C.POINTER(mlora_problem), C.POINTER(mlora_segment), i32, i32,
+                                       C.POINTER(i32), C.POINTER(C.c_double)]
+        L.mlora_shard_jobs.restype = i32
         _lib = L
     return _lib
 
@@ -178,3 +189,18 @@ def mlora_launch_count() -> int:
 def mlora_forward_static_ws(plan, X, Wt, Y, H, stream) -> None:
     """Forward pass using the library's static device scratch instead of a caller workspace."""
     _check(lib().mlora_forward_static_ws(plan, X, Wt, Y, H, stream), "mlora_forward_static_ws")
+
+
+def mlora_memory_estimate(plan) -> dict:
+    m = mlora_memory()
+    _check(lib().mlora_memory_estimate(plan, C.byref(m)), "mlora_memory_estimate")
+    return {k: int(getattr(m, k)) for k, _ in mlora_memory._fields_}
+
+
+def mlora_shard_jobs(problem: mlora_problem, segs, n_ranks: int):
+    """Returns (rank of each job, load per rank)."""
+    arr = (mlora_segment * len(segs))(*segs)
+    ranks = (C.c_int32 * len(segs))()
+    load = (C.c_double * n_ranks)()
+    _check(lib().mlora_shard_jobs(C.byref(problem), arr, len(segs), n_ranks, ranks, load), "mlora_shard_jobs")
+    return list(ranks), list(load)

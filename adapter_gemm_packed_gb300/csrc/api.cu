@@ -772,6 +772,51 @@ const char* mlora_kernel_name(int32_t id) { return (id >= 0 && id < K_COUNT) ? k
 
 int64_t mlora_launch_count(void) { return g_launches; }
 
+mlora_status mlora_memory_estimate(const mlora_plan_t* P, mlora_memory* out) {
+  if (!P || !out) return fail(MLORA_ERR_INVALID, "null plan or output");
+  const mlora_problem& pr = P->prob;
+  const int64_t e = pr.dtype == MLORA_BF16 ? 2 : 4;
+  int64_t params = 0;
+  for (const DevSeg& d : P->segs) params += static_cast<int64_t>(d.r) * (pr.d_in + pr.d_out);
+  mlora_memory m{};
+  m.base_weight = static_cast<int64_t>(pr.d_in) * pr.d_out * e;
+  m.activations = 2 * pr.n_tokens * (static_cast<int64_t>(pr.d_in) + pr.d_out) * e;
+  m.lora_params = params * 4;
+  m.lora_grad_state = 3 * m.lora_params;
+  m.lora_act = 2 * P->h_elems * 4;
+  m.workspace = static_cast<int64_t>(P->ws_bytes);
+  m.plan_tables = static_cast<int64_t>(table_bytes(P->segs) + table_bytes(P->mtiles) + table_bytes(P->img_tile) +
+                                       table_bytes(P->col_seg) + table_bytes(P->win) + table_bytes(P->da) +
+                                       table_bytes(P->db) + table_bytes(P->adam) + 256);
+  m.total = m.base_weight + m.activations + m.lora_params + m.lora_grad_state + m.lora_act + m.workspace +
+            m.plan_tables;
+  *out = m;
+  return MLORA_OK;
+}
+
+mlora_status mlora_shard_jobs(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
+                              int32_t n_ranks, int32_t* rank_of_job, double* load) {
+  if (!problem || !segs || !rank_of_job || n_segs < 1 || n_ranks < 1)
+    return fail(MLORA_ERR_INVALID, "bad arguments to mlora_shard_jobs");
+  const double din = problem->d_in, dout = problem->d_out;
+  std::vector<std::pair<double, int>> cost(n_segs);
+  for (int i = 0; i < n_segs; ++i) {
+    if (segs[i].n_tokens < 1 || segs[i].rank < 1) return fail(MLORA_ERR_INVALID, "bad job in mlora_shard_jobs");
+    cost[i] = {static_cast<double>(segs[i].n_tokens) * (din * dout + 3.0 * segs[i].rank * (din + dout)), i};
+  }
+  std::stable_sort(cost.begin(), cost.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
+  std::vector<double> l(n_ranks, 0.0);
+  for (const auto& c : cost) {
+    int best = 0;
+    for (int r = 1; r < n_ranks; ++r)
+      if (l[r] < l[best]) best = r;
+    rank_of_job[c.second] = best;
+    l[best] += c.first;
+  }
+  if (load) std::copy(l.begin(), l.end(), load);
+  return MLORA_OK;
+}
+
 const char* mlora_status_string(mlora_status s) {
   switch (s) {
     case MLORA_OK: return "ok";

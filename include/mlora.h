@@ -190,6 +190,35 @@ const char* mlora_kernel_name(int32_t id);
 /* Number of CUDA kernels this library has launched in this process so far. */
 int64_t mlora_launch_count(void);
 
+/* Device memory of one packed layer, in bytes (the single-GPU capacity check of the memory
+ * model in "PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §8, for one
+ * layer of one device).  lora_params is the paper's M_lora_param with fp32 masters (4 bytes
+ * per parameter); lora_grad_state is c_grad = 3 times it (gradient, first and second moment:
+ * the page multiplies by the precision a second time, which double-counts the bytes; read
+ * as c_grad x M_lora_param); lora_act is the paper's M_lora_act (b x s x r per job = H, fp32)
+ * plus the backward's dH of the same size.  The others are this library's buffers. */
+typedef struct mlora_memory {
+    int64_t base_weight;      /* W */
+    int64_t activations;      /* X, Y, dY, dX */
+    int64_t lora_params;      /* A_i, B_i */
+    int64_t lora_grad_state;  /* dA_i, dB_i and the AdamW moments */
+    int64_t lora_act;         /* H and dH */
+    int64_t workspace;        /* mlora_plan's workspace_bytes */
+    int64_t plan_tables;      /* the plan's own device tables */
+    int64_t total;
+} mlora_memory;
+
+/* Fill *out for the plan (host only; valid for host-only plans too). */
+mlora_status mlora_memory_estimate(const mlora_plan_t* plan, mlora_memory* out);
+
+/* Split whole jobs across n_ranks GPUs that each hold a replica of W (the layer shards by job
+ * with no collective: every job's gradients and optimizer step stay on its GPU).  Jobs are
+ * assigned longest-first to the least-loaded rank, with a job's cost taken as its share of
+ * the step's arithmetic, n_i (d_in d_out + 3 r_i (d_in + d_out)).  rank_of_job[i] receives the
+ * rank of segs[i]; load[r] (may be NULL, n_ranks entries) the summed cost of rank r.  Host only. */
+mlora_status mlora_shard_jobs(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
+                              int32_t n_ranks, int32_t* rank_of_job, double* load);
+
 /* Forward pass without a caller workspace, for callers that cannot allocate device memory
  * when they run the layer (a runtime that forbids cudaMalloc after start-up, a framework whose
  * memory comes only from its own pools, code running while another thread captures a graph).
