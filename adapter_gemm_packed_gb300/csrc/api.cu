@@ -9,7 +9,7 @@
 // 128-token tile to the jobs and chunks it covers, and builds one static work list per kernel:
 //   * base GEMMs: (token tile x 256 output columns), rastered in groups of M tiles for L2 reuse;
 //   * shrink / dH: (token tile, <= 2 64-column chunks of its window);
-//   * dA / dB: (128-row block of d_in / d_out, job, <= 2 chunks), sorted longest-first so the
+//   * dA / dB: (256-row block of d_in / d_out, job, <= 2 chunks), sorted longest-first so the
 //     persistent grid's round-robin assignment balances uneven jobs.
 #include <algorithm>
 #include <cmath>
@@ -307,7 +307,7 @@ void build_tables(mlora_plan_t* P) {
       const int qa = d.c / CHUNK_COLS, qb = (d.c + d.rp + CHUNK_COLS - 1) / CHUNK_COLS;
       // chunks innermost: the items that read the same X / dY block sit side by side in the
       // list, so the persistent grid runs them concurrently and the block is read from HBM once
-      for (int r0 = 0; r0 < rows; r0 += BM)
+      for (int r0 = 0; r0 < rows; r0 += 2 * BM)
         for (int q = qa; q < qb; q += MAX_ITEM_CHUNKS)
           v.push_back(WItem{r0, i, ga, gb, q, std::min(MAX_ITEM_CHUNKS, qb - q), 0, 0});
     }

@@ -69,7 +69,7 @@ struct WinItem {
   int tile, q0, nq, pad0;
 };
 
-// Weight-gradient work item (dA / dB): one 128-row block of d_in (dA) or d_out (dB), one
+// Weight-gradient work item (dA / dB): one 256-row block of d_in (dA) or d_out (dB), one
 // job, its 64-token half-tiles [ga, gb), chunks [q0, q0 + nq) of its rank window (nq <= MAX_ITEM_CHUNKS).
 struct WItem {
   int row0, seg, ga, gb, q0, nq, pad0, pad1;

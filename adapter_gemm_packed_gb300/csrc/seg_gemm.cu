@@ -42,11 +42,14 @@ namespace {
 // many CTAs re-read from L2 (up to two 64-column rank chunks, <= 16 KB, evict-last): six stages
 // keep 96 KB of the streamed operand in flight per SM (a bare TMA streaming loop on a GB300
 // reaches 6.6 TB/s with 4 x 16 KB per SM).
+// dA / dB items cover 256 rows of d_in / d_out (two M = 128 MMAs per K step sharing one staged
+// image operand), so their ring holds 32 KB of the streamed operand per stage.
 template <int MODE>
 struct Ring {
   static constexpr bool kBase = MODE == MODE_FWD || MODE == MODE_BWD;
-  static constexpr int kStages = kBase ? 4 : 6;
-  static constexpr int kABytes = A_STAGE_BYTES;
+  static constexpr bool kWgrad = MODE == MODE_DA || MODE == MODE_DB;
+  static constexpr int kStages = kBase ? 4 : (kWgrad ? 4 : 6);
+  static constexpr int kABytes = kWgrad ? 2 * A_STAGE_BYTES : A_STAGE_BYTES;
   static constexpr int kBBytes = kBase ? B_STAGE_BYTES : MAX_ITEM_CHUNKS * CHUNK_COLS * BK * 2;
   static constexpr int kSmem = kStages * (kABytes + kBBytes) + 1024 + 256;
 };
@@ -136,10 +139,11 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
     const int gh = w.ga + kb;            // 64-token half tile
     const int t = gh >> 1, h = gh & 1;
     const MTile mt = g.mtiles[t];
-    mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (IMG_BYTES / 2));
-    // X (dA) or dY (dB) as an MN-major operand: 64 hidden columns x 64 tokens per box.
-    tma_load_2d_hint(sA, tmA, full, w.row0, gh * 64, pol_stream);
-    tma_load_2d_hint(sA + 64 * 64 * 2, tmA, full, w.row0 + 64, gh * 64, pol_stream);
+    mbar_arrive_expect_tx(full, 2 * A_STAGE_BYTES + w.nq * (IMG_BYTES / 2));
+    // X (dA) or dY (dB) as an MN-major operand: 64 hidden columns x 64 tokens per box, four boxes
+    // for the item's 256 rows (two M = 128 operands, 16 KB each)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tma_load_2d_hint(sA + j * (64 * 64 * 2), tmA, full, w.row0 + 64 * j, gh * 64, pol_stream);
     // staged images as an MN-major operand: 64 rank columns x 64 tokens per box
     for (int j = 0; j < w.nq; ++j)
       tma_load_2d_hint(sB + j * (IMG_BYTES / 2), tmI, full, 0, (mt.img_off + w.q0 + j - mt.q_lo) * BM + h * 64,
@@ -169,11 +173,14 @@ __device__ __forceinline__ void mma_kblock(const GemmArgs& g, int item, int kb, 
       umma_bf16(d_tmem, smem_desc(sA + k * 32, 16, 1024), b, idesc, (kb > 0 || k > 0) ? 1u : 0u);
     }
   } else {
+    // two 128-row halves of the item into accumulator columns [0, N) and [128, 128 + N)
     const uint32_t idesc = idesc_bf16(BM, ncols, true, true);
 #pragma unroll
     for (int k = 0; k < BK / 16; ++k) {
-      umma_bf16(d_tmem, smem_desc(sA + k * 2048, 64 * 64 * 2, 1024), smem_desc(sB + k * 2048, IMG_BYTES / 2, 1024),
-                idesc, (kb > 0 || k > 0) ? 1u : 0u);
+      const uint64_t b = smem_desc(sB + k * 2048, IMG_BYTES / 2, 1024);
+      umma_bf16(d_tmem, smem_desc(sA + k * 2048, 64 * 64 * 2, 1024), b, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+      umma_bf16(d_tmem + 128, smem_desc(sA + A_STAGE_BYTES + k * 2048, 64 * 64 * 2, 1024), b, idesc,
+                (kb > 0 || k > 0) ? 1u : 0u);
     }
   }
 }
@@ -286,14 +293,16 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
   } else {
     const WItem w = g.witems[item];
     const DevSeg sg = g.segs[w.seg];
-    const int row = w.row0 + rit;                       // d_in (DA) or d_out (DB) index
     const int bound = (MODE == MODE_DA) ? g.d_in : g.d_out;
 #pragma unroll 1
+    for (int mh = 0; mh < 2; ++mh)
+#pragma unroll 1
     for (int jq = 0; jq < w.nq; ++jq) {
+      const int row = w.row0 + mh * BM + rit;             // d_in (DA) or d_out (DB) index
       // both 32-column halves of the chunk in flight before one wait
       uint32_t v[64];
-      tmem_ld32(t_acc + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(t_acc + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait();
       const int cbase = (w.q0 + jq) * CHUNK_COLS - sg.c;   // rank index of v[0]
       if (row >= bound) continue;

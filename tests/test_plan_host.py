@@ -112,7 +112,7 @@ def test_planner_tables(name):
     for items, rows_total in ((da, d_in), (db, d_out)):
         cover = {}
         for row0, j, ga, gb, q0, nq in items:
-            assert row0 % 128 == 0 and 0 <= row0 < rows_total and 1 <= nq <= 4
+            assert row0 % 256 == 0 and 0 <= row0 < rows_total and 1 <= nq <= 2
             assert ga * 64 <= offs[j] and (offs[j] + ns[j]) <= gb * 64 and gb - ga <= -(-ns[j] // 64) + 1
             for q in range(q0, q0 + nq):
                 key = (row0, j, q)
@@ -121,7 +121,7 @@ def test_planner_tables(name):
         want = set()
         for j in range(len(ns)):
             qa, qb = cols[j, 0] // 64, -(-(cols[j, 0] + cols[j, 1]) // 64)
-            want |= {(r0, j, q) for r0 in range(0, rows_total, 128) for q in range(qa, qb)}
+            want |= {(r0, j, q) for r0 in range(0, rows_total, 256) for q in range(qa, qb)}
         assert set(cover) == want
         lens = [(gb - ga) * (16 + nq) for _, _, ga, gb, _, nq in items]
         assert lens == sorted(lens, reverse=True)       # longest first
