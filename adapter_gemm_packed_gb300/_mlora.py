@@ -13,7 +13,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmlora.so")
 
 MLORA_OK, MLORA_ERR_INVALID, MLORA_ERR_UNSUPPORTED, MLORA_ERR_CUDA, MLORA_ERR_TIMEOUT, MLORA_ERR_OOM = range(6)
-MLORA_F32, MLORA_BF16 = 0, 1
+MLORA_F32, MLORA_BF16, MLORA_BF16_W4 = 0, 1, 2
 MLORA_PLAN_HOST_ONLY = 1
 MLORA_DEBUG_SHORT_TIMEOUT = 2
 MLORA_GEMM_SINGLE_CTA = 4
@@ -27,7 +27,7 @@ EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward"
            "mlora_sync_status", "mlora_h_elems", "mlora_plan_describe", "mlora_status_string",
            "mlora_last_error", "mlora_version", "mlora_profile_enable", "mlora_profile_read",
            "mlora_kernel_name", "mlora_launch_count", "mlora_forward_static_ws", "mlora_memory_estimate",
-           "mlora_shard_jobs"]
+           "mlora_shard_jobs", "mlora_forward_w4", "mlora_backward_w4"]
 
 
 class mlora_segment(C.Structure):
@@ -96,6 +96,10 @@ def lib() -> C.CDLL:
         L.mlora_launch_count.restype = i64
         L.mlora_forward_static_ws.argtypes = [vp, vp, vp, vp, vp, vp]
         L.mlora_forward_static_ws.restype = i32
+        L.mlora_forward_w4.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+        L.mlora_forward_w4.restype = i32
+        L.mlora_backward_w4.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.mlora_backward_w4.restype = i32
         L.mlora_memory_estimate.argtypes = [vp, C.POINTER(mlora_memory)]
         L.mlora_memory_estimate.restype = i32
         L.mlora_shard_jobs.argtypes = [C.POINTER(mlora_problem), C.POINTER(mlora_segment), i32, i32,
@@ -129,6 +133,14 @@ def mlora_plan_destroy(plan: int) -> None:
 
 def mlora_forward(plan, X, Wt, Y, H, workspace, stream) -> None:
     _check(lib().mlora_forward(plan, X, Wt, Y, H, workspace, stream), "mlora_forward")
+
+
+def mlora_forward_w4(plan, X, Wq, Wscale, Y, H, workspace, stream) -> None:
+    _check(lib().mlora_forward_w4(plan, X, Wq, Wscale, Y, H, workspace, stream), "mlora_forward_w4")
+
+
+def mlora_backward_w4(plan, X, Wq, Wscale, dY, H, dX, dH, workspace, stream) -> None:
+    _check(lib().mlora_backward_w4(plan, X, Wq, Wscale, dY, H, dX, dH, workspace, stream), "mlora_backward_w4")
 
 
 def mlora_backward(plan, X, Wt, dY, H, dX, dH, workspace, stream) -> None:

@@ -31,6 +31,9 @@ cudaError_t launch_seg_gemm(const CUtensorMap&, const CUtensorMap&, const CUtens
 template <int MODE>
 cudaError_t launch_gemm_2sm(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                             const GemmArgs&, int, cudaStream_t);
+template <int MODE>
+cudaError_t launch_gemm_2sm_w4(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                               const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 cudaError_t launch_pack_fwd(const DevSeg*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, int,
                             cudaStream_t, bool);
 cudaError_t launch_h_images(const DevSeg*, const MTile*, const int*, int, long long, const float*, uint8_t*,
@@ -109,6 +112,21 @@ mlora_status make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64
   return MLORA_OK;
 }
 
+// 2-D map without swizzle (4-bit codes as bytes, fp32 scales).
+mlora_status make_map_plain(CUtensorMap* map, CUtensorMapDataType dt, uint32_t esize, const void* base, uint64_t inner,
+                            uint64_t outer, uint64_t row_elems, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_elems * esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MLORA_ERR_CUDA, "cuTensorMapEncodeTiled failed for a 4-bit weight map");
+  return MLORA_OK;
+}
+
 }  // namespace
 
 struct mlora_plan_s {
@@ -160,9 +178,12 @@ namespace {
 mlora_status validate(const mlora_problem* p, const mlora_segment* s, int32_t n) {
   if (!p || !s) return fail(MLORA_ERR_INVALID, "null problem or segment table");
   if (n < 1) return fail(MLORA_ERR_INVALID, "n_segs must be >= 1");
-  if (p->dtype != MLORA_F32 && p->dtype != MLORA_BF16) return fail(MLORA_ERR_INVALID, "unknown dtype");
+  if (p->dtype != MLORA_F32 && p->dtype != MLORA_BF16 && p->dtype != MLORA_BF16_W4)
+    return fail(MLORA_ERR_INVALID, "unknown dtype");
+  if (p->dtype == MLORA_BF16_W4 && (p->d_in % 64 || (p->flags & MLORA_GEMM_SINGLE_CTA)))
+    return fail(MLORA_ERR_UNSUPPORTED, "a 4-bit base needs d_in a multiple of 64 and the CTA-pair GEMMs");
   if (p->d_in < 1 || p->d_out < 1) return fail(MLORA_ERR_INVALID, "d_in and d_out must be >= 1");
-  const int q = p->dtype == MLORA_BF16 ? 8 : 4;
+  const int q = p->dtype == MLORA_F32 ? 4 : 8;
   if (p->d_in % q || p->d_out % q)
     return fail(MLORA_ERR_UNSUPPORTED, "d_in and d_out must be multiples of 8 (bf16) or 4 (fp32)");
   if (p->n_tokens < 1 || p->n_tokens > 0x7fffffffLL) return fail(MLORA_ERR_INVALID, "n_tokens out of range");
@@ -342,7 +363,7 @@ void build_tables(mlora_plan_t* P) {
 
   // workspace: the two bf16 shadows At_all, Bt_all (rebuilt by every forward and backward call),
   // then the two image sets
-  if (pr.dtype == MLORA_BF16) {
+  if (pr.dtype != MLORA_F32) {
     const size_t shadow = round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024) +
                           round_up(static_cast<size_t>(P->C_total) * pr.d_out * 2, 1024);
     P->off_shadow = 0;
@@ -509,14 +530,24 @@ void mlora_plan_destroy(mlora_plan_t* plan) {
 
 int64_t mlora_h_elems(const mlora_plan_t* plan) { return plan ? plan->h_elems : -1; }
 
-mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt, void* Y, float* H, void* workspace,
-                           void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Forward of any dtype: Wt for bf16 / fp32 plans, (Wq, Ws) for 4-bit-base plans.
+mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, const void* Wq, const float* Ws, void* Y,
+                          float* H, void* workspace, void* stream) {
   g_last_error.clear();
   mlora_status st = check_exec(P);
   if (st != MLORA_OK) return st;
-  if (!X || !Wt || !Y || (!H && P->h_elems > 0)) return fail(MLORA_ERR_INVALID, "null tensor argument");
-  if (!aligned16(X) || !aligned16(Wt) || !aligned16(Y) || !aligned16(H))
-    return fail(MLORA_ERR_INVALID, "X, Wt, Y and H must be 16-byte aligned");
+  const bool w4 = P->prob.dtype == MLORA_BF16_W4;
+  if (w4 != (Wt == nullptr))
+    return fail(MLORA_ERR_INVALID, w4 ? "this plan has a 4-bit base: use mlora_forward_w4"
+                                      : "this plan has a bf16/fp32 base: use mlora_forward");
+  const void* Wany = w4 ? Wq : Wt;
+  if (!X || !Wany || !Y || (w4 && !Ws) || (!H && P->h_elems > 0)) return fail(MLORA_ERR_INVALID, "null tensor argument");
+  if (!aligned16(X) || !aligned16(Wany) || !aligned16(Y) || !aligned16(H) || !aligned16(Ws))
+    return fail(MLORA_ERR_INVALID, "X, the base weight, Y and H must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const mlora_problem& pr = P->prob;
   cudaError_t e;
@@ -537,10 +568,20 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
 
   const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
-  CUtensorMap mX, mAt, mW, mBt, mI;
+  CUtensorMap mX, mAt, mW, mBt, mI, mQ, mS;
   if ((st = make_map(&mX, X, pr.d_in, pr.n_tokens, pr.d_in, 64, 128)) != MLORA_OK) return st;
   if ((st = make_map(&mAt, at_all, pr.d_in, P->C_total, pr.d_in, 64, 64)) != MLORA_OK) return st;
-  if ((st = make_map(&mW, Wt, pr.d_in, pr.d_out, pr.d_in, 64, pairs ? 128 : 256)) != MLORA_OK) return st;
+  if (w4) {
+    // codes [d_out, d_in/2] bytes, box 32 bytes x 128 rows; scales [d_in/64, d_out], box 128 x 1
+    if ((st = make_map_plain(&mQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, pr.d_in / 2, pr.d_out, pr.d_in / 2, 32, 128)) !=
+        MLORA_OK)
+      return st;
+    if ((st = make_map_plain(&mS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Ws, pr.d_out, pr.d_in / 64, pr.d_out, 128, 1)) !=
+        MLORA_OK)
+      return st;
+  } else if ((st = make_map(&mW, Wt, pr.d_in, pr.d_out, pr.d_in, 64, pairs ? 128 : 256)) != MLORA_OK) {
+    return st;
+  }
   if ((st = make_map(&mBt, bt_all, P->C_total, pr.d_out, P->C_total, 64, pairs ? 128 : 256)) != MLORA_OK) return st;
   if ((st = make_map(&mI, himg, CHUNK_COLS, P->n_images * BM, CHUNK_COLS, 64, 128)) != MLORA_OK) return st;
 
@@ -558,7 +599,12 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
   g.n_tiles_n = (pr.d_out + BN - 1) / BN;
   g.out = Y;
   g.ld_out = pr.d_out;
-  if (pairs) {
+  if (w4) {
+    g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
+    e = timed(P, K_FWD_GEMM, s, [&] {
+      return launch_gemm_2sm_w4<MODE_FWD>(mX, mQ, mS, mBt, mI, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
+    });
+  } else if (pairs) {
     g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
     e = timed(P, K_FWD_GEMM, s, [&] {
       return launch_gemm_2sm<MODE_FWD>(mX, mW, mBt, mI, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
@@ -577,15 +623,23 @@ mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt,
   return MLORA_OK;
 }
 
-mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt, const void* dY, const float* H,
-                            void* dX, float* dH, void* workspace, void* stream) {
+// Backward of any dtype (see forward_impl).
+mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt, const void* Wq, const float* Ws,
+                           const void* dY, const float* H, void* dX, float* dH, void* workspace, void* stream) {
   g_last_error.clear();
   mlora_status st = check_exec(P);
   if (st != MLORA_OK) return st;
   if (!P->can_backward) return fail(MLORA_ERR_INVALID, "the plan's segments have no dAt/dBt buffers");
-  if (!X || !Wt || !dY || !dX || ((!H || !dH) && P->h_elems > 0)) return fail(MLORA_ERR_INVALID, "null tensor argument");
-  if (!aligned16(X) || !aligned16(Wt) || !aligned16(dY) || !aligned16(dX) || !aligned16(H) || !aligned16(dH))
-    return fail(MLORA_ERR_INVALID, "X, Wt, dY, dX, H and dH must be 16-byte aligned");
+  const bool w4 = P->prob.dtype == MLORA_BF16_W4;
+  if (w4 != (Wt == nullptr))
+    return fail(MLORA_ERR_INVALID, w4 ? "this plan has a 4-bit base: use mlora_backward_w4"
+                                      : "this plan has a bf16/fp32 base: use mlora_backward");
+  const void* Wany = w4 ? Wq : Wt;
+  if (!X || !Wany || !dY || !dX || (w4 && !Ws) || ((!H || !dH) && P->h_elems > 0))
+    return fail(MLORA_ERR_INVALID, "null tensor argument");
+  if (!aligned16(X) || !aligned16(Wany) || !aligned16(dY) || !aligned16(dX) || !aligned16(H) || !aligned16(dH) ||
+      !aligned16(Ws))
+    return fail(MLORA_ERR_INVALID, "X, the base weight, dY, dX, H and dH must be 16-byte aligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const mlora_problem& pr = P->prob;
   cudaError_t e;
@@ -617,11 +671,21 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   }
 
   const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
-  CUtensorMap mdY, mdYt, mBt64, mWmn, mAt64, mXt, mHi, mdHi, mdHi64;
+  CUtensorMap mdY, mdYt, mBt64, mWmn, mAt64, mXt, mHi, mdHi, mdHi64, mQ, mS;
   if ((st = make_map(&mdY, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 128)) != MLORA_OK) return st;
   if ((st = make_map(&mdYt, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mBt64, bt_all, P->C_total, pr.d_out, P->C_total, 64, 64)) != MLORA_OK) return st;
-  if ((st = make_map(&mWmn, Wt, pr.d_in, pr.d_out, pr.d_in, 64, 64)) != MLORA_OK) return st;
+  if (w4) {
+    // codes: 64 rows (d_out) x 64 bytes (128 d_in); scales: 64 (d_out) x 2 groups (d_in)
+    if ((st = make_map_plain(&mQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, pr.d_in / 2, pr.d_out, pr.d_in / 2, 64, 64)) !=
+        MLORA_OK)
+      return st;
+    if ((st = make_map_plain(&mS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Ws, pr.d_out, pr.d_in / 64, pr.d_out, 64, 2)) !=
+        MLORA_OK)
+      return st;
+  } else if ((st = make_map(&mWmn, Wt, pr.d_in, pr.d_out, pr.d_in, 64, 64)) != MLORA_OK) {
+    return st;
+  }
   if ((st = make_map(&mAt64, at_all, pr.d_in, P->C_total, pr.d_in, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mXt, X, pr.d_in, pr.n_tokens, pr.d_in, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mHi, himg, CHUNK_COLS, P->n_images * BM, CHUNK_COLS, 64, 64)) != MLORA_OK) return st;
@@ -650,7 +714,12 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   g.n_tiles_n = (pr.d_in + BN - 1) / BN;
   g.out = dX;
   g.ld_out = pr.d_in;
-  if (pairs) {
+  if (w4) {
+    g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
+    e = timed(P, K_BWD_GEMM, s, [&] {
+      return launch_gemm_2sm_w4<MODE_BWD>(mdY, mQ, mS, mAt64, mdHi, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
+    });
+  } else if (pairs) {
     g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
     e = timed(P, K_BWD_GEMM, s, [&] {
       return launch_gemm_2sm<MODE_BWD>(mdY, mWmn, mAt64, mdHi, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
@@ -668,6 +737,34 @@ mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt
   e = timed(P, K_DA, s, [&] { return launch_seg_gemm<MODE_DA>(mXt, mXt, mXt, mdHi64, g, grid_of(P, g.n_items), s); });
   if (e != cudaSuccess) return cuda_fail(e, "dA launch");
   return MLORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mlora_status mlora_forward(const mlora_plan_t* P, const void* X, const void* Wt, void* Y, float* H, void* workspace,
+                           void* stream) {
+  if (!Wt) return fail(MLORA_ERR_INVALID, "null tensor argument");
+  return forward_impl(P, X, Wt, nullptr, nullptr, Y, H, workspace, stream);
+}
+
+mlora_status mlora_forward_w4(const mlora_plan_t* P, const void* X, const void* Wq, const float* Wscale, void* Y,
+                              float* H, void* workspace, void* stream) {
+  if (!Wq || !Wscale) return fail(MLORA_ERR_INVALID, "null tensor argument");
+  return forward_impl(P, X, nullptr, Wq, Wscale, Y, H, workspace, stream);
+}
+
+mlora_status mlora_backward(const mlora_plan_t* P, const void* X, const void* Wt, const void* dY, const float* H,
+                            void* dX, float* dH, void* workspace, void* stream) {
+  if (!Wt) return fail(MLORA_ERR_INVALID, "null tensor argument");
+  return backward_impl(P, X, Wt, nullptr, nullptr, dY, H, dX, dH, workspace, stream);
+}
+
+mlora_status mlora_backward_w4(const mlora_plan_t* P, const void* X, const void* Wq, const float* Wscale,
+                               const void* dY, const float* H, void* dX, float* dH, void* workspace, void* stream) {
+  if (!Wq || !Wscale) return fail(MLORA_ERR_INVALID, "null tensor argument");
+  return backward_impl(P, X, nullptr, Wq, Wscale, dY, H, dX, dH, workspace, stream);
 }
 
 mlora_status mlora_adamw(const mlora_plan_t* P, float lr, float beta1, float beta2, float eps, float weight_decay,
@@ -775,11 +872,13 @@ int64_t mlora_launch_count(void) { return g_launches; }
 mlora_status mlora_memory_estimate(const mlora_plan_t* P, mlora_memory* out) {
   if (!P || !out) return fail(MLORA_ERR_INVALID, "null plan or output");
   const mlora_problem& pr = P->prob;
-  const int64_t e = pr.dtype == MLORA_BF16 ? 2 : 4;
+  const int64_t e = pr.dtype == MLORA_F32 ? 4 : 2;
   int64_t params = 0;
   for (const DevSeg& d : P->segs) params += static_cast<int64_t>(d.r) * (pr.d_in + pr.d_out);
   mlora_memory m{};
-  m.base_weight = static_cast<int64_t>(pr.d_in) * pr.d_out * e;
+  m.base_weight = pr.dtype == MLORA_BF16_W4
+                      ? static_cast<int64_t>(pr.d_in) * pr.d_out / 2 + static_cast<int64_t>(pr.d_in / 64) * pr.d_out * 4
+                      : static_cast<int64_t>(pr.d_in) * pr.d_out * e;
   m.activations = 2 * pr.n_tokens * (static_cast<int64_t>(pr.d_in) + pr.d_out) * e;
   m.lora_params = params * 4;
   m.lora_grad_state = 3 * m.lora_params;

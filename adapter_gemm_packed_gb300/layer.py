@@ -13,7 +13,8 @@ import torch
 
 from . import _mlora as M
 
-_DT = {"bf16": (M.MLORA_BF16, torch.bfloat16), "f32": (M.MLORA_F32, torch.float32)}
+_DT = {"bf16": (M.MLORA_BF16, torch.bfloat16), "f32": (M.MLORA_F32, torch.float32),
+       "bf16_w4": (M.MLORA_BF16_W4, torch.bfloat16)}
 
 
 def _ptr(t) -> int | None:
@@ -64,17 +65,29 @@ class PackedLoRA:
 
     # ---------------------------------------------------------------- calls
     def forward(self, X, Wt, Y=None, stream=None):
+        """Wt: the bf16/fp32 weight, or a (codes, scales) pair for a 4-bit-base plan."""
         if Y is None:
             Y = torch.empty((self.N, self.d_out), dtype=self.tdtype, device=self.device)
-        M.mlora_forward(self.plan, X.data_ptr(), Wt.data_ptr(), Y.data_ptr(), self.H.data_ptr(),
-                        self.workspace.data_ptr(), _stream(stream))
+        if self.dtype == "bf16_w4":
+            Wq, Ws = Wt
+            M.mlora_forward_w4(self.plan, X.data_ptr(), Wq.data_ptr(), Ws.data_ptr(), Y.data_ptr(), self.H.data_ptr(),
+                               self.workspace.data_ptr(), _stream(stream))
+        else:
+            M.mlora_forward(self.plan, X.data_ptr(), Wt.data_ptr(), Y.data_ptr(), self.H.data_ptr(),
+                            self.workspace.data_ptr(), _stream(stream))
         return Y
 
     def backward(self, X, Wt, dY, dX=None, stream=None):
         if dX is None:
             dX = torch.empty((self.N, self.d_in), dtype=self.tdtype, device=self.device)
-        M.mlora_backward(self.plan, X.data_ptr(), Wt.data_ptr(), dY.data_ptr(), self.H.data_ptr(), dX.data_ptr(),
-                         self.dH.data_ptr(), self.workspace.data_ptr(), _stream(stream))
+        if self.dtype == "bf16_w4":
+            Wq, Ws = Wt
+            M.mlora_backward_w4(self.plan, X.data_ptr(), Wq.data_ptr(), Ws.data_ptr(), dY.data_ptr(),
+                                self.H.data_ptr(), dX.data_ptr(), self.dH.data_ptr(), self.workspace.data_ptr(),
+                                _stream(stream))
+        else:
+            M.mlora_backward(self.plan, X.data_ptr(), Wt.data_ptr(), dY.data_ptr(), self.H.data_ptr(), dX.data_ptr(),
+                             self.dH.data_ptr(), self.workspace.data_ptr(), _stream(stream))
         return dX
 
     def adamw(self, lr, beta1, beta2, eps, weight_decay, step, stream=None):

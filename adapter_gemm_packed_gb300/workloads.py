@@ -202,8 +202,18 @@ def custom(name: str, cfg_id: int, d_in: int, d_out: int, ranks, n_tokens, alpha
                     w_std=w_std, a_std=a_std, b_std=b_std)
 
 
+def llama8b_qproj_w4() -> Workload:
+    """The q_proj workload with a 4-bit base weight (int4 codes, fp32 scales per 64 inputs)."""
+    wl = llama8b_qproj()
+    wl.name = "llama3_8b_q_proj_4096x4096_8ad_16384tok_w4base"
+    wl.cfg_id = 6
+    wl.dtype = "bf16_w4"
+    return wl
+
+
 CONFIGS = {
     "tiny": tiny_f32,
+    "qproj_w4": llama8b_qproj_w4,
     "qproj": llama8b_qproj,
     "mlp_up": mlp_up_lognormal,
     "many_small": llama70b_down_many_small,
@@ -212,20 +222,41 @@ CONFIGS = {
 
 def _act(wl: Workload, tid: int, n: int, std: float) -> np.ndarray:
     x = normal_f32(wl.cfg_id, tid, n, std)
-    return to_bf16_bits(x) if wl.dtype == "bf16" else x
+    return x if wl.dtype == "f32" else to_bf16_bits(x)
+
+
+T_WQ, T_WSCALE = 6, 7
+
+
+def w4_weight(wl: Workload):
+    """A 4-bit base weight for a ``bf16_w4`` workload: uniformly random code bytes
+    Wq [d_out, d_in/2] and positive fp32 group scales Wscale [d_in/64, d_out] around w_std/4,
+    so the dequantised weight has about the spread of the bf16 workloads' W."""
+    g = rng(wl.cfg_id, T_WQ)
+    Wq = g.integers(0, 256, size=(wl.d_out, wl.d_in // 2), dtype=np.uint8)
+    s = normal_f32(wl.cfg_id, T_WSCALE, (wl.d_in // 64) * wl.d_out, 0.1)
+    Wscale = (np.float32(wl.w_std / 4.0) * (np.float32(1.0) + np.abs(s))).reshape(wl.d_in // 64, wl.d_out)
+    return Wq, Wscale.astype(np.float32)
 
 
 def materialise(wl: Workload, with_dY: bool = True) -> Tensors:
-    """Draw every tensor of the workload (storage layout, see module doc)."""
+    """Draw every tensor of the workload (storage layout, see module doc).  For ``bf16_w4``
+    workloads ``Wt`` is None and ``Wq`` / ``Wscale`` hold the 4-bit base."""
     N = wl.N
-    Wt = _act(wl, T_W, wl.d_out * wl.d_in, wl.w_std).reshape(wl.d_out, wl.d_in)
+    if wl.dtype == "bf16_w4":
+        Wt = None
+    else:
+        Wt = _act(wl, T_W, wl.d_out * wl.d_in, wl.w_std).reshape(wl.d_out, wl.d_in)
     X = _act(wl, T_X, N * wl.d_in, 1.0).reshape(N, wl.d_in)
     dY = _act(wl, T_DY, N * wl.d_out, 1.0).reshape(N, wl.d_out) if with_dY else None
     At, Bt = [], []
     for i, r in enumerate(wl.ranks):
         At.append(normal_f32(wl.cfg_id, T_ADAPTER_BASE + 4 * i, r * wl.d_in, wl.a_std).reshape(r, wl.d_in))
         Bt.append(normal_f32(wl.cfg_id, T_ADAPTER_BASE + 4 * i + 1, wl.d_out * r, wl.b_std).reshape(wl.d_out, r))
-    return Tensors(wl, Wt, X, dY, At, Bt)
+    T = Tensors(wl, Wt, X, dY, At, Bt)
+    if wl.dtype == "bf16_w4":
+        T.Wq, T.Wscale = w4_weight(wl)
+    return T
 
 
 def optimizer_state(wl: Workload, which: str, i: int, shape, kind: str) -> np.ndarray:
@@ -241,6 +272,6 @@ def optimizer_state(wl: Workload, which: str, i: int, shape, kind: str) -> np.nd
 
 def rows_as_f64(a: np.ndarray, dtype: str) -> np.ndarray:
     """Exact fp64 view of stored values (bf16 bit patterns or fp32)."""
-    if dtype == "bf16":
+    if dtype in ("bf16", "bf16_w4"):
         return bf16_bits_to_f32(a).astype(np.float64)
     return np.asarray(a, dtype=np.float64)

@@ -158,7 +158,10 @@ def oracle_sample(wl, T, per_job):
     rows = np.concatenate([np.arange(o, o + min(per_job, n)) for o, n in zip(wl.offsets, wl.n_tokens)])
     X = W.rows_as_f64(T.X[rows], wl.dtype)
     dY = W.rows_as_f64(T.dY[rows], wl.dtype)
-    Wm = W.rows_as_f64(T.Wt, wl.dtype).T.copy()
+    if wl.dtype == "bf16_w4":
+        Wm = orc.dequantize_w4(T.Wq, T.Wscale)
+    else:
+        Wm = W.rows_as_f64(T.Wt, wl.dtype).T.copy()
     segs, off = [], 0
     for i, n in enumerate(wl.n_tokens):
         k = min(per_job, n)
@@ -256,14 +259,18 @@ def run_ours(args, wl, rank, world, local_rank):
     scales = [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
     layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At, Bt=T.Bt,
                        flags=0 if args.no_reuse else M.MLORA_REUSE_STAGING)
-    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
 
     def host(a):
-        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if wl.dtype == "bf16" else torch.from_numpy(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if wl.dtype != "f32" else torch.from_numpy(a)
         return t.pin_memory()
 
-    X_h, Wt_h, dY_h = host(T.X), host(T.Wt), host(T.dY)
-    X, Wt, dY = X_h.cuda(), Wt_h.cuda(), dY_h.cuda()
+    X_h, dY_h = host(T.X), host(T.dY)
+    X, dY = X_h.cuda(), dY_h.cuda()
+    if wl.dtype == "bf16_w4":
+        Wt = (torch.from_numpy(T.Wq).cuda(), torch.from_numpy(T.Wscale).cuda())
+    else:
+        Wt = host(T.Wt).cuda()
     Y = torch.empty((wl.N, wl.d_out), dtype=tdt, device="cuda")
     dX = torch.empty((wl.N, wl.d_in), dtype=tdt, device="cuda")
     stream = torch.cuda.current_stream()
@@ -399,7 +406,7 @@ def run_ours(args, wl, rank, world, local_rank):
             v["tflops"] = f / (v["ms_per_launch"] * 1e-3) / 1e12
         if b:
             v["gbs"] = b / (v["ms_per_launch"] * 1e-3) / 1e9
-    if wl.dtype == "bf16":
+    if wl.dtype != "f32":
         dom = max(("fwd_gemm", "bwd_gemm"), key=lambda k: kernels.get(k, {}).get("ms_per_launch", 0))
         dk = kernels[dom]
         # The burst figure is the larger (stricter) denominator; the sustained one is what a
@@ -428,7 +435,7 @@ def run_ours(args, wl, rank, world, local_rank):
     value = weak_scaling_rate(wl.N, world, args.steps, ms)
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "vs_baseline": None, "dtype": {"bf16": "bf16", "f32": "f32", "bf16_w4": "bf16 (4-bit base)"}[wl.dtype],
             "data": "synthetic (seeded Philox; shapes of the named workload, random-init adapters)",
             "config": config_of(wl, world, None if args.no_reuse else
                                 "MLORA_REUSE_STAGING (backward reuses the forward's bf16 shadows and staged H)"),

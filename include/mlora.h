@@ -59,8 +59,10 @@ typedef enum mlora_status {
 } mlora_status;
 
 typedef enum mlora_dtype {
-    MLORA_F32 = 0,   /* X, W, dY, Y, dX in fp32; true fp32 FFMA arithmetic */
-    MLORA_BF16 = 1   /* X, W, dY, Y, dX in bf16; tensor-core products with fp32 accumulation */
+    MLORA_F32 = 0,     /* X, W, dY, Y, dX in fp32; true fp32 FFMA arithmetic */
+    MLORA_BF16 = 1,    /* X, W, dY, Y, dX in bf16; tensor-core products with fp32 accumulation */
+    MLORA_BF16_W4 = 2  /* X, dY, Y, dX in bf16, the frozen W as 4-bit codes with fp32 group scales
+                          (mlora_forward_w4 / mlora_backward_w4); d_in a multiple of 64 */
 } mlora_dtype;
 
 /* mlora_problem.flags */
@@ -134,6 +136,22 @@ void mlora_plan_destroy(mlora_plan_t* plan);
  * H (fp32, packed as described above).  Reads At_i/Bt_i of every segment. */
 mlora_status mlora_forward(const mlora_plan_t* plan, const void* X, const void* Wt, void* Y, float* H,
                            void* workspace, void* stream);
+
+/* 4-bit base ("PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §5 and
+ * §11.3: a QLoRA-quantised base composes with packing; the pages do not fix the format).
+ * For plans of dtype MLORA_BF16_W4 the frozen W is given as
+ *   Wq     [d_out, d_in / 2] bytes: the signed 4-bit code q[o][k] in [-8, 7] of W[k][o], two per
+ *          byte, even k in the low nibble (two's complement);
+ *   Wscale [d_in / 64, d_out] fp32: one scale per 64 consecutive k of each output column;
+ * and the layer uses W[k][o] = bf16(q[o][k] * Wscale[k / 64][o]) (the product in fp32, rounded
+ * to nearest bf16), which is what the bf16 entry points would compute with that Wt.  Everything
+ * else (arguments, layouts, errors) is as for mlora_forward / mlora_backward.  Both pointers
+ * 16-byte aligned. */
+mlora_status mlora_forward_w4(const mlora_plan_t* plan, const void* X, const void* Wq, const float* Wscale,
+                              void* Y, float* H, void* workspace, void* stream);
+mlora_status mlora_backward_w4(const mlora_plan_t* plan, const void* X, const void* Wq, const float* Wscale,
+                               const void* dY, const float* H, void* dX, float* dH, void* workspace,
+                               void* stream);
 
 /* Backward pass given the upstream gradient dY and the forward's H:
  * writes dX, dH (fp32, packed like H) and every segment's dAt/dBt. */

@@ -155,6 +155,27 @@ def lora_grads(X: np.ndarray, dY: np.ndarray, segs: list[Seg]):
     return H, dH, dA, dB
 
 
+def dequantize_w4(Wq: np.ndarray, Wscale: np.ndarray) -> np.ndarray:
+    """The frozen base weight of a 4-bit-base layer, W (d_in x d_out), in float64.
+
+    "PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §5 / §11.3 name a
+    4-bit (QLoRA) base without fixing its format; the reading used here: Wq [d_out, d_in/2]
+    bytes hold signed 4-bit codes q[o][k] in [-8, 7] (even k in the low nibble, two's
+    complement) and Wscale [d_in/64, d_out] one scale per 64 consecutive k of each column:
+    W[k][o] = q[o][k] * Wscale[k // 64][o]."""
+    Wq = np.asarray(Wq, dtype=np.uint8)
+    d_out, half = Wq.shape
+    d_in = 2 * half
+    lo = (Wq & 0x0F).astype(np.int64)
+    hi = (Wq >> 4).astype(np.int64)
+    nib = np.empty((d_out, d_in), dtype=np.int64)
+    nib[:, 0::2] = lo
+    nib[:, 1::2] = hi
+    q = np.where(nib >= 8, nib - 16, nib).astype(np.float64)          # two's complement nibble
+    scale = np.repeat(np.asarray(Wscale, dtype=np.float64), 64, axis=0)  # [d_in, d_out]
+    return q.T * scale
+
+
 def adamw(p, g, m, v, lr, beta1, beta2, eps, weight_decay, t):
     """One decoupled-weight-decay AdamW step at step count t >= 1 (PLoRA §8 names the state;
     the order is PyTorch's AdamW): returns new (p, m, v)."""

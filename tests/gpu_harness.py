@@ -14,7 +14,7 @@ from adapter_gemm_packed_gb300 import workloads as W
 from adapter_gemm_packed_gb300.layer import PackedLoRA
 from oracle import lora_oracle as orc
 
-TOL = {"f32": 1e-4, "bf16": 2e-2}
+TOL = {"f32": 1e-4, "bf16": 2e-2, "bf16_w4": 2e-2}
 
 
 def rel_err(got, want) -> float:
@@ -29,13 +29,13 @@ def rel_err(got, want) -> float:
 
 
 def to_dev(a: np.ndarray, dtype: str):
-    if dtype == "bf16":
+    if dtype in ("bf16", "bf16_w4"):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
 
 
 def from_dev(t, dtype: str) -> np.ndarray:
-    if dtype == "bf16":
+    if dtype in ("bf16", "bf16_w4"):
         return W.bf16_bits_to_f32(t.view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
     return t.float().cpu().numpy().astype(np.float64)
 
@@ -59,7 +59,10 @@ class GpuRun:
         self.layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales_of(wl), dtype=wl.dtype,
                                 At=T.At, Bt=T.Bt, flags=flags)
         self.X = to_dev(T.X, wl.dtype)
-        self.Wt = to_dev(T.Wt if Wt_override is None else Wt_override, wl.dtype)
+        if wl.dtype == "bf16_w4":
+            self.Wt = (torch.from_numpy(T.Wq).cuda(), torch.from_numpy(T.Wscale).cuda())
+        else:
+            self.Wt = to_dev(T.Wt if Wt_override is None else Wt_override, wl.dtype)
         self.dY = to_dev(T.dY, wl.dtype)
         self.Y = self.layer.forward(self.X, self.Wt)
         self.dX = self.layer.backward(self.X, self.Wt, self.dY)
@@ -86,10 +89,17 @@ class GpuRun:
         self.layer.close()
 
 
+def base_weight_f64(wl, T, Wt_override=None):
+    """W (d_in x d_out) in fp64: the stored bf16/fp32 values, or the dequantised 4-bit base."""
+    if wl.dtype == "bf16_w4":
+        return orc.dequantize_w4(T.Wq, T.Wscale)
+    return W.rows_as_f64(T.Wt if Wt_override is None else Wt_override, wl.dtype).T
+
+
 def oracle_full(wl, T, Wt_override=None):
     """Every output of the layer (and the AdamW step at t=1 from zero moments), fp64."""
     X = W.rows_as_f64(T.X, wl.dtype)
-    Wm = W.rows_as_f64(T.Wt if Wt_override is None else Wt_override, wl.dtype).T
+    Wm = base_weight_f64(wl, T, Wt_override)
     dY = W.rows_as_f64(T.dY, wl.dtype)
     segs = oracle_segs(wl, T)
     Y, H = orc.forward(X, Wm, segs)

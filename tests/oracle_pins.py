@@ -344,6 +344,30 @@ def pin_adamw_torch(orc, seed=19):
     return None
 
 
+def pin_dequantize_w4(orc):
+    """Hand-worked codes: byte 0x7F holds code -1 (low nibble, even k) and code 7 (high nibble);
+    0x80 holds 0 and -8; 0x08 holds -8 and 0.  Columns k < 64 use scale row 0, k >= 64 row 1."""
+    d_out, d_in = 2, 128
+    Wq = np.zeros((d_out, d_in // 2), dtype=np.uint8)
+    Wq[0, 0] = 0x7F          # k=0: -1, k=1: 7
+    Wq[0, 40] = 0x80         # k=80 (byte 40, low): 0, k=81: -8
+    Wq[1, 10] = 0x08         # k=20: -8, k=21: 0
+    Wq[1, 63] = 0x5A         # k=126: 0xA -> -6, k=127: 5
+    Ws = np.array([[0.5, 2.0], [0.25, 4.0]])
+    W = orc.dequantize_w4(Wq, Ws)
+    want = {(0, 0): -0.5, (1, 0): 3.5, (80, 0): 0.0, (81, 0): -2.0, (20, 1): -16.0, (21, 1): 0.0,
+            (126, 1): -24.0, (127, 1): 20.0, (2, 0): 0.0, (64, 1): 0.0}
+    if W.shape != (d_in, d_out):
+        return f"dequantize_w4 shape {W.shape}"
+    for (k, o), v in want.items():
+        if W[k, o] != v:
+            return f"dequantize_w4 W[{k},{o}] = {W[k, o]}, want {v}"
+    full = orc.dequantize_w4(np.full((3, 64), 0x88, dtype=np.uint8), np.full((2, 3), 0.125))
+    if not np.all(full == -1.0):
+        return "dequantize_w4: all codes -8 at scale 1/8 must give -1"
+    return None
+
+
 ALL_PINS = [pin_hand_worked, pin_brute_force, pin_explicit_product, pin_special_cases,
             pin_packed_equals_separate, pin_finite_differences, pin_autograd, pin_linearity,
-            pin_adamw_hand_worked, pin_adamw_closed_form, pin_adamw_torch]
+            pin_adamw_hand_worked, pin_adamw_closed_form, pin_adamw_torch, pin_dequantize_w4]

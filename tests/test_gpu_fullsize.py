@@ -49,7 +49,7 @@ def check_fullsize(wl, step=True):
     errs = {}
     # sampled rows of Y and dX
     rows = sample_rows(wl)
-    Wm = W.rows_as_f64(T.Wt, wl.dtype).T
+    Wm = G.base_weight_f64(wl, T)
     segs = G.oracle_segs(wl, T)
     Yo = orc.forward_rows(W.rows_as_f64(T.X[rows], wl.dtype), rows, Wm, segs)
     dXo = orc.backward_rows(W.rows_as_f64(T.dY[rows], wl.dtype), rows, Wm, segs)
@@ -81,6 +81,10 @@ def check_fullsize(wl, step=True):
 
 def test_qproj_llama8b_fullsize():
     check_fullsize(W.llama8b_qproj())
+
+
+def test_qproj_llama8b_w4_base_fullsize():
+    check_fullsize(W.llama8b_qproj_w4())
 
 
 def test_mlp_up_lognormal_fullsize():

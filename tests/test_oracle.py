@@ -19,7 +19,7 @@ def test_oracle_pin(pin):
 def _mutant(**over):
     ns = types.SimpleNamespace(Seg=orc.Seg, forward=orc.forward, backward=orc.backward,
                                forward_rows=orc.forward_rows, backward_rows=orc.backward_rows,
-                               lora_grads=orc.lora_grads, adamw=orc.adamw)
+                               lora_grads=orc.lora_grads, adamw=orc.adamw, dequantize_w4=orc.dequantize_w4)
     for k, v in over.items():
         setattr(ns, k, v)
     return ns
@@ -88,7 +88,22 @@ def _adamw_eps_in_sqrt(p, g, m, v, lr, b1, b2, eps, wd, t):
     return p - lr * (m / (1 - b1 ** t)) / np.sqrt(v / (1 - b2 ** t) + eps), m, v
 
 
+def _dq_unsigned(Wq, Ws):
+    # mistake: codes read as unsigned 0..15
+    Wq = np.asarray(Wq, dtype=np.uint8)
+    nib = np.empty((Wq.shape[0], 2 * Wq.shape[1]))
+    nib[:, 0::2] = Wq & 15
+    nib[:, 1::2] = Wq >> 4
+    return nib.T * np.repeat(np.asarray(Ws, float), 64, axis=0)
+
+
+def _dq_swapped_nibbles(Wq, Ws):
+    return orc.dequantize_w4(((np.asarray(Wq, dtype=np.uint8) >> 4) | (np.asarray(Wq, dtype=np.uint8) << 4)).astype(np.uint8), Ws)
+
+
 MUTANTS = {
+    "w4_codes_unsigned": _mutant(dequantize_w4=_dq_unsigned),
+    "w4_nibbles_swapped": _mutant(dequantize_w4=_dq_swapped_nibbles),
     "scale_alpha_not_alpha_over_r": _mutant(Seg=SegAlphaScale),
     "forward_drops_lora_term": _mutant(forward=_fwd_no_lora),
     "dB_missing_scale": _mutant(backward=_bwd_dB_unscaled),

@@ -22,7 +22,7 @@ def built():
 
 def test_header_symbols_exported():
     hdr = open(os.path.join(ROOT, "include", "mlora.h")).read()
-    declared = set(re.findall(r"\b(mlora_[a-z_]+)\s*\(", hdr))
+    declared = set(re.findall(r"\b(mlora_[a-z0-9_]+)\s*\(", hdr))
     assert declared == set(M.EXPORTS)
     L = M.lib()
     for name in declared:
