@@ -38,16 +38,18 @@ __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ float code(uint32_t word, int e) {
-  const int nib = static_cast<int>((word >> (4 * e)) & 0xFu);
-  return static_cast<float>((nib ^ 8) - 8);
+// Code e (0..7) of a word whose nibbles were pre-flipped with 0x88888888, as an exact float:
+// 2^23 + (nib ^ 8) built by a bit-OR, minus 2^23 + 8, gives the signed code in [-8, 7].
+__device__ __forceinline__ float code(uint32_t flipped, int e) {
+  return __int_as_float(static_cast<int>(((flipped >> (4 * e)) & 0xFu) | 0x4B000000u)) - 8388616.0f;
 }
 
-// Forward: B row n (an output column) = 64 codes along d_in, one scale.
+// Forward: B row n = ct (an output column) = 64 codes along d_in, one scale.
 __device__ __forceinline__ void convert_fwd(const uint8_t* raw, const float* sc, uint8_t* b, int ct) {
   const uint4* rp = reinterpret_cast<const uint4*>(raw + ct * 32);
   const uint4 r0 = rp[0], r1 = rp[1];
-  const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+  const uint32_t w[8] = {r0.x ^ 0x88888888u, r0.y ^ 0x88888888u, r0.z ^ 0x88888888u, r0.w ^ 0x88888888u,
+                         r1.x ^ 0x88888888u, r1.y ^ 0x88888888u, r1.z ^ 0x88888888u, r1.w ^ 0x88888888u};
   const float s = sc[ct];
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
@@ -58,21 +60,25 @@ __device__ __forceinline__ void convert_fwd(const uint8_t* raw, const float* sc,
   }
 }
 
-// Backward: B row n (an input column) = the codes of 64 output rows at column n, one scale per row.
+// Backward: B row n (an input column) = the codes of 64 output rows k at column n, one scale per
+// row.  Thread ct converts an 8 (n) x 8 (k) block: n = 8 (ct >> 3) .. +7, k = 8 (ct & 7) .. +7,
+// from eight 32-bit loads (8 codes of one k row each), transposed in registers.
 __device__ __forceinline__ void convert_bwd(const uint8_t* raw, const float* sc, uint8_t* b, int ct) {
-  const int byte = ct >> 1, shift = (ct & 1) * 4;
-  const float* s = sc + (ct >> 6) * 64;
+  const int ng = ct >> 3, kg = ct & 7;
+  uint32_t wk[8];
+  float sk[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int kk = 0; kk < 8; ++kk) {
+    const int k = 8 * kg + kk;
+    wk[kk] = *reinterpret_cast<const uint32_t*>(raw + k * 64 + 4 * ng) ^ 0x88888888u;
+    sk[kk] = sc[(ng >> 3) * 64 + k];
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
     uint32_t pk[4];
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const int k = 8 * c + e;
-      const uint32_t n0 = (raw[k * 64 + byte] >> shift) & 0xFu, n1 = (raw[(k + 1) * 64 + byte] >> shift) & 0xFu;
-      pk[e / 2] = pack_bf16x2(static_cast<float>((static_cast<int>(n0) ^ 8) - 8) * s[k],
-                              static_cast<float>((static_cast<int>(n1) ^ 8) - 8) * s[k + 1]);
-    }
-    *reinterpret_cast<uint4*>(b + swz128_offset(ct, 8 * c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    for (int kk = 0; kk < 8; kk += 2) pk[kk / 2] = pack_bf16x2(code(wk[kk], j) * sk[kk], code(wk[kk + 1], j) * sk[kk + 1]);
+    *reinterpret_cast<uint4*>(b + swz128_offset(8 * ng + j, 8 * kg)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   }
 }
 
