@@ -19,6 +19,7 @@ MLORA_DEBUG_SHORT_TIMEOUT = 2
 MLORA_GEMM_SINGLE_CTA = 4
 MLORA_NO_OVERLAP = 8
 MLORA_REUSE_STAGING = 32
+MLORA_W4_FUSED = 64
 MLORA_DEBUG_DROP_COPY = 16
 MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD_B, MLORA_Q_WINDOW = range(6)
 

@@ -39,6 +39,7 @@ cudaError_t launch_pack_fwd(const DevSeg*, const int*, int, int, int, __nv_bfloa
 cudaError_t launch_h_images(const DevSeg*, const MTile*, const int*, int, long long, const float*, uint8_t*,
                             cudaStream_t, bool);
 cudaError_t launch_adamw(const AdamItem*, int, float, float, float, float, float, int, int, cudaStream_t, bool);
+cudaError_t launch_w4_expand(const void*, const float*, __nv_bfloat16*, int, int, int, cudaStream_t, bool);
 cudaError_t launch_f32_forward(const DevSeg*, int, long long, int, int, long long, const float*, const float*, float*,
                                float*, cudaStream_t);
 cudaError_t launch_f32_backward(const DevSeg*, int, long long, int, int, long long, int, const float*, const float*,
@@ -143,7 +144,8 @@ struct mlora_plan_s {
   std::vector<WItem> da, db;
   std::vector<AdamItem> adam;
   bool can_backward = false, can_adamw = false;
-  size_t off_shadow = 0, off_himg = 0, off_dhimg = 0, ws_bytes = 0;
+  size_t off_shadow = 0, off_himg = 0, off_dhimg = 0, off_wexp = 0, ws_bytes = 0;
+  bool w4_fused = false;   // 4-bit base expanded inside the GEMMs instead of into the workspace
   int group_m = 8;
   // device
   bool on_device = false;
@@ -166,6 +168,8 @@ struct mlora_plan_s {
   bool staged_valid = false;
   const void* staged_ws = nullptr;
   const float* staged_H = nullptr;
+  const void* staged_wq = nullptr;     // 4-bit base whose bf16 expansion the workspace holds
+  const float* staged_wscale = nullptr;
   // optional per-kernel timing with CUDA events recorded on the launching stream
   bool profiling = false;
   std::vector<cudaEvent_t> ev_pool;
@@ -180,8 +184,10 @@ mlora_status validate(const mlora_problem* p, const mlora_segment* s, int32_t n)
   if (n < 1) return fail(MLORA_ERR_INVALID, "n_segs must be >= 1");
   if (p->dtype != MLORA_F32 && p->dtype != MLORA_BF16 && p->dtype != MLORA_BF16_W4)
     return fail(MLORA_ERR_INVALID, "unknown dtype");
-  if (p->dtype == MLORA_BF16_W4 && (p->d_in % 64 || (p->flags & MLORA_GEMM_SINGLE_CTA)))
-    return fail(MLORA_ERR_UNSUPPORTED, "a 4-bit base needs d_in a multiple of 64 and the CTA-pair GEMMs");
+  if (p->dtype == MLORA_BF16_W4 && p->d_in % 64)
+    return fail(MLORA_ERR_UNSUPPORTED, "a 4-bit base needs d_in a multiple of 64");
+  if (p->dtype == MLORA_BF16_W4 && (p->flags & MLORA_W4_FUSED) && (p->flags & MLORA_GEMM_SINGLE_CTA))
+    return fail(MLORA_ERR_UNSUPPORTED, "the fused 4-bit GEMMs run on CTA pairs only");
   if (p->d_in < 1 || p->d_out < 1) return fail(MLORA_ERR_INVALID, "d_in and d_out must be >= 1");
   const int q = p->dtype == MLORA_F32 ? 4 : 8;
   if (p->d_in % q || p->d_out % q)
@@ -370,6 +376,11 @@ void build_tables(mlora_plan_t* P) {
     P->off_himg = round_up(shadow, 1024);
     P->off_dhimg = P->off_himg + static_cast<size_t>(P->n_images) * IMG_BYTES;
     P->ws_bytes = P->off_dhimg + static_cast<size_t>(P->n_images) * IMG_BYTES;
+    if (pr.dtype == MLORA_BF16_W4 && !P->w4_fused) {
+      // the bf16 expansion of the 4-bit base, Wt [d_out, d_in]
+      P->off_wexp = round_up(P->ws_bytes, 1024);
+      P->ws_bytes = P->off_wexp + static_cast<size_t>(pr.d_out) * pr.d_in * 2;
+    }
   } else {
     P->ws_bytes = 0;
   }
@@ -422,13 +433,13 @@ mlora_status upload(mlora_plan_t* P) {
 
 enum KernelId {
   K_PACK_FWD = 0, K_SHRINK, K_FWD_GEMM, K_PACK_BWD, K_H_IMAGES, K_DH, K_DB, K_BWD_GEMM, K_DA, K_ADAMW,
-  K_F32_FWD, K_F32_BWD, K_COUNT
+  K_F32_FWD, K_F32_BWD, K_W4_EXPAND, K_COUNT
 };
 const char* const kKernelNames[K_COUNT] = {
     "pack_fwd", "shrink", "fwd_gemm", "pack_bwd", "h_images", "dH", "dB", "bwd_gemm", "dA", "adamw",
-    "f32_forward", "f32_backward"};
+    "f32_forward", "f32_backward", "w4_expand"};
 // kernels launched by each id (a pack step is two kernels, the fp32 passes several)
-const int kKernelLaunches[K_COUNT] = {2, 1, 1, 2, 1, 1, 1, 1, 1, 1, 2, 4};   // pack steps are two kernels
+const int kKernelLaunches[K_COUNT] = {2, 1, 1, 2, 1, 1, 1, 1, 1, 1, 2, 4, 1};   // pack steps are two kernels
 
 long long g_launches = 0;
 
@@ -506,6 +517,7 @@ mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs,
   if (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT) P->timeout_ns = SHORT_TIMEOUT_NS;
   if (problem->flags & MLORA_NO_OVERLAP) P->pdl = false;
   if (problem->flags & MLORA_REUSE_STAGING) P->reuse_staging = true;
+  if (problem->flags & MLORA_W4_FUSED) P->w4_fused = true;
   // the copy-withholding test hook is honoured only with the 1 ms wait limit
   if ((problem->flags & MLORA_DEBUG_DROP_COPY) && (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT)) P->debug_drop = true;
   build_tables(P);
@@ -564,6 +576,15 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
       reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow + round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024));
   uint8_t* himg = ws + P->off_himg;
 
+  // A 4-bit base is expanded once into the workspace (then everything below is the bf16 path),
+  // unless the plan asked for the GEMMs that expand it in shared memory.
+  const bool fused4 = w4 && P->w4_fused;
+  if (w4 && !fused4) {
+    __nv_bfloat16* wexp = reinterpret_cast<__nv_bfloat16*>(ws + P->off_wexp);
+    e = timed(P, K_W4_EXPAND, s, [&] { return launch_w4_expand(Wq, Ws, wexp, pr.d_in, pr.d_out, P->num_sms, s, P->pdl); });
+    if (e != cudaSuccess) return cuda_fail(e, "4-bit expansion launch");
+    Wt = wexp;
+  }
   e = timed(P, K_PACK_FWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
 
@@ -571,7 +592,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
   CUtensorMap mX, mAt, mW, mBt, mI, mQ, mS;
   if ((st = make_map(&mX, X, pr.d_in, pr.n_tokens, pr.d_in, 64, 128)) != MLORA_OK) return st;
   if ((st = make_map(&mAt, at_all, pr.d_in, P->C_total, pr.d_in, 64, 64)) != MLORA_OK) return st;
-  if (w4) {
+  if (fused4) {
     // codes [d_out, d_in/2] bytes, box 32 bytes x 128 rows; scales [d_in/64, d_out], box 128 x 1
     if ((st = make_map_plain(&mQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, pr.d_in / 2, pr.d_out, pr.d_in / 2, 32, 128)) !=
         MLORA_OK)
@@ -599,7 +620,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
   g.n_tiles_n = (pr.d_out + BN - 1) / BN;
   g.out = Y;
   g.ld_out = pr.d_out;
-  if (w4) {
+  if (fused4) {
     g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
     e = timed(P, K_FWD_GEMM, s, [&] {
       return launch_gemm_2sm_w4<MODE_FWD>(mX, mQ, mS, mBt, mI, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
@@ -619,6 +640,8 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
     Pm->staged_valid = true;
     Pm->staged_ws = workspace;
     Pm->staged_H = H;
+    Pm->staged_wq = w4 && !fused4 ? Wq : nullptr;
+    Pm->staged_wscale = w4 && !fused4 ? Ws : nullptr;
   }
   return MLORA_OK;
 }
@@ -663,6 +686,17 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   // MLORA_REUSE_STAGING, when this workspace and H are the ones the last forward used (and no
   // AdamW step ran since), they are still in place and are not rebuilt.
   const bool reuse = P->reuse_staging && P->staged_valid && P->staged_ws == workspace && P->staged_H == H;
+  const bool fused4 = w4 && P->w4_fused;
+  if (w4 && !fused4) {
+    // the bf16 expansion of the 4-bit base; with reuse, the forward's is still in place when it
+    // expanded the same codes and scales
+    __nv_bfloat16* wexp = reinterpret_cast<__nv_bfloat16*>(ws + P->off_wexp);
+    if (!(reuse && P->staged_wq == Wq && P->staged_wscale == Ws)) {
+      e = timed(P, K_W4_EXPAND, s, [&] { return launch_w4_expand(Wq, Ws, wexp, pr.d_in, pr.d_out, P->num_sms, s, P->pdl); });
+      if (e != cudaSuccess) return cuda_fail(e, "4-bit expansion launch");
+    }
+    Wt = wexp;
+  }
   if (!reuse) {
     e = timed(P, K_PACK_BWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
@@ -675,7 +709,7 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   if ((st = make_map(&mdY, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 128)) != MLORA_OK) return st;
   if ((st = make_map(&mdYt, dY, pr.d_out, pr.n_tokens, pr.d_out, 64, 64)) != MLORA_OK) return st;
   if ((st = make_map(&mBt64, bt_all, P->C_total, pr.d_out, P->C_total, 64, 64)) != MLORA_OK) return st;
-  if (w4) {
+  if (fused4) {
     // codes: 64 rows (d_out) x 64 bytes (128 d_in); scales: 64 (d_out) x 2 groups (d_in)
     if ((st = make_map_plain(&mQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, pr.d_in / 2, pr.d_out, pr.d_in / 2, 64, 64)) !=
         MLORA_OK)
@@ -714,7 +748,7 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   g.n_tiles_n = (pr.d_in + BN - 1) / BN;
   g.out = dX;
   g.ld_out = pr.d_in;
-  if (w4) {
+  if (fused4) {
     g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
     e = timed(P, K_BWD_GEMM, s, [&] {
       return launch_gemm_2sm_w4<MODE_BWD>(mdY, mQ, mS, mAt64, mdHi, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);

@@ -8,77 +8,92 @@
 //   Wscale [d_in / 64, d_out] fp32 (group-major, so one K slice's scales are contiguous)
 //
 // The kernel is the bf16 CTA-pair kernel of gemm_2sm.cu with the B operand of the main K loop
-// produced in shared memory by four converter warps instead of copied by TMA: the producer
-// copies the 4-bit tile and its scales (4.5 KB per CTA per K slice instead of 16 KB), the
-// converters expand them to bf16 (round to nearest) in the 128B-swizzled K-major layout the
-// MMA reads, fence the writes for the tensor core's async proxy and arrive on the even CTA's
-// full barrier.  Forward B rows are output columns (codes read along d_in); backward B rows are
-// input columns (codes read across d_out rows, transposed on the way).  The rank term's K slices
-// are bf16 and arrive by TMA exactly as in the bf16 kernel.
+// produced in shared memory by eight converter warps instead of copied by TMA.  A separate
+// producer warp copies the 4-bit tiles and their scales (4.5 KB per CTA per K slice instead of
+// 16 KB) into an 8-slot ring of their own, so those copies run ahead of the MMA.  A converter
+// warp expands its share of a tile into registers (bf16, round to nearest) before the slot of
+// the main ring is free, then only stores it, fences the writes for the tensor core's async
+// proxy and signals the even CTA's full barrier with a 16-byte bulk copy (its transaction bytes
+// are part of the barrier's expected count; a cluster-scope release arrive would put a memory
+// barrier on the converters' serial path).  Forward B rows are output columns and the codes run
+// along them (K-major B); backward B is read MN-major, so the codes of one d_out row, which
+// run along d_in, land in place without a transpose.  The rank term's K slices are bf16 and
+// arrive by TMA exactly as in the bf16 kernel.
 //
-// Roles (320 threads): warp 0 TMA, warp 1 MMA (even CTA), warps 2-5 epilogue, warps 6-9 converters.
+// Roles (480 threads): warp 0 TMA for A (and the rank term), warp 1 MMA (even CTA), warps 2-5
+// epilogue, warps 6-13 converters, warp 14 TMA for the 4-bit tiles.
 #include "common.cuh"
 #include "pair.cuh"
+#include "w4.cuh"
 
 namespace mlora {
 
 using namespace pair;
+using w4::expand8;
 
 namespace {
 
-constexpr int SW = 5;                          // pipeline stages
-constexpr int W4_THREADS = 320;
+constexpr int SW = 5;                          // main ring stages (A and bf16 B)
+constexpr int RW = 8;                          // 4-bit ring stages
+constexpr int N_CONV_WARPS = 8;
+constexpr int W4_THREADS = 32 * (7 + N_CONV_WARPS);
+constexpr int RAWP_WARP = 6 + N_CONV_WARPS;    // the 4-bit tile producer
 constexpr int A_BYTES = 128 * BK * 2;          // this CTA's 128 rows of A per stage
 constexpr int B_BYTES = 128 * BK * 2;          // this CTA's 128-row half of B per stage (bf16)
 constexpr int RAW_BYTES = 128 * BK / 2;        // the same half of B as 4-bit codes
 constexpr int SC_BYTES = 128 * 4;              // its scales
-constexpr int SMEM_W4 = SW * (A_BYTES + B_BYTES + RAW_BYTES + SC_BYTES) + 1024 + 512;
+constexpr int SIG_BYTES = 16;                  // one converter warp's ready signal
+constexpr int N_SIG = 2 * N_CONV_WARPS;        // signals per stage (both CTAs)
+constexpr int BAR_AREA = 2048;
+constexpr int SMEM_W4 = SW * (A_BYTES + B_BYTES) + RW * (RAW_BYTES + SC_BYTES) + BAR_AREA + 1024;
 
 __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Code e (0..7) of a word whose nibbles were pre-flipped with 0x88888888, as an exact float:
-// 2^23 + (nib ^ 8) built by a bit-OR, minus 2^23 + 8, gives the signed code in [-8, 7].
-__device__ __forceinline__ float code(uint32_t flipped, int e) {
-  return __int_as_float(static_cast<int>(((flipped >> (4 * e)) & 0xFu) | 0x4B000000u)) - 8388616.0f;
+// One converter thread's share of a K slice: 32 codes, as four 16-byte bf16 groups.
+struct Share {
+  uint4 v[4];
+};
+
+// Forward: B row n (an output column) holds 64 codes along d_in with one scale.  Thread ct
+// (0..255) takes half a row: n = ct / 2, codes 32 (ct % 2) .. +31 (one 16-byte load; a warp
+// reads 512 contiguous bytes).
+__device__ __forceinline__ void expand_fwd(const uint8_t* raw, const float* sc, int ct, uint64_t magic2, Share& o) {
+  const uint4 w = *reinterpret_cast<const uint4*>(raw + ct * 16);
+  const float s = sc[ct >> 1];
+  o.v[0] = expand8(w.x, s, magic2);
+  o.v[1] = expand8(w.y, s, magic2);
+  o.v[2] = expand8(w.z, s, magic2);
+  o.v[3] = expand8(w.w, s, magic2);
 }
 
-// Forward: B row n = ct (an output column) = 64 codes along d_in, one scale.
-__device__ __forceinline__ void convert_fwd(const uint8_t* raw, const float* sc, uint8_t* b, int ct) {
-  const uint4* rp = reinterpret_cast<const uint4*>(raw + ct * 32);
-  const uint4 r0 = rp[0], r1 = rp[1];
-  const uint32_t w[8] = {r0.x ^ 0x88888888u, r0.y ^ 0x88888888u, r0.z ^ 0x88888888u, r0.w ^ 0x88888888u,
-                         r1.x ^ 0x88888888u, r1.y ^ 0x88888888u, r1.z ^ 0x88888888u, r1.w ^ 0x88888888u};
-  const float s = sc[ct];
+__device__ __forceinline__ void store_fwd(uint8_t* b, int ct, const Share& o) {
+  const int n = ct >> 1, c0 = 4 * (ct & 1);
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint32_t pk[4];
+  for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(b + swz128_offset(n, 8 * (c0 + j))) = o.v[j];
+}
+
+// Backward: row k of the tile (a d_out row, K of dX = dY W^T) holds 128 codes along d_in (N);
+// scale (n / 64, k).  Word L = 256 j + ct (j = 0..3) is codes n = 8 (L % 16) .. +7 of row
+// k = L / 16; it lands, still in n order, in the MN-major 128B-swizzled layout: 64-wide n
+// blocks 8 KB apart, one 128-byte line per k.
+__device__ __forceinline__ void expand_bwd(const uint8_t* raw, const float* sc, int ct, uint64_t magic2, Share& o) {
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) pk[e / 2] = pack_bf16x2(code(w[c], e) * s, code(w[c], e + 1) * s);
-    *reinterpret_cast<uint4*>(b + swz128_offset(ct, 8 * c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  for (int j = 0; j < 4; ++j) {
+    const int L = 256 * j + ct;
+    const int k = L >> 4, ng = L & 15;
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + 4 * L);
+    o.v[j] = expand8(w, sc[(ng >> 3) * 64 + k], magic2);
   }
 }
 
-// Backward: B row n (an input column) = the codes of 64 output rows k at column n, one scale per
-// row.  Thread ct converts an 8 (n) x 8 (k) block: n = 8 (ct >> 3) .. +7, k = 8 (ct & 7) .. +7,
-// from eight 32-bit loads (8 codes of one k row each), transposed in registers.
-__device__ __forceinline__ void convert_bwd(const uint8_t* raw, const float* sc, uint8_t* b, int ct) {
-  const int ng = ct >> 3, kg = ct & 7;
-  uint32_t wk[8];
-  float sk[8];
+__device__ __forceinline__ void store_bwd(uint8_t* b, int ct, const Share& o) {
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const int k = 8 * kg + kk;
-    wk[kk] = *reinterpret_cast<const uint32_t*>(raw + k * 64 + 4 * ng) ^ 0x88888888u;
-    sk[kk] = sc[(ng >> 3) * 64 + k];
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint32_t pk[4];
-#pragma unroll
-    for (int kk = 0; kk < 8; kk += 2) pk[kk / 2] = pack_bf16x2(code(wk[kk], j) * sk[kk], code(wk[kk + 1], j) * sk[kk + 1]);
-    *reinterpret_cast<uint4*>(b + swz128_offset(8 * ng + j, 8 * kg)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  for (int j = 0; j < 4; ++j) {
+    const int L = 256 * j + ct;
+    const int k = L >> 4, ng = L & 15;
+    *reinterpret_cast<uint4*>(b + (ng >> 3) * 8192 + swz128_offset(k, 8 * (ng & 7))) = o.v[j];
   }
 }
 
@@ -97,16 +112,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + SW * A_BYTES;
   uint8_t* sQ = sB + SW * B_BYTES;
-  uint8_t* sS = sQ + SW * RAW_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + SW * SC_BYTES);
-  uint64_t* full = bars;               // [SW] (even CTA) A bytes of both CTAs + 8 converter warps + producer
-  uint64_t* empty = bars + SW;         // [SW] MMA -> producer and converters of each CTA
-  uint64_t* qfull = bars + 2 * SW;     // [SW] this CTA's 4-bit tile and scales -> its converters
-  uint64_t* tfull = bars + 3 * SW;     // [2]
+  uint8_t* sS = sQ + RW * RAW_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + RW * SC_BYTES);
+  uint64_t* full = bars;               // [SW] (even CTA) producer + A bytes of both CTAs + warp signals
+  uint64_t* empty = full + SW;         // [SW] MMA -> producer and converters of each CTA
+  uint64_t* qfull = empty + SW;        // [RW] this CTA's 4-bit tile and scales -> its converters
+  uint64_t* qempty = qfull + RW;       // [RW] this CTA's converter warps -> the 4-bit producer
+  uint64_t* tfull = qempty + RW;       // [2]
   uint64_t* tempty = tfull + 2;        // [2]  (even CTA) both CTAs' epilogues
   uint64_t* done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint8_t* sig_dst = reinterpret_cast<uint8_t*>(bars) + 1024;    // [N_SIG][16] (even CTA) signal landing slots
+  uint8_t* sig_src = sig_dst + N_SIG * SIG_BYTES;               // [16] this CTA's signal payload
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -115,9 +133,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SW; ++s) {
-      mbar_init(&full[s], 9);   // the even CTA's producer (arrive.expect_tx) + 8 converter warps
+      mbar_init(&full[s], 1);   // the even CTA's producer (arrive.expect_tx); the rest is bytes
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < RW; ++s) {
       mbar_init(&qfull[s], 1);
+      mbar_init(&qempty[s], N_CONV_WARPS);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -160,19 +181,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
             break;
           }
           const bool main_part = kb < g.kmain;
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * A_BYTES + (main_part ? 0 : 2 * B_BYTES));
+          if (leader)
+            mbar_arrive_expect_tx(&full[stage], 2 * A_BYTES + (main_part ? 0 : 2 * B_BYTES) + N_SIG * SIG_BYTES);
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
           uint8_t* a = sA + stage * A_BYTES;
           if (main_part) {
             tma_load_2d_pair(a, &tmA, bar, kb * BK, m0);
-            mbar_arrive_expect_tx(&qfull[stage], RAW_BYTES + SC_BYTES);
-            if constexpr (MODE == MODE_FWD) {
-              tma_load_2d(sQ + stage * RAW_BYTES, &tmQ, &qfull[stage], kb * (BK / 2), nh0);
-              tma_load_2d(sS + stage * SC_BYTES, &tmS, &qfull[stage], nh0, kb);
-            } else {
-              tma_load_2d(sQ + stage * RAW_BYTES, &tmQ, &qfull[stage], nh0 / 2, kb * BK);
-              tma_load_2d(sS + stage * SC_BYTES, &tmS, &qfull[stage], kb * BK, nh0 / 64);
-            }
           } else {
             const int e = kb - g.kmain;
             uint8_t* b = sB + stage * B_BYTES;
@@ -191,6 +205,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
         }
       }
     }
+  } else if (warp == RAWP_WARP) {
+    if (lane == 0) {
+      // the 4-bit tiles of every main K slice, in the order the converters take them
+      const uint64_t keep = l2_policy_evict_last();
+      int rs = 0;
+      uint32_t rphase = 0;
+      bool ok = true;
+      for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
+        int mp, n;
+        decode_pair(g, item, mp, n);
+        const int nh0 = n * BN + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < g.kmain; ++kb) {
+          if (!mbar_wait(&qempty[rs], rphase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&qfull[rs], RAW_BYTES + SC_BYTES);
+          if constexpr (MODE == MODE_FWD) {
+            tma_load_2d_hint(sQ + rs * RAW_BYTES, &tmQ, &qfull[rs], kb * (BK / 2), nh0, keep);
+            tma_load_2d_hint(sS + rs * SC_BYTES, &tmS, &qfull[rs], nh0, kb, keep);
+          } else {
+            tma_load_2d_hint(sQ + rs * RAW_BYTES, &tmQ, &qfull[rs], nh0 / 2, kb * BK, keep);
+            tma_load_2d_hint(sS + rs * SC_BYTES, &tmS, &qfull[rs], kb * BK, nh0 / 64, keep);
+          }
+          if (++rs == RW) {
+            rs = 0;
+            rphase ^= 1u;
+          }
+        }
+      }
+    }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
       int stage = 0;
@@ -198,8 +243,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      const uint32_t idesc_k = idesc_bf16(2 * BM, BN, false, false);
-      const uint32_t idesc_mn = idesc_bf16(2 * BM, BN, false, true);
+      // backward B is MN-major throughout (converted W^T slices and the rank term alike)
+      const uint32_t idesc = idesc_bf16(2 * BM, BN, false, MODE == MODE_BWD);
       for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
         int mp, n;
         decode_pair(g, item, mp, n);
@@ -218,13 +263,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
           tc_fence_after();
           const uint32_t a = smem_u32(sA + stage * A_BYTES);
           const uint32_t b = smem_u32(sB + stage * B_BYTES);
-          // main K slices: converted B, K-major; rank-term slices: as in the bf16 kernel
-          const bool b_mn = (MODE == MODE_BWD) && kb >= g.kmain;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = smem_desc(a + k * 32, 16, 1024);
-            const uint64_t bd = b_mn ? smem_desc(b + k * 2048, 64 * 64 * 2, 1024) : smem_desc(b + k * 32, 16, 1024);
-            umma_pair_bf16(d_tmem, ad, bd, b_mn ? idesc_mn : idesc_k, (kb > 0 || k > 0) ? 1u : 0u);
+            const uint64_t bd = MODE == MODE_BWD ? smem_desc(b + k * 2048, 64 * 64 * 2, 1024)
+                                                 : smem_desc(b + k * 32, 16, 1024);
+            umma_pair_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           umma_pair_commit_mc(&empty[stage], 0x3);
           if (++stage == SW) {
@@ -294,40 +338,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
       if (acc == 0) acc_phase ^= 1u;
     }
   } else {
-    // converters: 128 threads, thread ct expands row ct of this CTA's B half
+    // converters: 256 threads; every K slice of the main ring gets one signal per warp
     const int ct = threadIdx.x - 192;
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t qphase = 0;   // bit s: parity of qfull[s], which completes only on main-K uses of slot s
+    const int cw = ct >> 5;
+    const uint32_t my_sig = mapa_shared(smem_u32(sig_dst + (N_CONV_WARPS * static_cast<int>(rank) + cw) * SIG_BYTES), 0);
+    const uint64_t magic2 = w4::magic_pair();
+    int stage = 0, rs = 0;
+    uint32_t phase = 0, rphase = 0;
     bool ok = true;
     for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
       int mp, n;
       decode_pair(g, item, mp, n);
       const int nkb = g.kmain + g.mtiles[min(2 * mp + static_cast<int>(rank), g.n_mtiles - 1)].nch;
       for (int kb = 0; kb < nkb; ++kb) {
-        // the slot is free (MMA done with its previous use) ...
+        const bool main_part = kb < g.kmain;
+        Share sh;
+        if (main_part) {
+          // expand this share of the 4-bit tile into registers and hand its slot back ...
+          if (!mbar_wait(&qfull[rs], rphase, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* raw = sQ + rs * RAW_BYTES;
+          const float* sc = reinterpret_cast<const float*>(sS + rs * SC_BYTES);
+          if constexpr (MODE == MODE_FWD)
+            expand_fwd(raw, sc, ct, magic2, sh);
+          else
+            expand_bwd(raw, sc, ct, magic2, sh);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&qempty[rs]);
+          if (++rs == RW) {
+            rs = 0;
+            rphase ^= 1u;
+          }
+        }
+        // ... then wait for the main ring's slot (the MMA done with its previous use)
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
           ok = false;
           break;
         }
-        if (kb < g.kmain) {
-          // ... and its 4-bit tile has landed
-          if (!mbar_wait(&qfull[stage], (qphase >> stage) & 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
-            ok = false;
-            break;
-          }
-          qphase ^= 1u << stage;
-          const uint8_t* raw = sQ + stage * RAW_BYTES;
-          const float* sc = reinterpret_cast<const float*>(sS + stage * SC_BYTES);
+        if (main_part) {
           uint8_t* b = sB + stage * B_BYTES;
           if constexpr (MODE == MODE_FWD)
-            convert_fwd(raw, sc, b, ct);
+            store_fwd(b, ct, sh);
           else
-            convert_bwd(raw, sc, b, ct);
+            store_bwd(b, ct, sh);
           fence_async_shared();   // generic-proxy writes -> visible to the tensor core
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&full[stage]), 0));
+        if (lane == 0) bulk_signal_remote(my_sig, sig_src, mapa_shared(smem_u32(&full[stage]), 0));
         if (++stage == SW) {
           stage = 0;
           phase ^= 1u;

@@ -69,6 +69,17 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 
+// Signal a barrier of a CTA of the cluster through the async proxy: a 16-byte bulk copy from
+// this CTA's shared memory into `dst_cluster`, completing 16 bytes of transaction count on
+// `bar_cluster` (a barrier in the destination CTA).  Unlike a cluster-scope release arrive, the
+// issuing thread does not wait for its earlier memory operations to be acknowledged.
+__device__ __forceinline__ void bulk_signal_remote(uint32_t dst_cluster, const void* src, uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], 16, [%2];" ::"r"(
+                   dst_cluster),
+               "r"(smem_u32(src)), "r"(bar_cluster)
+               : "memory");
+}
+
 __device__ __forceinline__ void decode_pair(const GemmArgs& g, int item, int& mp, int& n) {
   const int n_pairs = (g.n_mtiles + 1) >> 1;
   const int per_group = g.group_m * g.n_tiles_n;

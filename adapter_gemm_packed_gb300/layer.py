@@ -121,7 +121,7 @@ class PackedLoRA:
 
 
 def host_plan(d_in, d_out, ranks, n_tokens, dtype="bf16", scales=None, offsets=None, n_total=None,
-              with_moments=True):
+              with_moments=True, flags=0):
     """Build a host-only plan (no CUDA call) over placeholder pointers, for inspecting the
     planner's tables.  Returns (handle, workspace_bytes); destroy with mlora_plan_destroy."""
     code = _DT[dtype][0]
@@ -135,5 +135,6 @@ def host_plan(d_in, d_out, ranks, n_tokens, dtype="bf16", scales=None, offsets=N
             ptrs[4:] = [None] * 4
         segs.append(M.mlora_segment(o, n, r, s, *ptrs))
         off += n
-    prob = M.mlora_problem(sum(n_tokens) if n_total is None else n_total, d_in, d_out, code, M.MLORA_PLAN_HOST_ONLY)
+    prob = M.mlora_problem(sum(n_tokens) if n_total is None else n_total, d_in, d_out, code,
+                           M.MLORA_PLAN_HOST_ONLY | flags)
     return M.mlora_plan(prob, segs)

@@ -80,6 +80,9 @@ def kernel_bytes(wl, kernel):
         return wl.N * wl.d_out * e + lora * 2 + wl.d_out * sr * 4
     if kernel == "adamw":
         return params * 28
+    if kernel == "w4_expand":
+        # codes (half a byte), scales (4 bytes per 64 weights) in; bf16 W^T out
+        return wl.d_in * wl.d_out * (0.5 + 4 / 64 + 2)
     return None
 
 
@@ -230,6 +233,16 @@ def config_of(wl, ngpus, options=None):
     return c
 
 
+def options_of(wl, args):
+    opts = []
+    if not args.no_reuse:
+        opts.append("MLORA_REUSE_STAGING (backward reuses the forward's bf16 shadows and staged H)")
+    if wl.dtype == "bf16_w4":
+        opts.append("MLORA_W4_FUSED (codes expanded inside the base GEMMs)" if args.w4_fused else
+                    "4-bit base expanded to bf16 once per call, then the bf16 GEMMs")
+    return "; ".join(opts) or None
+
+
 def traffic_record(kernel):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -257,8 +270,9 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     T = W.materialise(wl)
     scales = [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
+    flags = (0 if args.no_reuse else M.MLORA_REUSE_STAGING) | (M.MLORA_W4_FUSED if args.w4_fused else 0)
     layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At, Bt=T.Bt,
-                       flags=0 if args.no_reuse else M.MLORA_REUSE_STAGING)
+                       flags=flags)
     tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
 
     def host(a):
@@ -429,7 +443,7 @@ def run_ours(args, wl, rank, world, local_rank):
         roof = {"kernel": dom, "bound": "alu", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
                 "peak_source": "derived: SMs x 128 FP32 lanes x 2 FLOP x max SM clock", "traffic": None}
     hbm = peaks.get("hbm_gbs")
-    for k in ("shrink", "dH", "dA", "dB", "adamw"):
+    for k in ("shrink", "dH", "dA", "dB", "adamw", "w4_expand"):
         if k in kernels and "gbs" in kernels[k]:
             kernels[k]["frac_of_hbm"] = kernels[k]["gbs"] / hbm
     value = weak_scaling_rate(wl.N, world, args.steps, ms)
@@ -437,8 +451,7 @@ def run_ours(args, wl, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": {"bf16": "bf16", "f32": "f32", "bf16_w4": "bf16 (4-bit base)"}[wl.dtype],
             "data": "synthetic (seeded Philox; shapes of the named workload, random-init adapters)",
-            "config": config_of(wl, world, None if args.no_reuse else
-                                "MLORA_REUSE_STAGING (backward reuses the forward's bf16 shadows and staged H)"),
+            "config": config_of(wl, world, options_of(wl, args)),
             "tflops": flops_per_step(wl) * world * args.steps / (ms / 1e3) / 1e12,
             "roofline": roof, "kernels": kernels, "kernel_timing_ms_per_step": prof_step_ms,
             "gpu_launches": launches, "e2e": e2e,
@@ -468,6 +481,7 @@ def main():
     ap.add_argument("--workload", default="qproj")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-reuse", action="store_true", help="rebuild the backward's staging (no MLORA_REUSE_STAGING)")
+    ap.add_argument("--w4-fused", action="store_true", help="4-bit base: expand inside the GEMMs (MLORA_W4_FUSED)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens-per-job", type=int, default=64)

@@ -76,14 +76,21 @@ typedef enum mlora_dtype {
                                           MLORA_ERR_TIMEOUT; that call's outputs are undefined */
 #define MLORA_REUSE_STAGING 32u       /* mlora_backward skips rebuilding the bf16 adapter shadows and the
                                           staged s*H images when its workspace and H are the ones the last
-                                          mlora_forward of this plan used and no mlora_adamw ran since; the
-                                          caller guarantees that neither At/Bt, H nor that workspace changed
-                                          in between (results are then identical to the full backward) */
+                                          mlora_forward of this plan used and no mlora_adamw ran since (and,
+                                          for a 4-bit base, the bf16 expansion of W when Wq and Wscale are the
+                                          forward's pointers); the caller guarantees that neither At/Bt, H,
+                                          Wq/Wscale nor that workspace changed in between (results are then
+                                          identical to the full backward) */
 #define MLORA_NO_OVERLAP 8u            /* launch every kernel strictly after the previous one (no programmatic
                                           dependent launch overlapping a kernel's prologue with the tail of
                                           the one before); results are identical either way */
 #define MLORA_GEMM_SINGLE_CTA 4u       /* run the two base GEMMs on single-CTA 128x256 tiles instead of
                                           CTA pairs (256x256 tiles); same results up to rounding order */
+#define MLORA_W4_FUSED 64u             /* 4-bit base only: expand the codes to bf16 inside the CTA-pair base
+                                          GEMMs (converter warps, once per 256-token tile pair) instead of
+                                          once per call into the workspace; the workspace is smaller by
+                                          2 d_in d_out bytes, the GEMMs slower when the pack spans many
+                                          tile pairs; identical results; not with MLORA_GEMM_SINGLE_CTA */
 
 /* One job of the pack.  Pointers are device pointers to fp32 buffers of the
  * shapes given above, each 16-byte aligned.  dAt/dBt are overwritten (not
@@ -144,9 +151,11 @@ mlora_status mlora_forward(const mlora_plan_t* plan, const void* X, const void* 
  *          byte, even k in the low nibble (two's complement);
  *   Wscale [d_in / 64, d_out] fp32: one scale per 64 consecutive k of each output column;
  * and the layer uses W[k][o] = bf16(q[o][k] * Wscale[k / 64][o]) (the product in fp32, rounded
- * to nearest bf16), which is what the bf16 entry points would compute with that Wt.  Everything
- * else (arguments, layouts, errors) is as for mlora_forward / mlora_backward.  Both pointers
- * 16-byte aligned. */
+ * to nearest bf16), which is what the bf16 entry points would compute with that Wt.  Unless the
+ * plan has MLORA_W4_FUSED, each call first expands W into the workspace as bf16 Wt (which is
+ * why the workspace of such a plan holds 2 d_in d_out more bytes) and then runs the bf16 path.
+ * Everything else (arguments, layouts, errors) is as for mlora_forward / mlora_backward.  Both
+ * pointers 16-byte aligned. */
 mlora_status mlora_forward_w4(const mlora_plan_t* plan, const void* X, const void* Wq, const float* Wscale,
                               void* Y, float* H, void* workspace, void* stream);
 mlora_status mlora_backward_w4(const mlora_plan_t* plan, const void* X, const void* Wq, const float* Wscale,

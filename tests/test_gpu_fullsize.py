@@ -37,9 +37,9 @@ def sample_rows(wl, max_rows=768, seed=0):
     return np.unique(np.concatenate([np.array(rows, dtype=np.int64), extra]))
 
 
-def check_fullsize(wl, step=True):
+def check_fullsize(wl, step=True, flags=0):
     T = W.materialise(wl)
-    run = G.GpuRun(wl, T, step=step)
+    run = G.GpuRun(wl, T, step=step, flags=flags)
     try:
         assert run.status_after_backward == M.MLORA_OK
         got = run.res
@@ -83,8 +83,9 @@ def test_qproj_llama8b_fullsize():
     check_fullsize(W.llama8b_qproj())
 
 
-def test_qproj_llama8b_w4_base_fullsize():
-    check_fullsize(W.llama8b_qproj_w4())
+@pytest.mark.parametrize("fused", [False, True], ids=["expand", "fused"])
+def test_qproj_llama8b_w4_base_fullsize(fused):
+    check_fullsize(W.llama8b_qproj_w4(), flags=M.MLORA_W4_FUSED if fused else 0)
 
 
 def test_mlp_up_lognormal_fullsize():

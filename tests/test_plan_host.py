@@ -180,3 +180,30 @@ def test_h_elems_is_sum_n_r():
         assert M.mlora_h_elems(plan) == 4 * 10 + 8 * 7 + 3 * 5
     finally:
         M.mlora_plan_destroy(plan)
+
+
+def test_w4_workspace_holds_the_expansion_unless_fused():
+    """A 4-bit-base plan's workspace adds the bf16 expansion of W (2 d_in d_out bytes, 1 KB
+    aligned) to the bf16 plan's; with MLORA_W4_FUSED it is the bf16 plan's."""
+    d_in, d_out, ranks, ns = 512, 384, [8, 64], [300, 100]
+    h16, ws16 = host_plan(d_in, d_out, ranks, ns)
+    h4, ws4 = host_plan(d_in, d_out, ranks, ns, dtype="bf16_w4")
+    hf, wsf = host_plan(d_in, d_out, ranks, ns, dtype="bf16_w4", flags=M.MLORA_W4_FUSED)
+    for h in (h16, h4, hf):
+        M.mlora_plan_destroy(h)
+    assert wsf == ws16
+    assert ws4 == -(-ws16 // 1024) * 1024 + 2 * d_in * d_out
+
+
+@pytest.mark.parametrize("flags,status", [
+    (0, M.MLORA_OK),
+    (M.MLORA_GEMM_SINGLE_CTA, M.MLORA_OK),
+    (M.MLORA_W4_FUSED, M.MLORA_OK),
+    (M.MLORA_W4_FUSED | M.MLORA_GEMM_SINGLE_CTA, M.MLORA_ERR_UNSUPPORTED),
+])
+def test_w4_plan_flags(flags, status):
+    assert _status_of(lambda: M.mlora_plan_destroy(
+        host_plan(512, 384, [8], [100], dtype="bf16_w4", flags=flags)[0])) == status
+    # d_in must hold whole 64-wide scale groups
+    assert _status_of(lambda: M.mlora_plan_destroy(
+        host_plan(520, 384, [8], [100], dtype="bf16_w4", flags=flags)[0])) == M.MLORA_ERR_UNSUPPORTED
