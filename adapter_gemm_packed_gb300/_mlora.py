@@ -21,14 +21,15 @@ MLORA_NO_OVERLAP = 8
 MLORA_REUSE_STAGING = 32
 MLORA_W4_FUSED = 64
 MLORA_DEBUG_DROP_COPY = 16
-MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD_B, MLORA_Q_WINDOW = range(6)
+(MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD_B, MLORA_Q_WINDOW,
+ MLORA_Q_ADAPTERS) = range(7)
 
 # every symbol include/mlora.h declares
 EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward", "mlora_adamw",
            "mlora_sync_status", "mlora_h_elems", "mlora_plan_describe", "mlora_status_string",
            "mlora_last_error", "mlora_version", "mlora_profile_enable", "mlora_profile_read",
            "mlora_kernel_name", "mlora_launch_count", "mlora_forward_static_ws", "mlora_memory_estimate",
-           "mlora_shard_jobs", "mlora_forward_w4", "mlora_backward_w4"]
+           "mlora_shard_jobs", "mlora_forward_w4", "mlora_backward_w4", "mlora_plan_grouped"]
 
 
 class mlora_segment(C.Structure):
@@ -40,6 +41,10 @@ class mlora_segment(C.Structure):
 class mlora_problem(C.Structure):
     _fields_ = [("n_tokens", C.c_int64), ("d_in", C.c_int32), ("d_out", C.c_int32), ("dtype", C.c_int32),
                 ("flags", C.c_uint32)]
+
+
+class mlora_group(C.Structure):
+    _fields_ = [("col_offset", C.c_int32), ("d_out", C.c_int32)]
 
 
 class mlora_memory(C.Structure):
@@ -67,6 +72,9 @@ def lib() -> C.CDLL:
         L.mlora_plan.argtypes = [C.POINTER(mlora_problem), C.POINTER(mlora_segment), i32, C.POINTER(C.c_size_t),
                                  C.POINTER(vp)]
         L.mlora_plan.restype = i32
+        L.mlora_plan_grouped.argtypes = [C.POINTER(mlora_problem), C.POINTER(mlora_group), i32,
+                                         C.POINTER(mlora_segment), i32, C.POINTER(C.c_size_t), C.POINTER(vp)]
+        L.mlora_plan_grouped.restype = i32
         L.mlora_plan_destroy.argtypes = [vp]
         L.mlora_plan_destroy.restype = None
         L.mlora_forward.argtypes = [vp, vp, vp, vp, vp, vp, vp]
@@ -125,6 +133,18 @@ def mlora_plan(problem: mlora_problem, segs) -> tuple[int, int]:
     ws = C.c_size_t(0)
     h = C.c_void_p(0)
     _check(lib().mlora_plan(C.byref(problem), arr, len(segs), C.byref(ws), C.byref(h)), "mlora_plan")
+    return h.value, ws.value
+
+
+def mlora_plan_grouped(problem: mlora_problem, groups, segs) -> tuple[int, int]:
+    """groups: [(col_offset, d_out), ...]; segs: n_jobs x n_groups entries, job-major.
+    Returns (plan handle, workspace bytes)."""
+    garr = (mlora_group * len(groups))(*[mlora_group(int(o), int(w)) for o, w in groups])
+    arr = (mlora_segment * len(segs))(*segs)
+    ws = C.c_size_t(0)
+    h = C.c_void_p(0)
+    _check(lib().mlora_plan_grouped(C.byref(problem), garr, len(groups), arr, len(segs), C.byref(ws), C.byref(h)),
+           "mlora_plan_grouped")
     return h.value, ws.value
 
 

@@ -34,10 +34,10 @@ cudaError_t launch_gemm_2sm(const CUtensorMap&, const CUtensorMap&, const CUtens
 template <int MODE>
 cudaError_t launch_gemm_2sm_w4(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
-cudaError_t launch_pack_fwd(const DevSeg*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, int,
+cudaError_t launch_pack_fwd(const DevSub*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, int,
                             cudaStream_t, bool);
-cudaError_t launch_h_images(const DevSeg*, const MTile*, const int*, int, long long, const float*, uint8_t*,
-                            cudaStream_t, bool);
+cudaError_t launch_h_images(const DevSeg*, const float*, const MTile*, const int*, int, long long, const float*,
+                            uint8_t*, cudaStream_t, bool);
 cudaError_t launch_adamw(const AdamItem*, int, float, float, float, float, float, int, int, cudaStream_t, bool);
 cudaError_t launch_w4_expand(const void*, const float*, __nv_bfloat16*, int, int, int, cudaStream_t, bool);
 cudaError_t launch_f32_forward(const DevSeg*, int, long long, int, int, long long, const float*, const float*, float*,
@@ -132,14 +132,19 @@ mlora_status make_map_plain(CUtensorMap* map, CUtensorMapDataType dt, uint32_t e
 
 struct mlora_plan_s {
   mlora_problem prob{};
-  int n_segs = 0;
+  int n_segs = 0;                       // user entries: n_jobs x n_groups, job-major
+  int n_jobs = 0, n_groups = 1;
+  bool grouped = false;                 // more than one output-column group (shared-input pack)
+  std::vector<mlora_group> groups;
   std::vector<mlora_segment> user;
-  std::vector<DevSeg> segs;
+  std::vector<DevSeg> segs;             // one per job
+  std::vector<DevSub> subs;             // one per user entry
+  std::vector<float> col_scale;         // per packed column (chunk-padded), 0 in padding
   int C_total = 0, n_chunks = 0, n_mtiles = 0, max_rank = 0;
   long long n_images = 0, h_elems = 0;
   std::vector<MTile> mtiles;
   std::vector<int> img_tile;
-  std::vector<int> col_seg;
+  std::vector<int> col_sub;             // per packed column (chunk-padded), -1 in padding
   std::vector<WinItem> win;
   std::vector<WItem> da, db;
   std::vector<AdamItem> adam;
@@ -154,7 +159,9 @@ struct mlora_plan_s {
   DevSeg* d_segs = nullptr;
   MTile* d_mtiles = nullptr;
   int* d_img_tile = nullptr;
-  int* d_col_seg = nullptr;
+  DevSub* d_subs = nullptr;
+  int* d_col_sub = nullptr;
+  float* d_col_scale = nullptr;
   WinItem* d_win = nullptr;
   WItem* d_da = nullptr;
   WItem* d_db = nullptr;
@@ -179,9 +186,12 @@ struct mlora_plan_s {
 
 namespace {
 
-mlora_status validate(const mlora_problem* p, const mlora_segment* s, int32_t n) {
-  if (!p || !s) return fail(MLORA_ERR_INVALID, "null problem or segment table");
+mlora_status validate(const mlora_problem* p, const mlora_group* groups, int32_t n_groups, const mlora_segment* s,
+                      int32_t n) {
+  if (!p || !s || !groups) return fail(MLORA_ERR_INVALID, "null problem, group or segment table");
+  if (n_groups < 1) return fail(MLORA_ERR_INVALID, "n_groups must be >= 1");
   if (n < 1) return fail(MLORA_ERR_INVALID, "n_segs must be >= 1");
+  if (n % n_groups) return fail(MLORA_ERR_INVALID, "n_segs must be a multiple of n_groups (one entry per job and group)");
   if (p->dtype != MLORA_F32 && p->dtype != MLORA_BF16 && p->dtype != MLORA_BF16_W4)
     return fail(MLORA_ERR_INVALID, "unknown dtype");
   if (p->dtype == MLORA_BF16_W4 && p->d_in % 64)
@@ -193,13 +203,30 @@ mlora_status validate(const mlora_problem* p, const mlora_segment* s, int32_t n)
   if (p->d_in % q || p->d_out % q)
     return fail(MLORA_ERR_UNSUPPORTED, "d_in and d_out must be multiples of 8 (bf16) or 4 (fp32)");
   if (p->n_tokens < 1 || p->n_tokens > 0x7fffffffLL) return fail(MLORA_ERR_INVALID, "n_tokens out of range");
+  if (n_groups > 1 && p->dtype == MLORA_F32)
+    return fail(MLORA_ERR_UNSUPPORTED, "shared-input packs (several groups) need a bf16 plan");
+  {
+    long long o = 0;
+    for (int g = 0; g < n_groups; ++g) {
+      if (groups[g].col_offset != o || groups[g].d_out < 1)
+        return fail(MLORA_ERR_INVALID, "groups must tile [0, d_out) in order, each at least one column wide");
+      o += groups[g].d_out;
+    }
+    if (o != p->d_out) return fail(MLORA_ERR_INVALID, "the groups' widths must add up to d_out");
+  }
   long long expect = 0;
   for (int i = 0; i < n; ++i) {
     const mlora_segment& g = s[i];
+    const mlora_segment& first = s[i - i % n_groups];   // the job's entry for group 0
     char buf[160];
-    if (g.tok_offset != expect) {
-      snprintf(buf, sizeof buf, "segment %d starts at row %lld, expected %lld (segments must tile [0, N) in order)", i,
-               static_cast<long long>(g.tok_offset), expect);
+    if (i % n_groups == 0) {
+      if (g.tok_offset != expect) {
+        snprintf(buf, sizeof buf, "segment %d starts at row %lld, expected %lld (segments must tile [0, N) in order)", i,
+                 static_cast<long long>(g.tok_offset), expect);
+        return fail(MLORA_ERR_INVALID, buf);
+      }
+    } else if (g.tok_offset != first.tok_offset || g.n_tokens != first.n_tokens) {
+      snprintf(buf, sizeof buf, "segment %d: a job's entries for every group must cover the same rows", i);
       return fail(MLORA_ERR_INVALID, buf);
     }
     if (g.n_tokens < 1) {
@@ -228,7 +255,7 @@ mlora_status validate(const mlora_problem* p, const mlora_segment* s, int32_t n)
         snprintf(buf, sizeof buf, "segment %d: adapter buffers must be 16-byte aligned", i);
         return fail(MLORA_ERR_INVALID, buf);
       }
-    expect += g.n_tokens;
+    if (i % n_groups == n_groups - 1) expect += g.n_tokens;
   }
   if (expect != p->n_tokens) {
     char buf[160];
@@ -242,38 +269,64 @@ mlora_status validate(const mlora_problem* p, const mlora_segment* s, int32_t n)
 void build_tables(mlora_plan_t* P) {
   const mlora_problem& pr = P->prob;
   const long long N = pr.n_tokens;
-  // jobs and the packed rank space
+  const int G = P->n_groups;
+  // Jobs and the packed rank space.  Job j's adapters (one per group) sit side by side in its
+  // window in group order, without padding between them; the window is padded to RANK_PAD.
   int c = 0;
   long long h = 0;
-  P->segs.resize(P->n_segs);
+  P->segs.resize(P->n_jobs);
+  P->subs.resize(P->n_segs);
   P->can_backward = P->can_adamw = true;
-  for (int i = 0; i < P->n_segs; ++i) {
-    const mlora_segment& u = P->user[i];
-    DevSeg& d = P->segs[i];
-    d.off = u.tok_offset;
-    d.n = u.n_tokens;
-    d.r = u.rank;
-    d.rp = static_cast<int>(round_up(u.rank, RANK_PAD));
+  for (int j = 0; j < P->n_jobs; ++j) {
+    const mlora_segment& u0 = P->user[static_cast<size_t>(j) * G];
+    DevSeg& d = P->segs[j];
+    d.off = u0.tok_offset;
+    d.n = u0.n_tokens;
     d.c = c;
-    d.s = u.scale;
     d.pad0 = 0;
     d.h_off = h;
-    d.At = u.At;
-    d.Bt = u.Bt;
-    d.dAt = u.dAt;
-    d.dBt = u.dBt;
+    int R = 0;
+    for (int g = 0; g < G; ++g) {
+      const int i = j * G + g;
+      const mlora_segment& u = P->user[i];
+      DevSub& sb = P->subs[i];
+      sb.At = u.At;
+      sb.Bt = u.Bt;
+      sb.dAt = u.dAt;
+      sb.dBt = u.dBt;
+      sb.c0 = c + R;
+      sb.r = u.rank;
+      sb.o_lo = P->groups[g].col_offset;
+      sb.o_hi = P->groups[g].col_offset + P->groups[g].d_out;
+      sb.s = u.scale;
+      sb.job = j;
+      sb.pad0 = sb.pad1 = 0;
+      R += u.rank;
+      P->max_rank = std::max(P->max_rank, u.rank);
+      if (!u.dAt || !u.dBt) P->can_backward = false;
+      if (!u.dAt || !u.dBt || !u.mA || !u.vA || !u.mB || !u.vB) P->can_adamw = false;
+    }
+    // one adapter per job: the job carries it (the kernels' fast paths read these)
+    d.r = R;
+    d.rp = static_cast<int>(round_up(R, RANK_PAD));
+    d.s = G == 1 ? u0.scale : 0.f;
+    d.At = G == 1 ? u0.At : nullptr;
+    d.Bt = G == 1 ? u0.Bt : nullptr;
+    d.dAt = G == 1 ? u0.dAt : nullptr;
+    d.dBt = G == 1 ? u0.dBt : nullptr;
     c += d.rp;
-    h += static_cast<long long>(u.n_tokens) * u.rank;
-    P->max_rank = std::max(P->max_rank, u.rank);
-    if (!u.dAt || !u.dBt) P->can_backward = false;
-    if (!u.dAt || !u.dBt || !u.mA || !u.vA || !u.mB || !u.vB) P->can_adamw = false;
+    h += static_cast<long long>(d.n) * R;
   }
   P->C_total = c;
   P->h_elems = h;
   P->n_chunks = (c + CHUNK_COLS - 1) / CHUNK_COLS;
-  P->col_seg.resize(c);
+  P->col_sub.assign(static_cast<size_t>(P->n_chunks) * CHUNK_COLS, -1);
+  P->col_scale.assign(static_cast<size_t>(P->n_chunks) * CHUNK_COLS, 0.f);
   for (int i = 0; i < P->n_segs; ++i)
-    for (int t = 0; t < P->segs[i].rp; ++t) P->col_seg[P->segs[i].c + t] = i;
+    for (int t = 0; t < P->subs[i].r; ++t) {
+      P->col_sub[P->subs[i].c0 + t] = i;
+      P->col_scale[P->subs[i].c0 + t] = P->subs[i].s;
+    }
 
   // token tiles -> jobs -> chunks -> staged images
   P->n_mtiles = static_cast<int>((N + BM - 1) / BM);
@@ -321,39 +374,67 @@ void build_tables(mlora_plan_t* P) {
   for (int t = 0; t < P->n_mtiles; ++t) {
     const MTile& m = P->mtiles[t];
     for (int q = 0; q < m.nch; q += MAX_ITEM_CHUNKS)
-      P->win.push_back(WinItem{t, m.q_lo + q, std::min(MAX_ITEM_CHUNKS, m.nch - q), 0});
+    {
+      WinItem w{};
+      w.tile = t;
+      w.q0 = m.q_lo + q;
+      w.nq = std::min(MAX_ITEM_CHUNKS, m.nch - q);
+      // dH reads only the d_out slices that the adapters owning these chunks' columns cover
+      int o_lo = pr.d_out, o_hi = 0;
+      for (int c = w.q0 * CHUNK_COLS; c < std::min(P->C_total, (w.q0 + w.nq) * CHUNK_COLS); ++c) {
+        const int a = P->col_sub[c];
+        if (a < 0) continue;
+        o_lo = std::min(o_lo, P->subs[a].o_lo);
+        o_hi = std::max(o_hi, P->subs[a].o_hi);
+      }
+      if (o_hi <= o_lo) o_lo = 0, o_hi = std::min(pr.d_out, BK);
+      w.dh_kb0 = o_lo / BK;
+      w.dh_nkb = (o_hi + BK - 1) / BK - w.dh_kb0;
+      P->win.push_back(w);
+    }
   }
 
-  // dA / dB work: (row block, job, <= 4 chunks), longest first
-  auto wgrad = [&](int rows) {
+  // dA / dB work: (256-row block, job, <= MAX_ITEM_CHUNKS chunks), longest first.  A dB block
+  // needs only the columns of the job's adapters whose output range meets it.
+  auto wgrad = [&](int rows, bool by_output) {
     std::vector<WItem> v;
-    for (int i = 0; i < P->n_segs; ++i) {
+    for (int i = 0; i < P->n_jobs; ++i) {
       const DevSeg& d = P->segs[i];
       const int ga = static_cast<int>(d.off / 64);
       const int gb = static_cast<int>((d.off + d.n + 63) / 64);
-      const int qa = d.c / CHUNK_COLS, qb = (d.c + d.rp + CHUNK_COLS - 1) / CHUNK_COLS;
       // chunks innermost: the items that read the same X / dY block sit side by side in the
       // list, so the persistent grid runs them concurrently and the block is read from HBM once
-      for (int r0 = 0; r0 < rows; r0 += 2 * BM)
+      for (int r0 = 0; r0 < rows; r0 += 2 * BM) {
+        int c_lo = d.c + d.r, c_hi = d.c;
+        for (int g = 0; g < G; ++g) {
+          const DevSub& sb = P->subs[static_cast<size_t>(i) * G + g];
+          if (by_output && (sb.o_hi <= r0 || sb.o_lo >= r0 + 2 * BM)) continue;
+          c_lo = std::min(c_lo, sb.c0);
+          c_hi = std::max(c_hi, sb.c0 + sb.r);
+        }
+        if (c_hi <= c_lo) continue;
+        const int qa = c_lo / CHUNK_COLS, qb = (c_hi + CHUNK_COLS - 1) / CHUNK_COLS;
         for (int q = qa; q < qb; q += MAX_ITEM_CHUNKS)
           v.push_back(WItem{r0, i, ga, gb, q, std::min(MAX_ITEM_CHUNKS, qb - q), 0, 0});
+      }
     }
     std::stable_sort(v.begin(), v.end(), [](const WItem& a, const WItem& b) {
       return static_cast<long long>(a.gb - a.ga) * (16 + a.nq) > static_cast<long long>(b.gb - b.ga) * (16 + b.nq);
     });
     return v;
   };
-  P->da = wgrad(pr.d_in);
-  P->db = wgrad(pr.d_out);
+  P->da = wgrad(pr.d_in, false);
+  P->db = wgrad(pr.d_out, true);
 
   // AdamW pieces
   P->adam.clear();
   if (P->can_adamw) {
     for (int i = 0; i < P->n_segs; ++i) {
       const mlora_segment& u = P->user[i];
+      const long long width = P->subs[i].o_hi - P->subs[i].o_lo;
       struct T { float *p, *g, *m, *v; long long n; } ts[2] = {
           {u.At, u.dAt, u.mA, u.vA, static_cast<long long>(u.rank) * pr.d_in},
-          {u.Bt, u.dBt, u.mB, u.vB, static_cast<long long>(u.rank) * pr.d_out}};
+          {u.Bt, u.dBt, u.mB, u.vB, static_cast<long long>(u.rank) * width}};
       for (const T& tt : ts)
         for (long long s0 = 0; s0 < tt.n; s0 += ADAM_CHUNK) {
           AdamItem a{};
@@ -399,9 +480,10 @@ mlora_status upload(mlora_plan_t* P) {
   e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   const size_t b_segs = table_bytes(P->segs), b_mt = table_bytes(P->mtiles), b_it = table_bytes(P->img_tile),
-               b_cs = table_bytes(P->col_seg), b_win = table_bytes(P->win), b_da = table_bytes(P->da),
-               b_db = table_bytes(P->db), b_adam = table_bytes(P->adam), b_err = 256;
-  const size_t total = b_segs + b_mt + b_it + b_cs + b_win + b_da + b_db + b_adam + b_err;
+               b_cs = table_bytes(P->col_sub), b_sc = table_bytes(P->col_scale), b_sub = table_bytes(P->subs),
+               b_win = table_bytes(P->win), b_da = table_bytes(P->da), b_db = table_bytes(P->db),
+               b_adam = table_bytes(P->adam), b_err = 256;
+  const size_t total = b_segs + b_mt + b_it + b_cs + b_sc + b_sub + b_win + b_da + b_db + b_adam + b_err;
   e = cudaMalloc(&P->dev_block, total);
   if (e != cudaSuccess) {
     P->dev_block = nullptr;
@@ -420,7 +502,9 @@ mlora_status upload(mlora_plan_t* P) {
   if ((e = place(P->d_segs, P->segs, b_segs)) != cudaSuccess ||
       (e = place(P->d_mtiles, P->mtiles, b_mt)) != cudaSuccess ||
       (e = place(P->d_img_tile, P->img_tile, b_it)) != cudaSuccess ||
-      (e = place(P->d_col_seg, P->col_seg, b_cs)) != cudaSuccess ||
+      (e = place(P->d_col_sub, P->col_sub, b_cs)) != cudaSuccess ||
+      (e = place(P->d_col_scale, P->col_scale, b_sc)) != cudaSuccess ||
+      (e = place(P->d_subs, P->subs, b_sub)) != cudaSuccess ||
       (e = place(P->d_win, P->win, b_win)) != cudaSuccess || (e = place(P->d_da, P->da, b_da)) != cudaSuccess ||
       (e = place(P->d_db, P->db, b_db)) != cudaSuccess || (e = place(P->d_adam, P->adam, b_adam)) != cudaSuccess)
     return cuda_fail(e, "uploading the plan tables");
@@ -481,6 +565,11 @@ GemmArgs base_args(const mlora_plan_t* P) {
   g.mtiles = P->d_mtiles;
   g.win = P->d_win;
   g.segs = P->d_segs;
+  if (P->grouped) {
+    g.subs = P->d_subs;
+    g.col_sub = P->d_col_sub;
+    g.col_scale = P->d_col_scale;
+  }
   g.err = P->d_err;
   g.timeout_ns = P->timeout_ns;
   g.pdl = P->pdl ? 1 : 0;
@@ -502,17 +591,22 @@ mlora_status check_exec(const mlora_plan_t* P) {
 
 extern "C" {
 
-mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
-                        size_t* workspace_bytes, mlora_plan_t** out) {
+mlora_status mlora_plan_grouped(const mlora_problem* problem, const mlora_group* groups, int32_t n_groups,
+                                const mlora_segment* segs, int32_t n_segs, size_t* workspace_bytes,
+                                mlora_plan_t** out) {
   g_last_error.clear();
   if (!out || !workspace_bytes) return fail(MLORA_ERR_INVALID, "null output pointer");
   *out = nullptr;
-  mlora_status st = validate(problem, segs, n_segs);
+  mlora_status st = validate(problem, groups, n_groups, segs, n_segs);
   if (st != MLORA_OK) return st;
   mlora_plan_t* P = new (std::nothrow) mlora_plan_s();
   if (!P) return fail(MLORA_ERR_OOM, "host allocation failed");
   P->prob = *problem;
   P->n_segs = n_segs;
+  P->n_groups = n_groups;
+  P->n_jobs = n_segs / n_groups;
+  P->grouped = n_groups > 1;
+  P->groups.assign(groups, groups + n_groups);
   P->user.assign(segs, segs + n_segs);
   if (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT) P->timeout_ns = SHORT_TIMEOUT_NS;
   if (problem->flags & MLORA_NO_OVERLAP) P->pdl = false;
@@ -530,6 +624,14 @@ mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs,
   }
   *workspace_bytes = P->ws_bytes;
   *out = P;
+  return MLORA_OK;
+}
+
+mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
+                        size_t* workspace_bytes, mlora_plan_t** out) {
+  if (!problem) return fail(MLORA_ERR_INVALID, "null problem, group or segment table");
+  const mlora_group all{0, problem->d_out};
+  return mlora_plan_grouped(problem, &all, 1, segs, n_segs, workspace_bytes, out);
   return MLORA_OK;
 }
 
@@ -564,7 +666,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
   const mlora_problem& pr = P->prob;
   cudaError_t e;
   if (pr.dtype == MLORA_F32) {
-    e = timed(P, K_F32_FWD, s, [&] { return launch_f32_forward(P->d_segs, P->n_segs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems,
+    e = timed(P, K_F32_FWD, s, [&] { return launch_f32_forward(P->d_segs, P->n_jobs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems,
                            static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<float*>(Y), H, s); });
     return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 forward launch");
   }
@@ -585,7 +687,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
     if (e != cudaSuccess) return cuda_fail(e, "4-bit expansion launch");
     Wt = wexp;
   }
-  e = timed(P, K_PACK_FWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
+  e = timed(P, K_PACK_FWD, s, [&] { return launch_pack_fwd(P->d_subs, P->d_col_sub, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
   if (e != cudaSuccess) return cuda_fail(e, "pack launch");
 
   const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
@@ -667,7 +769,7 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   const mlora_problem& pr = P->prob;
   cudaError_t e;
   if (pr.dtype == MLORA_F32) {
-    e = timed(P, K_F32_BWD, s, [&] { return launch_f32_backward(P->d_segs, P->n_segs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems, P->max_rank,
+    e = timed(P, K_F32_BWD, s, [&] { return launch_f32_backward(P->d_segs, P->n_jobs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems, P->max_rank,
                             static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<const float*>(dY),
                             H, static_cast<float*>(dX), dH, s); });
     return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 backward launch");
@@ -698,9 +800,9 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
     Wt = wexp;
   }
   if (!reuse) {
-    e = timed(P, K_PACK_BWD, s, [&] { return launch_pack_fwd(P->d_segs, P->d_col_seg, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
+    e = timed(P, K_PACK_BWD, s, [&] { return launch_pack_fwd(P->d_subs, P->d_col_sub, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
-    e = timed(P, K_H_IMAGES, s, [&] { return launch_h_images(P->d_segs, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s, P->pdl); });
+    e = timed(P, K_H_IMAGES, s, [&] { return launch_h_images(P->d_segs, P->d_col_scale, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s, P->pdl); });
     if (e != cudaSuccess) return cuda_fail(e, "image launch");
   }
 
@@ -860,7 +962,10 @@ mlora_status mlora_plan_describe(const mlora_plan_t* P, int32_t what, int64_t* o
         v.insert(v.end(), {w.row0, w.seg, w.ga, w.gb, w.q0, w.nq});
       break;
     case MLORA_Q_WINDOW:
-      for (const WinItem& w : P->win) v.insert(v.end(), {w.tile, w.q0, w.nq});
+      for (const WinItem& w : P->win) v.insert(v.end(), {w.tile, w.q0, w.nq, w.dh_kb0, w.dh_nkb});
+      break;
+    case MLORA_Q_ADAPTERS:
+      for (const DevSub& sb : P->subs) v.insert(v.end(), {sb.job, sb.c0, sb.r, sb.o_lo, sb.o_hi});
       break;
     default:
       return fail(MLORA_ERR_INVALID, "unknown table");
@@ -908,7 +1013,7 @@ mlora_status mlora_memory_estimate(const mlora_plan_t* P, mlora_memory* out) {
   const mlora_problem& pr = P->prob;
   const int64_t e = pr.dtype == MLORA_F32 ? 4 : 2;
   int64_t params = 0;
-  for (const DevSeg& d : P->segs) params += static_cast<int64_t>(d.r) * (pr.d_in + pr.d_out);
+  for (const DevSub& sb : P->subs) params += static_cast<int64_t>(sb.r) * (pr.d_in + (sb.o_hi - sb.o_lo));
   mlora_memory m{};
   m.base_weight = pr.dtype == MLORA_BF16_W4
                       ? static_cast<int64_t>(pr.d_in) * pr.d_out / 2 + static_cast<int64_t>(pr.d_in / 64) * pr.d_out * 4
@@ -919,7 +1024,8 @@ mlora_status mlora_memory_estimate(const mlora_plan_t* P, mlora_memory* out) {
   m.lora_act = 2 * P->h_elems * 4;
   m.workspace = static_cast<int64_t>(P->ws_bytes);
   m.plan_tables = static_cast<int64_t>(table_bytes(P->segs) + table_bytes(P->mtiles) + table_bytes(P->img_tile) +
-                                       table_bytes(P->col_seg) + table_bytes(P->win) + table_bytes(P->da) +
+                                       table_bytes(P->col_sub) + table_bytes(P->col_scale) +
+                                       table_bytes(P->subs) + table_bytes(P->win) + table_bytes(P->da) +
                                        table_bytes(P->db) + table_bytes(P->adam) + 256);
   m.total = m.base_weight + m.activations + m.lora_params + m.lora_grad_state + m.lora_act + m.workspace +
             m.plan_tables;

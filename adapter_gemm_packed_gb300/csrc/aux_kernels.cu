@@ -11,8 +11,9 @@ namespace mlora {
 
 namespace {
 
-// At_all [C_total, d_in] bf16: row c = At_i[c - c_i] for c in job i's window, zero in padding.
-__global__ void k_pack_at(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_in,
+// At_all [C_total, d_in] bf16: row c = At[c - c0] of the adapter owning packed column c, zero in
+// padding.
+__global__ void k_pack_at(const DevSub* __restrict__ subs, const int* __restrict__ col_sub, int C_total, int d_in,
                           __nv_bfloat16* __restrict__ at_all) {
   griddep_wait();
   griddep_launch_dependents();
@@ -22,23 +23,25 @@ __global__ void k_pack_at(const DevSeg* __restrict__ segs, const int* __restrict
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int c = static_cast<int>(i / d8);
     const int k = static_cast<int>(i - static_cast<long long>(c) * d8) * 8;
-    const DevSeg& sg = segs[col_seg[c]];
-    const int t = c - sg.c;
+    const int a = col_sub[c];
     uint4 o = make_uint4(0, 0, 0, 0);
-    if (t < sg.r) {
-      const float4* src = reinterpret_cast<const float4*>(sg.At + static_cast<size_t>(t) * d_in + k);
-      const float4 a = src[0], b = src[1];
-      o.x = pack_bf16x2(a.x, a.y);
-      o.y = pack_bf16x2(a.z, a.w);
-      o.z = pack_bf16x2(b.x, b.y);
-      o.w = pack_bf16x2(b.z, b.w);
+    if (a >= 0) {
+      const DevSub& sb = subs[a];
+      const float4* src = reinterpret_cast<const float4*>(sb.At + static_cast<size_t>(c - sb.c0) * d_in + k);
+      const float4 x = src[0], y = src[1];
+      o.x = pack_bf16x2(x.x, x.y);
+      o.y = pack_bf16x2(x.z, x.w);
+      o.z = pack_bf16x2(y.x, y.y);
+      o.w = pack_bf16x2(y.z, y.w);
     }
     *reinterpret_cast<uint4*>(at_all + static_cast<size_t>(c) * d_in + k) = o;
   }
 }
 
-// Bt_all [d_out, C_total] bf16: Bt_all[o][c] = Bt_i[o][c - c_i] (zero in padding).
-__global__ void k_pack_bt(const DevSeg* __restrict__ segs, const int* __restrict__ col_seg, int C_total, int d_out,
+// Bt_all [d_out, C_total] bf16: Bt_all[o][c] = Bt[o - o_lo][c - c0] of the adapter owning packed
+// column c when output column o lies in that adapter's range [o_lo, o_hi), else zero (padding,
+// and the other projections' columns of a shared-input pack).
+__global__ void k_pack_bt(const DevSub* __restrict__ subs, const int* __restrict__ col_sub, int C_total, int d_out,
                           __nv_bfloat16* __restrict__ bt_all) {
   griddep_wait();
   griddep_launch_dependents();
@@ -48,13 +51,15 @@ __global__ void k_pack_bt(const DevSeg* __restrict__ segs, const int* __restrict
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int o = static_cast<int>(i / c8);
     const int c = static_cast<int>(i - static_cast<long long>(o) * c8) * 8;
-    const DevSeg& sg = segs[col_seg[c]];   // 8 columns never straddle two windows (windows are 16-aligned)
-    const float* src = sg.Bt + static_cast<size_t>(o) * sg.r;
     float f[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const int t = c - sg.c + u;
-      f[u] = t < sg.r ? src[t] : 0.f;
+      const int a = col_sub[c + u];
+      f[u] = 0.f;
+      if (a >= 0) {
+        const DevSub& sb = subs[a];
+        if (o >= sb.o_lo && o < sb.o_hi) f[u] = sb.Bt[static_cast<size_t>(o - sb.o_lo) * sb.r + (c + u - sb.c0)];
+      }
     }
     uint4 v;
     v.x = pack_bf16x2(f[0], f[1]);
@@ -66,11 +71,12 @@ __global__ void k_pack_bt(const DevSeg* __restrict__ segs, const int* __restrict
 }
 
 // Staged Htilde images from H (row-major [128 x 64] bf16 blocks):
-// image (tile t, chunk q) row r col u = s_j H_j[row - off_j][64q + u - c_j]
-// when token row (128 t + r) belongs to job j and column 64q+u lies in job j's rank window, else 0.
-__global__ void k_h_images(const DevSeg* __restrict__ segs, const MTile* __restrict__ mtiles,
-                           const int* __restrict__ img_tile, long long N, const float* __restrict__ H,
-                           uint8_t* __restrict__ img_out) {
+// image (tile t, chunk q) row r col u = s_c H_j[row - off_j][c - c_j], c = 64q + u, s_c the scale of
+// the adapter owning column c, when token row (128 t + r) belongs to job j and column c lies in
+// job j's rank window, else 0.
+__global__ void k_h_images(const DevSeg* __restrict__ segs, const float* __restrict__ col_scale,
+                           const MTile* __restrict__ mtiles, const int* __restrict__ img_tile, long long N,
+                           const float* __restrict__ H, uint8_t* __restrict__ img_out) {
   griddep_wait();
   griddep_launch_dependents();
   const int img = blockIdx.x;
@@ -80,7 +86,6 @@ __global__ void k_h_images(const DevSeg* __restrict__ segs, const MTile* __restr
   const int rit = threadIdx.x;   // 128 threads: one row each
   const long long row = static_cast<long long>(t) * BM + rit;
   int c_lo = 0, c_hi = 0;
-  float s = 0.f;
   const float* hrow = nullptr;
   if (row < N) {
     int j = mt.seg_first;
@@ -88,7 +93,6 @@ __global__ void k_h_images(const DevSeg* __restrict__ segs, const MTile* __restr
     const DevSeg& sg = segs[j];
     c_lo = sg.c;
     c_hi = sg.c + sg.r;
-    s = sg.s;
     hrow = H + sg.h_off + (row - sg.off) * sg.r - sg.c;
   }
   uint8_t* base = img_out + static_cast<size_t>(img) * IMG_BYTES;
@@ -98,8 +102,8 @@ __global__ void k_h_images(const DevSeg* __restrict__ segs, const MTile* __restr
 #pragma unroll
     for (int u = 0; u < 8; u += 2) {
       const int c0 = q * CHUNK_COLS + k8 * 8 + u, c1 = c0 + 1;
-      const float a0 = (c0 >= c_lo && c0 < c_hi) ? s * hrow[c0] : 0.f;
-      const float a1 = (c1 >= c_lo && c1 < c_hi) ? s * hrow[c1] : 0.f;
+      const float a0 = (c0 >= c_lo && c0 < c_hi) ? col_scale[c0] * hrow[c0] : 0.f;
+      const float a1 = (c1 >= c_lo && c1 < c_hi) ? col_scale[c1] * hrow[c1] : 0.f;
       pk[u / 2] = pack_bf16x2(a0, a1);
     }
     *reinterpret_cast<uint4*>(base + rit * (CHUNK_COLS * 2) + k8 * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -164,21 +168,22 @@ inline int grid_for(long long work, int threads, int num_sms) {
 
 }  // namespace
 
-cudaError_t launch_pack_fwd(const DevSeg* segs, const int* col_seg, int C_total, int d_in, int d_out,
+cudaError_t launch_pack_fwd(const DevSub* subs, const int* col_sub, int C_total, int d_in, int d_out,
                             __nv_bfloat16* at_all, __nv_bfloat16* bt_all, int num_sms, cudaStream_t st, bool pdl) {
   const long long w1 = static_cast<long long>(C_total) * (d_in / 8);
-  cudaError_t e = launch_k(k_pack_at, dim3(grid_for(w1, 256, num_sms)), dim3(256), 0, st, pdl, segs, col_seg, C_total,
+  cudaError_t e = launch_k(k_pack_at, dim3(grid_for(w1, 256, num_sms)), dim3(256), 0, st, pdl, subs, col_sub, C_total,
                            d_in, at_all);
   if (e != cudaSuccess) return e;
   const long long w2 = static_cast<long long>(d_out) * (C_total / 8);
-  return launch_k(k_pack_bt, dim3(grid_for(w2, 256, num_sms)), dim3(256), 0, st, pdl, segs, col_seg, C_total, d_out,
+  return launch_k(k_pack_bt, dim3(grid_for(w2, 256, num_sms)), dim3(256), 0, st, pdl, subs, col_sub, C_total, d_out,
                   bt_all);
 }
 
-cudaError_t launch_h_images(const DevSeg* segs, const MTile* mtiles, const int* img_tile, int n_images, long long N,
-                            const float* H, uint8_t* img_out, cudaStream_t st, bool pdl) {
+cudaError_t launch_h_images(const DevSeg* segs, const float* col_scale, const MTile* mtiles, const int* img_tile,
+                            int n_images, long long N, const float* H, uint8_t* img_out, cudaStream_t st, bool pdl) {
   if (n_images <= 0) return cudaSuccess;
-  return launch_k(k_h_images, dim3(n_images), dim3(BM), 0, st, pdl, segs, mtiles, img_tile, N, H, img_out);
+  return launch_k(k_h_images, dim3(n_images), dim3(BM), 0, st, pdl, segs, col_scale, mtiles, img_tile, N, H,
+                  img_out);
 }
 
 cudaError_t launch_adamw(const AdamItem* items, int n_items, float lr, float beta1, float beta2, float eps,

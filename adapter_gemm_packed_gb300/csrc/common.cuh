@@ -56,6 +56,22 @@ struct DevSeg {
   float* dBt;
 };
 
+// One adapter of a job (a job has one per projection of a shared-input pack, else one): its
+// ranks occupy the packed columns [c0, c0 + r) of the job's window, its B covers the output
+// columns [o_lo, o_hi) (B^T is [o_hi - o_lo, r]).
+struct DevSub {
+  float* At;
+  float* Bt;
+  float* dAt;
+  float* dBt;
+  int c0;
+  int r;
+  int o_lo, o_hi;
+  float s;
+  int job;
+  int pad0, pad1;
+};
+
 // Per 128-token tile: which jobs it covers and where its staged rank images live.
 struct MTile {
   int seg_first, seg_last;   // jobs overlapping the tile (inclusive)
@@ -66,7 +82,10 @@ struct MTile {
 
 // Rank-window work item (shrink / dH): one tile, up to MAX_ITEM_CHUNKS chunks.
 struct WinItem {
-  int tile, q0, nq, pad0;
+  int tile, q0, nq;
+  int dh_kb0, dh_nkb;   // dH: the 64-wide d_out slices its chunks' adapters cover (all of d_out
+                        // unless the pack shares its input across projections)
+  int pad0, pad1, pad2;
 };
 
 // Weight-gradient work item (dA / dB): one 256-row block of d_in (dA) or d_out (dB), one
@@ -105,6 +124,11 @@ struct GemmArgs {
   unsigned long long timeout_ns;
   int pdl;                 // launched with programmatic dependent launch
   int debug_drop;          // test hook: CTA 0 arms its first slot but issues no copy into it
+  // Shared-input packs (several adapters per job): per packed column, its adapter (-1 in the
+  // padding) and scale.  Null for plans with one adapter per job, whose kernels read the job's.
+  const DevSub* subs;
+  const int* col_sub;
+  const float* col_scale;
 };
 
 // Status codes written to the device status word (first one wins).

@@ -70,8 +70,10 @@ __device__ __forceinline__ int item_kblocks(const GemmArgs& g, int item) {
     int m, n;
     decode_mn(g, item, m, n);
     return g.kmain + g.mtiles[m].nch;
-  } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
+  } else if constexpr (MODE == MODE_SHRINK) {
     return g.kmain;
+  } else if constexpr (MODE == MODE_DH) {
+    return g.win[item].dh_nkb;
   } else {
     const WItem w = g.witems[item];
     return w.gb - w.ga;
@@ -126,13 +128,14 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
   } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
     const WinItem w = g.win[item];
     const int m0 = w.tile * BM;
+    const int k = (MODE == MODE_DH) ? w.dh_kb0 + kb : kb;   // dH: only the covered d_out slices
     mbar_arrive_expect_tx(full, A_STAGE_BYTES + w.nq * (CHUNK_COLS * BK * 2));
-    tma_load_2d_hint(sA, tmA, full, kb * BK, m0, pol_stream);
+    tma_load_2d_hint(sA, tmA, full, k * BK, m0, pol_stream);
     for (int j = 0; j < w.nq; ++j) {
       if constexpr (MODE == MODE_SHRINK)   // At_all rows (K-major, k = d_in)
-        tma_load_2d_hint(sB + j * (CHUNK_COLS * BK * 2), tmB, full, kb * BK, (w.q0 + j) * CHUNK_COLS, pol_keep);
+        tma_load_2d_hint(sB + j * (CHUNK_COLS * BK * 2), tmB, full, k * BK, (w.q0 + j) * CHUNK_COLS, pol_keep);
       else                                 // Bt_all [d_out, C] as MN-major (n = rank column, k = d_out)
-        tma_load_2d_hint(sB + j * (CHUNK_COLS * BK * 2), tmB, full, (w.q0 + j) * CHUNK_COLS, kb * BK, pol_keep);
+        tma_load_2d_hint(sB + j * (CHUNK_COLS * BK * 2), tmB, full, (w.q0 + j) * CHUNK_COLS, k * BK, pol_keep);
     }
   } else {
     const WItem w = g.witems[item];
@@ -269,9 +272,15 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
             a[k] = __uint_as_float(v[u + k]);
             in[k] = c0 + k >= c_lo && c0 + k < c_hi;
           }
+          // the scale of each column's adapter (one per job unless the pack shares its input)
+          float sk[4] = {s, s, s, s};
+          if (g.col_scale) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) sk[k] = __ldg(g.col_scale + c0 + k);
+          }
           float hv[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) hv[k] = (MODE == MODE_SHRINK) ? a[k] : s * a[k];
+          for (int k = 0; k < 4; ++k) hv[k] = (MODE == MODE_SHRINK) ? a[k] : sk[k] * a[k];
           // H / dH row segment: one 16-byte store when the four columns are in the window and aligned
           float* hp = g.hout + hbase + c0;
           if (in[0] && in[3] && ((reinterpret_cast<uintptr_t>(hp) & 15u) == 0)) {
@@ -281,8 +290,8 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
             for (int k = 0; k < 4; ++k)
               if (in[k]) hp[k] = hv[k];
           }
-          pk[u / 2] = pack_bf16x2(in[0] ? s * a[0] : 0.f, in[1] ? s * a[1] : 0.f);
-          pk[u / 2 + 1] = pack_bf16x2(in[2] ? s * a[2] : 0.f, in[3] ? s * a[3] : 0.f);
+          pk[u / 2] = pack_bf16x2(in[0] ? sk[0] * a[0] : 0.f, in[1] ? sk[1] * a[1] : 0.f);
+          pk[u / 2 + 1] = pack_bf16x2(in[2] ? sk[2] * a[2] : 0.f, in[3] ? sk[3] * a[3] : 0.f);
         }
         uint4* dst = reinterpret_cast<uint4*>(img + rit * (CHUNK_COLS * 2) + half * 64);
 #pragma unroll
@@ -306,6 +315,28 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
       tmem_ld_wait();
       const int cbase = (w.q0 + jq) * CHUNK_COLS - sg.c;   // rank index of v[0]
       if (row >= bound) continue;
+      if (g.col_sub) {
+        // several adapters per job: each column of this item's job goes to its own adapter's
+        // gradient (dB only for the output rows that adapter's B covers).  A chunk can also hold
+        // other jobs' columns; this item reduced over its own job's tokens only, so those are
+        // left to the other jobs' items.
+        const int c_first = (w.q0 + jq) * CHUNK_COLS;
+#pragma unroll
+        for (int u = 0; u < 64; ++u) {
+          const int c = c_first + u;
+          const int a = (c >= sg.c && c < sg.c + sg.r) ? __ldg(g.col_sub + c) : -1;
+          if (a >= 0) {
+            const DevSub* sb = g.subs + a;
+            if constexpr (MODE == MODE_DA) {
+              sb->dAt[static_cast<size_t>(c_first + u - sb->c0) * g.d_in + row] = __uint_as_float(v[u]);
+            } else {
+              if (row >= sb->o_lo && row < sb->o_hi)
+                sb->dBt[static_cast<size_t>(row - sb->o_lo) * sb->r + (c_first + u - sb->c0)] = __uint_as_float(v[u]);
+            }
+          }
+        }
+        continue;
+      }
       if constexpr (MODE == MODE_DA) {
         // dAt_i[t][row]: for a fixed t the 32 lanes write 32 consecutive rows (coalesced)
 #pragma unroll

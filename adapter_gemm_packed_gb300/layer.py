@@ -27,37 +27,63 @@ def _stream(stream) -> int:
 
 
 class PackedLoRA:
+    """One plan and its buffers.
+
+    ``groups`` (optional, a list of output widths summing to d_out) makes a shared-input pack:
+    then ``ranks[j]``, ``scales[j]`` (and ``At[j]``, ``Bt[j]`` if given) are lists with one entry
+    per group, job j's adapter on that group, whose Bt is [width_g, r].  The flat lists
+    ``self.At``, ``self.Bt``, ``self.dAt``, ... follow the segment table's job-major order."""
+
     def __init__(self, d_in: int, d_out: int, ranks, n_tokens, scales, dtype: str = "bf16",
                  device: str | torch.device = "cuda", flags: int = 0, At=None, Bt=None,
-                 with_grads: bool = True, with_moments: bool = True):
+                 with_grads: bool = True, with_moments: bool = True, groups=None):
         self.d_in, self.d_out = int(d_in), int(d_out)
-        self.ranks = [int(r) for r in ranks]
         self.n_tokens = [int(n) for n in n_tokens]
-        self.scales = [float(s) for s in scales]
+        self.groups = None if groups is None else [int(w) for w in groups]
+        G = 1 if groups is None else len(self.groups)
+        widths = [self.d_out] if groups is None else self.groups
+        nest = (lambda x: [[v] for v in x]) if groups is None else (lambda x: [list(v) for v in x])
+        ranks_jg = nest(ranks)
+        scales_jg = nest(scales)
+        At_jg = None if At is None else nest(At)
+        Bt_jg = None if Bt is None else nest(Bt)
+        self.ranks = [int(r) for rj in ranks_jg for r in rj]              # per entry, job-major
+        self.scales = [float(x) for sj in scales_jg for x in sj]
+        self.job_rank = [sum(int(r) for r in rj) for rj in ranks_jg]       # R_j: width of job j's H block
         self.dtype = dtype
         self.code, self.tdtype = _DT[dtype]
         self.device = torch.device(device)
         self.N = sum(self.n_tokens)
         f32 = dict(dtype=torch.float32, device=self.device)
-        self.At = [torch.as_tensor(a).to(**f32).contiguous() if At is not None else torch.zeros((r, self.d_in), **f32)
-                   for r, a in zip(self.ranks, At if At is not None else self.ranks)]
-        self.Bt = [torch.as_tensor(b).to(**f32).contiguous() if Bt is not None else torch.zeros((self.d_out, r), **f32)
-                   for r, b in zip(self.ranks, Bt if Bt is not None else self.ranks)]
+        self.At, self.Bt = [], []
+        for j, rj in enumerate(ranks_jg):
+            for g, r in enumerate(rj):
+                self.At.append(torch.as_tensor(At_jg[j][g]).to(**f32).contiguous() if At is not None
+                               else torch.zeros((r, self.d_in), **f32))
+                self.Bt.append(torch.as_tensor(Bt_jg[j][g]).to(**f32).contiguous() if Bt is not None
+                               else torch.zeros((widths[g], r), **f32))
         z = lambda t: torch.zeros_like(t)
-        self.dAt = [z(a) for a in self.At] if with_grads else [None] * len(self.ranks)
-        self.dBt = [z(b) for b in self.Bt] if with_grads else [None] * len(self.ranks)
-        self.mA = [z(a) for a in self.At] if with_moments else [None] * len(self.ranks)
-        self.vA = [z(a) for a in self.At] if with_moments else [None] * len(self.ranks)
-        self.mB = [z(b) for b in self.Bt] if with_moments else [None] * len(self.ranks)
-        self.vB = [z(b) for b in self.Bt] if with_moments else [None] * len(self.ranks)
+        n_e = len(self.ranks)
+        self.dAt = [z(a) for a in self.At] if with_grads else [None] * n_e
+        self.dBt = [z(b) for b in self.Bt] if with_grads else [None] * n_e
+        self.mA = [z(a) for a in self.At] if with_moments else [None] * n_e
+        self.vA = [z(a) for a in self.At] if with_moments else [None] * n_e
+        self.mB = [z(b) for b in self.Bt] if with_moments else [None] * n_e
+        self.vB = [z(b) for b in self.Bt] if with_moments else [None] * n_e
         segs, off = [], 0
-        for i, (r, n, s) in enumerate(zip(self.ranks, self.n_tokens, self.scales)):
-            segs.append(M.mlora_segment(off, n, r, s, _ptr(self.At[i]), _ptr(self.Bt[i]), _ptr(self.dAt[i]),
-                                        _ptr(self.dBt[i]), _ptr(self.mA[i]), _ptr(self.vA[i]), _ptr(self.mB[i]),
-                                        _ptr(self.vB[i])))
+        for j, n in enumerate(self.n_tokens):
+            for g in range(G):
+                i = j * G + g
+                segs.append(M.mlora_segment(off, n, self.ranks[i], self.scales[i], _ptr(self.At[i]), _ptr(self.Bt[i]),
+                                            _ptr(self.dAt[i]), _ptr(self.dBt[i]), _ptr(self.mA[i]), _ptr(self.vA[i]),
+                                            _ptr(self.mB[i]), _ptr(self.vB[i])))
             off += n
         self.problem = M.mlora_problem(self.N, self.d_in, self.d_out, self.code, flags)
-        self.plan, self.ws_bytes = M.mlora_plan(self.problem, segs)
+        if groups is None:
+            self.plan, self.ws_bytes = M.mlora_plan(self.problem, segs)
+        else:
+            offs = [sum(widths[:g]) for g in range(G)]
+            self.plan, self.ws_bytes = M.mlora_plan_grouped(self.problem, list(zip(offs, widths)), segs)
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=self.device)
         h = M.mlora_h_elems(self.plan)
         self.H = torch.zeros(max(h, 1), **f32)
@@ -100,10 +126,11 @@ class PackedLoRA:
         return M.mlora_plan_describe(self.plan, what)
 
     def h_blocks(self, H=None):
-        """Split the packed H (or dH) into per-job [n_i, r_i] views."""
+        """Split the packed H (or dH) into per-job [n_j, R_j] views (R_j = r_j, or the sum of the
+        job's ranks over the groups of a shared-input pack)."""
         H = self.H if H is None else H
         out, o = [], 0
-        for n, r in zip(self.n_tokens, self.ranks):
+        for n, r in zip(self.n_tokens, self.job_rank):
             out.append(H[o:o + n * r].view(n, r))
             o += n * r
         return out
@@ -138,3 +165,18 @@ def host_plan(d_in, d_out, ranks, n_tokens, dtype="bf16", scales=None, offsets=N
     prob = M.mlora_problem(sum(n_tokens) if n_total is None else n_total, d_in, d_out, code,
                            M.MLORA_PLAN_HOST_ONLY | flags)
     return M.mlora_plan(prob, segs)
+
+
+def host_plan_grouped(d_in, widths, ranks_jg, n_tokens, dtype="bf16", flags=0):
+    """Host-only shared-input plan over placeholder pointers (see host_plan); ranks_jg[j][g] is
+    job j's rank on group g.  Returns (handle, workspace_bytes)."""
+    code = _DT[dtype][0]
+    segs, off, k = [], 0, 0
+    for rj, n in zip(ranks_jg, n_tokens):
+        for r in rj:
+            segs.append(M.mlora_segment(off, n, r, 1.0, *[0x100000 * (1 + 16 * k + u) for u in range(8)]))
+            k += 1
+        off += n
+    offs = [sum(widths[:g]) for g in range(len(widths))]
+    prob = M.mlora_problem(sum(n_tokens), d_in, sum(widths), code, M.MLORA_PLAN_HOST_ONLY | flags)
+    return M.mlora_plan_grouped(prob, list(zip(offs, widths)), segs)

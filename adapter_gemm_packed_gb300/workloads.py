@@ -104,10 +104,42 @@ class Workload:
     beta2: float = 0.999
     eps: float = 1e-8
     weight_decay: float = 0.01
+    # Shared-input pack: output widths of the projections stacked in W (None = one projection).
+    # Then ``ranks`` / ``alphas`` hold one entry per (job, projection), job-major, and adapter
+    # entry i = j * G + g has Bt [groups[g], r].
+    groups: list = None
 
     @property
     def n_adapters(self) -> int:
         return len(self.ranks)
+
+    @property
+    def n_groups(self) -> int:
+        return 1 if self.groups is None else len(self.groups)
+
+    @property
+    def widths(self) -> list:
+        return [self.d_out] if self.groups is None else list(self.groups)
+
+    @property
+    def group_offsets(self) -> list:
+        w = self.widths
+        return [sum(w[:g]) for g in range(len(w))]
+
+    @property
+    def entry_tokens(self) -> list:
+        """Tokens of each adapter entry (a job's count repeated once per projection)."""
+        return [n for n in self.n_tokens for _ in range(self.n_groups)]
+
+    @property
+    def entry_width(self) -> list:
+        """Output width of each adapter entry's B."""
+        return [w for _ in self.n_tokens for w in self.widths]
+
+    def nest(self, flat) -> list:
+        """Per-entry list -> per-job lists of per-projection values."""
+        G = self.n_groups
+        return [list(flat[j * G:(j + 1) * G]) for j in range(len(self.n_tokens))]
 
     @property
     def offsets(self) -> list:
@@ -202,6 +234,28 @@ def custom(name: str, cfg_id: int, d_in: int, d_out: int, ranks, n_tokens, alpha
                     w_std=w_std, a_std=a_std, b_std=b_std)
 
 
+def custom_grouped(name: str, cfg_id: int, d_in: int, widths, ranks_jg, n_tokens, alphas_jg=None, dtype="bf16",
+                   w_std=0.02, a_std=None, b_std=0.02) -> Workload:
+    """A shared-input pack: the projections of widths ``widths`` stacked in W, job j with rank
+    ranks_jg[j][g] on projection g (alpha = 2 r unless given)."""
+    ranks = [int(r) for rj in ranks_jg for r in rj]
+    alphas = [2.0 * r for r in ranks] if alphas_jg is None else [float(a) for aj in alphas_jg for a in aj]
+    a_std = (1.0 / d_in) ** 0.5 if a_std is None else a_std
+    return Workload(name, cfg_id, d_in, int(sum(widths)), dtype, ranks, [int(n) for n in n_tokens], alphas,
+                    w_std=w_std, a_std=a_std, b_std=b_std, groups=[int(w) for w in widths])
+
+
+def llama8b_qkv_shared() -> Workload:
+    """The q, k and v projections of a Llama-3-8B layer as one shared-input pack (4096 ->
+    4096 + 1024 + 1024): the jobs, ranks and token counts of the per-projection layer workloads,
+    each job's rank the same on all three projections."""
+    q = llama8b_layer(0)
+    ranks_jg = [[r, r, r] for r in q.ranks]
+    wl = custom_grouped("llama3_8b_layer_qkv_shared_4096x6144_32ad", 50, 4096, [4096, 1024, 1024], ranks_jg,
+                        q.n_tokens, a_std=(1.0 / 4096) ** 0.5)
+    return wl
+
+
 def llama8b_qproj_w4() -> Workload:
     """The q_proj workload with a 4-bit base weight (int4 codes, fp32 scales per 64 inputs)."""
     wl = llama8b_qproj()
@@ -217,6 +271,7 @@ CONFIGS = {
     "qproj": llama8b_qproj,
     "mlp_up": mlp_up_lognormal,
     "many_small": llama70b_down_many_small,
+    "qkv_shared": llama8b_qkv_shared,
 }
 
 
@@ -250,9 +305,9 @@ def materialise(wl: Workload, with_dY: bool = True) -> Tensors:
     X = _act(wl, T_X, N * wl.d_in, 1.0).reshape(N, wl.d_in)
     dY = _act(wl, T_DY, N * wl.d_out, 1.0).reshape(N, wl.d_out) if with_dY else None
     At, Bt = [], []
-    for i, r in enumerate(wl.ranks):
+    for i, (r, w) in enumerate(zip(wl.ranks, wl.entry_width)):
         At.append(normal_f32(wl.cfg_id, T_ADAPTER_BASE + 4 * i, r * wl.d_in, wl.a_std).reshape(r, wl.d_in))
-        Bt.append(normal_f32(wl.cfg_id, T_ADAPTER_BASE + 4 * i + 1, wl.d_out * r, wl.b_std).reshape(wl.d_out, r))
+        Bt.append(normal_f32(wl.cfg_id, T_ADAPTER_BASE + 4 * i + 1, w * r, wl.b_std).reshape(w, r))
     T = Tensors(wl, Wt, X, dY, At, Bt)
     if wl.dtype == "bf16_w4":
         T.Wq, T.Wscale = w4_weight(wl)

@@ -49,35 +49,42 @@ def workload(name):
     raise SystemExit(f"unknown workload {name}")
 
 
+def _entries(wl):
+    """(tokens, rank, output width of B) of every adapter (one per job, or one per job and
+    projection of a shared-input pack)."""
+    return list(zip(wl.entry_tokens, wl.ranks, wl.entry_width))
+
+
 def flops_per_step(wl):
-    lora = sum(n * r for n, r in zip(wl.n_tokens, wl.ranks))
-    return 4.0 * wl.N * wl.d_in * wl.d_out + 6.0 * lora * (wl.d_in + wl.d_out)
+    # 4 N d_in d_out for the two base GEMMs, 6 n r (d_in + width) per adapter (shrink, expand,
+    # dH, dB, dA, dX term); the zero padding and other projections' zero blocks are not counted
+    return 4.0 * wl.N * wl.d_in * wl.d_out + sum(6.0 * n * r * (wl.d_in + w) for n, r, w in _entries(wl))
 
 
 def kernel_flops(wl, kernel):
     """Algorithmic FLOPs of one launch of a tensor-core kernel."""
-    lora = sum(n * r for n, r in zip(wl.n_tokens, wl.ranks))
     if kernel == "fwd_gemm":
-        return 2.0 * wl.N * wl.d_in * wl.d_out + 2.0 * lora * wl.d_out
+        return 2.0 * wl.N * wl.d_in * wl.d_out + sum(2.0 * n * r * w for n, r, w in _entries(wl))
     if kernel == "bwd_gemm":
-        return 2.0 * wl.N * wl.d_in * wl.d_out + 2.0 * lora * wl.d_in
+        return 2.0 * wl.N * wl.d_in * wl.d_out + sum(2.0 * n * r * wl.d_in for n, r, w in _entries(wl))
     return None
 
 
 def kernel_bytes(wl, kernel):
     """Algorithmic HBM bytes of one launch of a memory-bound kernel (bf16 activations)."""
     e = 2
-    lora = sum(n * r for n, r in zip(wl.n_tokens, wl.ranks))
+    lora = sum(n * r for n, r, w in _entries(wl))
     sr = sum(wl.ranks)
-    params = sr * (wl.d_in + wl.d_out)
+    srw = sum(r * w for n, r, w in _entries(wl))
+    params = sr * wl.d_in + srw
     if kernel == "shrink":
         return wl.N * wl.d_in * e + sr * wl.d_in * 2 + lora * 4
     if kernel == "dH":
-        return wl.N * wl.d_out * e + sr * wl.d_out * 2 + lora * 4
+        return wl.N * wl.d_out * e + srw * 2 + lora * 4
     if kernel == "dA":
         return wl.N * wl.d_in * e + lora * 2 + wl.d_in * sr * 4
     if kernel == "dB":
-        return wl.N * wl.d_out * e + lora * 2 + wl.d_out * sr * 4
+        return wl.N * wl.d_out * e + lora * 2 + srw * 4
     if kernel == "adamw":
         return params * 28
     if kernel == "w4_expand":
@@ -165,24 +172,37 @@ def oracle_sample(wl, T, per_job):
         Wm = orc.dequantize_w4(T.Wq, T.Wscale)
     else:
         Wm = W.rows_as_f64(T.Wt, wl.dtype).T.copy()
-    segs, off = [], 0
-    for i, n in enumerate(wl.n_tokens):
-        k = min(per_job, n)
-        segs.append(orc.Seg(off, k, T.At[i].astype(np.float64).T.copy(), T.Bt[i].astype(np.float64).T.copy(),
-                            wl.alphas[i]))
-        off += k
+    # per projection (one unless the workload is a shared-input pack): its jobs' adapters
+    G = wl.n_groups
+    segs = []
+    for g in range(G):
+        sg, off = [], 0
+        for j, n in enumerate(wl.n_tokens):
+            k = min(per_job, n)
+            i = j * G + g
+            sg.append(orc.Seg(off, k, T.At[i].astype(np.float64).T.copy(), T.Bt[i].astype(np.float64).T.copy(),
+                              wl.alphas[i]))
+            off += k
+        segs.append(sg)
     return X, Wm, dY, segs, len(rows)
 
 
 def oracle_step(wl, X, Wm, dY, segs, state, t):
+    """One oracle step: each projection's column slice with its adapters (Y side by side, dX
+    summed), then AdamW on every adapter."""
+    import numpy as np
     from oracle import lora_oracle as orc
-    Y, H = orc.forward(X, Wm, segs)
-    dX, dA, dB, dH = orc.backward(X, Wm, dY, segs)
-    for i, sg in enumerate(segs):
-        for name, p, g in (("A", sg.A, dA[i]), ("B", sg.B, dB[i])):
-            m, v = state.get((name, i), (0.0, 0.0))
-            p2, m, v = orc.adamw(p, g, m, v, wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, t)
-            state[(name, i)] = (m, v)
+    Y = np.zeros((X.shape[0], Wm.shape[1]))
+    dX = np.zeros_like(X)
+    for g, (o, w) in enumerate(zip(wl.group_offsets, wl.widths)):
+        Y[:, o:o + w], H = orc.forward(X, Wm[:, o:o + w], segs[g])
+        dXg, dA, dB, dH = orc.backward(X, Wm[:, o:o + w], dY[:, o:o + w], segs[g])
+        dX += dXg
+        for i, sg in enumerate(segs[g]):
+            for name, p, gr in (("A", sg.A, dA[i]), ("B", sg.B, dB[i])):
+                m, v = state.get((name, g, i), (0.0, 0.0))
+                p2, m, v = orc.adamw(p, gr, m, v, wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, t)
+                state[(name, g, i)] = (m, v)
     return Y, dX
 
 
@@ -202,7 +222,7 @@ def run_reference(args, wl, rank):
     oracle_step(wl, X, Wm, dY, segs, {}, 1)
     per_tok = (time.perf_counter() - t0) / ntok
     budget = args.ref_budget_s / max(1, args.steps + args.warmup)
-    per_job = int(max(1, min(args.ref_tokens_per_job, budget / per_tok / wl.n_adapters)))
+    per_job = int(max(1, min(args.ref_tokens_per_job, budget / per_tok / len(wl.n_tokens))))
     X, Wm, dY, segs, ntok = oracle_sample(wl, T, per_job)
     state = {}
     for t in range(1, args.warmup + 1):
@@ -212,7 +232,7 @@ def run_reference(args, wl, rank):
         oracle_step(wl, X, Wm, dY, segs, state, t)
     dt = time.perf_counter() - t0
     value = ntok * args.steps / dt
-    sample = f"first {per_job} tokens of each of the {wl.n_adapters} jobs ({ntok} tokens), full d_in x d_out"
+    sample = f"first {per_job} tokens of each of the {len(wl.n_tokens)} jobs ({ntok} tokens), full d_in x d_out"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -271,8 +291,13 @@ def run_ours(args, wl, rank, world, local_rank):
     T = W.materialise(wl)
     scales = [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
     flags = (0 if args.no_reuse else M.MLORA_REUSE_STAGING) | (M.MLORA_W4_FUSED if args.w4_fused else 0)
-    layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At, Bt=T.Bt,
-                       flags=flags)
+    if wl.groups is None:
+        layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At, Bt=T.Bt,
+                           flags=flags)
+    else:
+        # shared-input pack: one adapter per job and projection, the projections stacked in W
+        layer = PackedLoRA(wl.d_in, wl.d_out, wl.nest(wl.ranks), wl.n_tokens, wl.nest(scales), dtype=wl.dtype,
+                           At=wl.nest(T.At), Bt=wl.nest(T.Bt), flags=flags, groups=wl.groups)
     tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
 
     def host(a):

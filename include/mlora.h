@@ -136,6 +136,36 @@ typedef struct mlora_plan_s mlora_plan_t;
 mlora_status mlora_plan(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
                         size_t* workspace_bytes, mlora_plan_t** out);
 
+/* Shared-input pack: several projections read the same input X (the q, k and v projections of
+ * an attention block, or gate and up of an MLP), and each job trains one adapter per
+ * projection.  Their frozen weights are stacked into one W^T [d_out, d_in] whose output columns
+ * fall into n_groups groups, group g covering [col_offset_g, col_offset_g + d_out_g) (the
+ * groups tile [0, d_out) in order), and Y = X W is the projections' outputs side by side.
+ * ("PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §8 names the seven
+ * adaptable projections of a block; sharing their input across one pass over X is this
+ * library's design, the pages describe no such kernel.)
+ *
+ * segs holds n_jobs x n_groups entries, job-major: segs[j * n_groups + g] is job j's adapter
+ * on group g, with Bt [d_out_g, r] (its own group's columns only; dBt, mB, vB alike) and
+ * At [r, d_in]; all entries of a job give the same tok_offset and n_tokens, and the jobs tile
+ * [0, N) in order.  Each adapter computes exactly what a one-group plan would on its group:
+ *     Y_j[:, group g] = X_j W_g + s_jg (X_j A_jg) B_jg,
+ *     dX_j = dY_j W^T + sum_g s_jg dY_j[:, group g] B_jg^T A_jg^T,
+ * with its own gradients and AdamW state.  H and dH hold job j's block [n_j, R_j] at element
+ * offset sum_{i<j} n_i R_i, R_j = sum_g r_jg, adapter g in columns [sum_{h<g} r_jh, ... + r_jg).
+ * One pass over X computes every adapter's H (and one pass over dY every dH).  bf16 and 4-bit
+ * bases only (MLORA_ERR_UNSUPPORTED for fp32 with more than one group); otherwise errors,
+ * ownership and the entry points are those of mlora_plan, which is this call with one group
+ * {0, d_out}. */
+typedef struct mlora_group {
+    int32_t col_offset;   /* first output column of the group in Y / dY / rows of W^T */
+    int32_t d_out;        /* its width (>= 1) */
+} mlora_group;
+
+mlora_status mlora_plan_grouped(const mlora_problem* problem, const mlora_group* groups, int32_t n_groups,
+                                const mlora_segment* segs, int32_t n_segs, size_t* workspace_bytes,
+                                mlora_plan_t** out);
+
 /* Free the plan's device tables (after work using it has finished). NULL is a no-op. */
 void mlora_plan_destroy(mlora_plan_t* plan);
 
@@ -191,13 +221,16 @@ int64_t mlora_h_elems(const mlora_plan_t* plan);
  *   MLORA_Q_COLUMNS : per job: first column of its rank window, padded width
  *   MLORA_Q_WGRAD_A : per dA work item: row block, job, first and end half-tile, first chunk, chunks
  *   MLORA_Q_WGRAD_B : per dB work item: same fields
- *   MLORA_Q_WINDOW  : per shrink / dH work item: tile, first chunk, chunks */
+ *   MLORA_Q_WINDOW  : per shrink / dH work item: tile, first chunk, chunks
+ *   MLORA_Q_ADAPTERS: per segment-table entry: job, first packed column, rank, first and end
+ *                     output column of its B */
 #define MLORA_Q_SUMMARY 0
 #define MLORA_Q_MTILES 1
 #define MLORA_Q_COLUMNS 2
 #define MLORA_Q_WGRAD_A 3
 #define MLORA_Q_WGRAD_B 4
 #define MLORA_Q_WINDOW 5
+#define MLORA_Q_ADAPTERS 6
 mlora_status mlora_plan_describe(const mlora_plan_t* plan, int32_t what, int64_t* out, int64_t cap,
                                  int64_t* count);
 

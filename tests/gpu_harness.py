@@ -45,9 +45,21 @@ def scales_of(wl):
     return [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
 
 
-def oracle_segs(wl, T):
-    return [orc.Seg(o, n, T.At[i].astype(np.float64).T, T.Bt[i].astype(np.float64).T, wl.alphas[i])
-            for i, (o, n) in enumerate(zip(wl.offsets, wl.n_tokens))]
+def make_layer(wl, T, flags=0):
+    """The PackedLoRA of a workload (a shared-input pack when the workload has groups)."""
+    if wl.groups is None:
+        return PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales_of(wl), dtype=wl.dtype,
+                          At=T.At, Bt=T.Bt, flags=flags)
+    return PackedLoRA(wl.d_in, wl.d_out, wl.nest(wl.ranks), wl.n_tokens, wl.nest(scales_of(wl)), dtype=wl.dtype,
+                      At=wl.nest(T.At), Bt=wl.nest(T.Bt), flags=flags, groups=wl.groups)
+
+
+def oracle_segs(wl, T, g=0):
+    """The oracle's job list for projection g (the only one unless the workload has groups)."""
+    G = wl.n_groups
+    return [orc.Seg(o, n, T.At[j * G + g].astype(np.float64).T, T.Bt[j * G + g].astype(np.float64).T,
+                    wl.alphas[j * G + g])
+            for j, (o, n) in enumerate(zip(wl.offsets, wl.n_tokens))]
 
 
 class GpuRun:
@@ -56,8 +68,7 @@ class GpuRun:
     def __init__(self, wl, T, step=True, flags=0, Wt_override=None):
         self.wl = wl
         torch.cuda.synchronize()
-        self.layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales_of(wl), dtype=wl.dtype,
-                                At=T.At, Bt=T.Bt, flags=flags)
+        self.layer = make_layer(wl, T, flags)
         self.X = to_dev(T.X, wl.dtype)
         if wl.dtype == "bf16_w4":
             self.Wt = (torch.from_numpy(T.Wq).cuda(), torch.from_numpy(T.Wscale).cuda())
@@ -97,14 +108,31 @@ def base_weight_f64(wl, T, Wt_override=None):
 
 
 def oracle_full(wl, T, Wt_override=None):
-    """Every output of the layer (and the AdamW step at t=1 from zero moments), fp64."""
+    """Every output of the layer (and the AdamW step at t=1 from zero moments), fp64.
+
+    A shared-input pack is the oracle applied to each projection's column slice of W and dY
+    with that projection's adapters: Y is the slices side by side, dX their sum, a job's H and
+    dH its adapters' blocks side by side."""
     X = W.rows_as_f64(T.X, wl.dtype)
     Wm = base_weight_f64(wl, T, Wt_override)
     dY = W.rows_as_f64(T.dY, wl.dtype)
-    segs = oracle_segs(wl, T)
-    Y, H = orc.forward(X, Wm, segs)
-    dX, dA, dB, dH = orc.backward(X, Wm, dY, segs)
-    out = dict(Y=Y, dX=dX, H=H, dH=dH, dAt=[a.T for a in dA], dBt=[b.T for b in dB])
+    G, J = wl.n_groups, len(wl.n_tokens)
+    Y = np.zeros((wl.N, wl.d_out))
+    dX = np.zeros((wl.N, wl.d_in))
+    Hj, dHj = [[] for _ in range(J)], [[] for _ in range(J)]
+    dAt, dBt = [None] * wl.n_adapters, [None] * wl.n_adapters
+    for g, (o, w) in enumerate(zip(wl.group_offsets, wl.widths)):
+        segs = oracle_segs(wl, T, g)
+        Yg, Hg = orc.forward(X, Wm[:, o:o + w], segs)
+        dXg, dAg, dBg, dHg = orc.backward(X, Wm[:, o:o + w], dY[:, o:o + w], segs)
+        Y[:, o:o + w] = Yg
+        dX += dXg
+        for j in range(J):
+            Hj[j].append(Hg[j])
+            dHj[j].append(dHg[j])
+            dAt[j * G + g] = dAg[j].T
+            dBt[j * G + g] = dBg[j].T
+    out = dict(Y=Y, dX=dX, H=[np.hstack(h) for h in Hj], dH=[np.hstack(h) for h in dHj], dAt=dAt, dBt=dBt)
     out.update(adamw_expect(wl, T, out["dAt"], out["dBt"]))
     return out
 

@@ -47,32 +47,45 @@ def check_fullsize(wl, step=True, flags=0):
         run.close()
     tol = G.TOL[wl.dtype]
     errs = {}
-    # sampled rows of Y and dX
+    # sampled rows of Y and dX (a shared-input pack: per projection's column slice, dX summed)
     rows = sample_rows(wl)
     Wm = G.base_weight_f64(wl, T)
-    segs = G.oracle_segs(wl, T)
-    Yo = orc.forward_rows(W.rows_as_f64(T.X[rows], wl.dtype), rows, Wm, segs)
-    dXo = orc.backward_rows(W.rows_as_f64(T.dY[rows], wl.dtype), rows, Wm, segs)
+    Xr, dYr = W.rows_as_f64(T.X[rows], wl.dtype), W.rows_as_f64(T.dY[rows], wl.dtype)
+    Yo = np.zeros((len(rows), wl.d_out))
+    dXo = np.zeros((len(rows), wl.d_in))
+    for g, (o, w) in enumerate(zip(wl.group_offsets, wl.widths)):
+        segs = G.oracle_segs(wl, T, g)
+        Yo[:, o:o + w] = orc.forward_rows(Xr, rows, Wm[:, o:o + w], segs)
+        dXo += orc.backward_rows(dYr[:, o:o + w], rows, Wm[:, o:o + w], segs)
     errs["Y_rows"] = G.rel_err(got["Y"][rows], Yo)
     errs["dX_rows"] = G.rel_err(got["dX"][rows], dXo)
     del Wm
-    # adapter-side results in full, one job at a time
+    # adapter-side results in full, one adapter at a time (a job's H / dH hold its adapters'
+    # blocks side by side)
     worst = {k: 0.0 for k in ("H", "dH", "dAt", "dBt", "At", "Bt", "mA", "vA", "mB", "vB")}
-    for i, sg in enumerate(segs):
-        rs = slice(sg.offset, sg.offset + sg.n)
-        one = [orc.Seg(0, sg.n, sg.A, sg.B, sg.alpha)]
-        H, dH, dA, dB = orc.lora_grads(W.rows_as_f64(T.X[rs], wl.dtype), W.rows_as_f64(T.dY[rs], wl.dtype), one)
-        cmp = {"H": (got["H"][i], H[0]), "dH": (got["dH"][i], dH[0]), "dAt": (got["dAt"][i], dA[0].T),
-               "dBt": (got["dBt"][i], dB[0].T)}
-        if step:
-            for name, p, g, mk, vk in (("At", T.At[i], dA[0].T, "mA", "vA"), ("Bt", T.Bt[i], dB[0].T, "mB", "vB")):
-                p2, m2, v2 = orc.adamw(p.astype(np.float64), g, 0.0, 0.0, wl.lr, wl.beta1, wl.beta2, wl.eps,
-                                       wl.weight_decay, 1)
-                cmp[name] = (got[name][i], p2)
-                cmp[mk] = (got[mk][i], m2)
-                cmp[vk] = (got[vk][i], v2)
-        for k, (a, b) in cmp.items():
-            worst[k] = max(worst[k], G.rel_err(a, b))
+    Gn = wl.n_groups
+    for j, (off, n) in enumerate(zip(wl.offsets, wl.n_tokens)):
+        rs = slice(off, off + n)
+        Xj = W.rows_as_f64(T.X[rs], wl.dtype)
+        dYj = W.rows_as_f64(T.dY[rs], wl.dtype)
+        t0 = 0
+        for g, (o, w) in enumerate(zip(wl.group_offsets, wl.widths)):
+            i = j * Gn + g
+            r = wl.ranks[i]
+            one = [orc.Seg(0, n, T.At[i].astype(np.float64).T, T.Bt[i].astype(np.float64).T, wl.alphas[i])]
+            H, dH, dA, dB = orc.lora_grads(Xj, dYj[:, o:o + w], one)
+            cmp = {"H": (got["H"][j][:, t0:t0 + r], H[0]), "dH": (got["dH"][j][:, t0:t0 + r], dH[0]),
+                   "dAt": (got["dAt"][i], dA[0].T), "dBt": (got["dBt"][i], dB[0].T)}
+            if step:
+                for name, p, gr, mk, vk in (("At", T.At[i], dA[0].T, "mA", "vA"), ("Bt", T.Bt[i], dB[0].T, "mB", "vB")):
+                    p2, m2, v2 = orc.adamw(p.astype(np.float64), gr, 0.0, 0.0, wl.lr, wl.beta1, wl.beta2, wl.eps,
+                                           wl.weight_decay, 1)
+                    cmp[name] = (got[name][i], p2)
+                    cmp[mk] = (got[mk][i], m2)
+                    cmp[vk] = (got[vk][i], v2)
+            for k, (a, b) in cmp.items():
+                worst[k] = max(worst[k], G.rel_err(a, b))
+            t0 += r
     errs.update(worst)
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"tolerance {tol} exceeded: {bad} (all: {errs})"
@@ -86,6 +99,10 @@ def test_qproj_llama8b_fullsize():
 @pytest.mark.parametrize("fused", [False, True], ids=["expand", "fused"])
 def test_qproj_llama8b_w4_base_fullsize(fused):
     check_fullsize(W.llama8b_qproj_w4(), flags=M.MLORA_W4_FUSED if fused else 0)
+
+
+def test_qkv_shared_input_llama8b_fullsize():
+    check_fullsize(W.llama8b_qkv_shared())
 
 
 def test_mlp_up_lognormal_fullsize():

@@ -38,7 +38,7 @@ def _tables(plan):
     summ = dict(zip(keys, s))
     mt = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_MTILES)).reshape(-1, 5)
     cols = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_COLUMNS)).reshape(-1, 2)
-    win = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WINDOW)).reshape(-1, 3)
+    win = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WINDOW)).reshape(-1, 5)
     da = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WGRAD_A)).reshape(-1, 6)
     db = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WGRAD_B)).reshape(-1, 6)
     return summ, mt, cols, win, da, db
@@ -101,8 +101,9 @@ def test_planner_tables(name):
     assert summ["n_images"] == img
     # window work: each tile's chunks exactly once, <= 4 per item
     seen = {}
-    for t, q0, nq in win:
+    for t, q0, nq, kb0, nkb in win:
         assert 1 <= nq <= 4
+        assert (kb0, nkb) == (0, -(-d_out // 64))    # one projection: dH reads all of d_out
         for q in range(q0, q0 + nq):
             assert (t, q) not in seen
             seen[(t, q)] = 1
@@ -207,3 +208,115 @@ def test_w4_plan_flags(flags, status):
     # d_in must hold whole 64-wide scale groups
     assert _status_of(lambda: M.mlora_plan_destroy(
         host_plan(520, 384, [8], [100], dtype="bf16_w4", flags=flags)[0])) == M.MLORA_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- shared-input packs
+
+def _describe(plan, what):
+    return np.array(M.mlora_plan_describe(plan, what), dtype=np.int64)
+
+
+def test_grouped_plan_tables():
+    """A job's adapters sit side by side in its window (no padding between them, the window
+    padded to 16); H holds sum_g r_jg columns per job; dB items cover exactly the chunks of the
+    adapters whose output range meets their 256-row block; dA items cover the whole window."""
+    from adapter_gemm_packed_gb300.layer import host_plan_grouped
+    d_in, widths = 512, [256, 64, 320]
+    ranks_jg = [[8, 8, 8], [64, 16, 1], [3, 128, 32], [16, 16, 16]]
+    ns = [200, 56, 300, 17]
+    plan, ws = host_plan_grouped(d_in, widths, ranks_jg, ns)
+    try:
+        ad = _describe(plan, M.MLORA_Q_ADAPTERS).reshape(-1, 5)
+        cols = _describe(plan, M.MLORA_Q_COLUMNS).reshape(-1, 2)
+        wa = _describe(plan, M.MLORA_Q_WGRAD_A).reshape(-1, 6)
+        wb = _describe(plan, M.MLORA_Q_WGRAD_B).reshape(-1, 6)
+        h = M.mlora_h_elems(plan)
+    finally:
+        M.mlora_plan_destroy(plan)
+    offs = [0, 256, 320]
+    c, k = 0, 0
+    for j, rj in enumerate(ranks_jg):
+        assert cols[j][0] == c and cols[j][1] == -(-sum(rj) // 16) * 16
+        t = c
+        for g, r in enumerate(rj):
+            assert list(ad[k]) == [j, t, r, offs[g], offs[g] + widths[g]]
+            t += r
+            k += 1
+        c += cols[j][1]
+    assert h == sum(n * sum(rj) for n, rj in zip(ns, ranks_jg))
+    d_out = sum(widths)
+    for j, rj in enumerate(ranks_jg):
+        sub = ad[ad[:, 0] == j]
+        for r0 in range(0, d_out, 256):
+            meets = sub[(sub[:, 3] < r0 + 256) & (sub[:, 4] > r0)]
+            got = sorted(q for row0, job, ga, gb, q0, nq in wb if job == j and row0 == r0 for q in range(q0, q0 + nq))
+            if len(meets) == 0:
+                assert got == []
+                continue
+            lo, hi = meets[:, 1].min(), (meets[:, 1] + meets[:, 2]).max()
+            assert got == list(range(lo // 64, -(-hi // 64)))
+        for r0 in range(0, d_in, 256):
+            got = sorted(q for row0, job, ga, gb, q0, nq in wa if job == j and row0 == r0 for q in range(q0, q0 + nq))
+            lo, hi = cols[j][0], cols[j][0] + sum(rj)
+            assert got == list(range(lo // 64, -(-hi // 64)))
+
+
+def test_grouped_memory_model_counts_each_adapters_own_width():
+    from adapter_gemm_packed_gb300.layer import host_plan_grouped
+    d_in, widths = 512, [256, 64, 320]
+    ranks_jg = [[8, 8, 8], [64, 16, 1]]
+    plan, _ = host_plan_grouped(d_in, widths, ranks_jg, [100, 30])
+    try:
+        m = M.mlora_memory_estimate(plan)
+    finally:
+        M.mlora_plan_destroy(plan)
+    params = sum(r * (d_in + w) for rj in ranks_jg for r, w in zip(rj, widths))
+    assert m["lora_params"] == 4 * params
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(widths_off=[(0, 256), (200, 128)]), M.MLORA_ERR_INVALID),       # groups overlap
+    (dict(widths_off=[(0, 256), (256, 0)]), M.MLORA_ERR_INVALID),         # zero width
+    (dict(widths_off=[(0, 256), (256, 64)]), M.MLORA_ERR_INVALID),        # do not reach d_out
+    (dict(rows=[(0, 10), (0, 11)]), M.MLORA_ERR_INVALID),                 # a job's entries disagree
+    (dict(drop_last=True), M.MLORA_ERR_INVALID),                          # not n_jobs x n_groups
+    (dict(dtype=M.MLORA_F32), M.MLORA_ERR_UNSUPPORTED),                   # fp32 has one group only
+    (dict(rank=257), M.MLORA_ERR_UNSUPPORTED),
+])
+def test_grouped_plan_rejects(bad, status):
+    d_out = 384
+    groups = bad.get("widths_off", [(0, 256), (256, 128)])
+    rows = bad.get("rows", [(0, 10), (0, 10)])
+    segs = []
+    for j in range(2):
+        for g in range(2):
+            o, n = rows[g] if j == 0 else (10, 5)
+            segs.append(M.mlora_segment(o, n, bad.get("rank", 4) if (j, g) == (1, 1) else 4, 1.0,
+                                        *[0x100000 * (1 + 16 * (2 * j + g) + u) for u in range(8)]))
+    if bad.get("drop_last"):
+        segs = segs[:3]
+    prob = M.mlora_problem(15, 128, d_out, bad.get("dtype", M.MLORA_BF16), M.MLORA_PLAN_HOST_ONLY)
+    assert _status_of(lambda: M.mlora_plan_destroy(M.mlora_plan_grouped(prob, groups, segs)[0])) == status
+
+
+def test_grouped_dh_items_read_only_their_projections_slices():
+    """A dH item of a shared-input pack streams only the d_out slices covered by the adapters
+    that own its chunks' columns: chunks holding only k columns read only k's slice of dY."""
+    from adapter_gemm_packed_gb300.layer import host_plan_grouped
+    widths = [4096, 1024, 1024]
+    ranks_jg = [[128, 128, 128], [8, 8, 8]]
+    plan, _ = host_plan_grouped(512, widths, ranks_jg, [256, 256])
+    try:
+        ad = _describe(plan, M.MLORA_Q_ADAPTERS).reshape(-1, 5)
+        win = _describe(plan, M.MLORA_Q_WINDOW).reshape(-1, 5)
+    finally:
+        M.mlora_plan_destroy(plan)
+    for t, q0, nq, kb0, nkb in win:
+        lo, hi = 1 << 30, 0
+        for job, c0, r, o_lo, o_hi in ad:
+            if c0 < (q0 + nq) * 64 and c0 + r > q0 * 64:
+                lo, hi = min(lo, o_lo), max(hi, o_hi)
+        assert (kb0, nkb) == (lo // 64, -(-hi // 64) - lo // 64)
+    # job 0 (rank 128 per projection) spans chunks 0-5: q in 0-1, k in 2-3, v in 4-5
+    by_q0 = {q0: (kb0, nkb) for t, q0, nq, kb0, nkb in win if t == 0}
+    assert by_q0[0] == (0, 64) and by_q0[2] == (64, 16) and by_q0[4] == (80, 16)
