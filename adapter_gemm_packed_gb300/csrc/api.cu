@@ -569,6 +569,7 @@ GemmArgs base_args(const mlora_plan_t* P) {
     g.subs = P->d_subs;
     g.col_sub = P->d_col_sub;
     g.col_scale = P->d_col_scale;
+    g.n_groups = P->n_groups;
   }
   g.err = P->d_err;
   g.timeout_ns = P->timeout_ns;

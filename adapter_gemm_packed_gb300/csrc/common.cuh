@@ -126,9 +126,10 @@ struct GemmArgs {
   int debug_drop;          // test hook: CTA 0 arms its first slot but issues no copy into it
   // Shared-input packs (several adapters per job): per packed column, its adapter (-1 in the
   // padding) and scale.  Null for plans with one adapter per job, whose kernels read the job's.
-  const DevSub* subs;
+  const DevSub* subs;      // job j's adapters are subs[j * n_groups .. j * n_groups + n_groups)
   const int* col_sub;
   const float* col_scale;
+  int n_groups;
 };
 
 // Status codes written to the device status word (first one wins).

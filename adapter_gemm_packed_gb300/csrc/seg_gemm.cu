@@ -315,23 +315,40 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
       tmem_ld_wait();
       const int cbase = (w.q0 + jq) * CHUNK_COLS - sg.c;   // rank index of v[0]
       if (row >= bound) continue;
-      if (g.col_sub) {
-        // several adapters per job: each column of this item's job goes to its own adapter's
-        // gradient (dB only for the output rows that adapter's B covers).  A chunk can also hold
-        // other jobs' columns; this item reduced over its own job's tokens only, so those are
-        // left to the other jobs' items.
+      if (g.subs) {
+        // several adapters per job (one per projection): each adapter of this item's job takes
+        // its own run of the chunk's columns (dB only for the output rows its B covers).  A chunk
+        // can also hold other jobs' columns; this item reduced over its own job's tokens only,
+        // so those are left to the other jobs' items.
         const int c_first = (w.q0 + jq) * CHUNK_COLS;
+#pragma unroll 1
+        for (int a = w.seg * g.n_groups; a < (w.seg + 1) * g.n_groups; ++a) {
+          const DevSub sb = g.subs[a];
+          const int lo = max(sb.c0, c_first), hi = min(sb.c0 + sb.r, c_first + CHUNK_COLS);
+          if (lo >= hi) continue;
+          if constexpr (MODE == MODE_DA) {
+            // dAt[t][row]: for a fixed t the 32 lanes write 32 consecutive rows (coalesced)
 #pragma unroll
-        for (int u = 0; u < 64; ++u) {
-          const int c = c_first + u;
-          const int a = (c >= sg.c && c < sg.c + sg.r) ? __ldg(g.col_sub + c) : -1;
-          if (a >= 0) {
-            const DevSub* sb = g.subs + a;
-            if constexpr (MODE == MODE_DA) {
-              sb->dAt[static_cast<size_t>(c_first + u - sb->c0) * g.d_in + row] = __uint_as_float(v[u]);
-            } else {
-              if (row >= sb->o_lo && row < sb->o_hi)
-                sb->dBt[static_cast<size_t>(row - sb->o_lo) * sb->r + (c_first + u - sb->c0)] = __uint_as_float(v[u]);
+            for (int u = 0; u < 64; ++u) {
+              const int c = c_first + u;
+              if (c >= lo && c < hi) sb.dAt[static_cast<size_t>(c - sb.c0) * g.d_in + row] = __uint_as_float(v[u]);
+            }
+          } else {
+            if (row < sb.o_lo || row >= sb.o_hi) continue;
+            // dBt[row - o_lo][t]: one contiguous run per thread, 16-byte stores where aligned
+            float* dst = sb.dBt + static_cast<size_t>(row - sb.o_lo) * sb.r + (c_first - sb.c0);   // + u
+            const bool al = ((static_cast<long long>(row - sb.o_lo) * sb.r + (c_first - sb.c0)) & 3) == 0;
+#pragma unroll
+            for (int u = 0; u < 64; u += 4) {
+              const int c = c_first + u;
+              if (al && c >= lo && c + 3 < hi) {
+                *reinterpret_cast<float4*>(dst + u) = make_float4(__uint_as_float(v[u]), __uint_as_float(v[u + 1]),
+                                                                  __uint_as_float(v[u + 2]), __uint_as_float(v[u + 3]));
+              } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  if (c + k >= lo && c + k < hi) dst[u + k] = __uint_as_float(v[u + k]);
+              }
             }
           }
         }

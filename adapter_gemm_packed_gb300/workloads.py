@@ -256,6 +256,14 @@ def llama8b_qkv_shared() -> Workload:
     return wl
 
 
+def llama8b_qkv_shared_small() -> Workload:
+    """qkv_shared with an eighth of each job's tokens (about 18K; X and dY still above the L2),
+    a case small enough for detailed profiler captures."""
+    q = llama8b_layer(0)
+    return custom_grouped("llama3_8b_layer_qkv_shared_4096x6144_32ad_eighth", 51, 4096, [4096, 1024, 1024],
+                          [[r, r, r] for r in q.ranks], [n // 8 for n in q.n_tokens], a_std=(1.0 / 4096) ** 0.5)
+
+
 def llama8b_qproj_w4() -> Workload:
     """The q_proj workload with a 4-bit base weight (int4 codes, fp32 scales per 64 inputs)."""
     wl = llama8b_qproj()
@@ -272,6 +280,7 @@ CONFIGS = {
     "mlp_up": mlp_up_lognormal,
     "many_small": llama70b_down_many_small,
     "qkv_shared": llama8b_qkv_shared,
+    "qkv_shared_small": llama8b_qkv_shared_small,
 }
 
 

@@ -160,6 +160,45 @@ def weak_scaling_rate(units_per_rank: int, world: int, steps: int, max_ms: float
     return units_per_rank * world * steps / (max_ms / 1e3)
 
 
+def link_probe(x_h, x_d, y_h, y_d, s_in, s_out, reps=3):
+    """Host link bandwidth with pinned buffers: H2D alone, D2H alone, both at once (GB/s per
+    direction), timed with events bracketing the copies' streams."""
+    import torch
+
+    def run(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        s = torch.cuda.current_stream()
+        s.wait_stream(s_in)
+        s.wait_stream(s_out)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / reps
+
+    def h2d():
+        s_in.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s_in):
+            x_d.copy_(x_h, non_blocking=True)
+
+    def d2h():
+        s_out.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s_out):
+            y_h.copy_(y_d, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    bx, by = x_h.numel() * x_h.element_size(), y_h.numel() * y_h.element_size()
+    t_both = run(both)
+    return {"h2d_gbs": bx / run(h2d) / 1e9, "d2h_gbs": by / run(d2h) / 1e9,
+            "concurrent_gbs_per_direction": max(bx, by) / t_both / 1e9}
+
+
 def oracle_sample(wl, T, per_job):
     """A bounded sample of the workload for the CPU oracle: the first `per_job` tokens of every job."""
     import numpy as np
@@ -428,6 +467,12 @@ def run_ours(args, wl, rank, world, local_rank):
         e2e = {"value": weak_scaling_rate(wl.N, world, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": b_in, "d2h_bytes_per_step": b_out, "ms_per_step": ems / args.steps,
                "pipelined": "H2D and D2H copies on their own streams, double-buffered device buffers"}
+        # The host link bounds this number: measure it here (one direction at a time, then both at
+        # once, on X-sized pinned copies) and report the per-direction rate the pipeline reached.
+        link = link_probe(X_h, X, Y_h, Y, s_in, s_out)
+        step_s = ems / args.steps / 1e3
+        e2e["link"] = dict(link, achieved_h2d_gbs=b_in / step_s / 1e9, achieved_d2h_gbs=b_out / step_s / 1e9,
+                           frac_of_concurrent=max(b_in, b_out) / step_s / 1e9 / link["concurrent_gbs_per_direction"])
         if layer.sync_status() != M.MLORA_OK:
             raise SystemExit("device status error in the end-to-end region")
 
