@@ -34,6 +34,8 @@ cudaError_t launch_gemm_2sm(const CUtensorMap&, const CUtensorMap&, const CUtens
 template <int MODE>
 cudaError_t launch_gemm_2sm_w4(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+template <int MODE>
+cudaError_t launch_win_2sm(const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 cudaError_t launch_pack_fwd(const DevSub*, const int*, int, int, int, __nv_bfloat16*, __nv_bfloat16*, int,
                             cudaStream_t, bool);
 cudaError_t launch_h_images(const DevSeg*, const float*, const MTile*, const int*, int, long long, const float*,
@@ -145,7 +147,9 @@ struct mlora_plan_s {
   std::vector<MTile> mtiles;
   std::vector<int> img_tile;
   std::vector<int> col_sub;             // per packed column (chunk-padded), -1 in padding
-  std::vector<WinItem> win;
+  std::vector<WinItem> win;             // shrink / dH items of the single-CTA engine (tile, <= 2 chunks)
+  std::vector<WinItem> win2;            // the same work on CTA pairs (tile = pair, 2 or 4 chunks)
+  bool win_pairs = false;               // which of the two the shrink / dH launches run
   std::vector<WItem> da, db;
   std::vector<AdamItem> adam;
   bool can_backward = false, can_adamw = false;
@@ -163,6 +167,7 @@ struct mlora_plan_s {
   int* d_col_sub = nullptr;
   float* d_col_scale = nullptr;
   WinItem* d_win = nullptr;
+  WinItem* d_win2 = nullptr;
   WItem* d_da = nullptr;
   WItem* d_db = nullptr;
   AdamItem* d_adam = nullptr;
@@ -369,30 +374,56 @@ void build_tables(mlora_plan_t* P) {
   for (int t = 0; t < P->n_mtiles; ++t)
     for (int e = 0; e < P->mtiles[t].nch; ++e) P->img_tile[P->mtiles[t].img_off + e] = t;
 
-  // shrink / dH work: one item per (tile, <= 4 chunks)
+  // dH reads only the d_out slices that the adapters owning the item's columns cover
+  auto dh_range = [&](WinItem& w, int q0, int nq) {
+    int o_lo = pr.d_out, o_hi = 0;
+    for (int c = q0 * CHUNK_COLS; c < std::min(P->C_total, (q0 + nq) * CHUNK_COLS); ++c) {
+      const int a = P->col_sub[c];
+      if (a < 0) continue;
+      o_lo = std::min(o_lo, P->subs[a].o_lo);
+      o_hi = std::max(o_hi, P->subs[a].o_hi);
+    }
+    if (o_hi <= o_lo) o_lo = 0, o_hi = std::min(pr.d_out, BK);
+    w.dh_kb0 = o_lo / BK;
+    w.dh_nkb = (o_hi + BK - 1) / BK - w.dh_kb0;
+  };
+  // shrink / dH work, single-CTA engine: one item per (tile, <= MAX_ITEM_CHUNKS chunks)
   P->win.clear();
+  long long chunk_sum = 0;
   for (int t = 0; t < P->n_mtiles; ++t) {
     const MTile& m = P->mtiles[t];
-    for (int q = 0; q < m.nch; q += MAX_ITEM_CHUNKS)
-    {
+    chunk_sum += m.nch;
+    for (int q = 0; q < m.nch; q += MAX_ITEM_CHUNKS) {
       WinItem w{};
       w.tile = t;
       w.q0 = m.q_lo + q;
       w.nq = std::min(MAX_ITEM_CHUNKS, m.nch - q);
-      // dH reads only the d_out slices that the adapters owning these chunks' columns cover
-      int o_lo = pr.d_out, o_hi = 0;
-      for (int c = w.q0 * CHUNK_COLS; c < std::min(P->C_total, (w.q0 + w.nq) * CHUNK_COLS); ++c) {
-        const int a = P->col_sub[c];
-        if (a < 0) continue;
-        o_lo = std::min(o_lo, P->subs[a].o_lo);
-        o_hi = std::max(o_hi, P->subs[a].o_hi);
-      }
-      if (o_hi <= o_lo) o_lo = 0, o_hi = std::min(pr.d_out, BK);
-      w.dh_kb0 = o_lo / BK;
-      w.dh_nkb = (o_hi + BK - 1) / BK - w.dh_kb0;
+      dh_range(w, w.q0, w.nq);
       P->win.push_back(w);
     }
   }
+  // ... and on CTA pairs: one item per (256-token pair, <= 4 chunks of its shared window), the
+  // chunk count rounded up to even so that each CTA holds whole chunks
+  P->win2.clear();
+  for (int t = 0; t < P->n_mtiles; t += 2) {
+    const MTile& m = P->mtiles[t];
+    for (int q = 0; q < m.nch; q += 4) {
+      WinItem w{};
+      w.tile = t / 2;
+      w.q0 = m.q_lo + q;
+      const int real = std::min(4, m.nch - q);
+      w.nq = real + (real & 1);
+      dh_range(w, w.q0, real);
+      P->win2.push_back(w);
+    }
+  }
+  // Pairs halve the rank operand's bytes per token and the re-reads of X / dY for wide windows;
+  // a one-chunk window gains nothing (it is padded to two), so pairs run when tiles average
+  // more than 1.25 chunks, unless a flag forces either engine.
+  P->win_pairs = 4 * chunk_sum > 5LL * P->n_mtiles;
+  if (pr.flags & MLORA_WINDOW_PAIRS) P->win_pairs = true;
+  if (pr.flags & MLORA_WINDOW_SINGLE) P->win_pairs = false;
+  if (P->debug_drop) P->win_pairs = false;   // the copy-withholding hook lives in the single-CTA shrink
 
   // dA / dB work: (256-row block, job, <= MAX_ITEM_CHUNKS chunks), longest first.  A dB block
   // needs only the columns of the job's adapters whose output range meets it.
@@ -481,9 +512,9 @@ mlora_status upload(mlora_plan_t* P) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   const size_t b_segs = table_bytes(P->segs), b_mt = table_bytes(P->mtiles), b_it = table_bytes(P->img_tile),
                b_cs = table_bytes(P->col_sub), b_sc = table_bytes(P->col_scale), b_sub = table_bytes(P->subs),
-               b_win = table_bytes(P->win), b_da = table_bytes(P->da), b_db = table_bytes(P->db),
-               b_adam = table_bytes(P->adam), b_err = 256;
-  const size_t total = b_segs + b_mt + b_it + b_cs + b_sc + b_sub + b_win + b_da + b_db + b_adam + b_err;
+               b_win = table_bytes(P->win), b_win2 = table_bytes(P->win2), b_da = table_bytes(P->da),
+               b_db = table_bytes(P->db), b_adam = table_bytes(P->adam), b_err = 256;
+  const size_t total = b_segs + b_mt + b_it + b_cs + b_sc + b_sub + b_win + b_win2 + b_da + b_db + b_adam + b_err;
   e = cudaMalloc(&P->dev_block, total);
   if (e != cudaSuccess) {
     P->dev_block = nullptr;
@@ -505,7 +536,8 @@ mlora_status upload(mlora_plan_t* P) {
       (e = place(P->d_col_sub, P->col_sub, b_cs)) != cudaSuccess ||
       (e = place(P->d_col_scale, P->col_scale, b_sc)) != cudaSuccess ||
       (e = place(P->d_subs, P->subs, b_sub)) != cudaSuccess ||
-      (e = place(P->d_win, P->win, b_win)) != cudaSuccess || (e = place(P->d_da, P->da, b_da)) != cudaSuccess ||
+      (e = place(P->d_win, P->win, b_win)) != cudaSuccess || (e = place(P->d_win2, P->win2, b_win2)) != cudaSuccess ||
+      (e = place(P->d_da, P->da, b_da)) != cudaSuccess ||
       (e = place(P->d_db, P->db, b_db)) != cudaSuccess || (e = place(P->d_adam, P->adam, b_adam)) != cudaSuccess)
     return cuda_fail(e, "uploading the plan tables");
   P->d_err = reinterpret_cast<int*>(b + o);
@@ -711,11 +743,19 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
 
   GemmArgs g = base_args(P);
   g.kmain = (pr.d_in + BK - 1) / BK;
-  g.n_items = static_cast<int>(P->win.size());
   g.img_out = himg;
   g.hout = H;
-  g.debug_drop = P->debug_drop ? 1 : 0;
-  e = timed(P, K_SHRINK, s, [&] { return launch_seg_gemm<MODE_SHRINK>(mX, mAt, mAt, mX, g, grid_of(P, g.n_items), s); });
+  if (P->win_pairs) {
+    g.win = P->d_win2;
+    g.n_items = static_cast<int>(P->win2.size());
+    e = timed(P, K_SHRINK, s, [&] {
+      return launch_win_2sm<MODE_SHRINK>(mX, mAt, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
+    });
+  } else {
+    g.n_items = static_cast<int>(P->win.size());
+    g.debug_drop = P->debug_drop ? 1 : 0;
+    e = timed(P, K_SHRINK, s, [&] { return launch_seg_gemm<MODE_SHRINK>(mX, mAt, mAt, mX, g, grid_of(P, g.n_items), s); });
+  }
   if (e != cudaSuccess) return cuda_fail(e, "shrink launch");
 
   g = base_args(P);
@@ -832,10 +872,18 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   // dH = s dY B^T  (+ staged dHtilde images)
   GemmArgs g = base_args(P);
   g.kmain = (pr.d_out + BK - 1) / BK;
-  g.n_items = static_cast<int>(P->win.size());
   g.img_out = dhimg;
   g.hout = dH;
-  e = timed(P, K_DH, s, [&] { return launch_seg_gemm<MODE_DH>(mdY, mBt64, mBt64, mdY, g, grid_of(P, g.n_items), s); });
+  if (P->win_pairs) {
+    g.win = P->d_win2;
+    g.n_items = static_cast<int>(P->win2.size());
+    e = timed(P, K_DH, s, [&] {
+      return launch_win_2sm<MODE_DH>(mdY, mBt64, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
+    });
+  } else {
+    g.n_items = static_cast<int>(P->win.size());
+    e = timed(P, K_DH, s, [&] { return launch_seg_gemm<MODE_DH>(mdY, mBt64, mBt64, mdY, g, grid_of(P, g.n_items), s); });
+  }
   if (e != cudaSuccess) return cuda_fail(e, "dH launch");
 
   // dB = Htilde^T dY
@@ -965,6 +1013,10 @@ mlora_status mlora_plan_describe(const mlora_plan_t* P, int32_t what, int64_t* o
     case MLORA_Q_WINDOW:
       for (const WinItem& w : P->win) v.insert(v.end(), {w.tile, w.q0, w.nq, w.dh_kb0, w.dh_nkb});
       break;
+    case MLORA_Q_WINDOW_PAIRS:
+      v.push_back(P->win_pairs ? 1 : 0);
+      for (const WinItem& w : P->win2) v.insert(v.end(), {w.tile, w.q0, w.nq, w.dh_kb0, w.dh_nkb});
+      break;
     case MLORA_Q_ADAPTERS:
       for (const DevSub& sb : P->subs) v.insert(v.end(), {sb.job, sb.c0, sb.r, sb.o_lo, sb.o_hi});
       break;
@@ -1026,7 +1078,8 @@ mlora_status mlora_memory_estimate(const mlora_plan_t* P, mlora_memory* out) {
   m.workspace = static_cast<int64_t>(P->ws_bytes);
   m.plan_tables = static_cast<int64_t>(table_bytes(P->segs) + table_bytes(P->mtiles) + table_bytes(P->img_tile) +
                                        table_bytes(P->col_sub) + table_bytes(P->col_scale) +
-                                       table_bytes(P->subs) + table_bytes(P->win) + table_bytes(P->da) +
+                                       table_bytes(P->subs) + table_bytes(P->win) + table_bytes(P->win2) +
+                                       table_bytes(P->da) +
                                        table_bytes(P->db) + table_bytes(P->adam) + 256);
   m.total = m.base_weight + m.activations + m.lora_params + m.lora_grad_state + m.lora_act + m.workspace +
             m.plan_tables;

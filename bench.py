@@ -296,6 +296,8 @@ def options_of(wl, args):
     opts = []
     if not args.no_reuse:
         opts.append("MLORA_REUSE_STAGING (backward reuses the forward's bf16 shadows and staged H)")
+    if args.window != "auto":
+        opts.append({"pairs": "MLORA_WINDOW_PAIRS", "single": "MLORA_WINDOW_SINGLE"}[args.window])
     if wl.dtype == "bf16_w4":
         opts.append("MLORA_W4_FUSED (codes expanded inside the base GEMMs)" if args.w4_fused else
                     "4-bit base expanded to bf16 once per call, then the bf16 GEMMs")
@@ -330,6 +332,7 @@ def run_ours(args, wl, rank, world, local_rank):
     T = W.materialise(wl)
     scales = [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
     flags = (0 if args.no_reuse else M.MLORA_REUSE_STAGING) | (M.MLORA_W4_FUSED if args.w4_fused else 0)
+    flags |= {"auto": 0, "pairs": M.MLORA_WINDOW_PAIRS, "single": M.MLORA_WINDOW_SINGLE}[args.window]
     if wl.groups is None:
         layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At, Bt=T.Bt,
                            flags=flags)
@@ -552,6 +555,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-reuse", action="store_true", help="rebuild the backward's staging (no MLORA_REUSE_STAGING)")
     ap.add_argument("--w4-fused", action="store_true", help="4-bit base: expand inside the GEMMs (MLORA_W4_FUSED)")
+    ap.add_argument("--window", choices=["auto", "pairs", "single"], default="auto",
+                    help="engine of the shrink / dH products (default: the planner's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens-per-job", type=int, default=64)

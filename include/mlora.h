@@ -86,6 +86,12 @@ typedef enum mlora_dtype {
                                           the one before); results are identical either way */
 #define MLORA_GEMM_SINGLE_CTA 4u       /* run the two base GEMMs on single-CTA 128x256 tiles instead of
                                           CTA pairs (256x256 tiles); same results up to rounding order */
+#define MLORA_WINDOW_PAIRS 128u        /* run the shrink and dH products on CTA pairs (256-token tiles sharing
+                                          the rank operand, up to four 64-column chunks per item) whatever
+                                          the planner would pick; same results up to rounding order */
+#define MLORA_WINDOW_SINGLE 256u       /* run them on the single-CTA engine (128-token tiles, two chunks per
+                                          item).  Without either flag the planner takes pairs when the
+                                          token tiles' rank windows average more than 1.25 chunks */
 #define MLORA_W4_FUSED 64u             /* 4-bit base only: expand the codes to bf16 inside the CTA-pair base
                                           GEMMs (converter warps, once per 256-token tile pair) instead of
                                           once per call into the workspace; the workspace is smaller by
@@ -221,9 +227,12 @@ int64_t mlora_h_elems(const mlora_plan_t* plan);
  *   MLORA_Q_COLUMNS : per job: first column of its rank window, padded width
  *   MLORA_Q_WGRAD_A : per dA work item: row block, job, first and end half-tile, first chunk, chunks
  *   MLORA_Q_WGRAD_B : per dB work item: same fields
- *   MLORA_Q_WINDOW  : per shrink / dH work item: tile, first chunk, chunks
+ *   MLORA_Q_WINDOW  : per single-CTA shrink / dH work item: tile, first chunk, chunks, first dH K
+ *                     slice, dH K slices
  *   MLORA_Q_ADAPTERS: per segment-table entry: job, first packed column, rank, first and end
- *                     output column of its B */
+ *                     output column of its B
+ *   MLORA_Q_WINDOW_PAIRS: 1 if the shrink / dH run on CTA pairs, else 0; then per pair item:
+ *                     pair, first chunk, chunks (even), first dH K slice, dH K slices */
 #define MLORA_Q_SUMMARY 0
 #define MLORA_Q_MTILES 1
 #define MLORA_Q_COLUMNS 2
@@ -231,6 +240,7 @@ int64_t mlora_h_elems(const mlora_plan_t* plan);
 #define MLORA_Q_WGRAD_B 4
 #define MLORA_Q_WINDOW 5
 #define MLORA_Q_ADAPTERS 6
+#define MLORA_Q_WINDOW_PAIRS 7
 mlora_status mlora_plan_describe(const mlora_plan_t* plan, int32_t what, int64_t* out, int64_t cap,
                                  int64_t* count);
 

@@ -42,11 +42,12 @@ def _wl(name, dtype="bf16"):
                             c["widths"], c["ranks_jg"], c["n_tokens"], dtype=dtype, b_std=0.05)
 
 
+@pytest.mark.parametrize("window", ["win_pairs", "win_single"])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_grouped_vs_oracle(name):
+def test_grouped_vs_oracle(name, window):
     wl = _wl(name)
     T = W.materialise(wl)
-    run = G.GpuRun(wl, T)
+    run = G.GpuRun(wl, T, flags=M.MLORA_WINDOW_PAIRS if window == "win_pairs" else M.MLORA_WINDOW_SINGLE)
     try:
         assert run.status_after_backward == M.MLORA_OK
         G.compare(run.res, G.oracle_full(wl, T), G.TOL["bf16"])

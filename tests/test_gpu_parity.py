@@ -49,15 +49,18 @@ SMALL_BF16 = {
 
 
 ENGINES = {"cta_pairs": 0, "single_cta": M.MLORA_GEMM_SINGLE_CTA}
+# the shrink / dH products: on CTA pairs (256-token tiles, up to 4 chunks) or single CTAs
+WINDOWS = {"win_pairs": M.MLORA_WINDOW_PAIRS, "win_single": M.MLORA_WINDOW_SINGLE}
 
 
+@pytest.mark.parametrize("window", sorted(WINDOWS))
 @pytest.mark.parametrize("engine", sorted(ENGINES))
 @pytest.mark.parametrize("name", sorted(SMALL_BF16))
-def test_bf16_small(name, engine):
+def test_bf16_small(name, engine, window):
     cfg = SMALL_BF16[name]
     wl = W.custom(f"small_{name}", 900 + sorted(SMALL_BF16).index(name), cfg["d_in"], cfg["d_out"], cfg["ranks"],
                   cfg["n_tokens"], dtype="bf16", w_std=0.05, b_std=0.05)
-    _run(wl, flags=ENGINES[engine])
+    _run(wl, flags=ENGINES[engine] | WINDOWS[window])
 
 
 def test_bf16_zero_base_weight_isolates_rank_term():

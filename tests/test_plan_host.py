@@ -320,3 +320,45 @@ def test_grouped_dh_items_read_only_their_projections_slices():
     # job 0 (rank 128 per projection) spans chunks 0-5: q in 0-1, k in 2-3, v in 4-5
     by_q0 = {q0: (kb0, nkb) for t, q0, nq, kb0, nkb in win if t == 0}
     assert by_q0[0] == (0, 64) and by_q0[2] == (64, 16) and by_q0[4] == (80, 16)
+
+
+# ---------------------------------------------------------------- shrink / dH on CTA pairs
+
+@pytest.mark.parametrize("name", ["ragged", "tiny_segments", "one_token", "qproj", "many_small"])
+def test_pair_window_items(name):
+    """Pair items cover each 256-token pair's shared chunk range exactly once, in groups of at most
+    four chunks padded to an even count (the padding chunk sits right after the range)."""
+    d_in, d_out, ranks, ns = _case(name)
+    plan, _ = host_plan(d_in, d_out, ranks, ns)
+    try:
+        mt = _describe(plan, M.MLORA_Q_MTILES).reshape(-1, 5)
+        pw = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)
+    finally:
+        M.mlora_plan_destroy(plan)
+    items = pw[1:].reshape(-1, 5)
+    n_pairs = (len(mt) + 1) // 2
+    for p in range(n_pairs):
+        q_lo, nch = mt[2 * p, 2], mt[2 * p, 3]
+        mine = items[items[:, 0] == p]
+        got = []
+        for _, q0, nq, kb0, nkb in mine:
+            assert nq in (2, 4)
+            assert (kb0, nkb) == (0, -(-d_out // 64))
+            got.extend(range(q0, q0 + nq))
+        real = list(range(q_lo, q_lo + nch))
+        assert got[:nch] == real and len(got) - nch in (0, 1)
+
+
+def test_window_engine_choice():
+    """Pairs when the token tiles' windows average more than 1.25 chunks, unless a flag says."""
+    def pairs(ranks, ns, flags=0):
+        plan, _ = host_plan(512, 256, ranks, ns, flags=flags)
+        try:
+            return _describe(plan, M.MLORA_Q_WINDOW_PAIRS)[0] == 1
+        finally:
+            M.mlora_plan_destroy(plan)
+    assert not pairs([8, 8], [1024, 1024])                   # both windows in chunk 0: one chunk per tile
+    assert pairs([8, 64], [1024, 1024])                      # the second window [16, 80) spans two chunks
+    assert pairs([128, 256], [1024, 1024])                   # 2 and 4 chunks per tile
+    assert pairs([8, 8], [1024, 1024], M.MLORA_WINDOW_PAIRS)
+    assert not pairs([128, 256], [1024, 1024], M.MLORA_WINDOW_SINGLE)
