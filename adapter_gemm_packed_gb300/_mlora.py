@@ -31,7 +31,7 @@ EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward"
            "mlora_sync_status", "mlora_h_elems", "mlora_plan_describe", "mlora_status_string",
            "mlora_last_error", "mlora_version", "mlora_profile_enable", "mlora_profile_read",
            "mlora_kernel_name", "mlora_launch_count", "mlora_forward_static_ws", "mlora_memory_estimate",
-           "mlora_shard_jobs", "mlora_forward_w4", "mlora_backward_w4", "mlora_plan_grouped"]
+           "mlora_shard_jobs", "mlora_forward_w4", "mlora_backward_w4", "mlora_plan_grouped", "mlora_adamw_ws"]
 
 
 class mlora_segment(C.Structure):
@@ -85,6 +85,8 @@ def lib() -> C.CDLL:
         L.mlora_backward.restype = i32
         L.mlora_adamw.argtypes = [vp, f32, f32, f32, f32, f32, i32, vp]
         L.mlora_adamw.restype = i32
+        L.mlora_adamw_ws.argtypes = [vp, f32, f32, f32, f32, f32, i32, vp, vp]
+        L.mlora_adamw_ws.restype = i32
         L.mlora_sync_status.argtypes = [vp, vp]
         L.mlora_sync_status.restype = i32
         L.mlora_h_elems.argtypes = [vp]
@@ -172,6 +174,11 @@ def mlora_backward(plan, X, Wt, dY, H, dX, dH, workspace, stream) -> None:
 
 def mlora_adamw(plan, lr, beta1, beta2, eps, weight_decay, step, stream) -> None:
     _check(lib().mlora_adamw(plan, lr, beta1, beta2, eps, weight_decay, step, stream), "mlora_adamw")
+
+
+def mlora_adamw_ws(plan, lr, beta1, beta2, eps, weight_decay, step, workspace, stream) -> None:
+    _check(lib().mlora_adamw_ws(plan, lr, beta1, beta2, eps, weight_decay, step, workspace, stream),
+           "mlora_adamw_ws")
 
 
 def mlora_sync_status(plan, stream) -> int:

@@ -40,7 +40,8 @@ cudaError_t launch_pack_fwd(const DevSub*, const int*, int, int, int, __nv_bfloa
                             cudaStream_t, bool);
 cudaError_t launch_h_images(const DevSeg*, const float*, const MTile*, const int*, int, long long, const float*,
                             uint8_t*, cudaStream_t, bool);
-cudaError_t launch_adamw(const AdamItem*, int, float, float, float, float, float, int, int, cudaStream_t, bool);
+cudaError_t launch_adamw(const AdamItem*, int, float, float, float, float, float, int, int, cudaStream_t, bool,
+                         __nv_bfloat16*, __nv_bfloat16*, int);
 cudaError_t launch_w4_expand(const void*, const float*, __nv_bfloat16*, int, int, int, cudaStream_t, bool);
 cudaError_t launch_f32_forward(const DevSeg*, int, long long, int, int, long long, const float*, const float*, float*,
                                float*, cudaStream_t);
@@ -180,6 +181,8 @@ struct mlora_plan_s {
   bool staged_valid = false;
   const void* staged_ws = nullptr;
   const float* staged_H = nullptr;
+  bool shadows_valid = false;          // the bf16 shadows in shadows_ws match the fp32 masters
+  const void* shadows_ws = nullptr;
   const void* staged_wq = nullptr;     // 4-bit base whose bf16 expansion the workspace holds
   const float* staged_wscale = nullptr;
   // optional per-kernel timing with CUDA events recorded on the launching stream
@@ -462,10 +465,15 @@ void build_tables(mlora_plan_t* P) {
   if (P->can_adamw) {
     for (int i = 0; i < P->n_segs; ++i) {
       const mlora_segment& u = P->user[i];
-      const long long width = P->subs[i].o_hi - P->subs[i].o_lo;
-      struct T { float *p, *g, *m, *v; long long n; } ts[2] = {
-          {u.At, u.dAt, u.mA, u.vA, static_cast<long long>(u.rank) * pr.d_in},
-          {u.Bt, u.dBt, u.mB, u.vB, static_cast<long long>(u.rank) * width}};
+      const DevSub& sb = P->subs[i];
+      const long long width = sb.o_hi - sb.o_lo;
+      // shadow copies: At rows are rows c0.. of At_all (contiguous); B^T row o, rank t is
+      // Bt_all[o_lo + o][c0 + t]
+      struct T { float *p, *g, *m, *v; long long n; int kind; long long base; } ts[2] = {
+          {u.At, u.dAt, u.mA, u.vA, static_cast<long long>(u.rank) * pr.d_in, 1,
+           static_cast<long long>(sb.c0) * pr.d_in},
+          {u.Bt, u.dBt, u.mB, u.vB, static_cast<long long>(u.rank) * width, 2,
+           static_cast<long long>(sb.o_lo) * P->C_total + sb.c0}};
       for (const T& tt : ts)
         for (long long s0 = 0; s0 < tt.n; s0 += ADAM_CHUNK) {
           AdamItem a{};
@@ -474,6 +482,10 @@ void build_tables(mlora_plan_t* P) {
           a.m = tt.m + s0;
           a.v = tt.v + s0;
           a.count = static_cast<int>(std::min<long long>(ADAM_CHUNK, tt.n - s0));
+          a.sh_kind = tt.kind;
+          a.sh_base = tt.kind == 1 ? tt.base + s0 : tt.base;
+          a.sh_r = u.rank;
+          a.sh_e0 = static_cast<int>(s0);
           P->adam.push_back(a);
         }
     }
@@ -720,8 +732,12 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
     if (e != cudaSuccess) return cuda_fail(e, "4-bit expansion launch");
     Wt = wexp;
   }
-  e = timed(P, K_PACK_FWD, s, [&] { return launch_pack_fwd(P->d_subs, P->d_col_sub, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
-  if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+  // With MLORA_REUSE_STAGING the shadows are not rebuilt when this workspace already holds them
+  // for the current masters (written by the last forward, or refreshed by mlora_adamw_ws).
+  if (!(P->reuse_staging && P->shadows_valid && P->shadows_ws == workspace)) {
+    e = timed(P, K_PACK_FWD, s, [&] { return launch_pack_fwd(P->d_subs, P->d_col_sub, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
+    if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+  }
 
   const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
   CUtensorMap mX, mAt, mW, mBt, mI, mQ, mS;
@@ -783,6 +799,8 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
     Pm->staged_valid = true;
     Pm->staged_ws = workspace;
     Pm->staged_H = H;
+    Pm->shadows_valid = true;
+    Pm->shadows_ws = workspace;
     Pm->staged_wq = w4 && !fused4 ? Wq : nullptr;
     Pm->staged_wscale = w4 && !fused4 ? Ws : nullptr;
   }
@@ -843,6 +861,9 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   if (!reuse) {
     e = timed(P, K_PACK_BWD, s, [&] { return launch_pack_fwd(P->d_subs, P->d_col_sub, P->C_total, pr.d_in, pr.d_out, at_all, bt_all, P->num_sms, s, P->pdl); });
     if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+    mlora_plan_t* Pm = const_cast<mlora_plan_t*>(P);
+    Pm->shadows_valid = true;
+    Pm->shadows_ws = workspace;
     e = timed(P, K_H_IMAGES, s, [&] { return launch_h_images(P->d_segs, P->d_col_scale, P->d_mtiles, P->d_img_tile, static_cast<int>(P->n_images), pr.n_tokens, H, himg, s, P->pdl); });
     if (e != cudaSuccess) return cuda_fail(e, "image launch");
   }
@@ -952,23 +973,61 @@ mlora_status mlora_backward_w4(const mlora_plan_t* P, const void* X, const void*
   return backward_impl(P, X, nullptr, Wq, Wscale, dY, H, dX, dH, workspace, stream);
 }
 
-mlora_status mlora_adamw(const mlora_plan_t* P, float lr, float beta1, float beta2, float eps, float weight_decay,
-                         int32_t step, void* stream) {
+}  // extern "C"
+
+namespace {
+
+mlora_status adamw_impl(const mlora_plan_t* P, float lr, float beta1, float beta2, float eps, float weight_decay,
+                        int32_t step, void* workspace, void* stream) {
   g_last_error.clear();
   mlora_status st = check_exec(P);
   if (st != MLORA_OK) return st;
   if (!P->can_adamw) return fail(MLORA_ERR_INVALID, "the plan's segments lack gradient or moment buffers");
   if (step < 1) return fail(MLORA_ERR_INVALID, "step must be >= 1");
-  const_cast<mlora_plan_t*>(P)->staged_valid = false;   // the masters change: shadows are stale
   if (!(beta1 >= 0.f && beta1 < 1.f && beta2 >= 0.f && beta2 < 1.f) || !std::isfinite(lr) || !std::isfinite(eps) ||
       !std::isfinite(weight_decay))
     return fail(MLORA_ERR_INVALID, "bad AdamW hyper-parameters");
+  const bool refresh = workspace != nullptr && P->prob.dtype != MLORA_F32;
+  if (refresh && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(MLORA_ERR_INVALID, "workspace must be a 256-byte aligned device buffer");
+  mlora_plan_t* Pm = const_cast<mlora_plan_t*>(P);
+  Pm->staged_valid = false;   // the masters change: the backward's staging is stale
+  Pm->shadows_valid = false;
+  __nv_bfloat16* at_all = nullptr;
+  __nv_bfloat16* bt_all = nullptr;
+  if (refresh) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    at_all = reinterpret_cast<__nv_bfloat16*>(ws + P->off_shadow);
+    bt_all = reinterpret_cast<__nv_bfloat16*>(
+        ws + P->off_shadow + round_up(static_cast<size_t>(P->C_total) * P->prob.d_in * 2, 1024));
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = timed(P, K_ADAMW, s, [&] {
     return launch_adamw(P->d_adam, static_cast<int>(P->adam.size()), lr, beta1, beta2, eps, weight_decay, step,
-                        P->num_sms, s, P->pdl);
+                        P->num_sms, s, P->pdl, at_all, bt_all, P->C_total);
   });
-  return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "AdamW launch");
+  if (e != cudaSuccess) return cuda_fail(e, "AdamW launch");
+  if (refresh) {
+    // Only the adapters' columns were written: the padding of the packed space must already be
+    // zero, which holds when a forward or backward packed this workspace before.
+    Pm->shadows_valid = P->shadows_ws == workspace;
+  }
+  return MLORA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mlora_status mlora_adamw(const mlora_plan_t* P, float lr, float beta1, float beta2, float eps, float weight_decay,
+                         int32_t step, void* stream) {
+  return adamw_impl(P, lr, beta1, beta2, eps, weight_decay, step, nullptr, stream);
+}
+
+mlora_status mlora_adamw_ws(const mlora_plan_t* P, float lr, float beta1, float beta2, float eps,
+                            float weight_decay, int32_t step, void* workspace, void* stream) {
+  if (!workspace) return fail(MLORA_ERR_INVALID, "null workspace");
+  return adamw_impl(P, lr, beta1, beta2, eps, weight_decay, step, workspace, stream);
 }
 
 mlora_status mlora_sync_status(const mlora_plan_t* P, void* stream) {

@@ -112,11 +112,15 @@ __global__ void k_h_images(const DevSeg* __restrict__ segs, const float* __restr
 
 // AdamW over a list of <= ADAM_CHUNK-element pieces of every adapter's A and B.
 __global__ void k_adamw(const AdamItem* __restrict__ items, int n_items, float lr, float beta1, float beta2,
-                        float eps, float decay, float bc1, float bc2) {
+                        float eps, float decay, float bc1, float bc2, __nv_bfloat16* __restrict__ at_all,
+                        __nv_bfloat16* __restrict__ bt_all, int C_total) {
   griddep_wait();
   griddep_launch_dependents();
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const AdamItem w = items[it];
+    // with shadows to refresh, each new value also goes to its bf16 copy in the packed rank space
+    // (rounded as the pack kernels round, so a later forward sees what a fresh pack would give)
+    const int kind = at_all ? w.sh_kind : 0;
     const int n4 = w.count >> 2;
     float4* p4 = reinterpret_cast<float4*>(w.p);
     const float4* g4 = reinterpret_cast<const float4*>(w.g);
@@ -145,15 +149,33 @@ __global__ void k_adamw(const AdamItem* __restrict__ items, int n_items, float l
       p4[i] = p;
       m4[i] = m;
       v4[i] = v;
+      if (kind == 1) {
+        *reinterpret_cast<uint2*>(at_all + w.sh_base + 4 * i) = make_uint2(pack_bf16x2(p.x, p.y), pack_bf16x2(p.z, p.w));
+      } else if (kind == 2) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = w.sh_e0 + 4 * i + u;
+          const int o = e / w.sh_r;
+          bt_all[w.sh_base + static_cast<long long>(o) * C_total + (e - o * w.sh_r)] = __float2bfloat16_rn(pp[u]);
+        }
+      }
     }
     for (int i = (n4 << 2) + threadIdx.x; i < w.count; i += blockDim.x) {
       const float gu = w.g[i];
       const float pd = w.p[i] * decay;
       const float mu = beta1 * w.m[i] + (1.f - beta1) * gu;
       const float vu = beta2 * w.v[i] + (1.f - beta2) * gu * gu;
-      w.p[i] = pd - lr * (mu / bc1) / (sqrtf(vu / bc2) + eps);
+      const float pn = pd - lr * (mu / bc1) / (sqrtf(vu / bc2) + eps);
+      w.p[i] = pn;
       w.m[i] = mu;
       w.v[i] = vu;
+      if (kind == 1) {
+        at_all[w.sh_base + i] = __float2bfloat16_rn(pn);
+      } else if (kind == 2) {
+        const int e = w.sh_e0 + i;
+        const int o = e / w.sh_r;
+        bt_all[w.sh_base + static_cast<long long>(o) * C_total + (e - o * w.sh_r)] = __float2bfloat16_rn(pn);
+      }
     }
   }
 }
@@ -187,7 +209,8 @@ cudaError_t launch_h_images(const DevSeg* segs, const float* col_scale, const MT
 }
 
 cudaError_t launch_adamw(const AdamItem* items, int n_items, float lr, float beta1, float beta2, float eps,
-                         float weight_decay, int step, int num_sms, cudaStream_t st, bool pdl) {
+                         float weight_decay, int step, int num_sms, cudaStream_t st, bool pdl, __nv_bfloat16* at_all,
+                         __nv_bfloat16* bt_all, int C_total) {
   if (n_items <= 0) return cudaSuccess;
   const double bc1 = 1.0 - pow(static_cast<double>(beta1), step);
   const double bc2 = 1.0 - pow(static_cast<double>(beta2), step);
@@ -195,7 +218,7 @@ cudaError_t launch_adamw(const AdamItem* items, int n_items, float lr, float bet
   int grid = n_items;
   if (grid > num_sms * 16) grid = num_sms * 16;
   return launch_k(k_adamw, dim3(grid), dim3(256), 0, st, pdl, items, n_items, lr, beta1, beta2, eps, decay,
-                  static_cast<float>(bc1), static_cast<float>(bc2));
+                  static_cast<float>(bc1), static_cast<float>(bc2), at_all, bt_all, C_total);
 }
 
 }  // namespace mlora

@@ -100,8 +100,14 @@ struct AdamItem {
   float* m;
   float* v;
   int count;
-  int pad0;
-  long long pad1;
+  // the bf16 shadow this piece's new values are copied to (when the step refreshes the shadows):
+  // 1 = At_all, contiguous from element sh_base; 2 = Bt_all, element e of the tensor at
+  // sh_base + (e / sh_r) * C + e % sh_r, the piece starting at tensor element sh_e0
+  int sh_kind;
+  long long sh_base;
+  int sh_r;
+  int sh_e0;
+  long long pad0;
 };
 
 struct GemmArgs {

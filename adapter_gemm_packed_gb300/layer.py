@@ -116,8 +116,14 @@ class PackedLoRA:
                              self.dH.data_ptr(), self.workspace.data_ptr(), _stream(stream))
         return dX
 
-    def adamw(self, lr, beta1, beta2, eps, weight_decay, step, stream=None):
-        M.mlora_adamw(self.plan, lr, beta1, beta2, eps, weight_decay, step, _stream(stream))
+    def adamw(self, lr, beta1, beta2, eps, weight_decay, step, stream=None, refresh_shadows=True):
+        """One AdamW step on every adapter; by default it also refreshes the bf16 shadows in this
+        layer's workspace (mlora_adamw_ws), which the next forward reuses under MLORA_REUSE_STAGING."""
+        if refresh_shadows:
+            M.mlora_adamw_ws(self.plan, lr, beta1, beta2, eps, weight_decay, step, self.workspace.data_ptr(),
+                             _stream(stream))
+        else:
+            M.mlora_adamw(self.plan, lr, beta1, beta2, eps, weight_decay, step, _stream(stream))
 
     def sync_status(self, stream=None) -> int:
         return M.mlora_sync_status(self.plan, _stream(stream))

@@ -76,11 +76,14 @@ typedef enum mlora_dtype {
                                           MLORA_ERR_TIMEOUT; that call's outputs are undefined */
 #define MLORA_REUSE_STAGING 32u       /* mlora_backward skips rebuilding the bf16 adapter shadows and the
                                           staged s*H images when its workspace and H are the ones the last
-                                          mlora_forward of this plan used and no mlora_adamw ran since (and,
+                                          mlora_forward of this plan used and no AdamW step ran since (and,
                                           for a 4-bit base, the bf16 expansion of W when Wq and Wscale are the
-                                          forward's pointers); the caller guarantees that neither At/Bt, H,
-                                          Wq/Wscale nor that workspace changed in between (results are then
-                                          identical to the full backward) */
+                                          forward's pointers); mlora_forward skips rebuilding the shadows when
+                                          its workspace holds them for the current masters (left by the last
+                                          forward or backward with no AdamW step since, or refreshed by
+                                          mlora_adamw_ws).  The caller guarantees that neither At/Bt, H,
+                                          Wq/Wscale nor that workspace changed in between except through
+                                          these calls (results are then identical to the full passes) */
 #define MLORA_NO_OVERLAP 8u            /* launch every kernel strictly after the previous one (no programmatic
                                           dependent launch overlapping a kernel's prologue with the tail of
                                           the one before); results are identical either way */
@@ -209,6 +212,16 @@ mlora_status mlora_backward(const mlora_plan_t* plan, const void* X, const void*
  * At/Bt/mA/vA/mB/vB in place.  Moments start at zero at t = 1 (caller-zeroed). */
 mlora_status mlora_adamw(const mlora_plan_t* plan, float lr, float beta1, float beta2, float eps,
                          float weight_decay, int32_t step, void* stream);
+
+/* mlora_adamw that also writes the updated A_i, B_i into the bf16 shadows held in `workspace`
+ * (the copies the kernels read, rounded as a fresh pack would round them), so that the next
+ * mlora_forward with that workspace under MLORA_REUSE_STAGING starts without rebuilding them.
+ * The shadows count as current only if a forward or backward built them in this workspace
+ * before (their zero padding is not rewritten); otherwise the next forward rebuilds them.
+ * fp32 plans have no shadows: this is mlora_adamw.  Errors as mlora_adamw, plus MLORA_ERR_INVALID
+ * for a null or misaligned workspace. */
+mlora_status mlora_adamw_ws(const mlora_plan_t* plan, float lr, float beta1, float beta2, float eps,
+                            float weight_decay, int32_t step, void* workspace, void* stream);
 
 /* Synchronise the stream, then read and clear the plan's device status word:
  * MLORA_OK, or MLORA_ERR_TIMEOUT if a device-side wait gave up since the last

@@ -189,3 +189,37 @@ def test_device_wait_timeout_is_reported_and_context_survives():
     finally:
         bad.close()
     _run(wl)                                           # the context is still usable
+
+
+@pytest.mark.parametrize("grouped", [False, True], ids=["one_group", "qkv_groups"])
+def test_adamw_shadow_refresh_matches_repacking(grouped):
+    """Three steps with MLORA_REUSE_STAGING and mlora_adamw_ws (the forward reuses the shadows the
+    AdamW step refreshed) give bit-identical results to three steps that repack every time."""
+    if grouped:
+        wl = W.custom_grouped("shadow_refresh_g", 931, 512, [256, 64, 64], [[8, 8, 8], [64, 16, 1], [3, 128, 32]],
+                              [200, 56, 300], b_std=0.05)
+    else:
+        wl = W.custom("shadow_refresh", 930, 512, 640, [1, 7, 64, 256], [200, 56, 300, 17], b_std=0.05)
+    T = W.materialise(wl)
+    X, dY = G.to_dev(T.X, "bf16"), G.to_dev(T.dY, "bf16")
+    Wt = G.to_dev(T.Wt, "bf16")
+    outs = []
+    for flags, refresh in ((M.MLORA_REUSE_STAGING, True), (0, False)):
+        layer = G.make_layer(wl, T, flags)
+        try:
+            res = []
+            for step in range(1, 4):
+                Y = layer.forward(X, Wt)
+                dX = layer.backward(X, Wt, dY)
+                layer.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, step, refresh_shadows=refresh)
+                res.append((Y.clone(), dX.clone()))
+            torch.cuda.synchronize()
+            assert layer.sync_status() == M.MLORA_OK
+            outs.append((res, [a.clone() for a in layer.At], [b.clone() for b in layer.Bt]))
+        finally:
+            layer.close()
+    (r1, A1, B1), (r2, A2, B2) = outs
+    for (y1, x1), (y2, x2) in zip(r1, r2):
+        assert torch.equal(y1, y2) and torch.equal(x1, x2)
+    assert all(torch.equal(a, b) for a, b in zip(A1, A2))
+    assert all(torch.equal(a, b) for a, b in zip(B1, B2))
