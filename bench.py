@@ -86,7 +86,9 @@ def kernel_bytes(wl, kernel):
     if kernel == "dB":
         return wl.N * wl.d_out * e + lora * 2 + srw * 4
     if kernel == "adamw":
-        return params * 28
+        # p, g, m, v read and p, m, v written (28 B), plus the bf16 shadow copy of p (2 B) that the
+        # step refreshes for the next forward
+        return params * 30
     if kernel == "w4_expand":
         # codes (half a byte), scales (4 bytes per 64 weights) in; bf16 W^T out
         return wl.d_in * wl.d_out * (0.5 + 4 / 64 + 2)
