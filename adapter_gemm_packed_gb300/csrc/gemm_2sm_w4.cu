@@ -1,4 +1,7 @@
-// Base GEMMs on CTA pairs with a 4-bit frozen base weight.
+// Base GEMMs on CTA pairs that expand a 4-bit frozen base weight in shared memory (the
+// MLORA_W4_FUSED variant; by default the library expands the weight once per call with
+// w4_expand.cu and runs the bf16 GEMMs, which is faster at training batch sizes because this
+// kernel repeats the expansion for every 256-token tile pair).
 //
 // "PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §5 and §11.3: a 4-bit
 // quantised base (QLoRA) composes with packing.  The pages do not fix the 4-bit format; this

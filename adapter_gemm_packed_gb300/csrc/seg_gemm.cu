@@ -1,8 +1,10 @@
 // Segmented tensor-core GEMM engine for the packed LoRA layer (sm_103a: tcgen05 + TMEM + TMA).
 //
-// One persistent, warp-specialised kernel template computes every product of the layer
-// ("PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §9.2: tiles run
-// along the token and hidden dimensions, never along the rank):
+// One persistent, warp-specialised kernel template computes the products of the layer on
+// single CTAs ("PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §9.2: tiles
+// run along the token and hidden dimensions, never along the rank).  The base GEMMs run on CTA
+// pairs by default (gemm_2sm.cu; this engine's FWD/BWD with MLORA_GEMM_SINGLE_CTA), and shrink /
+// dH move to CTA pairs for wide rank windows (win_2sm.cu):
 //
 //   MODE_FWD    Y  = X W + s_i H_i B_i        base GEMM; the rank term is appended as extra
 //                                              K slices of the same TMEM accumulator
