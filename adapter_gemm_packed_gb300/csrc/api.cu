@@ -629,6 +629,10 @@ mlora_status check_exec(const mlora_plan_t* P) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != P->device)
     return fail(MLORA_ERR_INVALID, "the current device is not the one the plan was built on");
+  // Make the device's primary context current on this thread: a thread that has only selected
+  // the device (an autograd worker, say) may not have it yet, and the tensor-map encoder needs it.
+  cudaError_t e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   return MLORA_OK;
 }
 

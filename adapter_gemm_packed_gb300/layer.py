@@ -186,3 +186,44 @@ def host_plan_grouped(d_in, widths, ranks_jg, n_tokens, dtype="bf16", flags=0):
     offs = [sum(widths[:g]) for g in range(len(widths))]
     prob = M.mlora_problem(sum(n_tokens), d_in, sum(widths), code, M.MLORA_PLAN_HOST_ONLY | flags)
     return M.mlora_plan_grouped(prob, list(zip(offs, widths)), segs)
+
+
+class _PackedLoRAFn(torch.autograd.Function):
+    """Autograd bridge: forward -> mlora_forward, backward -> mlora_backward (dX to the caller,
+    the adapters' gradients into the layer's dAt / dBt buffers)."""
+
+    @staticmethod
+    def forward(ctx, X, layer, Wt):
+        ctx.layer = layer
+        ctx.Wt = Wt
+        ctx.save_for_backward(X)
+        return layer.forward(X, Wt)
+
+    @staticmethod
+    def backward(ctx, dY):
+        (X,) = ctx.saved_tensors
+        dX = ctx.layer.backward(X, ctx.Wt, dY.contiguous())
+        return dX, None, None
+
+
+class PackedLoRALinear(torch.nn.Module):
+    """A packed LoRA layer as a module: ``y = mod(x)`` runs the fused forward, ``backward`` of the
+    graph runs the fused backward (the gradient of x flows on; the adapters' gradients stay in
+    ``mod.layer.dAt`` / ``dBt``), and ``mod.step(...)`` applies the library's AdamW to every adapter.
+
+    The frozen weight ``Wt`` (bf16 / fp32 tensor, or a (codes, scales) pair for a 4-bit base) is
+    held as given; each forward must be followed by its backward before the next forward (the
+    layer keeps one H)."""
+
+    def __init__(self, layer: PackedLoRA, Wt):
+        super().__init__()
+        self.layer = layer
+        self.Wt = Wt
+        self._t = 0
+
+    def forward(self, X):
+        return _PackedLoRAFn.apply(X, self.layer, self.Wt)
+
+    def step(self, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01):
+        self._t += 1
+        self.layer.adamw(lr, betas[0], betas[1], eps, weight_decay, self._t)

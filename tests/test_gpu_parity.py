@@ -270,3 +270,32 @@ def test_cuda_graph_replay_matches_eager_steps():
     (y1, x1, a1, b1), (y2, x2, a2, b2) = results
     assert torch.equal(y1, y2) and torch.equal(x1, x2)
     assert all(torch.equal(p, q) for p, q in zip(a1, a2)) and all(torch.equal(p, q) for p, q in zip(b1, b2))
+
+
+def test_autograd_module_matches_direct_calls():
+    """PackedLoRALinear through torch.autograd gives the same Y, dX (as X.grad), adapter gradients
+    and AdamW step as calling the layer directly."""
+    from adapter_gemm_packed_gb300.layer import PackedLoRALinear
+    wl = W.custom("autograd", 934, 512, 640, [1, 7, 64, 256], [200, 56, 300, 17], b_std=0.05)
+    T = W.materialise(wl)
+    Wt = G.to_dev(T.Wt, "bf16")
+    dY = G.to_dev(T.dY, "bf16")
+    direct = G.make_layer(wl, T, M.MLORA_REUSE_STAGING)
+    viaag = G.make_layer(wl, T, M.MLORA_REUSE_STAGING)
+    try:
+        X = G.to_dev(T.X, "bf16")
+        Y1 = direct.forward(X, Wt)
+        dX1 = direct.backward(X, Wt, dY)
+        direct.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, 1)
+        mod = PackedLoRALinear(viaag, Wt)
+        Xg = G.to_dev(T.X, "bf16").requires_grad_(True)
+        Y2 = mod(Xg)
+        Y2.backward(dY)
+        mod.step(wl.lr, (wl.beta1, wl.beta2), wl.eps, wl.weight_decay)
+        torch.cuda.synchronize()
+        assert torch.equal(Y1, Y2.detach()) and torch.equal(dX1, Xg.grad)
+        for k in ("dAt", "dBt", "At", "Bt"):
+            assert all(torch.equal(a, b) for a, b in zip(getattr(direct, k), getattr(viaag, k))), k
+    finally:
+        direct.close()
+        viaag.close()
