@@ -569,7 +569,7 @@ const char* const kKernelNames[K_COUNT] = {
 // kernels launched by each id (a pack step is two kernels, the fp32 passes several)
 const int kKernelLaunches[K_COUNT] = {2, 1, 1, 2, 1, 1, 1, 1, 1, 1, 2, 4, 1};   // pack steps are two kernels
 
-long long g_launches = 0;
+std::atomic<long long> g_launches{0};
 
 cudaEvent_t next_event(mlora_plan_t* P) {
   if (P->ev_next == P->ev_pool.size()) {

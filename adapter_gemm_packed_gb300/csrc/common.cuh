@@ -3,6 +3,7 @@
 // wrappers for the sm_103a features the kernels use (tcgen05 MMA/TMEM, TMA bulk tensor
 // copies, mbarriers).
 #pragma once
+#include <atomic>
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -355,6 +356,20 @@ __host__ __device__ __forceinline__ uint32_t swz128_offset(uint32_t row, uint32_
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once per device (the
+// attribute is per device; `done` is the kernel's bitmask of devices already set).
+template <typename K>
+inline cudaError_t ensure_smem_attr(K kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 // Launch `kernel` on `stream`, allowed to overlap the previous kernel's tail when `pdl`.

@@ -250,12 +250,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 template <int MODE>
 cudaError_t launch_gemm_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmE,
                             const CUtensorMap& tmI, const GemmArgs& g, int n_pairs, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_2sm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_2SM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = ensure_smem_attr(k_gemm_2sm<MODE>, SMEM_2SM, attr_done);
+  if (e != cudaSuccess) return e;
   if (g.n_items <= 0) return cudaSuccess;
   return launch_k(k_gemm_2sm<MODE>, dim3(2 * n_pairs), dim3(GEMM_THREADS), SMEM_2SM, stream, g.pdl != 0, tmA, tmB,
                   tmE, tmI, g);

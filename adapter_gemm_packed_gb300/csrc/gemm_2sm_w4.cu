@@ -415,12 +415,9 @@ template <int MODE>
 cudaError_t launch_gemm_2sm_w4(const CUtensorMap& tmA, const CUtensorMap& tmQ, const CUtensorMap& tmS,
                                const CUtensorMap& tmE, const CUtensorMap& tmI, const GemmArgs& g, int n_pairs,
                                cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_2sm_w4<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_W4);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = ensure_smem_attr(k_gemm_2sm_w4<MODE>, SMEM_W4, attr_done);
+  if (e != cudaSuccess) return e;
   if (g.n_items <= 0) return cudaSuccess;
   return launch_k(k_gemm_2sm_w4<MODE>, dim3(2 * n_pairs), dim3(W4_THREADS), SMEM_W4, stream, g.pdl != 0, tmA, tmQ,
                   tmS, tmE, tmI, g);

@@ -553,13 +553,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 template <int MODE>
 cudaError_t launch_seg_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmE,
                             const CUtensorMap& tmI, const GemmArgs& g, int grid, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_seg_gemm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<MODE>::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = ensure_smem_attr(k_seg_gemm<MODE>, Ring<MODE>::kSmem, attr_done);
+  if (e != cudaSuccess) return e;
   if (g.n_items <= 0) return cudaSuccess;
   return launch_k(k_seg_gemm<MODE>, dim3(grid), dim3(GEMM_THREADS), Ring<MODE>::kSmem, stream, g.pdl != 0, tmA, tmB,
                   tmE, tmI, g);

@@ -38,6 +38,9 @@
  * anything detectable on the host; nothing crosses the ABI as an exception.
  * A device-side wait that gives up (see MLORA_ERR_TIMEOUT) records its code in
  * the plan's status word, read back by mlora_sync_status().
+ * Threads: different plans may be used from different host threads at once (each call makes
+ * the plan device's primary context current on its thread); calls on one plan must not overlap
+ * on the host.  Every call can be captured into a CUDA graph.
  */
 #ifndef MLORA_H
 #define MLORA_H

@@ -299,3 +299,45 @@ def test_autograd_module_matches_direct_calls():
     finally:
         direct.close()
         viaag.close()
+
+
+def test_two_plans_on_two_threads_and_streams():
+    """Two plans driven at once from two host threads on their own streams (the library's host
+    code runs concurrently: ctypes releases the GIL) match the same plans run one after the other."""
+    import threading
+    cases = [W.custom("thr_a", 935, 512, 640, [1, 7, 64, 256], [200, 56, 300, 17], b_std=0.05),
+             W.custom("thr_b", 936, 384, 256, [16, 128, 8], [256, 384, 130], b_std=0.05)]
+    data = []
+    for wl in cases:
+        T = W.materialise(wl)
+        data.append((wl, T, G.to_dev(T.X, "bf16"), G.to_dev(T.dY, "bf16"), G.to_dev(T.Wt, "bf16")))
+
+    def run(i, stream, out):
+        wl, T, X, dY, Wt = data[i]
+        layer = G.make_layer(wl, T, M.MLORA_REUSE_STAGING)
+        try:
+            with torch.cuda.stream(stream):
+                for step in range(1, 4):
+                    Y = layer.forward(X, Wt, stream=stream)
+                    dX = layer.backward(X, Wt, dY, stream=stream)
+                    layer.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, step, stream=stream)
+            stream.synchronize()
+            assert layer.sync_status(stream) == M.MLORA_OK
+            out[i] = (Y.clone(), dX.clone(), [a.clone() for a in layer.At])
+        finally:
+            layer.close()
+
+    seq = [None, None]
+    for i in range(2):
+        run(i, torch.cuda.Stream(), seq)
+    par = [None, None]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    threads = [threading.Thread(target=run, args=(i, streams[i], par)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    for a, b in zip(seq, par):
+        assert b is not None
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+        assert all(torch.equal(x, y) for x, y in zip(a[2], b[2]))
