@@ -341,3 +341,31 @@ def test_two_plans_on_two_threads_and_streams():
         assert b is not None
         assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
         assert all(torch.equal(x, y) for x, y in zip(a[2], b[2]))
+
+
+def _random_wl(seed):
+    g = np.random.default_rng(5000 + seed)
+    n_jobs = int(g.integers(1, 9))
+    ns = [int(n) for n in g.choice([1, 7, 64, 127, 128, 129, 200, 300], size=n_jobs)]
+    d_in = 64 * int(g.integers(1, 9))
+    if seed % 3 == 2:   # a shared-input pack of two or three projections
+        widths = [8 * int(w) for w in g.integers(2, 40, size=int(g.integers(2, 4)))]
+        ranks_jg = [[int(r) for r in g.choice([1, 4, 8, 16, 32, 64, 128], size=len(widths))] for _ in ns]
+        return W.custom_grouped(f"rand_g{seed}", 940 + seed, d_in, widths, ranks_jg, ns, b_std=0.05)
+    d_out = 8 * int(g.integers(2, 80))
+    ranks = [int(r) for r in g.choice([1, 3, 8, 16, 33, 64, 128, 256], size=n_jobs)]
+    return W.custom(f"rand_{seed}", 940 + seed, d_in, d_out, ranks, ns, b_std=0.05, w_std=0.05)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_vs_oracle(seed):
+    """Seeded random job tables (1-8 jobs of 1-300 tokens, ranks 1-256, ragged widths, every third a
+    shared-input pack), the shrink / dH engine alternating between pairs and single CTAs."""
+    wl = _random_wl(seed)
+    T = W.materialise(wl)
+    run = G.GpuRun(wl, T, flags=M.MLORA_WINDOW_PAIRS if seed % 2 else M.MLORA_WINDOW_SINGLE)
+    try:
+        assert run.status_after_backward == M.MLORA_OK
+        G.compare(run.res, G.oracle_full(wl, T), G.TOL["bf16"])
+    finally:
+        run.close()

@@ -66,7 +66,38 @@ def _case(name):
 
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_planner_tables(name):
-    d_in, d_out, ranks, ns = _case(name)
+    _check_tables(*_case(name))
+
+
+def _random_case(seed):
+    g = np.random.default_rng(1000 + seed)
+    n_jobs = int(g.integers(1, 24))
+    ranks = [int(r) for r in g.choice([1, 2, 3, 5, 8, 16, 24, 32, 48, 64, 100, 128, 200, 256], size=n_jobs)]
+    ns = [int(n) for n in g.choice([1, 5, 17, 64, 100, 127, 128, 129, 250, 256, 300, 700], size=n_jobs)]
+    d_in = 8 * int(g.integers(8, 160))
+    d_out = 8 * int(g.integers(8, 160))
+    return d_in, d_out, ranks, ns
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_planner_tables_random(seed):
+    """The same invariants on seeded random job tables (ranks 1-256, jobs of 1-700 tokens,
+    ragged d_in / d_out), plus the CTA-pair window items."""
+    d_in, d_out, ranks, ns = _random_case(seed)
+    _check_tables(d_in, d_out, ranks, ns)
+    plan, _ = host_plan(d_in, d_out, ranks, ns)
+    try:
+        mt = _describe(plan, M.MLORA_Q_MTILES).reshape(-1, 5)
+        items = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)[1:].reshape(-1, 5)
+    finally:
+        M.mlora_plan_destroy(plan)
+    for p in range((len(mt) + 1) // 2):
+        q_lo, nch = mt[2 * p, 2], mt[2 * p, 3]
+        got = [q for _, q0, nq, _, _ in items[items[:, 0] == p] for q in range(q0, q0 + nq)]
+        assert got[:nch] == list(range(q_lo, q_lo + nch)) and len(got) - nch in (0, 1)
+
+
+def _check_tables(d_in, d_out, ranks, ns):
     plan, ws = host_plan(d_in, d_out, ranks, ns)
     try:
         summ, mt, cols, win, da, db = _tables(plan)
