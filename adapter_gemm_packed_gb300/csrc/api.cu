@@ -30,7 +30,7 @@ cudaError_t launch_seg_gemm(const CUtensorMap&, const CUtensorMap&, const CUtens
                             const GemmArgs&, int, cudaStream_t);
 template <int MODE>
 cudaError_t launch_gemm_2sm(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                            const GemmArgs&, int, cudaStream_t);
+                            const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 template <int MODE>
 cudaError_t launch_gemm_2sm_w4(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
@@ -599,6 +599,19 @@ cudaError_t timed(const mlora_plan_t* Pc, int id, cudaStream_t s, F&& launch) {
   return e;
 }
 
+// Work list of the CTA-pair base GEMMs: 256x256 tiles, except that when the last wave would fill at
+// most half of the pairs its tiles are split into 256x128 halves, which finish that wave in half
+// the time (and give small problems twice the pairs).  Returns the number of pairs to launch.
+int pair_gemm_items(const mlora_plan_t* P, GemmArgs& g) {
+  const int n_tiles = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
+  const int pairs = std::max(1, P->num_sms / 2);
+  const int tail = n_tiles <= pairs ? n_tiles : n_tiles % pairs;
+  const bool split = tail > 0 && 2 * tail <= pairs;
+  g.n_full_items = split ? n_tiles - tail : n_tiles;
+  g.n_items = split ? n_tiles + tail : n_tiles;
+  return std::max(1, std::min(g.n_items, pairs));
+}
+
 GemmArgs base_args(const mlora_plan_t* P) {
   GemmArgs g{};
   g.N = static_cast<int>(P->prob.n_tokens);
@@ -744,7 +757,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
   }
 
   const bool pairs = !(pr.flags & MLORA_GEMM_SINGLE_CTA);
-  CUtensorMap mX, mAt, mW, mBt, mI, mQ, mS;
+  CUtensorMap mX, mAt, mW, mBt, mI, mQ, mS, mW64, mBt64;
   if ((st = make_map(&mX, X, pr.d_in, pr.n_tokens, pr.d_in, 64, 128)) != MLORA_OK) return st;
   if ((st = make_map(&mAt, at_all, pr.d_in, P->C_total, pr.d_in, 64, 64)) != MLORA_OK) return st;
   if (fused4) {
@@ -759,6 +772,10 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
     return st;
   }
   if ((st = make_map(&mBt, bt_all, P->C_total, pr.d_out, P->C_total, 64, pairs ? 128 : 256)) != MLORA_OK) return st;
+  if (pairs && !fused4) {   // 64-row boxes of the same tensors for half-width tail tiles
+    if ((st = make_map(&mW64, Wt, pr.d_in, pr.d_out, pr.d_in, 64, 64)) != MLORA_OK) return st;
+    if ((st = make_map(&mBt64, bt_all, P->C_total, pr.d_out, P->C_total, 64, 64)) != MLORA_OK) return st;
+  }
   if ((st = make_map(&mI, himg, CHUNK_COLS, P->n_images * BM, CHUNK_COLS, 64, 128)) != MLORA_OK) return st;
 
   GemmArgs g = base_args(P);
@@ -789,10 +806,8 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
       return launch_gemm_2sm_w4<MODE_FWD>(mX, mQ, mS, mBt, mI, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
     });
   } else if (pairs) {
-    g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
-    e = timed(P, K_FWD_GEMM, s, [&] {
-      return launch_gemm_2sm<MODE_FWD>(mX, mW, mBt, mI, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
-    });
+    const int n_pairs = pair_gemm_items(P, g);
+    e = timed(P, K_FWD_GEMM, s, [&] { return launch_gemm_2sm<MODE_FWD>(mX, mW, mBt, mI, mW64, mBt64, g, n_pairs, s); });
   } else {
     g.n_items = P->n_mtiles * g.n_tiles_n;
     e = timed(P, K_FWD_GEMM, s, [&] { return launch_seg_gemm<MODE_FWD>(mX, mW, mBt, mI, g, grid_of(P, g.n_items), s); });
@@ -930,9 +945,9 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
       return launch_gemm_2sm_w4<MODE_BWD>(mdY, mQ, mS, mAt64, mdHi, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
     });
   } else if (pairs) {
-    g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
+    const int n_pairs = pair_gemm_items(P, g);
     e = timed(P, K_BWD_GEMM, s, [&] {
-      return launch_gemm_2sm<MODE_BWD>(mdY, mWmn, mAt64, mdHi, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
+      return launch_gemm_2sm<MODE_BWD>(mdY, mWmn, mAt64, mdHi, mWmn, mAt64, g, n_pairs, s);
     });
   } else {
     g.n_items = P->n_mtiles * g.n_tiles_n;

@@ -117,6 +117,7 @@ struct GemmArgs {
   int kmain;           // 64-wide K slices of the main product (FWD/BWD/SHRINK/DH)
   int n_items;
   int n_tiles_n;       // FWD/BWD: output column tiles of 256
+  int n_full_items;    // CTA-pair base GEMMs: items from here on are half-width tiles (see gemm_2sm.cu)
   int group_m;         // FWD/BWD raster: M tiles per group
   int n_mtiles;
   const MTile* mtiles;

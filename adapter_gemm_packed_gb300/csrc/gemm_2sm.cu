@@ -17,6 +17,9 @@
 // CTAs' empty[s] / tfull[a]; both CTAs' epilogue warps arrive on the even CTA's tempty[a].
 // The rank term's K extension is identical for both halves because the planner gives both
 // 128-token tiles of a pair the union of their rank-chunk ranges.
+// Tail: when the last wave of 256x256 tiles would fill at most half of the CTA pairs, the planner
+// splits those tiles into two 256x128 halves (items from g.n_full_items on), so the last wave
+// takes half the time; a half tile's MMA has N = 128 and each CTA loads 64 rows of its B.
 // Every wait is bounded (mbar_wait); on expiry the CTA records a status code and unwinds.
 #include "common.cuh"
 #include "pair.cuh"
@@ -32,12 +35,31 @@ constexpr int A2_BYTES = 128 * BK * 2;        // this CTA's 128 rows of A per st
 constexpr int B2_BYTES = 128 * BK * 2;        // this CTA's 128-row half of B per stage
 constexpr int SMEM_2SM = S2 * (A2_BYTES + B2_BYTES) + 1024 + 256;
 
+// Item -> (token pair, first output column, width): full tiles in the raster order of
+// decode_pair, then the halves of the remaining tiles (two items each).
+__device__ __forceinline__ void decode_item(const GemmArgs& g, int item, int& mp, int& col0, int& width) {
+  int n;
+  if (item < g.n_full_items) {
+    decode_pair(g, item, mp, n);
+    col0 = n * BN;
+    width = BN;
+  } else {
+    const int j = item - g.n_full_items;
+    decode_pair(g, g.n_full_items + (j >> 1), mp, n);
+    col0 = n * BN + (j & 1) * (BN / 2);
+    width = BN / 2;
+  }
+}
+
 }  // namespace
 
+// tmB / tmE: 128-row boxes for the forward's K-major B halves; tmB64 / tmE64: the same tensors
+// with 64-row boxes (half tiles).  The backward's MN-major B uses 64-wide boxes throughout.
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmI,
+               const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmE64,
                const __grid_constant__ GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -73,6 +95,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmE);
     prefetch_tmap(&tmI);
+    if (MODE == MODE_FWD && g.n_full_items < g.n_items) {
+      prefetch_tmap(&tmB64);
+      prefetch_tmap(&tmE64);
+    }
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
   tc_fence_before();
@@ -89,38 +115,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int item = pair; ok && item < g.n_items; item += n_pairs_grid) {
-        int mp, n;
-        decode_pair(g, item, mp, n);
+        int mp, col0, width;
+        decode_item(g, item, mp, col0, width);
+        const bool half = width < BN;
         const int tile = 2 * mp + static_cast<int>(rank);
         const MTile mt = g.mtiles[min(tile, g.n_mtiles - 1)];   // a missing odd tile borrows its partner's
         const int m0 = tile * BM;
-        const int nh0 = n * BN + static_cast<int>(rank) * 128;   // this CTA's half of the N tile
+        const int nh0 = col0 + static_cast<int>(rank) * (width / 2);   // this CTA's half of the item's columns
         const int nkb = g.kmain + mt.nch;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A2_BYTES + B2_BYTES));
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A2_BYTES + width * BK));
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
           uint8_t* a = sA + stage * A2_BYTES;
           uint8_t* b = sB + stage * B2_BYTES;
           if (kb < g.kmain) {
             tma_load_2d_pair(a, &tmA, bar, kb * BK, m0);
             if constexpr (MODE == MODE_FWD) {
-              tma_load_2d_pair(b, &tmB, bar, kb * BK, nh0);
+              tma_load_2d_pair(b, half ? &tmB64 : &tmB, bar, kb * BK, nh0);
             } else {
               tma_load_2d_pair(b, &tmB, bar, nh0, kb * BK);
-              tma_load_2d_pair(b + 64 * 64 * 2, &tmB, bar, nh0 + 64, kb * BK);
+              if (!half) tma_load_2d_pair(b + 64 * 64 * 2, &tmB, bar, nh0 + 64, kb * BK);
             }
           } else {
             const int e = kb - g.kmain;
             tma_load_2d_pair(a, &tmI, bar, 0, (mt.img_off + e) * BM);
-            if constexpr (MODE == MODE_FWD) {
-              tma_load_2d_pair(b, &tmE, bar, (mt.q_lo + e) * CHUNK_COLS, nh0);   // Bt_all rows, K-major
+            if constexpr (MODE == MODE_FWD) {   // Bt_all rows, K-major
+              tma_load_2d_pair(b, half ? &tmE64 : &tmE, bar, (mt.q_lo + e) * CHUNK_COLS, nh0);
             } else {   // At_all [C, d_in] as MN-major B (n = d_in index, k = rank column)
               tma_load_2d_pair(b, &tmE, bar, nh0, (mt.q_lo + e) * CHUNK_COLS);
-              tma_load_2d_pair(b + 64 * 64 * 2, &tmE, bar, nh0 + 64, (mt.q_lo + e) * CHUNK_COLS);
+              if (!half) tma_load_2d_pair(b + 64 * 64 * 2, &tmE, bar, nh0 + 64, (mt.q_lo + e) * CHUNK_COLS);
             }
           }
           if (++stage == S2) {
@@ -137,11 +164,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      const uint32_t idesc_k = idesc_bf16(2 * BM, BN, false, false);
-      const uint32_t idesc_main = idesc_bf16(2 * BM, BN, false, MODE == MODE_BWD);
       for (int item = pair; ok && item < g.n_items; item += n_pairs_grid) {
-        int mp, n;
-        decode_pair(g, item, mp, n);
+        int mp, col0, width;
+        decode_item(g, item, mp, col0, width);
+        const uint32_t idesc = idesc_bf16(2 * BM, width, false, MODE == MODE_BWD);
         const int nkb = g.kmain + g.mtiles[min(2 * mp, g.n_mtiles - 1)].nch;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
           ok = false;
@@ -162,7 +188,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = smem_desc(a + k * 32, 16, 1024);
             const uint64_t bd = b_mn ? smem_desc(b + k * 2048, 64 * 64 * 2, 1024) : smem_desc(b + k * 32, 16, 1024);
-            umma_pair_bf16(d_tmem, ad, bd, b_mn ? idesc_main : idesc_k, (kb > 0 || k > 0) ? 1u : 0u);
+            umma_pair_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           umma_pair_commit_mc(&empty[stage], 0x3);
           if (++stage == S2) {
@@ -194,13 +220,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      int mp, n;
-      decode_pair(g, item, mp, n);
+      int mp, col0, width;
+      decode_item(g, item, mp, col0, width);
       const long long row = static_cast<long long>(2 * mp + static_cast<int>(rank)) * BM + rit;
-      const int col0 = n * BN;
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
 #pragma unroll 1
-      for (int cb = 0; cb < BN; cb += 32) {
+      for (int cb = 0; cb < width; cb += 32) {
         uint32_t v[32];
         tmem_ld32(t_acc + cb, v);
         tmem_ld_wait();
@@ -249,18 +274,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 
 template <int MODE>
 cudaError_t launch_gemm_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmE,
-                            const CUtensorMap& tmI, const GemmArgs& g, int n_pairs, cudaStream_t stream) {
+                            const CUtensorMap& tmI, const CUtensorMap& tmB64, const CUtensorMap& tmE64,
+                            const GemmArgs& g, int n_pairs, cudaStream_t stream) {
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = ensure_smem_attr(k_gemm_2sm<MODE>, SMEM_2SM, attr_done);
   if (e != cudaSuccess) return e;
   if (g.n_items <= 0) return cudaSuccess;
   return launch_k(k_gemm_2sm<MODE>, dim3(2 * n_pairs), dim3(GEMM_THREADS), SMEM_2SM, stream, g.pdl != 0, tmA, tmB,
-                  tmE, tmI, g);
+                  tmE, tmI, tmB64, tmE64, g);
 }
 
 template cudaError_t launch_gemm_2sm<MODE_FWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                               const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+                                               const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                               const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_gemm_2sm<MODE_BWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                               const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+                                               const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                               const GemmArgs&, int, cudaStream_t);
 
 }  // namespace mlora
