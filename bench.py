@@ -7,6 +7,7 @@ tokens per step).  One step = mlora_forward + mlora_backward + mlora_adamw over 
 with inputs resident in HBM.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+  python bench.py --sweep        packed vs one plan per job vs a per-adapter PyTorch loop
 
 --impl reference times the fp64 CPU oracle (the reference arm of this metric) on a bounded
 sample of the same workload.  Under torchrun (N > 1) every rank runs its own replica of the
@@ -547,6 +548,136 @@ def run_ours(args, wl, rank, world, local_rank):
     layer.close()
 
 
+# Packed-kernel sweep: the attention and MLP-up projections of Qwen-2.5-3B and -7B, rank 64, one
+# 1024-token sequence per job, 1 to 32 jobs (the setting of the packed-kernel microbenchmark in
+# "PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §11.2.1).
+SWEEP_LAYERS = [("qwen2.5_3b_attn_2048x2048", 2048, 2048), ("qwen2.5_3b_mlp_up_2048x11008", 2048, 11008),
+                ("qwen2.5_7b_attn_3584x3584", 3584, 3584), ("qwen2.5_7b_mlp_up_3584x18944", 3584, 18944)]
+SWEEP_JOBS = [1, 2, 4, 8, 16, 32]
+
+
+def run_sweep(args):
+    """One JSON line per (layer, job count): a step of the whole pack (forward, backward, AdamW) as
+    one plan, the same jobs one plan at a time back to back, and a PyTorch / cuBLAS comparator that
+    batches the base GEMMs over all tokens but runs the LoRA products adapter by adapter (then one
+    fused torch AdamW over all adapters).  Inputs are seeded device draws; the L2 is flushed before
+    every timed step, outside the CUDA events."""
+    import torch
+    from adapter_gemm_packed_gb300 import _mlora as M
+    from adapter_gemm_packed_gb300.layer import PackedLoRA
+
+    torch.cuda.set_device(0)
+    r, n_tok, s = 64, 1024, 2.0                 # s = alpha / r with alpha = 2 r
+    lr, b1, b2, eps, wd = 1e-3, 0.9, 0.999, 1e-8, 0.01
+    bf = torch.bfloat16
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")    # twice the 129 MB L2
+
+    def timed(step):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        total = 0.0
+        for _ in range(args.sweep_steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            total += e0.elapsed_time(e1)
+        return total / args.sweep_steps
+
+    def rel(a, b):
+        return float((a.float() - b.float()).norm() / b.float().norm())
+
+    gen = torch.Generator(device="cuda")
+    for li, (name, d_in, d_out) in enumerate(SWEEP_LAYERS):
+        for n_jobs in SWEEP_JOBS:
+            gen.manual_seed(7000 + 100 * li + n_jobs)
+            N = n_jobs * n_tok
+            randn = lambda *shape: torch.randn(*shape, generator=gen, device="cuda")
+            Wt = (randn(d_out, d_in) * 0.02).to(bf)
+            At = [randn(r, d_in) * d_in ** -0.5 for _ in range(n_jobs)]
+            Bt = [randn(d_out, r) * 0.02 for _ in range(n_jobs)]
+            X = randn(N, d_in).to(bf)
+            dY = (randn(N, d_out) * 0.01).to(bf)
+            rows = [slice(j * n_tok, (j + 1) * n_tok) for j in range(n_jobs)]
+
+            # the pack as one plan (its own copies of the masters, as every arm below)
+            layer = PackedLoRA(d_in, d_out, [r] * n_jobs, [n_tok] * n_jobs, [s] * n_jobs, At=[a.clone() for a in At],
+                               Bt=[b.clone() for b in Bt],
+                               flags=M.MLORA_REUSE_STAGING)
+            Y, dX = torch.empty(N, d_out, dtype=bf, device="cuda"), torch.empty(N, d_in, dtype=bf, device="cuda")
+            layer.forward(X, Wt, Y)
+            layer.backward(X, Wt, dY, dX)
+            Y0, dX0 = Y.clone(), dX.clone()
+            t = [0]
+
+            def packed():
+                t[0] += 1
+                layer.forward(X, Wt, Y)
+                layer.backward(X, Wt, dY, dX)
+                layer.adamw(lr, b1, b2, eps, wd, t[0])
+
+            # the same jobs, one plan each, run one after another
+            singles = [PackedLoRA(d_in, d_out, [r], [n_tok], [s], At=[At[j].clone()], Bt=[Bt[j].clone()],
+                                  flags=M.MLORA_REUSE_STAGING)
+                       for j in range(n_jobs)]
+            t1 = [0]
+
+            def one_at_a_time():
+                t1[0] += 1
+                for j, L in enumerate(singles):
+                    L.forward(X[rows[j]], Wt, Y[rows[j]])
+                    L.backward(X[rows[j]], Wt, dY[rows[j]], dX[rows[j]])
+                    L.adamw(lr, b1, b2, eps, wd, t1[0])
+
+            # PyTorch comparator: batched base GEMMs, per-adapter LoRA products, fused AdamW
+            A = [a.clone() for a in At]
+            B = [b.clone() for b in Bt]
+            opt = torch.optim.AdamW(A + B, lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd, fused=True)
+
+            def torch_naive(update=True):
+                Yt = torch.nn.functional.linear(X, Wt)
+                Ab, Bb = [a.to(bf) for a in A], [b.to(bf) for b in B]
+                Hs = []
+                for j, sl in enumerate(rows):
+                    H = X[sl] @ Ab[j].t()
+                    Yt[sl] += s * (H @ Bb[j].t())
+                    Hs.append(H)
+                dXt = dY @ Wt
+                for j, sl in enumerate(rows):
+                    B[j].grad = (s * (dY[sl].t() @ Hs[j])).float()
+                    dH = s * (dY[sl] @ Bb[j])
+                    A[j].grad = (dH.t() @ X[sl]).float()
+                    dXt[sl] += dH @ Ab[j]
+                if update:
+                    opt.step()
+                return Yt, dXt
+
+            Yt, dXt = torch_naive(update=False)
+            agree = {"Y": rel(Y0, Yt), "dX": rel(dX0, dXt)}
+            ms_packed = timed(packed)
+            ms_single = timed(one_at_a_time)
+            ms_torch = timed(torch_naive)
+            if layer.sync_status() != M.MLORA_OK or any(L.sync_status() != M.MLORA_OK for L in singles):
+                raise SystemExit("device status error in the sweep")
+            flops = 4.0 * N * d_in * d_out + 6.0 * N * r * (d_in + d_out)
+            print(json.dumps({"sweep": "packed_vs_sequential", "layer": name, "d_in": d_in, "d_out": d_out, "rank": r,
+                              "jobs": n_jobs, "tokens": N, "packed_ms": ms_packed, "one_plan_per_job_ms": ms_single,
+                              "torch_per_adapter_ms": ms_torch, "speedup_vs_one_plan_per_job": ms_single / ms_packed,
+                              "speedup_vs_torch_per_adapter": ms_torch / ms_packed,
+                              "packed_tflops": flops / (ms_packed * 1e-3) / 1e12,
+                              "agreement_rel_frobenius": agree, "l2": "flushed before every timed step",
+                              "steps": args.sweep_steps, "warmup": 3}), flush=True)
+            layer.close()
+            for L in singles:
+                L.close()
+            del layer, singles, opt, A, B, X, dY, Y, dX, Wt, At, Bt
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -563,6 +694,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens-per-job", type=int, default=64)
     ap.add_argument("--ref-budget-s", type=float, default=90.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="packed vs sequential over Qwen-2.5 layer shapes (one JSON line per point, one GPU)")
+    ap.add_argument("--sweep-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
@@ -570,6 +704,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.sweep:
+        if world > 1:
+            raise SystemExit("--sweep runs on one GPU")
+        import __graft_entry__
+        __graft_entry__.build()
+        run_sweep(args)
+        return
     wl = workload(args.workload)
     if args.impl == "reference":
         run_reference(args, wl, rank)
