@@ -1,0 +1,68 @@
+"""The benchmark's JSON line: the keys and units every run prints, on both arms.
+
+The reference arm (the fp64 oracle on the host cores) runs on CPU; the GPU arm runs a short q_proj
+benchmark and checks the roofline, CPU-baseline, end-to-end, clock and launch-count records.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*argv, timeout=600):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *argv], cwd=ROOT, capture_output=True,
+                         text=True, timeout=timeout)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def _common(d, steps, warmup):
+    assert d["metric"].startswith("packed multi-LoRA fwd+bwd tokens/s")
+    assert d["unit"] == "tokens/s" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["steps"] == steps and d["warmup"] == warmup and d["n_gpus"] == 1 and d["scaling"] == "weak"
+    assert d["vs_baseline"] is None
+    e = d["e2e"]
+    assert set(e) >= {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"} and e["unit"] == "tokens/s"
+    c = d["cpu_baseline"]
+    assert set(c) >= {"value", "unit", "cores", "kind", "sample"} and c["kind"] == "oracle" and c["cores"] >= 1
+
+
+def test_reference_arm_line():
+    d = _run("--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "1", "--ref-budget-s", "5")
+    _common(d, 2, 1)
+    assert d["impl"] == "reference" and d["dtype"] == "f64"
+    assert d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"].startswith("tiny_f32")
+    # the arm times a token sample of the workload: a step's tokens over its time
+    assert d["ms_per_step"] > 0 and "tokens" in d["cpu_baseline"]["sample"]
+
+
+@pytest.mark.gpu
+def test_gpu_arm_line():
+    d = _run("--steps", "5", "--warmup", "3", "--cpu-seconds", "1")
+    _common(d, 5, 3)
+    assert "impl" not in d and d["dtype"] == "bf16"
+    assert d["config"]["workload"] == "llama3_8b_q_proj_4096x4096_8ad_16384tok"
+    assert d["config"]["tokens_per_step"] == 16384
+    assert d["ms_per_step"] == pytest.approx(16384 / d["value"] * 1e3, rel=1e-6)
+    # 7 launches a step with staging reuse and the AdamW shadow refresh (the first pack is in warm-up)
+    assert d["gpu_launches"] == 7 * 5
+    r = d["roofline"]
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] > 0
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"]) and 0.2 < r["frac"] < 1.3
+    assert r["kernel"] in ("fwd_gemm", "bwd_gemm")
+    e = d["e2e"]
+    # X, dY in and Y, dX out, bf16, every step
+    assert e["h2d_bytes_per_step"] == 16384 * (4096 + 4096) * 2
+    assert e["d2h_bytes_per_step"] == 16384 * (4096 + 4096) * 2
+    assert 0 < e["value"] < d["value"] * 1.05
+    clk = d["clocks"]
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
+    assert set(d["kernels"]) >= {"shrink", "fwd_gemm", "dH", "dB", "bwd_gemm", "dA", "adamw"}
