@@ -97,7 +97,9 @@ def kernel_bytes(wl, kernel):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 50 ms while running."""
+    """nvidia-smi clock / throttle samples every 50 ms, each stamped with the host's clock on
+    arrival; the summary keeps the samples that arrived inside the `with` block (the timed region).
+    The raw samples are also written to $BENCH_CLOCKS_DIR when that is set."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
@@ -105,47 +107,69 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.rows = []          # (host time, line)
+        self.t0 = self.t1 = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.monotonic(), line.strip()))
 
     def __enter__(self):
+        import threading
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "50"],
-                                         stdout=self.f, stderr=subprocess.DEVNULL)
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            deadline = time.monotonic() + 3.0      # the sampler is live before the region starts
+            while not self.rows and time.monotonic() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+        self.t0 = time.monotonic()
         return self
 
     def __exit__(self, *a):
+        self.t1 = time.monotonic()
         if self.proc:
+            time.sleep(0.06)                       # let the last in-region sample arrive
             self.proc.terminate()
             try:
                 self.proc.wait(5)
             except Exception:
                 self.proc.kill()
-            self.f.close()
+            self.thread.join(5)
+            out = os.environ.get("BENCH_CLOCKS_DIR")
+            if out:
+                os.makedirs(out, exist_ok=True)
+                with open(os.path.join(out, f"clocks_bench_{os.getpid()}.csv"), "w") as f:
+                    for t, line in self.rows:
+                        f.write(f"{t - self.t0:.3f},{line}\n")
 
     def summary(self):
         if not self.proc:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
-                except ValueError:
-                    continue
+        parsed = []
+        for t, line in self.rows:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                parsed.append((t, float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+            except ValueError:
+                continue
+        inside = [r for r in parsed if self.t0 <= r[0] <= self.t1 + 0.06]
+        rows = inside or parsed
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for r in rows for n, v in zip(names, r[3][1:]) if v.lower().startswith("active")})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4][1:]) if v.lower().startswith("active")})
+        out = {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+               "power_w_max": max(r[3] for r in rows), "samples": len(rows), "reasons": reasons}
+        if not inside:
+            out["note"] = "no sample arrived inside the timed region; these are the samples around it"
+        return out
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -681,7 +705,7 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="qproj")

@@ -66,3 +66,23 @@ def test_gpu_arm_line():
     clk = d["clocks"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
     assert set(d["kernels"]) >= {"shrink", "fwd_gemm", "dH", "dB", "bwd_gemm", "dA", "adamw"}
+
+
+def test_clock_summary_keeps_the_timed_region():
+    """The clock record summarises the samples that arrived inside the timed region, with the
+    throttle reasons seen there; with none inside it says so and falls back to the nearest ones."""
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler(0)
+    c.proc = object()
+    c.t0, c.t1 = 100.0, 101.0
+    idle = "0, 1980, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active"
+    capped = "0, 1500, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active"
+    hot = "0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active"
+    c.rows = [(99.5, idle), (100.2, capped), (100.4, hot), (100.6, hot), (101.5, idle), (100.8, "garbled")]
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 1390.0 and "note" not in s
+    c.rows = [(99.5, idle)]
+    s = c.summary()
+    assert s["samples"] == 1 and s["sm_mhz"] == 1980.0 and "note" in s
