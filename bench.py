@@ -616,8 +616,13 @@ def run_sweep(args):
         return float((a.float() - b.float()).norm() / b.float().norm())
 
     gen = torch.Generator(device="cuda")
-    for li, (name, d_in, d_out) in enumerate(SWEEP_LAYERS):
-        for n_jobs in SWEEP_JOBS:
+    layers = [x for x in SWEEP_LAYERS if not args.sweep_layers or x[0] in args.sweep_layers.split(",")]
+    jobs = [int(j) for j in args.sweep_jobs.split(",")] if args.sweep_jobs else SWEEP_JOBS
+    if not layers:
+        raise SystemExit(f"--sweep-layers: none of {[x[0] for x in SWEEP_LAYERS]}")
+    for name, d_in, d_out in layers:
+        li = [x[0] for x in SWEEP_LAYERS].index(name)
+        for n_jobs in jobs:
             gen.manual_seed(7000 + 100 * li + n_jobs)
             N = n_jobs * n_tok
             randn = lambda *shape: torch.randn(*shape, generator=gen, device="cuda")
@@ -721,6 +726,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="packed vs sequential over Qwen-2.5 layer shapes (one JSON line per point, one GPU)")
     ap.add_argument("--sweep-steps", type=int, default=10)
+    ap.add_argument("--sweep-layers", default="", help="comma-separated subset of the sweep's layer names")
+    ap.add_argument("--sweep-jobs", default="", help="comma-separated job counts (default 1,2,4,8,16,32)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

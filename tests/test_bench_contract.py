@@ -86,3 +86,19 @@ def test_clock_summary_keeps_the_timed_region():
     c.rows = [(99.5, idle)]
     s = c.summary()
     assert s["samples"] == 1 and s["sm_mhz"] == 1980.0 and "note" in s
+
+
+@pytest.mark.gpu
+def test_gpu_sweep_lines():
+    """The packed-vs-sequential sweep on one layer shape at two job counts: one JSON line per point,
+    the pack agreeing with the per-adapter PyTorch comparator to bf16 output rounding."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--sweep", "--sweep-layers",
+                          "qwen2.5_3b_attn_2048x2048", "--sweep-jobs", "1,4", "--sweep-steps", "2"], cwd=ROOT,
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [json.loads(l) for l in out.stdout.splitlines() if l.startswith("{")]
+    assert [d["jobs"] for d in lines] == [1, 4]
+    for d in lines:
+        assert d["sweep"] == "packed_vs_sequential" and d["tokens"] == 1024 * d["jobs"] and d["rank"] == 64
+        assert d["packed_ms"] > 0 and d["one_plan_per_job_ms"] > 0 and d["torch_per_adapter_ms"] > 0
+        assert d["agreement_rel_frobenius"]["Y"] < 2e-2 and d["agreement_rel_frobenius"]["dX"] < 2e-2

@@ -369,3 +369,58 @@ def test_random_shapes_vs_oracle(seed):
         G.compare(run.res, G.oracle_full(wl, T), G.TOL["bf16"])
     finally:
         run.close()
+
+
+@pytest.mark.parametrize("reuse", [False, True], ids=["repack", "reuse_staging"])
+def test_three_training_steps_vs_oracle(reuse):
+    """Three steps of forward, backward and AdamW (t = 1, 2, 3) with fresh X and dY each step: the
+    masters, moments and (with MLORA_REUSE_STAGING) the bf16 shadows refreshed by the AdamW step carry
+    over between steps as the oracle's state does.  Checked after the third step: Y, dX, H, dH, dA,
+    dB of that step and every adapter's A, B, m, v."""
+    wl = W.custom("three_steps", 906, 512, 384, [8, 64, 3, 24], [200, 77, 300, 129], w_std=0.05, b_std=0.05)
+    T = W.materialise(wl)
+    layer = G.make_layer(wl, T, flags=M.MLORA_REUSE_STAGING if reuse else 0)
+    Wt = G.to_dev(T.Wt, wl.dtype)
+    Wm = W.rows_as_f64(T.Wt, wl.dtype).T
+    J = len(wl.ranks)
+    A = [T.At[j].astype(np.float64).T for j in range(J)]          # d_in x r
+    B = [T.Bt[j].astype(np.float64).T for j in range(J)]          # r x d_out
+    mA = [np.zeros_like(a) for a in A]
+    vA = [np.zeros_like(a) for a in A]
+    mB = [np.zeros_like(b) for b in B]
+    vB = [np.zeros_like(b) for b in B]
+    for t in (1, 2, 3):
+        Xb = W.to_bf16_bits(W.normal_f32(906, 100 + 2 * t, wl.N * wl.d_in, 1.0).reshape(wl.N, wl.d_in))
+        dYb = W.to_bf16_bits(W.normal_f32(906, 101 + 2 * t, wl.N * wl.d_out, 1.0).reshape(wl.N, wl.d_out))
+        X, dY = G.to_dev(Xb, wl.dtype), G.to_dev(dYb, wl.dtype)
+        Y = layer.forward(X, Wt)
+        dX = layer.backward(X, Wt, dY)
+        torch.cuda.synchronize()
+        got = dict(Y=G.from_dev(Y, wl.dtype), dX=G.from_dev(dX, wl.dtype),
+                   H=[h.cpu().numpy().astype(np.float64) for h in layer.h_blocks()],
+                   dH=[h.cpu().numpy().astype(np.float64) for h in layer.h_blocks(layer.dH)],
+                   dAt=[a.cpu().numpy().astype(np.float64) for a in layer.dAt],
+                   dBt=[b.cpu().numpy().astype(np.float64) for b in layer.dBt])
+        layer.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, t)
+        segs = [orc.Seg(o, n, A[j], B[j], wl.alphas[j]) for j, (o, n) in enumerate(zip(wl.offsets, wl.n_tokens))]
+        Xf, dYf = W.rows_as_f64(Xb, wl.dtype), W.rows_as_f64(dYb, wl.dtype)
+        Yo, Ho = orc.forward(Xf, Wm, segs)
+        dXo, dAo, dBo, dHo = orc.backward(Xf, Wm, dYf, segs)
+        for j in range(J):
+            A[j], mA[j], vA[j] = orc.adamw(A[j], dAo[j], mA[j], vA[j], wl.lr, wl.beta1, wl.beta2, wl.eps,
+                                           wl.weight_decay, t)
+            B[j], mB[j], vB[j] = orc.adamw(B[j], dBo[j], mB[j], vB[j], wl.lr, wl.beta1, wl.beta2, wl.eps,
+                                           wl.weight_decay, t)
+    torch.cuda.synchronize()
+    assert layer.sync_status() == M.MLORA_OK
+    got.update(At=[a.cpu().numpy().astype(np.float64) for a in layer.At],
+               Bt=[b.cpu().numpy().astype(np.float64) for b in layer.Bt],
+               mA=[a.cpu().numpy().astype(np.float64) for a in layer.mA],
+               vA=[a.cpu().numpy().astype(np.float64) for a in layer.vA],
+               mB=[b.cpu().numpy().astype(np.float64) for b in layer.mB],
+               vB=[b.cpu().numpy().astype(np.float64) for b in layer.vB])
+    want = dict(Y=Yo, dX=dXo, H=Ho, dH=dHo, dAt=[a.T for a in dAo], dBt=[b.T for b in dBo],
+                At=[a.T for a in A], Bt=[b.T for b in B], mA=[m.T for m in mA], vA=[v.T for v in vA],
+                mB=[m.T for m in mB], vB=[v.T for v in vB])
+    G.compare(got, want, G.TOL[wl.dtype])
+    layer.close()
