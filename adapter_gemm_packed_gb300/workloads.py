@@ -185,6 +185,14 @@ def llama8b_qproj() -> Workload:
                     [2.0 * r for r in ranks], w_std=0.02, a_std=(1.0 / 4096) ** 0.5, b_std=0.02)
 
 
+def llama8b_qproj_tiny_ranks() -> Workload:
+    """The q_proj shape and tokens with ranks {1,1,2,2,4,4,4,4}: the small-rank regime, where the
+    shrink, dH, dA and dB are matrix-vector-like products (r FLOP per byte of X or dY)."""
+    ranks = [1, 1, 2, 2, 4, 4, 4, 4]
+    return Workload("llama3_8b_q_proj_4096x4096_8ad_16384tok_r1-4", 53, 4096, 4096, "bf16", ranks, [2048] * 8,
+                    [2.0 * r for r in ranks], w_std=0.02, a_std=(1.0 / 4096) ** 0.5, b_std=0.02)
+
+
 def mlp_up_lognormal() -> Workload:
     """4096->14336 bf16, 16 adapters, ranks U{4..128}, tokens lognormal(7,1) rounded to 16, clipped [64,8192], alpha=16."""
     cfg = 3
@@ -277,6 +285,7 @@ CONFIGS = {
     "tiny": tiny_f32,
     "qproj_w4": llama8b_qproj_w4,
     "qproj": llama8b_qproj,
+    "qproj_tiny_ranks": llama8b_qproj_tiny_ranks,
     "mlp_up": mlp_up_lognormal,
     "many_small": llama70b_down_many_small,
     "qkv_shared": llama8b_qkv_shared,

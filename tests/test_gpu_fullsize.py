@@ -96,6 +96,10 @@ def test_qproj_llama8b_fullsize():
     check_fullsize(W.llama8b_qproj())
 
 
+def test_qproj_tiny_ranks_fullsize():
+    check_fullsize(W.llama8b_qproj_tiny_ranks())
+
+
 @pytest.mark.parametrize("fused", [False, True], ids=["expand", "fused"])
 def test_qproj_llama8b_w4_base_fullsize(fused):
     check_fullsize(W.llama8b_qproj_w4(), flags=M.MLORA_W4_FUSED if fused else 0)
