@@ -272,6 +272,14 @@ def llama8b_qkv_shared_small() -> Workload:
                           [[r, r, r] for r in q.ranks], [n // 8 for n in q.n_tokens], a_std=(1.0 / 4096) ** 0.5)
 
 
+def llama8b_layer_k_half() -> Workload:
+    """The Llama-3-8B k projection workload with half of each job's tokens (about 72K; dY 147 MB, still
+    above the L2), a case small enough for detailed profiler captures."""
+    k = llama8b_layer(1)
+    return custom("llama3_8b_layer_k_4096x1024_32ad_half", 54, 4096, 1024, k.ranks, [n // 2 for n in k.n_tokens],
+                  alphas=k.alphas, a_std=(1.0 / 4096) ** 0.5)
+
+
 def llama8b_qproj_w4() -> Workload:
     """The q_proj workload with a 4-bit base weight (int4 codes, fp32 scales per 64 inputs)."""
     wl = llama8b_qproj()
@@ -290,6 +298,7 @@ CONFIGS = {
     "many_small": llama70b_down_many_small,
     "qkv_shared": llama8b_qkv_shared,
     "qkv_shared_small": llama8b_qkv_shared_small,
+    "k_proj_half": llama8b_layer_k_half,
 }
 
 
