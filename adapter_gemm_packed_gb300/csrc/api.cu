@@ -43,9 +43,9 @@ cudaError_t launch_h_images(const DevSeg*, const float*, const MTile*, const int
 cudaError_t launch_adamw(const AdamItem*, int, float, float, float, float, float, int, int, cudaStream_t, bool,
                          __nv_bfloat16*, __nv_bfloat16*, int);
 cudaError_t launch_w4_expand(const void*, const float*, __nv_bfloat16*, int, int, int, cudaStream_t, bool);
-cudaError_t launch_f32_forward(const DevSeg*, int, long long, int, int, long long, const float*, const float*, float*,
-                               float*, cudaStream_t);
-cudaError_t launch_f32_backward(const DevSeg*, int, long long, int, int, long long, int, const float*, const float*,
+cudaError_t launch_f32_forward(const DevSeg*, int, long long, int, int, long long, int, int, const float*, const float*,
+                               float*, float*, cudaStream_t);
+cudaError_t launch_f32_backward(const DevSeg*, int, long long, int, int, long long, int, int, const float*, const float*,
                                 const float*, const float*, float*, float*, cudaStream_t);
 }  // namespace mlora
 
@@ -143,7 +143,7 @@ struct mlora_plan_s {
   std::vector<DevSeg> segs;             // one per job
   std::vector<DevSub> subs;             // one per user entry
   std::vector<float> col_scale;         // per packed column (chunk-padded), 0 in padding
-  int C_total = 0, n_chunks = 0, n_mtiles = 0, max_rank = 0;
+  int C_total = 0, n_chunks = 0, n_mtiles = 0, max_rank = 0, max_tokens = 0;
   long long n_images = 0, h_elems = 0;
   std::vector<MTile> mtiles;
   std::vector<int> img_tile;
@@ -311,6 +311,7 @@ void build_tables(mlora_plan_t* P) {
       sb.pad0 = sb.pad1 = 0;
       R += u.rank;
       P->max_rank = std::max(P->max_rank, u.rank);
+      P->max_tokens = std::max(P->max_tokens, u.n_tokens);
       if (!u.dAt || !u.dBt) P->can_backward = false;
       if (!u.dAt || !u.dBt || !u.mA || !u.vA || !u.mB || !u.vB) P->can_adamw = false;
     }
@@ -729,7 +730,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
   cudaError_t e;
   if (pr.dtype == MLORA_F32) {
     e = timed(P, K_F32_FWD, s, [&] { return launch_f32_forward(P->d_segs, P->n_jobs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems,
-                           static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<float*>(Y), H, s); });
+                           P->max_rank, P->max_tokens, static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<float*>(Y), H, s); });
     return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 forward launch");
   }
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -847,7 +848,7 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   const mlora_problem& pr = P->prob;
   cudaError_t e;
   if (pr.dtype == MLORA_F32) {
-    e = timed(P, K_F32_BWD, s, [&] { return launch_f32_backward(P->d_segs, P->n_jobs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems, P->max_rank,
+    e = timed(P, K_F32_BWD, s, [&] { return launch_f32_backward(P->d_segs, P->n_jobs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems, P->max_rank, P->max_tokens,
                             static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<const float*>(dY),
                             H, static_cast<float*>(dX), dH, s); });
     return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 backward launch");

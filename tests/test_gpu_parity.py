@@ -38,6 +38,23 @@ def test_tiny_f32_all_outputs():
     assert errs["Y"] < 1e-5
 
 
+F32_CASES = {
+    "ragged": dict(d_in=200, d_out=136, ranks=[1, 7, 64, 256], n_tokens=[70, 1, 129, 33]),
+    "tiles": dict(d_in=512, d_out=384, ranks=[16, 32, 3], n_tokens=[300, 64, 513]),
+    "one_job_rank256": dict(d_in=256, d_out=320, ranks=[256], n_tokens=[200]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(F32_CASES))
+def test_f32_cases(name):
+    """The fp32 path beyond the tiny workload: several 64 x 64 tiles, ragged rows and columns, a
+    one-token job, jobs straddling row tiles, ranks 1 to 256 (true fp32 arithmetic, 1e-4)."""
+    cfg = F32_CASES[name]
+    wl = W.custom(f"f32_{name}", 940 + sorted(F32_CASES).index(name), cfg["d_in"], cfg["d_out"], cfg["ranks"],
+                  cfg["n_tokens"], dtype="f32", w_std=0.05, b_std=0.05)
+    _run(wl)
+
+
 SMALL_BF16 = {
     "ragged_tail": dict(d_in=512, d_out=640, ranks=[1, 7, 64, 256], n_tokens=[200, 56, 300, 17]),
     "jobs_straddle_tiles": dict(d_in=256, d_out=384, ranks=[1, 2, 4, 8, 16, 32, 64, 128, 256, 3],
