@@ -193,6 +193,13 @@ def llama8b_qproj_tiny_ranks() -> Workload:
                     [2.0 * r for r in ranks], w_std=0.02, a_std=(1.0 / 4096) ** 0.5, b_std=0.02)
 
 
+def llama8b_qproj_f32() -> Workload:
+    """The q_proj workload with fp32 activations and weight (the true-fp32 FFMA path at a real size)."""
+    q = llama8b_qproj()
+    return Workload("llama3_8b_q_proj_4096x4096_8ad_16384tok_f32", 55, 4096, 4096, "f32", q.ranks, q.n_tokens,
+                    q.alphas, w_std=0.02, a_std=(1.0 / 4096) ** 0.5, b_std=0.02)
+
+
 def mlp_up_lognormal() -> Workload:
     """4096->14336 bf16, 16 adapters, ranks U{4..128}, tokens lognormal(7,1) rounded to 16, clipped [64,8192], alpha=16."""
     cfg = 3
@@ -294,6 +301,7 @@ CONFIGS = {
     "qproj_w4": llama8b_qproj_w4,
     "qproj": llama8b_qproj,
     "qproj_tiny_ranks": llama8b_qproj_tiny_ranks,
+    "qproj_f32": llama8b_qproj_f32,
     "mlp_up": mlp_up_lognormal,
     "many_small": llama70b_down_many_small,
     "qkv_shared": llama8b_qkv_shared,

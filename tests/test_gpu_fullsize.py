@@ -37,6 +37,19 @@ def sample_rows(wl, max_rows=768, seed=0):
     return np.unique(np.concatenate([np.array(rows, dtype=np.int64), extra]))
 
 
+def _step1_param(got_p, want_p, g, lr):
+    """A parameter after the first AdamW step, whose update is -lr g / (|g| + eps), about -lr sign(g)
+    (PyTorch's AdamW at t = 1).  Where the oracle's gradient entry lies within 1e-4 of the gradient's rms
+    of zero, the sign is not fixed by the arithmetic: the GPU's gradient, correct to rounding, may carry
+    either sign there.  Those entries are held to the update's own bound (the two sides at most 2 lr
+    apart, plus 1e-4 lr: with beta1, beta2 and the bias corrections held in fp32 the kernel's step is
+    lr (1 + ~7e-6)); the others are returned for the usual comparison."""
+    got_p, want_p, g = (np.asarray(x, np.float64) for x in (got_p, want_p, g))
+    near = np.abs(g) <= 1e-4 * np.sqrt(np.mean(g * g))
+    assert np.all(np.abs(got_p[near] - want_p[near]) <= 2 * lr * (1 + 1e-4))
+    return got_p[~near], want_p[~near]
+
+
 def check_fullsize(wl, step=True, flags=0):
     T = W.materialise(wl)
     run = G.GpuRun(wl, T, step=step, flags=flags)
@@ -80,7 +93,7 @@ def check_fullsize(wl, step=True, flags=0):
                 for name, p, gr, mk, vk in (("At", T.At[i], dA[0].T, "mA", "vA"), ("Bt", T.Bt[i], dB[0].T, "mB", "vB")):
                     p2, m2, v2 = orc.adamw(p.astype(np.float64), gr, 0.0, 0.0, wl.lr, wl.beta1, wl.beta2, wl.eps,
                                            wl.weight_decay, 1)
-                    cmp[name] = (got[name][i], p2)
+                    cmp[name] = _step1_param(got[name][i], p2, gr, wl.lr)
                     cmp[mk] = (got[mk][i], m2)
                     cmp[vk] = (got[vk][i], v2)
             for k, (a, b) in cmp.items():
@@ -98,6 +111,10 @@ def test_qproj_llama8b_fullsize():
 
 def test_qproj_tiny_ranks_fullsize():
     check_fullsize(W.llama8b_qproj_tiny_ranks())
+
+
+def test_qproj_f32_fullsize():
+    check_fullsize(W.llama8b_qproj_f32())
 
 
 @pytest.mark.parametrize("fused", [False, True], ids=["expand", "fused"])
