@@ -43,10 +43,10 @@ cudaError_t launch_h_images(const DevSeg*, const float*, const MTile*, const int
 cudaError_t launch_adamw(const AdamItem*, int, float, float, float, float, float, int, int, cudaStream_t, bool,
                          __nv_bfloat16*, __nv_bfloat16*, int);
 cudaError_t launch_w4_expand(const void*, const float*, __nv_bfloat16*, int, int, int, cudaStream_t, bool);
-cudaError_t launch_f32_forward(const DevSeg*, int, long long, int, int, long long, int, int, const float*, const float*,
-                               float*, float*, cudaStream_t);
-cudaError_t launch_f32_backward(const DevSeg*, int, long long, int, int, long long, int, int, const float*, const float*,
-                                const float*, const float*, float*, float*, cudaStream_t);
+cudaError_t launch_f32_forward(const DevSeg*, int, long long, int, int, long long, int, int, int, const float*,
+                               const float*, float*, float*, cudaStream_t);
+cudaError_t launch_f32_backward(const DevSeg*, int, long long, int, int, long long, int, int, int, const float*,
+                                const float*, const float*, const float*, float*, float*, cudaStream_t);
 }  // namespace mlora
 
 using namespace mlora;
@@ -730,7 +730,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
   cudaError_t e;
   if (pr.dtype == MLORA_F32) {
     e = timed(P, K_F32_FWD, s, [&] { return launch_f32_forward(P->d_segs, P->n_jobs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems,
-                           P->max_rank, P->max_tokens, static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<float*>(Y), H, s); });
+                           P->max_rank, P->max_tokens, P->num_sms, static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<float*>(Y), H, s); });
     return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 forward launch");
   }
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -848,7 +848,7 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   const mlora_problem& pr = P->prob;
   cudaError_t e;
   if (pr.dtype == MLORA_F32) {
-    e = timed(P, K_F32_BWD, s, [&] { return launch_f32_backward(P->d_segs, P->n_jobs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems, P->max_rank, P->max_tokens,
+    e = timed(P, K_F32_BWD, s, [&] { return launch_f32_backward(P->d_segs, P->n_jobs, pr.n_tokens, pr.d_in, pr.d_out, P->h_elems, P->max_rank, P->max_tokens, P->num_sms,
                             static_cast<const float*>(X), static_cast<const float*>(Wt), static_cast<const float*>(dY),
                             H, static_cast<float*>(dX), dH, s); });
     return e == cudaSuccess ? MLORA_OK : cuda_fail(e, "fp32 backward launch");

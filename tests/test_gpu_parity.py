@@ -42,6 +42,8 @@ F32_CASES = {
     "ragged": dict(d_in=200, d_out=136, ranks=[1, 7, 64, 256], n_tokens=[70, 1, 129, 33]),
     "tiles": dict(d_in=512, d_out=384, ranks=[16, 32, 3], n_tokens=[300, 64, 513]),
     "one_job_rank256": dict(d_in=256, d_out=320, ranks=[256], n_tokens=[200]),
+    # enough 128 x 128 tiles (33 x 11) for the large-tile base products in both directions
+    "large_tiles": dict(d_in=1292, d_out=1288, ranks=[16, 200, 1, 64], n_tokens=[1500, 1100, 37, 1500]),
 }
 
 
