@@ -192,6 +192,28 @@ struct mlora_plan_s {
   size_t ev_next = 0;
 };
 
+namespace mlora {
+// Forget whatever the plan recorded about `workspace` (shadows, staged images, 4-bit
+// expansion), so that its next forward or backward with that buffer rebuilds them.  For
+// scratch that other plans also write, which the plan's own bookkeeping cannot see.
+void forget_workspace(const mlora_plan_t* Pc, const void* workspace) {
+  mlora_plan_t* P = const_cast<mlora_plan_t*>(Pc);
+  if (P->shadows_ws == workspace) {
+    P->shadows_valid = false;
+    P->shadows_ws = nullptr;
+  }
+  if (P->staged_ws == workspace) {
+    P->staged_valid = false;
+    P->staged_ws = nullptr;
+    P->staged_H = nullptr;
+    P->staged_wq = nullptr;
+    P->staged_wscale = nullptr;
+  }
+}
+
+bool plan_is_w4(const mlora_plan_t* P) { return P->prob.dtype == MLORA_BF16_W4; }
+}  // namespace mlora
+
 namespace {
 
 mlora_status validate(const mlora_problem* p, const mlora_group* groups, int32_t n_groups, const mlora_segment* s,

@@ -29,7 +29,9 @@ void* g_ws_ptr[MAX_DEVICES] = {};
 }  // namespace
 
 namespace mlora {
-void set_last_error(const std::string& msg);   // api.cu
+void set_last_error(const std::string& msg);                            // api.cu
+void forget_workspace(const mlora_plan_t* plan, const void* workspace);   // api.cu
+bool plan_is_w4(const mlora_plan_t* plan);                              // api.cu
 }
 
 extern "C" {
@@ -39,6 +41,12 @@ mlora_status mlora_forward_static_ws(const mlora_plan_t* plan, const void* X, co
   if (!plan) {
     mlora::set_last_error("null plan");
     return MLORA_ERR_INVALID;
+  }
+  if (mlora::plan_is_w4(plan)) {
+    // a 4-bit base would also need its bf16 expansion (2 d_in d_out bytes) in the scratch
+    mlora::set_last_error("mlora_forward_static_ws: plans with a 4-bit base (MLORA_BF16_W4) are not supported; "
+                          "use mlora_forward_w4 with a caller workspace");
+    return MLORA_ERR_UNSUPPORTED;
   }
   // The forward needs the plan's workspace minus the backward-only image set.
   int64_t summ[12] = {0};
@@ -76,8 +84,12 @@ mlora_status mlora_forward_static_ws(const mlora_plan_t* plan, const void* X, co
     }
     ws = g_ws_ptr[dev];
   }
-  // Nothing in the forward's scratch needs to start at zero: every byte it reads was written
-  // earlier in the same call.
+  // Every plan on this device writes the same array, so what this plan left there may have been
+  // overwritten since: make the forward rebuild its bf16 shadows instead of trusting its record
+  // (MLORA_REUSE_STAGING would otherwise skip the pack and read another plan's adapters).  With
+  // that, nothing in the scratch needs to start at zero: every byte the forward reads was
+  // written earlier in the same call.
+  mlora::forget_workspace(plan, ws);
   return mlora_forward(plan, X, Wt, Y, H, ws, stream);
 }
 

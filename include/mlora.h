@@ -315,11 +315,14 @@ mlora_status mlora_shard_jobs(const mlora_problem* problem, const mlora_segment*
  * process exits.  This call allocates nothing (no cudaMalloc, cudaFree or allocating library
  * routine).  Its first call on a device looks up that array's device address on the current
  * device (a one-time set-up per device); make that first call before any stream capture.
- * Plans whose forward needs more scratch than 64 MiB are rejected with MLORA_ERR_UNSUPPORTED
- * and a message in mlora_last_error(); use mlora_forward for them.  All calls on a device
- * share the one array and it keeps the last call's contents (nothing in it needs to start at
- * zero): calls that overlap on the GPU (different streams without ordering between them)
- * race on it, so order them on one stream or with events. */
+ * Plans whose forward needs more scratch than 64 MiB, and plans with a 4-bit base
+ * (MLORA_BF16_W4), are rejected with MLORA_ERR_UNSUPPORTED and a message in
+ * mlora_last_error(); use mlora_forward / mlora_forward_w4 for them.  All calls on a device
+ * share the one array and it keeps the last call's contents: because another plan may have
+ * written it since, every call rebuilds the plan's bf16 adapter copies in it (MLORA_REUSE_STAGING
+ * never skips that step here), so nothing in it needs to start at zero.  Calls that overlap on
+ * the GPU (different streams without ordering between them) race on it, so order them on one
+ * stream or with events. */
 mlora_status mlora_forward_static_ws(const mlora_plan_t* plan, const void* X, const void* Wt, void* Y, float* H,
                                      void* stream);
 
