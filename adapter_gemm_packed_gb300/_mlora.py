@@ -31,7 +31,8 @@ EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward"
            "mlora_sync_status", "mlora_h_elems", "mlora_plan_describe", "mlora_status_string",
            "mlora_last_error", "mlora_version", "mlora_profile_enable", "mlora_profile_read",
            "mlora_kernel_name", "mlora_launch_count", "mlora_forward_static_ws", "mlora_memory_estimate",
-           "mlora_shard_jobs", "mlora_forward_w4", "mlora_backward_w4", "mlora_plan_grouped", "mlora_adamw_ws"]
+           "mlora_shard_jobs", "mlora_shard_jobs_multi", "mlora_forward_w4", "mlora_backward_w4",
+           "mlora_plan_grouped", "mlora_adamw_ws"]
 
 
 class mlora_segment(C.Structure):
@@ -118,6 +119,9 @@ def lib() -> C.CDLL:
         L.mlora_shard_jobs.argtypes = [C.POINTER(mlora_problem), C.POINTER(mlora_segment), i32, i32,
                                        C.POINTER(i32), C.POINTER(C.c_double)]
         L.mlora_shard_jobs.restype = i32
+        L.mlora_shard_jobs_multi.argtypes = [C.POINTER(mlora_problem), i32, C.POINTER(mlora_segment), i32, i32,
+                                             C.POINTER(i32), C.POINTER(C.c_double)]
+        L.mlora_shard_jobs_multi.restype = i32
         _lib = L
     return _lib
 
@@ -245,4 +249,15 @@ def mlora_shard_jobs(problem: mlora_problem, segs, n_ranks: int):
     ranks = (C.c_int32 * len(segs))()
     load = (C.c_double * n_ranks)()
     _check(lib().mlora_shard_jobs(C.byref(problem), arr, len(segs), n_ranks, ranks, load), "mlora_shard_jobs")
+    return list(ranks), list(load)
+
+
+def mlora_shard_jobs_multi(problems, segs, n_ranks: int):
+    """Jobs shared by several projections (one problem each). Returns (rank of each job, load per rank)."""
+    parr = (mlora_problem * len(problems))(*problems)
+    arr = (mlora_segment * len(segs))(*segs)
+    ranks = (C.c_int32 * len(segs))()
+    load = (C.c_double * n_ranks)()
+    _check(lib().mlora_shard_jobs_multi(parr, len(problems), arr, len(segs), n_ranks, ranks, load),
+           "mlora_shard_jobs_multi")
     return list(ranks), list(load)

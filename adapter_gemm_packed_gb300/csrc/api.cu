@@ -1188,16 +1188,24 @@ mlora_status mlora_memory_estimate(const mlora_plan_t* P, mlora_memory* out) {
   return MLORA_OK;
 }
 
-mlora_status mlora_shard_jobs(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
-                              int32_t n_ranks, int32_t* rank_of_job, double* load) {
-  if (!problem || !segs || !rank_of_job || n_segs < 1 || n_ranks < 1)
+mlora_status mlora_shard_jobs_multi(const mlora_problem* problems, int32_t n_problems, const mlora_segment* segs,
+                                    int32_t n_segs, int32_t n_ranks, int32_t* rank_of_job, double* load) {
+  if (!problems || n_problems < 1 || !segs || !rank_of_job || n_segs < 1 || n_ranks < 1)
     return fail(MLORA_ERR_INVALID, "bad arguments to mlora_shard_jobs");
-  const double din = problem->d_in, dout = problem->d_out;
+  // a job's share of one step: per projection, its tokens through the base products plus its
+  // three rank-r_i passes over (d_in + d_out)
+  double dd = 0.0, ds = 0.0;
+  for (int p = 0; p < n_problems; ++p) {
+    if (problems[p].d_in < 1 || problems[p].d_out < 1) return fail(MLORA_ERR_INVALID, "bad problem in mlora_shard_jobs");
+    dd += static_cast<double>(problems[p].d_in) * problems[p].d_out;
+    ds += static_cast<double>(problems[p].d_in) + problems[p].d_out;
+  }
   std::vector<std::pair<double, int>> cost(n_segs);
   for (int i = 0; i < n_segs; ++i) {
     if (segs[i].n_tokens < 1 || segs[i].rank < 1) return fail(MLORA_ERR_INVALID, "bad job in mlora_shard_jobs");
-    cost[i] = {static_cast<double>(segs[i].n_tokens) * (din * dout + 3.0 * segs[i].rank * (din + dout)), i};
+    cost[i] = {static_cast<double>(segs[i].n_tokens) * (dd + 3.0 * segs[i].rank * ds), i};
   }
+  // longest processing time first onto the least-loaded rank (ties: lowest job index, lowest rank)
   std::stable_sort(cost.begin(), cost.end(), [](const auto& a, const auto& b) { return a.first > b.first; });
   std::vector<double> l(n_ranks, 0.0);
   for (const auto& c : cost) {
@@ -1209,6 +1217,11 @@ mlora_status mlora_shard_jobs(const mlora_problem* problem, const mlora_segment*
   }
   if (load) std::copy(l.begin(), l.end(), load);
   return MLORA_OK;
+}
+
+mlora_status mlora_shard_jobs(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
+                              int32_t n_ranks, int32_t* rank_of_job, double* load) {
+  return mlora_shard_jobs_multi(problem, problem ? 1 : 0, segs, n_segs, n_ranks, rank_of_job, load);
 }
 
 const char* mlora_status_string(mlora_status s) {

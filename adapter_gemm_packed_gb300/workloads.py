@@ -73,6 +73,32 @@ def normal_f32(cfg_id: int, tensor_id: int, n: int, std: float) -> np.ndarray:
     return out
 
 
+def normal_range(cfg_id: int, tensor_id: int, lo: int, hi: int, std: float, bf16: bool = False) -> np.ndarray:
+    """Elements [lo, hi) of the tensor that ``normal_f32(cfg_id, tensor_id, n, std)`` draws (for any
+    n >= hi), drawing only the chunks that hold them; rounded to bf16 bit patterns if ``bf16``.
+    The values are those of the whole-tensor draw, element for element."""
+    out = np.empty(max(0, hi - lo), dtype=np.uint16 if bf16 else np.float32)
+    if hi <= lo:
+        return out
+    c0, c1 = lo // CHUNK, (hi - 1) // CHUNK + 1
+
+    def work(c: int) -> None:
+        a, b = max(lo, c * CHUNK), min(hi, (c + 1) * CHUNK)
+        seg = np.empty(min(b, (c + 1) * CHUNK) - c * CHUNK, dtype=np.float32)
+        rng(cfg_id, tensor_id, c).standard_normal(out=seg, dtype=np.float32)
+        part = seg[a - c * CHUNK:]
+        if std != 1.0:
+            part *= np.float32(std)
+        out[a - lo:b - lo] = to_bf16_bits(part) if bf16 else part
+
+    if c1 - c0 <= 1:
+        work(c0)
+    else:
+        with _cf.ThreadPoolExecutor(min(_threads(), c1 - c0)) as ex:
+            list(ex.map(work, range(c0, c1)))
+    return out
+
+
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 to bfloat16 (round to nearest, ties to even); returns uint16 bit patterns."""
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
@@ -311,8 +337,16 @@ CONFIGS = {
 
 
 def _act(wl: Workload, tid: int, n: int, std: float) -> np.ndarray:
-    x = normal_f32(wl.cfg_id, tid, n, std)
-    return x if wl.dtype == "f32" else to_bf16_bits(x)
+    # bf16 tensors are rounded chunk by chunk in the drawing threads: the same values as
+    # to_bf16_bits(normal_f32(...)), without the full-size fp32 intermediate
+    return normal_range(wl.cfg_id, tid, 0, n, std, bf16=wl.dtype != "f32")
+
+
+def _act_rows(wl: Workload, tid: int, width: int, rows, std: float) -> np.ndarray:
+    """Rows ``rows`` (a list of (first, count) runs) of a [N, width] activation tensor."""
+    parts = [normal_range(wl.cfg_id, tid, a * width, (a + k) * width, std, bf16=wl.dtype != "f32").reshape(k, width)
+             for a, k in rows]
+    return np.concatenate(parts) if parts else np.empty((0, width), np.uint16 if wl.dtype != "f32" else np.float32)
 
 
 T_WQ, T_WSCALE = 6, 7
@@ -347,6 +381,72 @@ def materialise(wl: Workload, with_dY: bool = True) -> Tensors:
     if wl.dtype == "bf16_w4":
         T.Wq, T.Wscale = w4_weight(wl)
     return T
+
+
+def materialise_jobs(wl: Workload, jobs=None, per_job: int | None = None):
+    """The pack made of jobs ``jobs`` of ``wl`` (indices, in that order; default all), each cut to
+    its first ``per_job`` tokens if given, with the values ``materialise(wl)`` would give those
+    rows and adapters.  Only the chunks holding the chosen rows are drawn.  Returns
+    ``(sub, T)``: the sub-pack's Workload (same seeds, its own token table) and its Tensors.
+    This is how a shard of a pack, or a bounded token sample of it, is built."""
+    jobs = list(range(len(wl.n_tokens))) if jobs is None else [int(j) for j in jobs]
+    G = wl.n_groups
+    offs = wl.offsets
+    toks = [wl.n_tokens[j] if per_job is None else min(per_job, wl.n_tokens[j]) for j in jobs]
+    runs = [(offs[j], k) for j, k in zip(jobs, toks)]
+    entries = [j * G + g for j in jobs for g in range(G)]
+    sub = Workload(wl.name, wl.cfg_id, wl.d_in, wl.d_out, wl.dtype, [wl.ranks[i] for i in entries], toks,
+                   [wl.alphas[i] for i in entries], wl.w_std, wl.a_std, wl.b_std, wl.lr, wl.beta1, wl.beta2, wl.eps,
+                   wl.weight_decay, None if wl.groups is None else list(wl.groups))
+    if wl.dtype == "bf16_w4":
+        Wt = None
+    else:
+        Wt = _act(wl, T_W, wl.d_out * wl.d_in, wl.w_std).reshape(wl.d_out, wl.d_in)
+    X = _act_rows(wl, T_X, wl.d_in, runs, 1.0)
+    dY = _act_rows(wl, T_DY, wl.d_out, runs, 1.0)
+    width = wl.entry_width
+    At = [normal_f32(wl.cfg_id, T_ADAPTER_BASE + 4 * i, wl.ranks[i] * wl.d_in, wl.a_std).reshape(wl.ranks[i], wl.d_in)
+          for i in entries]
+    Bt = [normal_f32(wl.cfg_id, T_ADAPTER_BASE + 4 * i + 1, width[i] * wl.ranks[i], wl.b_std)
+          .reshape(width[i], wl.ranks[i]) for i in entries]
+    T = Tensors(sub, Wt, X, dY, At, Bt)
+    if wl.dtype == "bf16_w4":
+        T.Wq, T.Wscale = w4_weight(wl)
+    return sub, T
+
+
+@dataclass
+class Layer:
+    """Several projections trained as one step (a decoder layer): each part is a Workload with
+    its own base weight, inputs and adapters; all parts share the job table (token counts and
+    ranks), so the layer's tokens per step are one part's N."""
+    name: str
+    parts: list
+
+    @property
+    def N(self) -> int:
+        return self.parts[0].N
+
+    @property
+    def n_tokens(self) -> list:
+        return self.parts[0].n_tokens
+
+    @property
+    def ranks(self) -> list:
+        return self.parts[0].ranks
+
+
+def llama8b_layer_all(token_div: int = 1) -> Layer:
+    """All seven projections of a Llama-3-8B decoder layer (q, k, v, o, gate, up, down) with the
+    32 jobs of the per-projection layer workloads: every job has the same rank and tokens on each
+    projection, and each projection its own X, dY and adapters.  ``token_div`` > 1 keeps
+    1/token_div of every job's tokens (own seeds), a smaller case of the same layer."""
+    parts = [llama8b_layer(p) for p in range(len(LLAMA8B_PROJ))]
+    if token_div != 1:
+        parts = [custom(f"{w.name}_div{token_div}", 60 + 8 * token_div + p, w.d_in, w.d_out, w.ranks,
+                        [n // token_div for n in w.n_tokens], alphas=w.alphas, a_std=w.a_std)
+                 for p, w in enumerate(parts)]
+    return Layer(f"llama3_8b_layer_7proj_32ad_{parts[0].N}tok", parts)
 
 
 def optimizer_state(wl: Workload, which: str, i: int, shape, kind: str) -> np.ndarray:

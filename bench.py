@@ -1,18 +1,22 @@
 #!/usr/bin/env python
 """Throughput of the packed multi-adapter LoRA layer: forward + backward + AdamW per step.
 
-Default workload: Llama-3-8B-shaped q_proj (d_in = d_out = 4096, bf16 activations and weight,
-fp32 adapter masters), 8 jobs with ranks {8,8,16,16,32,32,64,64}, 2048 tokens each (16384
-tokens per step).  One step = mlora_forward + mlora_backward + mlora_adamw over the whole pack
-with inputs resident in HBM.  Prints one JSON line (rank 0).
+Default workload: all seven projections of a Llama-3-8B decoder layer (q, k, v, o 4096 -> 4096 /
+1024; gate, up 4096 -> 14336; down 14336 -> 4096), bf16 activations and weights, fp32 adapter
+masters, 32 jobs with ranks in {8..128} and 1..8 sequences of 1024 tokens each (143,360 tokens
+per step), every job training one adapter on every projection.  One step = the forward of every
+projection (q .. down), the backward of every projection (down .. q) and the AdamW step of every
+adapter, through mlora_forward / mlora_backward / mlora_adamw_ws, with inputs resident in HBM.
+Prints one JSON line (rank 0).
 
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
   python bench.py --sweep        packed vs one plan per job vs a per-adapter PyTorch loop
 
 --impl reference times the fp64 CPU oracle (the reference arm of this metric) on a bounded
-sample of the same workload.  Under torchrun (N > 1) every rank runs its own replica of the
-workload (weak scaling, no collective on the data path); the barrier and max-over-ranks
-timing bracket the timed region.
+sample of the same workload.  Under torchrun (N > 1) the pack's jobs are split across the ranks
+(whole jobs, longest first onto the least-loaded rank, mlora_shard_jobs_multi); each rank trains
+only its jobs, there is no collective on the data path, and the value is the whole pack's
+tokens over the slowest rank's time (strong scaling: the pack is fixed as N grows).
 """
 from __future__ import annotations
 
@@ -30,6 +34,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "packed multi-LoRA fwd+bwd tokens/s and TFLOP/s per layer; % of bf16/HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DEFAULT_WORKLOAD = "layer"
+# a timed region longer than this runs into the part's power cap: GEMMs are rated against the
+# sustained bf16 figure, shorter regions against the burst one
+SUSTAINED_AFTER_MS = 1000.0
 
 
 def load_peaks():
@@ -43,11 +51,27 @@ def load_peaks():
 
 def workload(name):
     from adapter_gemm_packed_gb300 import workloads as W
+    if name == "layer":
+        return W.llama8b_layer_all()
+    if name == "layer_eighth":
+        return W.llama8b_layer_all(token_div=8)
     if name in W.CONFIGS:
         return W.CONFIGS[name]()
     if name.startswith("llama8b_layer_"):
         return W.llama8b_layer(int(name.rsplit("_", 1)[1]))
     raise SystemExit(f"unknown workload {name}")
+
+
+def parts_of(wl):
+    """The projections one step runs: the seven of a decoder layer, or the one workload."""
+    return list(wl.parts) if hasattr(wl, "parts") else [wl]
+
+
+def labels_of(wl):
+    from adapter_gemm_packed_gb300 import workloads as W
+    if hasattr(wl, "parts"):
+        return [W.LLAMA8B_PROJ[i][0] for i in range(len(wl.parts))]
+    return ["main"]
 
 
 def _entries(wl):
@@ -59,6 +83,8 @@ def _entries(wl):
 def flops_per_step(wl):
     # 4 N d_in d_out for the two base GEMMs, 6 n r (d_in + width) per adapter (shrink, expand,
     # dH, dB, dA, dX term); the zero padding and other projections' zero blocks are not counted
+    if hasattr(wl, "parts"):
+        return sum(flops_per_step(p) for p in wl.parts)
     return 4.0 * wl.N * wl.d_in * wl.d_out + sum(6.0 * n * r * (wl.d_in + w) for n, r, w in _entries(wl))
 
 
@@ -94,6 +120,28 @@ def kernel_bytes(wl, kernel):
         # codes (half a byte), scales (4 bytes per 64 weights) in; bf16 W^T out
         return wl.d_in * wl.d_out * (0.5 + 4 / 64 + 2)
     return None
+
+
+def job_ranks(wl):
+    """Each job's summed rank over the projections of a shared-input pack (its own rank otherwise)."""
+    G = wl.n_groups
+    return [sum(wl.ranks[j * G:(j + 1) * G]) for j in range(len(wl.n_tokens))]
+
+
+def shard(wl, world):
+    """Rank of every job of the pack: whole jobs, longest processing time first onto the
+    least-loaded rank, a job's cost summed over the step's projections (mlora_shard_jobs_multi).
+    Returns (rank_of_job, load per rank)."""
+    from adapter_gemm_packed_gb300 import _mlora as M
+    parts = parts_of(wl)
+    probs = [M.mlora_problem(p.N, p.d_in, p.d_out, M.MLORA_BF16, M.MLORA_PLAN_HOST_ONLY) for p in parts]
+    base = parts[0]
+    segs = [M.mlora_segment(o, n, r, 1.0) for o, n, r in zip(base.offsets, base.n_tokens, job_ranks(base))]
+    return M.mlora_shard_jobs_multi(probs, segs, world)
+
+
+def jobs_of_rank(rank_of_job, rank):
+    return [j for j, r in enumerate(rank_of_job) if r == rank]
 
 
 class ClockSampler:
@@ -182,9 +230,10 @@ def max_over_ranks(x: float, device=None) -> float:
     return float(t.item())
 
 
-def weak_scaling_rate(units_per_rank: int, world: int, steps: int, max_ms: float) -> float:
-    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
-    return units_per_rank * world * steps / (max_ms / 1e3)
+def pack_rate(units: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed together (the whole pack, split across
+    the ranks) over the slowest rank's time."""
+    return units * steps / (max_ms / 1e3)
 
 
 def link_probe(x_h, x_d, y_h, y_d, s_in, s_out, reps=3):
@@ -226,36 +275,36 @@ def link_probe(x_h, x_d, y_h, y_d, s_in, s_out, reps=3):
             "concurrent_gbs_per_direction": max(bx, by) / t_both / 1e9}
 
 
-def oracle_sample(wl, T, per_job):
-    """A bounded sample of the workload for the CPU oracle: the first `per_job` tokens of every job."""
+def oracle_sample(wl, per_job):
+    """A bounded sample of one projection for the CPU oracle: the first `per_job` tokens of every
+    job (only those rows are drawn).  Returns (sub-workload, X, W, dY, per-projection job lists,
+    tokens)."""
     import numpy as np
     from adapter_gemm_packed_gb300 import workloads as W
     from oracle import lora_oracle as orc
-    rows = np.concatenate([np.arange(o, o + min(per_job, n)) for o, n in zip(wl.offsets, wl.n_tokens)])
-    X = W.rows_as_f64(T.X[rows], wl.dtype)
-    dY = W.rows_as_f64(T.dY[rows], wl.dtype)
+    sub, T = W.materialise_jobs(wl, None, per_job)
+    X = W.rows_as_f64(T.X, wl.dtype)
+    dY = W.rows_as_f64(T.dY, wl.dtype)
     if wl.dtype == "bf16_w4":
         Wm = orc.dequantize_w4(T.Wq, T.Wscale)
     else:
         Wm = W.rows_as_f64(T.Wt, wl.dtype).T.copy()
-    # per projection (one unless the workload is a shared-input pack): its jobs' adapters
-    G = wl.n_groups
+    # per projection of a shared-input pack (one otherwise): its jobs' adapters
+    G = sub.n_groups
     segs = []
     for g in range(G):
-        sg, off = [], 0
-        for j, n in enumerate(wl.n_tokens):
-            k = min(per_job, n)
+        sg = []
+        for j, (o, n) in enumerate(zip(sub.offsets, sub.n_tokens)):
             i = j * G + g
-            sg.append(orc.Seg(off, k, T.At[i].astype(np.float64).T.copy(), T.Bt[i].astype(np.float64).T.copy(),
-                              wl.alphas[i]))
-            off += k
+            sg.append(orc.Seg(o, n, T.At[i].astype(np.float64).T.copy(), T.Bt[i].astype(np.float64).T.copy(),
+                              sub.alphas[i]))
         segs.append(sg)
-    return X, Wm, dY, segs, len(rows)
+    return sub, X, Wm, dY, segs, sub.N
 
 
 def oracle_step(wl, X, Wm, dY, segs, state, t):
-    """One oracle step: each projection's column slice with its adapters (Y side by side, dX
-    summed), then AdamW on every adapter."""
+    """One oracle step of one projection: each output group's column slice with its adapters
+    (Y side by side, dX summed), then AdamW on every adapter."""
     import numpy as np
     from oracle import lora_oracle as orc
     Y = np.zeros((X.shape[0], Wm.shape[1]))
@@ -272,36 +321,47 @@ def oracle_step(wl, X, Wm, dY, segs, state, t):
     return Y, dX
 
 
+class OracleLayer:
+    """The oracle's step over every projection of the workload, on a token sample."""
+
+    def __init__(self, wl, per_job):
+        self.samples = [oracle_sample(p, per_job) for p in parts_of(wl)]
+        self.tokens = self.samples[0][-1]
+        self.states = [{} for _ in self.samples]
+
+    def step(self, t):
+        for (sub, X, Wm, dY, segs, _), st in zip(self.samples, self.states):
+            oracle_step(sub, X, Wm, dY, segs, st, t)
+
+
 def cores_used():
     return os.cpu_count() or 1
 
 
 def run_reference(args, wl, rank):
-    """The reference arm of this metric: the fp64 CPU oracle on the host cores."""
+    """The reference arm of this metric: the fp64 CPU oracle on the host cores (rank 0 only)."""
     if rank != 0:
         return
-    from adapter_gemm_packed_gb300 import workloads as W
-    T = W.materialise(wl)
     # size each step's sample so the whole run stays near --ref-budget-s seconds
-    X, Wm, dY, segs, ntok = oracle_sample(wl, T, 8)
+    probe = OracleLayer(wl, 8)
     t0 = time.perf_counter()
-    oracle_step(wl, X, Wm, dY, segs, {}, 1)
-    per_tok = (time.perf_counter() - t0) / ntok
+    probe.step(1)
+    per_tok = (time.perf_counter() - t0) / probe.tokens
     budget = args.ref_budget_s / max(1, args.steps + args.warmup)
     per_job = int(max(1, min(args.ref_tokens_per_job, budget / per_tok / len(wl.n_tokens))))
-    X, Wm, dY, segs, ntok = oracle_sample(wl, T, per_job)
-    state = {}
+    orl = OracleLayer(wl, per_job)
     for t in range(1, args.warmup + 1):
-        oracle_step(wl, X, Wm, dY, segs, state, t)
+        orl.step(t)
     t0 = time.perf_counter()
     for t in range(args.warmup + 1, args.warmup + args.steps + 1):
-        oracle_step(wl, X, Wm, dY, segs, state, t)
+        orl.step(t)
     dt = time.perf_counter() - t0
-    value = ntok * args.steps / dt
-    sample = f"first {per_job} tokens of each of the {len(wl.n_tokens)} jobs ({ntok} tokens), full d_in x d_out"
+    value = orl.tokens * args.steps / dt
+    sample = (f"first {per_job} tokens of each of the {len(wl.n_tokens)} jobs ({orl.tokens} tokens) through every "
+              f"projection, full d_in x d_out")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded Philox)", "config": config_of(wl, args.gpus),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
                              "sample": sample},
@@ -309,13 +369,23 @@ def run_reference(args, wl, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_of(wl, ngpus, options=None):
-    c = {"workload": wl.name, "d_in": wl.d_in, "d_out": wl.d_out, "adapters": wl.n_adapters,
-         "ranks": wl.ranks, "tokens_per_step": wl.N, "dtype_io": wl.dtype, "parallelism": f"replicas x{ngpus}",
-         "l2": "inputs larger than L2 (X and dY are N x d bf16, each above the 129 MB L2)"
-         if wl.N * min(wl.d_in, wl.d_out) * 2 > 129e6 else "inputs smaller than L2"}
-    if options:
-        c["options"] = options
+def config_of(wl, ngpus):
+    """The workload as both arms report it (identical dicts)."""
+    parts = parts_of(wl)
+    p0 = parts[0]
+    c = {"workload": wl.name}
+    if hasattr(wl, "parts"):
+        c["projections"] = [{"name": n, "d_in": p.d_in, "d_out": p.d_out} for n, p in zip(labels_of(wl), parts)]
+        c["jobs"] = len(p0.n_tokens)
+        c["adapters"] = sum(p.n_adapters for p in parts)
+    else:
+        c["d_in"], c["d_out"] = p0.d_in, p0.d_out
+        c["adapters"] = p0.n_adapters
+    c.update({"ranks": p0.ranks, "tokens_per_step": wl.N, "dtype_io": p0.dtype,
+              "parallelism": "one GPU" if ngpus == 1 else
+              f"jobs sharded over {ngpus} GPUs (whole jobs, longest first; no collective)",
+              "l2": "inputs larger than L2 (X and dY are N x d bf16, each above the 129 MB L2)"
+              if p0.N * min(p0.d_in, p0.d_out) * 2 > 129e6 else "inputs smaller than L2"})
     return c
 
 
@@ -325,80 +395,164 @@ def options_of(wl, args):
         opts.append("MLORA_REUSE_STAGING (backward reuses the forward's bf16 shadows and staged H)")
     if args.window != "auto":
         opts.append({"pairs": "MLORA_WINDOW_PAIRS", "single": "MLORA_WINDOW_SINGLE"}[args.window])
-    if wl.dtype == "bf16_w4":
+    if parts_of(wl)[0].dtype == "bf16_w4":
         opts.append("MLORA_W4_FUSED (codes expanded inside the base GEMMs)" if args.w4_fused else
                     "4-bit base expanded to bf16 once per call, then the bf16 GEMMs")
     return "; ".join(opts) or None
 
 
-def traffic_record(kernel):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source."""
+def traffic_record(wl_name, kernel):
+    """DRAM bytes of one step's launches of `kernel` on workload `wl_name` from a committed ncu
+    summary, if it was taken on the current source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         rec = json.load(open(path))
     except Exception:
         return None
-    r = rec.get(kernel)
+    r = rec.get(f"{wl_name}:{kernel}")
     if not r:
         return None
-    src = open(os.path.join(ROOT, r["source"]), "rb").read()
-    if hashlib.sha256(src).hexdigest()[:16] != r.get("source_sha"):
-        return None
-    return r.get("bytes_per_launch")
+    for src, sha in r["sources"].items():
+        data = open(os.path.join(ROOT, src), "rb").read()
+        if hashlib.sha256(data).hexdigest()[:16] != sha:
+            return None
+    return r.get("bytes_per_step")
+
+
+class PartRun:
+    """One projection on this GPU: its plan and buffers (PackedLoRA), device-resident inputs and
+    the pinned host copies the end-to-end pass streams in."""
+
+    def __init__(self, wl, T, flags, label):
+        import numpy as np
+        import torch
+        from adapter_gemm_packed_gb300.layer import PackedLoRA
+        self.wl, self.label = wl, label
+        scales = [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
+        if wl.groups is None:
+            self.layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At,
+                                    Bt=T.Bt, flags=flags)
+        else:
+            # shared-input pack: one adapter per job and projection, the projections stacked in W
+            self.layer = PackedLoRA(wl.d_in, wl.d_out, wl.nest(wl.ranks), wl.n_tokens, wl.nest(scales),
+                                    dtype=wl.dtype, At=wl.nest(T.At), Bt=wl.nest(T.Bt), flags=flags,
+                                    groups=wl.groups)
+        tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
+
+        def host(a):
+            t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if wl.dtype != "f32" else torch.from_numpy(a)
+            return t.pin_memory()
+
+        self.X_h, self.dY_h = host(T.X), host(T.dY)
+        self.X, self.dY = self.X_h.cuda(), self.dY_h.cuda()
+        if wl.dtype == "bf16_w4":
+            self.Wt = (torch.from_numpy(T.Wq).cuda(), torch.from_numpy(T.Wscale).cuda())
+        else:
+            self.Wt = host(T.Wt).cuda()
+        self.Y = torch.empty((wl.N, wl.d_out), dtype=tdt, device="cuda")
+        self.dX = torch.empty((wl.N, wl.d_in), dtype=tdt, device="cuda")
+
+    def in_bytes(self):
+        return self.X.numel() * self.X.element_size() + self.dY.numel() * self.dY.element_size()
+
+    def out_bytes(self):
+        return self.Y.numel() * self.Y.element_size() + self.dX.numel() * self.dX.element_size()
+
+
+def layer_step(runs, t, bufs=None, stream=None):
+    """One training step of the layer: every projection's forward (first to last), every
+    backward (last to first), then every AdamW step.  `bufs[i]` = (X, dY, Y, dX) of run i."""
+    wl = runs[0].wl
+    io = bufs or [(r.X, r.dY, r.Y, r.dX) for r in runs]
+    for r, (X, dY, Y, dX) in zip(runs, io):
+        r.layer.forward(X, r.Wt, Y, stream=stream)
+    for r, (X, dY, Y, dX) in reversed(list(zip(runs, io))):
+        r.layer.backward(X, r.Wt, dY, dX, stream=stream)
+    for r in runs:
+        r.layer.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, t, stream=stream)
+
+
+def aggregate_kernels(runs, profs, steps, prof_step_ms, layered):
+    """Per kernel over all projections: time per step, launches, share, and the achieved rate of
+    its algorithmic FLOPs or bytes (their sum over the launches over the launches' summed time)."""
+    agg = {}
+    for r, prof in zip(runs, profs):
+        for k, (ms_k, n_k) in prof.items():
+            if n_k == 0:
+                continue
+            e = agg.setdefault(k, {"ms": 0.0, "launches": 0, "flops": 0.0, "bytes": 0.0, "by_projection": {}})
+            e["ms"] += ms_k
+            e["launches"] += n_k
+            f, b = kernel_flops(r.wl, k), kernel_bytes(r.wl, k)
+            pp = {"ms_per_launch": ms_k / n_k}
+            if f:
+                e["flops"] += f * n_k
+                pp["tflops"] = f / (ms_k / n_k * 1e-3) / 1e12
+            if b:
+                e["bytes"] += b * n_k
+                pp["gbs"] = b / (ms_k / n_k * 1e-3) / 1e9
+            e["by_projection"][r.label] = pp
+    out = {}
+    for k, e in agg.items():
+        v = {"ms_per_launch": e["ms"] / e["launches"], "launches": e["launches"],
+             "launches_per_step": e["launches"] / steps, "ms_per_step": e["ms"] / steps,
+             "share_of_step": e["ms"] / steps / prof_step_ms}
+        if e["flops"]:
+            v["tflops"] = e["flops"] / (e["ms"] * 1e-3) / 1e12
+        if e["bytes"]:
+            v["gbs"] = e["bytes"] / (e["ms"] * 1e-3) / 1e9
+        if layered:
+            v["by_projection"] = e["by_projection"]
+        out[k] = v
+    return out
 
 
 def run_ours(args, wl, rank, world, local_rank):
-    import numpy as np
     import torch
     from adapter_gemm_packed_gb300 import _mlora as M
     from adapter_gemm_packed_gb300 import workloads as W
-    from adapter_gemm_packed_gb300.layer import PackedLoRA
 
     dist = world > 1
     torch.cuda.set_device(local_rank)
-    T = W.materialise(wl)
-    scales = [np.float32(a) / np.float32(r) for a, r in zip(wl.alphas, wl.ranks)]
+    parts, labels = parts_of(wl), labels_of(wl)
+    layered = hasattr(wl, "parts")
     flags = (0 if args.no_reuse else M.MLORA_REUSE_STAGING) | (M.MLORA_W4_FUSED if args.w4_fused else 0)
     flags |= {"auto": 0, "pairs": M.MLORA_WINDOW_PAIRS, "single": M.MLORA_WINDOW_SINGLE}[args.window]
-    if wl.groups is None:
-        layer = PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, scales, dtype=wl.dtype, At=T.At, Bt=T.Bt,
-                           flags=flags)
-    else:
-        # shared-input pack: one adapter per job and projection, the projections stacked in W
-        layer = PackedLoRA(wl.d_in, wl.d_out, wl.nest(wl.ranks), wl.n_tokens, wl.nest(scales), dtype=wl.dtype,
-                           At=wl.nest(T.At), Bt=wl.nest(T.Bt), flags=flags, groups=wl.groups)
-    tdt = torch.float32 if wl.dtype == "f32" else torch.bfloat16
-
-    def host(a):
-        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if wl.dtype != "f32" else torch.from_numpy(a)
-        return t.pin_memory()
-
-    X_h, dY_h = host(T.X), host(T.dY)
-    X, dY = X_h.cuda(), dY_h.cuda()
-    if wl.dtype == "bf16_w4":
-        Wt = (torch.from_numpy(T.Wq).cuda(), torch.from_numpy(T.Wscale).cuda())
-    else:
-        Wt = host(T.Wt).cuda()
-    Y = torch.empty((wl.N, wl.d_out), dtype=tdt, device="cuda")
-    dX = torch.empty((wl.N, wl.d_in), dtype=tdt, device="cuda")
+    # this rank's jobs (all of them on one GPU)
+    rank_of_job, load = shard(wl, world)
+    mine = jobs_of_rank(rank_of_job, rank)
+    runs = []
+    for p, lab in zip(parts, labels):
+        if not mine:
+            break
+        if world == 1:
+            T = W.materialise(p)
+            sub = p
+        else:
+            sub, T = W.materialise_jobs(p, mine)
+        runs.append(PartRun(sub, T, flags, lab))
+        del T
     stream = torch.cuda.current_stream()
-    step_no = [0]
+    t_no = [0]
 
     def step():
-        step_no[0] += 1
-        layer.forward(X, Wt, Y)
-        layer.backward(X, Wt, dY, dX)
-        layer.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, step_no[0])
+        t_no[0] += 1
+        if runs:
+            layer_step(runs, t_no[0])
 
     def barrier():
         if dist:
             torch.distributed.barrier()
 
+    def check(where):
+        for r in runs:
+            if r.layer.sync_status() != M.MLORA_OK:
+                raise SystemExit(f"device status error {where} ({r.label})")
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    if layer.sync_status() != M.MLORA_OK:
-        raise SystemExit("device status error during warm-up")
+    check("during warm-up")
 
     # ---- timed region (device): K steps back to back on one stream
     launches0 = M.mlora_launch_count()
@@ -415,15 +569,16 @@ def run_ours(args, wl, rank, world, local_rank):
     barrier()
     ms = ev0.elapsed_time(ev1)
     launches = M.mlora_launch_count() - launches0
-    if layer.sync_status() != M.MLORA_OK:
-        raise SystemExit("device status error in the timed region")
+    check("in the timed region")
+    ms_rank = ms
     ms = max_over_ranks(ms, device="cuda")
 
     # ---- per-kernel times: the same K steps again with the library recording a CUDA event pair
     # around every launch on the launching stream (events between launches serialise them, so
     # this pass is kept out of the headline number)
-    M.mlora_profile_enable(layer.plan, True)
-    M.mlora_profile_read(layer.plan)
+    for r in runs:
+        M.mlora_profile_enable(r.layer.plan, True)
+        M.mlora_profile_read(r.layer.plan)
     torch.cuda.synchronize()
     p0 = torch.cuda.Event(enable_timing=True)
     p1 = torch.cuda.Event(enable_timing=True)
@@ -433,21 +588,21 @@ def run_ours(args, wl, rank, world, local_rank):
     p1.record(stream)
     torch.cuda.synchronize()
     prof_ms = p0.elapsed_time(p1)
-    prof = M.mlora_profile_read(layer.plan)
-    M.mlora_profile_enable(layer.plan, False)
+    profs = [M.mlora_profile_read(r.layer.plan) for r in runs]
+    for r in runs:
+        M.mlora_profile_enable(r.layer.plan, False)
 
-    # ---- end to end through the public API: every step copies its inputs X, dY from pinned
-    # host memory to the device and its results Y, dX back.  The copies of step i+1 / i-1 run
-    # on their own streams while step i computes (double-buffered device buffers, ordered by
-    # events), as an input pipeline of a training loop would.
+    # ---- end to end through the public API: every step copies every projection's inputs X, dY
+    # from pinned host memory to the device and its results Y, dX back.  The copies of step
+    # i+1 / i-1 run on their own streams while step i computes (double-buffered device buffers,
+    # ordered by events), as an input pipeline of a training loop would.
     e2e = None
-    if not args.no_e2e:
-        Y_h = torch.empty_like(Y, device="cpu").pin_memory()
-        dX_h = torch.empty_like(dX, device="cpu").pin_memory()
-        Xd = [X, torch.empty_like(X)]
-        dYd = [dY, torch.empty_like(dY)]
-        Yd = [Y, torch.empty_like(Y)]
-        dXd = [dX, torch.empty_like(dX)]
+    if not args.no_e2e and runs:
+        Y_h = [torch.empty_like(r.Y, device="cpu").pin_memory() for r in runs]
+        dX_h = [torch.empty_like(r.dX, device="cpu").pin_memory() for r in runs]
+        dev = [[(r.X, r.dY, r.Y, r.dX),
+                (torch.empty_like(r.X), torch.empty_like(r.dY), torch.empty_like(r.Y), torch.empty_like(r.dX))]
+               for r in runs]
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         ev = lambda: torch.cuda.Event()
         h2d_done = [ev(), ev()]
@@ -459,22 +614,22 @@ def run_ours(args, wl, rank, world, local_rank):
             b = i & 1
             with torch.cuda.stream(s_in):
                 if started[b]:
-                    s_in.wait_event(comp_done[b])        # step i-2 has finished reading Xd[b], dYd[b]
-                Xd[b].copy_(X_h, non_blocking=True)
-                dYd[b].copy_(dY_h, non_blocking=True)
+                    s_in.wait_event(comp_done[b])        # step i-2 has finished reading these inputs
+                for r, d in zip(runs, dev):
+                    d[b][0].copy_(r.X_h, non_blocking=True)
+                    d[b][1].copy_(r.dY_h, non_blocking=True)
                 h2d_done[b].record(s_in)
             stream.wait_event(h2d_done[b])
             if started[b]:
-                stream.wait_event(d2h_done[b])           # step i-2's results have left Yd[b], dXd[b]
-            step_no[0] += 1
-            layer.forward(Xd[b], Wt, Yd[b], stream=stream)
-            layer.backward(Xd[b], Wt, dYd[b], dXd[b], stream=stream)
-            layer.adamw(wl.lr, wl.beta1, wl.beta2, wl.eps, wl.weight_decay, step_no[0], stream=stream)
+                stream.wait_event(d2h_done[b])           # step i-2's results have left these outputs
+            t_no[0] += 1
+            layer_step(runs, t_no[0], [d[b] for d in dev], stream=stream)
             comp_done[b].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(comp_done[b])
-                Y_h.copy_(Yd[b], non_blocking=True)
-                dX_h.copy_(dXd[b], non_blocking=True)
+                for j, d in enumerate(dev):
+                    Y_h[j].copy_(d[b][2], non_blocking=True)
+                    dX_h[j].copy_(d[b][3], non_blocking=True)
                 d2h_done[b].record(s_out)
             started[b] = True
 
@@ -492,51 +647,53 @@ def run_ours(args, wl, rank, world, local_rank):
         torch.cuda.synchronize()
         barrier()
         ems = max_over_ranks(e0.elapsed_time(e1), device="cuda")
-        b_in = X.numel() * X.element_size() + dY.numel() * dY.element_size()
-        b_out = Y.numel() * Y.element_size() + dX.numel() * dX.element_size()
-        e2e = {"value": weak_scaling_rate(wl.N, world, args.steps, ems), "unit": "tokens/s",
+        b_in = sum(r.in_bytes() for r in runs)
+        b_out = sum(r.out_bytes() for r in runs)
+        e2e = {"value": pack_rate(wl.N, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": b_in, "d2h_bytes_per_step": b_out, "ms_per_step": ems / args.steps,
                "pipelined": "H2D and D2H copies on their own streams, double-buffered device buffers"}
+        if dist:
+            e2e["bytes_note"] = "h2d / d2h bytes are rank 0's share of the pack"
         # The host link bounds this number: measure it here (one direction at a time, then both at
-        # once, on X-sized pinned copies) and report the per-direction rate the pipeline reached.
-        link = link_probe(X_h, X, Y_h, Y, s_in, s_out)
+        # once, on the largest X-sized pinned copies) and report the per-direction rate reached.
+        big = max(runs, key=lambda r: r.X.numel())
+        link = link_probe(big.X_h, big.X, Y_h[runs.index(big)], big.Y, s_in, s_out)
         step_s = ems / args.steps / 1e3
         e2e["link"] = dict(link, achieved_h2d_gbs=b_in / step_s / 1e9, achieved_d2h_gbs=b_out / step_s / 1e9,
                            frac_of_concurrent=max(b_in, b_out) / step_s / 1e9 / link["concurrent_gbs_per_direction"])
-        if layer.sync_status() != M.MLORA_OK:
-            raise SystemExit("device status error in the end-to-end region")
+        check("in the end-to-end region")
 
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
-    kernels = {k: {"ms_per_launch": v[0] / v[1], "launches": v[1]} for k, v in prof.items() if v[1] > 0}
     step_ms = ms / args.steps
     prof_step_ms = prof_ms / args.steps
-    for k, v in kernels.items():
-        v["share_of_step"] = v["ms_per_launch"] * (v["launches"] / args.steps) / prof_step_ms
-        f = kernel_flops(wl, k)
-        b = kernel_bytes(wl, k)
-        if f:
-            v["tflops"] = f / (v["ms_per_launch"] * 1e-3) / 1e12
-        if b:
-            v["gbs"] = b / (v["ms_per_launch"] * 1e-3) / 1e9
-    if wl.dtype != "f32":
-        dom = max(("fwd_gemm", "bwd_gemm"), key=lambda k: kernels.get(k, {}).get("ms_per_launch", 0))
+    kernels = aggregate_kernels(runs, profs, args.steps, prof_step_ms, layered)
+    sustained = ms_rank >= SUSTAINED_AFTER_MS
+    if parts[0].dtype != "f32":
+        dom = max(("fwd_gemm", "bwd_gemm"), key=lambda k: kernels.get(k, {}).get("ms_per_step", 0))
         dk = kernels[dom]
-        # The burst figure is the larger (stricter) denominator; the sustained one is what a
-        # seconds-long power-capped loop reaches and is reported beside it.
-        peak = peaks.get("bf16_tflops")
-        sust = peaks.get("bf16_tflops_sustained")
+        burst, sust = peaks.get("bf16_tflops"), peaks.get("bf16_tflops_sustained")
+        peak = sust if (sustained and sust) else burst
         roof = {"kernel": dom, "bound": "tensor", "achieved": dk["tflops"], "peak": peak, "unit": "TFLOP/s",
-                "frac": dk["tflops"] / peak, "peak_source": f"{peak_src} bf16_tflops (burst cuBLAS GEMM)",
-                "frac_of_sustained": (dk["tflops"] / sust) if sust else None,
-                "traffic": traffic_record(dom)}
+                "frac": dk["tflops"] / peak,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (long power-capped loop; this timed region is "
+                               f"{ms_rank / 1e3:.1f} s)" if peak == sust else
+                               f"{peak_src} bf16_tflops (burst cuBLAS GEMM; this timed region is {ms_rank:.0f} ms)",
+                "frac_of_burst": dk["tflops"] / burst if burst else None,
+                "frac_of_sustained": dk["tflops"] / sust if sust else None,
+                "launches_per_step": dk["launches_per_step"],
+                "traffic": traffic_record(wl.name, dom)}
+        if layered:
+            roof["achieved_is"] = (f"algorithmic FLOPs of one step's {dom} launches (one per projection) over "
+                                   f"their summed CUDA-event time; traffic is those launches' DRAM bytes")
     else:
         # fp32 path: plain FFMA.  Peak = SMs x 128 FFMA lanes x 2 FLOP x max SM clock.
-        dom = max(kernels, key=lambda k: kernels[k]["ms_per_launch"] * kernels[k]["launches"])
-        nr = sum(n * r for n, r in zip(wl.n_tokens, wl.ranks))
-        f = {"f32_forward": 2.0 * wl.N * wl.d_in * wl.d_out + 2.0 * nr * (wl.d_in + wl.d_out),     # XW, XA, HB
-             "f32_backward": 2.0 * wl.N * wl.d_in * wl.d_out + 4.0 * nr * (wl.d_in + wl.d_out)}    # dYW^T, dH, dX_lora, dA, dB
+        p0 = parts[0]
+        dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
+        nr = sum(n * r for n, r in zip(p0.n_tokens, p0.ranks))
+        f = {"f32_forward": 2.0 * p0.N * p0.d_in * p0.d_out + 2.0 * nr * (p0.d_in + p0.d_out),     # XW, XA, HB
+             "f32_backward": 2.0 * p0.N * p0.d_in * p0.d_out + 4.0 * nr * (p0.d_in + p0.d_out)}    # dYW^T, dH, dX_lora, dA, dB
         sms = torch.cuda.get_device_properties(local_rank).multi_processor_count
         peak = sms * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         ach = f.get(dom, 0.0) / (kernels[dom]["ms_per_launch"] * 1e-3) / 1e12
@@ -546,35 +703,39 @@ def run_ours(args, wl, rank, world, local_rank):
     for k in ("shrink", "dH", "dA", "dB", "adamw", "w4_expand"):
         if k in kernels and "gbs" in kernels[k]:
             kernels[k]["frac_of_hbm"] = kernels[k]["gbs"] / hbm
-    value = weak_scaling_rate(wl.N, world, args.steps, ms)
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": {"bf16": "bf16", "f32": "f32", "bf16_w4": "bf16 (4-bit base)"}[wl.dtype],
+    line = {"metric": METRIC, "value": pack_rate(wl.N, args.steps, ms), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None,
+            "dtype": {"bf16": "bf16", "f32": "f32", "bf16_w4": "bf16 (4-bit base)"}[parts[0].dtype],
             "data": "synthetic (seeded Philox; shapes of the named workload, random-init adapters)",
-            "config": config_of(wl, world, options_of(wl, args)),
-            "tflops": flops_per_step(wl) * world * args.steps / (ms / 1e3) / 1e12,
+            "config": config_of(wl, world), "options": options_of(wl, args),
+            "tflops": flops_per_step(wl) * args.steps / (ms / 1e3) / 1e12,
             "roofline": roof, "kernels": kernels, "kernel_timing_ms_per_step": prof_step_ms,
-            "gpu_launches": launches, "e2e": e2e,
-            "clocks": clk.summary()}
+            "gpu_launches": launches, "e2e": e2e, "clocks": clk.summary()}
+    if dist:
+        toks = [sum(parts[0].n_tokens[j] for j in jobs_of_rank(rank_of_job, q)) for q in range(world)]
+        line["shard"] = {"jobs_per_rank": [len(jobs_of_rank(rank_of_job, q)) for q in range(world)],
+                         "tokens_per_rank": toks, "cost_balance_max_over_mean": max(load) / (sum(load) / world),
+                         "note": "kernels, gpu_launches and e2e bytes are rank 0's"}
     if not args.no_cpu_baseline and world == 1:
-        X_, Wm, dY_, segs, ntok = oracle_sample(wl, T, args.ref_tokens_per_job)
-        state, t, dt, reps = {}, 0, 0.0, 0
+        orl = OracleLayer(wl, args.ref_tokens_per_job)
+        t, reps = 0, 0
         t0 = time.perf_counter()
         while reps < 1 or (time.perf_counter() - t0 < args.cpu_seconds and reps < 50):
             t += 1
-            oracle_step(wl, X_, Wm, dY_, segs, state, t)
+            orl.step(t)
             reps += 1
         dt = time.perf_counter() - t0
-        line["cpu_baseline"] = {"value": ntok * reps / dt, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
-                                "sample": f"first {args.ref_tokens_per_job} tokens of each job ({ntok} tokens) x {reps} "
-                                          f"steps, fp64 numpy (BLAS threads = cores)"}
+        line["cpu_baseline"] = {"value": orl.tokens * reps / dt, "unit": "tokens/s", "cores": cores_used(),
+                                "kind": "oracle",
+                                "sample": f"first {args.ref_tokens_per_job} tokens of each job ({orl.tokens} tokens) "
+                                          f"through every projection x {reps} steps, fp64 numpy "
+                                          f"(BLAS threads = cores)"}
     print(json.dumps(line), flush=True)
-    layer.close()
+    for r in runs:
+        r.layer.close()
 
 
-# Packed-kernel sweep: the attention and MLP-up projections of Qwen-2.5-3B and -7B, rank 64, one
-# 1024-token sequence per job, 1 to 32 jobs (the setting of the packed-kernel microbenchmark in
-# "PLoRA: Efficient Concurrent LoRA Training for Large Language Models", §11.2.1).
 SWEEP_LAYERS = [("qwen2.5_3b_attn_2048x2048", 2048, 2048), ("qwen2.5_3b_mlp_up_2048x11008", 2048, 11008),
                 ("qwen2.5_7b_attn_3584x3584", 3584, 3584), ("qwen2.5_7b_mlp_up_3584x18944", 3584, 18944)]
 SWEEP_JOBS = [1, 2, 4, 8, 16, 32]
@@ -710,10 +871,11 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="qproj")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="layer (default: the 7 projections of a Llama-3-8B decoder layer), qproj, mlp_up, many_small, ...")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-reuse", action="store_true", help="rebuild the backward's staging (no MLORA_REUSE_STAGING)")
     ap.add_argument("--w4-fused", action="store_true", help="4-bit base: expand inside the GEMMs (MLORA_W4_FUSED)")

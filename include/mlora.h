@@ -305,6 +305,15 @@ mlora_status mlora_memory_estimate(const mlora_plan_t* plan, mlora_memory* out);
 mlora_status mlora_shard_jobs(const mlora_problem* problem, const mlora_segment* segs, int32_t n_segs,
                               int32_t n_ranks, int32_t* rank_of_job, double* load);
 
+/* mlora_shard_jobs for jobs that train one adapter on each of several projections with the same
+ * tokens and rank (the projections of a decoder layer, each its own problem): a job's cost is
+ * the sum over the n_problems projections of n_i (d_in d_out + 3 r_i (d_in + d_out)), and every
+ * projection of a job goes to the same rank.  segs holds one entry per job (tok_offset,
+ * n_tokens and rank are read; pointers are ignored).  mlora_shard_jobs is this call with one
+ * problem.  Host only. */
+mlora_status mlora_shard_jobs_multi(const mlora_problem* problems, int32_t n_problems, const mlora_segment* segs,
+                                    int32_t n_segs, int32_t n_ranks, int32_t* rank_of_job, double* load);
+
 /* Forward pass without a caller workspace, for callers that cannot allocate device memory
  * when they run the layer (a runtime that forbids cudaMalloc after start-up, a framework whose
  * memory comes only from its own pools, code running while another thread captures a graph).

@@ -1,7 +1,8 @@
 """The benchmark's JSON line: the keys and units every run prints, on both arms.
 
 The reference arm (the fp64 oracle on the host cores) runs on CPU; the GPU arm runs a short q_proj
-benchmark and checks the roofline, CPU-baseline, end-to-end, clock and launch-count records.
+benchmark and a short run of the seven-projection layer at an eighth of its tokens, and checks the
+roofline, CPU-baseline, end-to-end, clock and launch-count records.
 """
 import json
 import os
@@ -25,7 +26,7 @@ def _run(*argv, timeout=600):
 def _common(d, steps, warmup):
     assert d["metric"].startswith("packed multi-LoRA fwd+bwd tokens/s")
     assert d["unit"] == "tokens/s" and d["value"] > 0 and d["higher_is_better"] is True
-    assert d["steps"] == steps and d["warmup"] == warmup and d["n_gpus"] == 1 and d["scaling"] == "weak"
+    assert d["steps"] == steps and d["warmup"] == warmup and d["n_gpus"] == 1 and d["scaling"] == "strong"
     assert d["vs_baseline"] is None
     e = d["e2e"]
     assert set(e) >= {"value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"} and e["unit"] == "tokens/s"
@@ -46,9 +47,9 @@ def test_reference_arm_line():
 
 @pytest.mark.gpu
 def test_gpu_arm_line():
-    d = _run("--steps", "5", "--warmup", "3", "--cpu-seconds", "1")
+    d = _run("--workload", "qproj", "--steps", "5", "--warmup", "3", "--cpu-seconds", "1")
     _common(d, 5, 3)
-    assert "impl" not in d and d["dtype"] == "bf16"
+    assert "impl" not in d and d["dtype"] == "bf16" and "MLORA_REUSE_STAGING" in d["options"]
     assert d["config"]["workload"] == "llama3_8b_q_proj_4096x4096_8ad_16384tok"
     assert d["config"]["tokens_per_step"] == 16384
     assert d["ms_per_step"] == pytest.approx(16384 / d["value"] * 1e3, rel=1e-6)
@@ -66,6 +67,42 @@ def test_gpu_arm_line():
     clk = d["clocks"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
     assert set(d["kernels"]) >= {"shrink", "fwd_gemm", "dH", "dB", "bwd_gemm", "dA", "adamw"}
+
+
+def test_both_arms_report_the_same_config():
+    sys.path.insert(0, ROOT)
+    import bench
+    for name in ("tiny", "qproj", "layer"):
+        wl = bench.workload(name)
+        c = bench.config_of(wl, 1)
+        assert c == bench.config_of(bench.workload(name), 1) and "options" not in c
+        assert c["tokens_per_step"] == wl.N
+    c = bench.config_of(bench.workload("layer"), 1)
+    assert [p["name"] for p in c["projections"]] == ["q", "k", "v", "o", "gate", "up", "down"]
+    assert c["jobs"] == 32 and c["adapters"] == 7 * 32 and c["parallelism"] == "one GPU"
+
+
+@pytest.mark.gpu
+def test_gpu_arm_line_layer():
+    """The seven-projection layer (an eighth of its tokens): one step is every projection's forward,
+    backward and AdamW, each kernel aggregated over the projections."""
+    d = _run("--workload", "layer_eighth", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1",
+             "--ref-tokens-per-job", "4")
+    _common(d, 3, 3)
+    c = d["config"]
+    assert len(c["projections"]) == 7 and c["jobs"] == 32
+    assert d["ms_per_step"] == pytest.approx(c["tokens_per_step"] / d["value"] * 1e3, rel=1e-6)
+    # 7 launches per projection and step with staging reuse and the shadow refresh
+    assert d["gpu_launches"] == 7 * 7 * 3
+    r = d["roofline"]
+    assert r["kernel"] in ("fwd_gemm", "bwd_gemm") and r["launches_per_step"] == 7
+    for k in ("shrink", "fwd_gemm", "dH", "dB", "bwd_gemm", "dA", "adamw"):
+        assert d["kernels"][k]["launches_per_step"] == 7
+        assert set(d["kernels"][k]["by_projection"]) == {"q", "k", "v", "o", "gate", "up", "down"}
+    e = d["e2e"]
+    N = c["tokens_per_step"]
+    width_in = sum(p["d_in"] + p["d_out"] for p in c["projections"])
+    assert e["h2d_bytes_per_step"] == N * width_in * 2 == e["d2h_bytes_per_step"]
 
 
 def test_clock_summary_keeps_the_timed_region():
