@@ -24,7 +24,7 @@ MLORA_WINDOW_PAIRS = 128
 MLORA_WINDOW_SINGLE = 256
 MLORA_DEBUG_DROP_COPY = 16
 (MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD_B, MLORA_Q_WINDOW,
- MLORA_Q_ADAPTERS, MLORA_Q_WINDOW_PAIRS) = range(8)
+ MLORA_Q_ADAPTERS, MLORA_Q_WINDOW_PAIRS, MLORA_Q_GEMM_FWD, MLORA_Q_GEMM_BWD) = range(10)
 
 # every symbol include/mlora.h declares
 EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward", "mlora_adamw",

@@ -23,6 +23,7 @@
 
 #include "common.cuh"
 #include "mlora.h"
+#include "pair.cuh"
 
 namespace mlora {
 template <int MODE>
@@ -659,6 +660,35 @@ GemmArgs base_args(const mlora_plan_t* P) {
 
 int grid_of(const mlora_plan_t* P, int items) { return std::max(1, std::min(items, P->num_sms)); }
 
+// L2 room for the resident panel of a CTA-pair base GEMM's raster (see decode_pair).
+constexpr double RASTER_PANEL_BUDGET = 48.0 * (1 << 20);
+
+// Order and group size of a CTA-pair base GEMM's raster over its m_pairs x n_tiles full tiles
+// (K = the main product's reduction length).  Every 256-token pair reads a 256 x K panel of A and
+// every output tile a 256 x K panel of B (bf16).  A group of g tiles along one dimension keeps
+// its g panels in L2 while it sweeps the other dimension, so that dimension's panels are read
+// from HBM once per group: DRAM bytes ~ (resident side, once) + (swept side) x (groups).  The
+// resident panels must fit the L2 budget; groups are made equal.  Ties go to output-tile groups
+// (the weight stays resident).
+void set_raster(GemmArgs& g, int K) {
+  const double panel = 256.0 * K * 2.0;
+  const double budget = RASTER_PANEL_BUDGET;
+  const long long m_pairs = (g.n_mtiles + 1) / 2, n_tiles = g.n_tiles_n;
+  const long long gmax = std::max(1LL, static_cast<long long>(budget / panel));
+  double best = 0.0;
+  for (int by_n = 1; by_n >= 0; --by_n) {
+    const long long res = by_n ? n_tiles : m_pairs, swept = by_n ? m_pairs : n_tiles;
+    const long long groups = (res + std::min(res, gmax) - 1) / std::min(res, gmax);
+    const long long gsz = (res + groups - 1) / groups;
+    const double bytes = panel * (static_cast<double>(res) + static_cast<double>(swept) * groups);
+    if (by_n == 1 || bytes < best) {
+      best = bytes;
+      g.raster_n = by_n;
+      g.group_m = static_cast<int>(gsz);
+    }
+  }
+}
+
 mlora_status check_exec(const mlora_plan_t* P) {
   if (!P) return fail(MLORA_ERR_INVALID, "null plan");
   if (!P->on_device) return fail(MLORA_ERR_INVALID, "plan was built with MLORA_PLAN_HOST_ONLY");
@@ -823,6 +853,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
   g.n_tiles_n = (pr.d_out + BN - 1) / BN;
   g.out = Y;
   g.ld_out = pr.d_out;
+  if (pairs || fused4) set_raster(g, pr.d_in);   // the single-CTA engine keeps its M-tile groups
   if (fused4) {
     g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
     e = timed(P, K_FWD_GEMM, s, [&] {
@@ -962,6 +993,7 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   g.n_tiles_n = (pr.d_in + BN - 1) / BN;
   g.out = dX;
   g.ld_out = pr.d_in;
+  if (pairs || fused4) set_raster(g, pr.d_out);   // the single-CTA engine keeps its M-tile groups
   if (fused4) {
     g.n_items = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
     e = timed(P, K_BWD_GEMM, s, [&] {
@@ -1121,6 +1153,22 @@ mlora_status mlora_plan_describe(const mlora_plan_t* P, int32_t what, int64_t* o
     case MLORA_Q_ADAPTERS:
       for (const DevSub& sb : P->subs) v.insert(v.end(), {sb.job, sb.c0, sb.r, sb.o_lo, sb.o_hi});
       break;
+    case MLORA_Q_GEMM_FWD:
+    case MLORA_Q_GEMM_BWD: {
+      // the CTA-pair base GEMM's work list exactly as the kernels decode it
+      const bool fwd = what == MLORA_Q_GEMM_FWD;
+      GemmArgs g = base_args(P);
+      g.n_tiles_n = ((fwd ? P->prob.d_out : P->prob.d_in) + BN - 1) / BN;
+      set_raster(g, fwd ? P->prob.d_in : P->prob.d_out);
+      const int n_pairs = pair_gemm_items(P, g);
+      v = {g.raster_n, g.group_m, g.n_items, g.n_full_items, n_pairs};
+      for (int it = 0; it < g.n_items; ++it) {
+        int mp, col0, width;
+        pair::decode_item(g, it, mp, col0, width);
+        v.insert(v.end(), {mp, col0, width});
+      }
+      break;
+    }
     default:
       return fail(MLORA_ERR_INVALID, "unknown table");
   }

@@ -118,7 +118,8 @@ struct GemmArgs {
   int n_items;
   int n_tiles_n;       // FWD/BWD: output column tiles of 256
   int n_full_items;    // CTA-pair base GEMMs: items from here on are half-width tiles (see gemm_2sm.cu)
-  int group_m;         // FWD/BWD raster: M tiles per group
+  int group_m;         // FWD/BWD raster: tiles per group (token tiles, or output tiles if raster_n)
+  int raster_n;        // CTA-pair base GEMMs: 1 = groups of output tiles sweep the token pairs
   int n_mtiles;
   const MTile* mtiles;
   const WinItem* win;

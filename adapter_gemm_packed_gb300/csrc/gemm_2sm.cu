@@ -35,22 +35,6 @@ constexpr int A2_BYTES = 128 * BK * 2;        // this CTA's 128 rows of A per st
 constexpr int B2_BYTES = 128 * BK * 2;        // this CTA's 128-row half of B per stage
 constexpr int SMEM_2SM = S2 * (A2_BYTES + B2_BYTES) + 1024 + 256;
 
-// Item -> (token pair, first output column, width): full tiles in the raster order of
-// decode_pair, then the halves of the remaining tiles (two items each).
-__device__ __forceinline__ void decode_item(const GemmArgs& g, int item, int& mp, int& col0, int& width) {
-  int n;
-  if (item < g.n_full_items) {
-    decode_pair(g, item, mp, n);
-    col0 = n * BN;
-    width = BN;
-  } else {
-    const int j = item - g.n_full_items;
-    decode_pair(g, g.n_full_items + (j >> 1), mp, n);
-    col0 = n * BN + (j & 1) * (BN / 2);
-    width = BN / 2;
-  }
-}
-
 }  // namespace
 
 // tmB / tmE: 128-row boxes for the forward's K-major B halves; tmB64 / tmE64: the same tensors

@@ -90,17 +90,43 @@ __device__ __forceinline__ void bulk_signal_remote(uint32_t dst_cluster, const v
                : "memory");
 }
 
-__device__ __forceinline__ void decode_pair(const GemmArgs& g, int item, int& mp, int& n) {
+// Raster of the CTA-pair base GEMMs' full tiles.  Items are visited in groups of g.group_m
+// tiles along one dimension, sweeping the other: with raster_n == 0 a group is group_m token
+// pairs (m fastest) and the group's rows of A stay in L2 while it sweeps every output tile;
+// with raster_n == 1 a group is group_m output tiles (n fastest) and its columns of B (the
+// weight) stay in L2 while it sweeps every token pair.  The planner picks the order and the
+// group size per GEMM from the operands' panel sizes.
+__host__ __device__ __forceinline__ void decode_pair(const GemmArgs& g, int item, int& mp, int& n) {
   const int n_pairs = (g.n_mtiles + 1) >> 1;
-  const int per_group = g.group_m * g.n_tiles_n;
+  const int outer_total = g.raster_n ? n_pairs : g.n_tiles_n;     // swept dimension
+  const int inner_total = g.raster_n ? g.n_tiles_n : n_pairs;     // grouped dimension
+  const int per_group = g.group_m * outer_total;
   const int group = item / per_group;
   const int first = group * g.group_m;
-  const int gm = min(g.group_m, n_pairs - first);
+  const int gsz = inner_total - first < g.group_m ? inner_total - first : g.group_m;
   const int in_group = item - group * per_group;
-  mp = first + in_group % gm;
-  n = in_group / gm;
+  const int inner = first + in_group % gsz;
+  const int outer = in_group / gsz;
+  mp = g.raster_n ? outer : inner;
+  n = g.raster_n ? inner : outer;
 }
 
+
+// Item -> (token pair, first output column, width): full tiles in the raster order of
+// decode_pair, then the halves of the remaining tiles (two items each).
+__host__ __device__ __forceinline__ void decode_item(const GemmArgs& g, int item, int& mp, int& col0, int& width) {
+  int n;
+  if (item < g.n_full_items) {
+    decode_pair(g, item, mp, n);
+    col0 = n * BN;
+    width = BN;
+  } else {
+    const int j = item - g.n_full_items;
+    decode_pair(g, g.n_full_items + (j >> 1), mp, n);
+    col0 = n * BN + (j & 1) * (BN / 2);
+    width = BN / 2;
+  }
+}
 
 }  // namespace pair
 }  // namespace mlora

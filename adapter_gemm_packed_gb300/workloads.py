@@ -265,6 +265,15 @@ def llama70b_down_many_small() -> Workload:
                     [float(r) for r in ranks], w_std=0.02, a_std=(1.0 / 4096) ** 0.5, b_std=0.02)
 
 
+def llama70b_down_many_small_half() -> Workload:
+    """The first 64 jobs of the many-small-jobs workload (same shape, ranks and token counts; own
+    seeds): X 0.5 GB and dY 0.15 GB, still above the L2, about 4 GB on the device in all, a case
+    small enough for detailed profiler captures."""
+    full = llama70b_down_many_small()
+    return custom(full.name + "_half", 56, full.d_in, full.d_out, full.ranks[:64], full.n_tokens[:64],
+                  alphas=full.alphas[:64], a_std=full.a_std)
+
+
 def custom(name: str, cfg_id: int, d_in: int, d_out: int, ranks, n_tokens, alphas=None, dtype="bf16",
            w_std=0.02, a_std=None, b_std=0.02) -> Workload:
     """Ad-hoc workload for edge-case tests (ragged tails, rank 1, straddling segments...)."""
@@ -330,6 +339,7 @@ CONFIGS = {
     "qproj_f32": llama8b_qproj_f32,
     "mlp_up": mlp_up_lognormal,
     "many_small": llama70b_down_many_small,
+    "many_small_half": llama70b_down_many_small_half,
     "qkv_shared": llama8b_qkv_shared,
     "qkv_shared_small": llama8b_qkv_shared_small,
     "k_proj_half": llama8b_layer_k_half,

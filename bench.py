@@ -655,9 +655,13 @@ def run_ours(args, wl, rank, world, local_rank):
         if dist:
             e2e["bytes_note"] = "h2d / d2h bytes are rank 0's share of the pack"
         # The host link bounds this number: measure it here (one direction at a time, then both at
-        # once, on the largest X-sized pinned copies) and report the per-direction rate reached.
-        big = max(runs, key=lambda r: r.X.numel())
-        link = link_probe(big.X_h, big.X, Y_h[runs.index(big)], big.Y, s_in, s_out)
+        # once, on equal-sized pinned copies: the largest run's X and Y cut to the smaller of the
+        # two) and report the per-direction rate the pipeline reached.
+        big = max(runs, key=lambda r: min(r.X.numel(), r.Y.numel()))
+        n = min(big.X.numel(), big.Y.numel())
+        j = runs.index(big)
+        link = link_probe(big.X_h.view(-1)[:n], big.X.view(-1)[:n], Y_h[j].view(-1)[:n], big.Y.view(-1)[:n],
+                          s_in, s_out)
         step_s = ems / args.steps / 1e3
         e2e["link"] = dict(link, achieved_h2d_gbs=b_in / step_s / 1e9, achieved_d2h_gbs=b_out / step_s / 1e9,
                            frac_of_concurrent=max(b_in, b_out) / step_s / 1e9 / link["concurrent_gbs_per_direction"])

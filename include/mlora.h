@@ -248,7 +248,12 @@ int64_t mlora_h_elems(const mlora_plan_t* plan);
  *   MLORA_Q_ADAPTERS: per segment-table entry: job, first packed column, rank, first and end
  *                     output column of its B
  *   MLORA_Q_WINDOW_PAIRS: 1 if the shrink / dH run on CTA pairs, else 0; then per pair item:
- *                     pair, first chunk, chunks (even), first dH K slice, dH K slices */
+ *                     pair, first chunk, chunks (even), first dH K slice, dH K slices
+ *   MLORA_Q_GEMM_FWD / MLORA_Q_GEMM_BWD: the CTA-pair base GEMM's work list in launch order:
+ *                     raster order (1 = groups of output tiles sweep the token pairs, 0 = groups
+ *                     of token pairs sweep the output tiles), group size, items, full-width
+ *                     items, CTA pairs launched; then per item: token pair, first output column,
+ *                     width (256, or 128 for the halves of a split last wave) */
 #define MLORA_Q_SUMMARY 0
 #define MLORA_Q_MTILES 1
 #define MLORA_Q_COLUMNS 2
@@ -257,6 +262,8 @@ int64_t mlora_h_elems(const mlora_plan_t* plan);
 #define MLORA_Q_WINDOW 5
 #define MLORA_Q_ADAPTERS 6
 #define MLORA_Q_WINDOW_PAIRS 7
+#define MLORA_Q_GEMM_FWD 8
+#define MLORA_Q_GEMM_BWD 9
 mlora_status mlora_plan_describe(const mlora_plan_t* plan, int32_t what, int64_t* out, int64_t cap,
                                  int64_t* count);
 

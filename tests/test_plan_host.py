@@ -393,3 +393,51 @@ def test_window_engine_choice():
     assert pairs([128, 256], [1024, 1024])                   # 2 and 4 chunks per tile
     assert pairs([8, 8], [1024, 1024], M.MLORA_WINDOW_PAIRS)
     assert not pairs([128, 256], [1024, 1024], M.MLORA_WINDOW_SINGLE)
+
+
+def _gemm_list(plan, what):
+    v = M.mlora_plan_describe(plan, what)
+    head, items = v[:5], v[5:]
+    return head, [tuple(items[i:i + 3]) for i in range(0, len(items), 3)]
+
+
+@pytest.mark.parametrize("d_in,d_out,n_tokens", [
+    (4096, 4096, [2048] * 8),            # q_proj: the whole weight fits the L2 budget
+    (4096, 14336, [1024] * 20),          # MLP up / gate
+    (14336, 4096, [1024] * 20),          # down: K = 14336, small groups
+    (512, 384, [300, 100, 150, 77]),     # ragged, less than one wave (split tail)
+    (1024, 640, [130, 500, 333]),        # odd number of 128-token tiles
+])
+def test_base_gemm_work_list_covers_every_output_tile_once(d_in, d_out, n_tokens):
+    """The CTA-pair GEMMs' work list, decoded exactly as the kernels decode it, covers every
+    (256-token pair, output column) once, with full tiles first and half tiles only in a split
+    last wave; the raster keeps its resident panels inside the L2 budget."""
+    plan, _ = host_plan(d_in, d_out, [16] * len(n_tokens), n_tokens)
+    try:
+        for what, K, width in ((M.MLORA_Q_GEMM_FWD, d_in, d_out), (M.MLORA_Q_GEMM_BWD, d_out, d_in)):
+            (raster_n, group, n_items, n_full, n_pairs), items = _gemm_list(plan, what)
+            assert len(items) == n_items and 1 <= n_pairs <= 74
+            m_pairs = (-(-sum(n_tokens) // 128) + 1) // 2
+            n_tiles = -(-width // 256)
+            cover = np.zeros((m_pairs, n_tiles * 2), dtype=int)     # 128-column halves
+            for i, (mp, col0, w) in enumerate(items):
+                assert (w == 256) == (i < n_full) and col0 % 128 == 0
+                cover[mp, col0 // 128:(col0 + w) // 128] += 1
+            assert (cover == 1).all()
+            # resident panels: group x 256 x K bf16 within the 48 MiB budget (or a group of one)
+            assert raster_n in (0, 1) and 1 <= group <= (n_tiles if raster_n else m_pairs)
+            assert group == 1 or group * 256 * K * 2 <= 48 << 20
+    finally:
+        M.mlora_plan_destroy(plan)
+
+
+def test_base_gemm_raster_keeps_the_weight_resident():
+    """q_proj: the whole weight (16 output tiles, 32 MiB) is one resident group; the MLP's 56 output
+    tiles split into three equal groups of 19; the down projection's K = 14336 panels allow 6."""
+    for d_in, d_out, want in ((4096, 4096, (1, 16)), (4096, 14336, (1, 19)), (14336, 4096, (1, 6))):
+        plan, _ = host_plan(d_in, d_out, [16] * 20, [1024] * 20)
+        try:
+            (raster_n, group, *_), _ = _gemm_list(plan, M.MLORA_Q_GEMM_FWD)
+            assert (raster_n, group) == want
+        finally:
+            M.mlora_plan_destroy(plan)
