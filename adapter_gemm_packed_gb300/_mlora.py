@@ -23,6 +23,7 @@ MLORA_W4_FUSED = 64
 MLORA_WINDOW_PAIRS = 128
 MLORA_WINDOW_SINGLE = 256
 MLORA_DEBUG_DROP_COPY = 16
+MLORA_DEBUG_DROP_COPY_PAIRS = 512
 (MLORA_Q_SUMMARY, MLORA_Q_MTILES, MLORA_Q_COLUMNS, MLORA_Q_WGRAD_A, MLORA_Q_WGRAD_B, MLORA_Q_WINDOW,
  MLORA_Q_ADAPTERS, MLORA_Q_WINDOW_PAIRS, MLORA_Q_GEMM_FWD, MLORA_Q_GEMM_BWD) = range(10)
 

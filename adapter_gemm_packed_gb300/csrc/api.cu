@@ -176,7 +176,8 @@ struct mlora_plan_s {
   int* d_err = nullptr;
   unsigned long long timeout_ns = DEFAULT_TIMEOUT_NS;
   bool pdl = true;
-  bool debug_drop = false;
+  bool debug_drop = false;             // single-CTA shrink withholds one copy (test hook)
+  bool debug_drop_pairs = false;       // the forward's CTA-pair kernels withhold one copy (test hook)
   // what the last forward left in a workspace (used with MLORA_REUSE_STAGING)
   bool reuse_staging = false;
   bool staged_valid = false;
@@ -729,6 +730,8 @@ mlora_status mlora_plan_grouped(const mlora_problem* problem, const mlora_group*
   if (problem->flags & MLORA_W4_FUSED) P->w4_fused = true;
   // the copy-withholding test hook is honoured only with the 1 ms wait limit
   if ((problem->flags & MLORA_DEBUG_DROP_COPY) && (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT)) P->debug_drop = true;
+  if ((problem->flags & MLORA_DEBUG_DROP_COPY_PAIRS) && (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT))
+    P->debug_drop_pairs = true;
   build_tables(P);
   if (!(problem->flags & MLORA_PLAN_HOST_ONLY)) {
     st = upload(P);
@@ -838,6 +841,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
   if (P->win_pairs) {
     g.win = P->d_win2;
     g.n_items = static_cast<int>(P->win2.size());
+    g.debug_drop = P->debug_drop_pairs ? 1 : 0;
     e = timed(P, K_SHRINK, s, [&] {
       return launch_win_2sm<MODE_SHRINK>(mX, mAt, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
     });
@@ -861,6 +865,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
     });
   } else if (pairs) {
     const int n_pairs = pair_gemm_items(P, g);
+    g.debug_drop = P->debug_drop_pairs ? 1 : 0;
     e = timed(P, K_FWD_GEMM, s, [&] { return launch_gemm_2sm<MODE_FWD>(mX, mW, mBt, mI, mW64, mBt64, g, n_pairs, s); });
   } else {
     g.n_items = P->n_mtiles * g.n_tiles_n;

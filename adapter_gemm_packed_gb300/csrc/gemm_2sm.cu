@@ -57,6 +57,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* done = tempty + 2;         // [1]   (even CTA) MMA drain at teardown
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* ring_hi = tmem_slot + 2;   // (even CTA) ring positions filled, max over both producers
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -74,6 +75,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     }
     mbar_init(done, 1);
     *abort_flag = 0;
+    *ring_hi = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -97,6 +99,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t filled = 0;
       bool ok = true;
       for (int item = pair; ok && item < g.n_items; item += n_pairs_grid) {
         int mp, col0, width;
@@ -116,7 +119,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
           uint8_t* a = sA + stage * A2_BYTES;
           uint8_t* b = sB + stage * B2_BYTES;
-          if (kb < g.kmain) {
+          ++filled;
+          if (g.debug_drop && leader && pair == 0 && filled == 1) {
+            // Test hook for the timeout path: the slot is armed for both CTAs' bytes but this CTA
+            // copies nothing into it, so the MMA's bounded wait runs out and records a status
+            // code; the teardown drain then waits out the peer's copies.  Nothing faults or hangs.
+          } else if (kb < g.kmain) {
             tma_load_2d_pair(a, &tmA, bar, kb * BK, m0);
             if constexpr (MODE == MODE_FWD) {
               tma_load_2d_pair(b, half ? &tmB64 : &tmB, bar, kb * BK, nh0);
@@ -140,6 +148,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
+      publish_ring_pos(ring_hi, filled);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -242,13 +251,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     }
   }
 
-  if (*abort_flag) {
-    // Give copies already issued by this CTA time to land before its shared memory goes away.
-    const unsigned long long t0 = global_timer_ns();
-    while (global_timer_ns() - t0 < 50000ull) {
-    }
-  }
+  // No copy is issued after this barrier; the even CTA then waits for the last ring positions'
+  // copies (both CTAs') to land, and the odd CTA's shared memory stays alive until it has.
   tc_fence_before();
+  cluster_sync_all();
+  if (leader && threadIdx.x == 0) drain_ring<S2>(full, *reinterpret_cast<volatile uint32_t*>(ring_hi), g.err, tmo);
+  __syncwarp();
   cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();

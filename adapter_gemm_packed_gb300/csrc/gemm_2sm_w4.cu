@@ -126,6 +126,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
   uint64_t* done = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* ring_hi = tmem_slot + 2;   // (even CTA) main-ring positions filled, max over every issuer
   uint8_t* sig_dst = reinterpret_cast<uint8_t*>(bars) + 1024;    // [N_SIG][16] (even CTA) signal landing slots
   uint8_t* sig_src = sig_dst + N_SIG * SIG_BYTES;               // [16] this CTA's signal payload
 
@@ -149,6 +150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
     }
     mbar_init(done, 1);
     *abort_flag = 0;
+    *ring_hi = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmQ);
@@ -169,6 +171,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t filled = 0;
       bool ok = true;
       for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
         int mp, n;
@@ -188,6 +191,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
             mbar_arrive_expect_tx(&full[stage], 2 * A_BYTES + (main_part ? 0 : 2 * B_BYTES) + N_SIG * SIG_BYTES);
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
           uint8_t* a = sA + stage * A_BYTES;
+          ++filled;
           if (main_part) {
             tma_load_2d_pair(a, &tmA, bar, kb * BK, m0);
           } else {
@@ -207,6 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
           }
         }
       }
+      publish_ring_pos(ring_hi, filled);
     }
   } else if (warp == RAWP_WARP) {
     if (lane == 0) {
@@ -214,6 +219,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
       const uint64_t keep = l2_policy_evict_last();
       int rs = 0;
       uint32_t rphase = 0;
+      uint32_t rfilled = 0;
       bool ok = true;
       for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
         int mp, n;
@@ -225,6 +231,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&qfull[rs], RAW_BYTES + SC_BYTES);
+          ++rfilled;
           if constexpr (MODE == MODE_FWD) {
             tma_load_2d_hint(sQ + rs * RAW_BYTES, &tmQ, &qfull[rs], kb * (BK / 2), nh0, keep);
             tma_load_2d_hint(sS + rs * SC_BYTES, &tmS, &qfull[rs], nh0, kb, keep);
@@ -238,6 +245,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
           }
         }
       }
+      // This CTA's own ring: slot p % RW was re-filled only after the converters released it, so
+      // the copies of every position but the last RW have landed; wait (bounded) for those.
+      volatile int no_abort = 0;
+      for (uint32_t p = rfilled > RW ? rfilled - RW : 0; p < rfilled; ++p)
+        if (!mbar_wait(&qfull[p % RW], (p / RW) & 1u, &no_abort, g.err, DEV_ERR_TIMEOUT_TEARDOWN, tmo)) break;
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -348,6 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
     const uint64_t magic2 = w4::magic_pair();
     int stage = 0, rs = 0;
     uint32_t phase = 0, rphase = 0;
+    uint32_t filled = 0;
     bool ok = true;
     for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
       int mp, n;
@@ -390,20 +403,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4_THREADS, 1)
         }
         __syncwarp();
         if (lane == 0) bulk_signal_remote(my_sig, sig_src, mapa_shared(smem_u32(&full[stage]), 0));
+        ++filled;
         if (++stage == SW) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
+    if (lane == 0) publish_ring_pos(ring_hi, filled);
   }
 
-  if (*abort_flag) {
-    const unsigned long long t0 = global_timer_ns();
-    while (global_timer_ns() - t0 < 50000ull) {
-    }
-  }
+  // No copy or signal is issued after this barrier; the even CTA then waits for the last main-ring
+  // positions (both CTAs' copies and converter signals) to land, and the odd CTA's shared memory
+  // stays alive until it has.
   tc_fence_before();
+  cluster_sync_all();
+  if (leader && threadIdx.x == 0) drain_ring<SW>(full, *reinterpret_cast<volatile uint32_t*>(ring_hi), g.err, tmo);
+  __syncwarp();
   cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();

@@ -90,6 +90,30 @@ __device__ __forceinline__ void bulk_signal_remote(uint32_t dst_cluster, const v
                : "memory");
 }
 
+// Teardown of a CTA pair's main ring.  Every copy into a ring slot, whichever CTA issues it,
+// counts on the even CTA's full barrier of that slot, and every issuer fills ring position p only
+// after the MMA released position p - S.  So once no thread can issue any more (a cluster barrier
+// after all roles have finished), the copies of every position below hi - S have landed, where hi
+// is one past the highest position any issuer of either CTA filled.  Each issuer publishes its
+// count of filled positions into the even CTA's `ring_hi` (cluster-scope max) before that barrier.
+__device__ __forceinline__ void publish_ring_pos(uint32_t* ring_hi, uint32_t filled) {
+  const uint32_t addr = mapa_shared(smem_u32(ring_hi), 0);
+  asm volatile("red.release.cluster.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(filled) : "memory");
+}
+
+// Then the even CTA waits, position by position and bounded, for the last S positions' full
+// barriers (position p is slot p % S, phase parity (p / S) & 1; older phases of the same slot have
+// completed, so the parity names the right phase).  A position whose copies were not all issued
+// never completes: its wait gives up after the timeout, by which time everything issued before
+// the barrier has landed, so the remaining positions need no wait.  The final cluster barrier
+// keeps the odd CTA's shared memory alive until this drain has finished.
+template <int S>
+__device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t hi, int* err, unsigned long long timeout_ns) {
+  volatile int no_abort = 0;
+  for (uint32_t p = hi > S ? hi - S : 0; p < hi; ++p)
+    if (!mbar_wait(&full[p % S], (p / S) & 1u, &no_abort, err, DEV_ERR_TIMEOUT_TEARDOWN, timeout_ns)) break;
+}
+
 // Raster of the CTA-pair base GEMMs' full tiles.  Items are visited in groups of g.group_m
 // tiles along one dimension, sweeping the other: with raster_n == 0 a group is group_m token
 // pairs (m fastest) and the group's rows of A stay in L2 while it sweeps every output tile;

@@ -57,6 +57,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* done = tempty + 2;         // [1]   (even CTA) MMA drain at teardown
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* ring_hi = tmem_slot + 2;   // (even CTA) ring positions filled, max over both producers
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -74,6 +75,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     }
     mbar_init(done, 1);
     *abort_flag = 0;
+    *ring_hi = 0;
     fence_mbar_init();
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
@@ -93,6 +95,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       const uint64_t pol_keep = l2_policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t filled = 0;
       bool ok = true;
       for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
         const WinItem w = g.win[item];
@@ -109,13 +112,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (WA_BYTES + nb * CHUNK_COLS * BK * 2));
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
           const int k = kb0 + kb;
-          tma_load_2d_pair_hint(sA + stage * WA_BYTES, &tmA, bar, k * BK, m0, pol_stream);
-          uint8_t* b = sB + stage * WB_BYTES;
-          for (int j = 0; j < nb; ++j) {
-            if constexpr (MODE == MODE_SHRINK)   // At_all rows (K-major, k = d_in)
-              tma_load_2d_pair_hint(b + j * (CHUNK_COLS * BK * 2), &tmB, bar, k * BK, (qb + j) * CHUNK_COLS, pol_keep);
-            else                                 // Bt_all [d_out, C] as MN-major (n = rank column, k = d_out)
-              tma_load_2d_pair_hint(b + j * (CHUNK_COLS * BK * 2), &tmB, bar, (qb + j) * CHUNK_COLS, k * BK, pol_keep);
+          ++filled;
+          if (g.debug_drop && leader && pair_id == 0 && filled == 1) {
+            // Test hook for the timeout path (see gemm_2sm.cu): armed, nothing copied by this CTA.
+          } else {
+            tma_load_2d_pair_hint(sA + stage * WA_BYTES, &tmA, bar, k * BK, m0, pol_stream);
+            uint8_t* b = sB + stage * WB_BYTES;
+            for (int j = 0; j < nb; ++j) {
+              if constexpr (MODE == MODE_SHRINK)   // At_all rows (K-major, k = d_in)
+                tma_load_2d_pair_hint(b + j * (CHUNK_COLS * BK * 2), &tmB, bar, k * BK, (qb + j) * CHUNK_COLS, pol_keep);
+              else                                 // Bt_all [d_out, C] as MN-major (n = rank column, k = d_out)
+                tma_load_2d_pair_hint(b + j * (CHUNK_COLS * BK * 2), &tmB, bar, (qb + j) * CHUNK_COLS, k * BK, pol_keep);
+            }
           }
           if (++stage == SW2) {
             stage = 0;
@@ -123,6 +131,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
+      publish_ring_pos(ring_hi, filled);
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
@@ -262,13 +271,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     }
   }
 
-  if (*abort_flag) {
-    // Give copies already issued by this CTA time to land before its shared memory goes away.
-    const unsigned long long t0 = global_timer_ns();
-    while (global_timer_ns() - t0 < 50000ull) {
-    }
-  }
+  // No copy is issued after this barrier; the even CTA then waits for the last ring positions'
+  // copies (both CTAs') to land, and the odd CTA's shared memory stays alive until it has.
   tc_fence_before();
+  cluster_sync_all();
+  if (leader && threadIdx.x == 0) drain_ring<SW2>(full, *reinterpret_cast<volatile uint32_t*>(ring_hi), g.err, tmo);
+  __syncwarp();
   cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();

@@ -77,6 +77,13 @@ typedef enum mlora_dtype {
                                           but copies nothing into it, so a device wait runs out (~1 ms),
                                           the status word records it and mlora_sync_status() returns
                                           MLORA_ERR_TIMEOUT; that call's outputs are undefined */
+#define MLORA_DEBUG_DROP_COPY_PAIRS 512u  /* test hook, honoured only with MLORA_DEBUG_SHORT_TIMEOUT: in the
+                                          forward's CTA-pair kernels (the shrink when it runs on pairs, and
+                                          the base GEMM) the first pair's even CTA arms its first pipeline
+                                          slot for both CTAs' bytes but copies nothing into it; the MMA's
+                                          wait runs out (~1 ms), each kernel drains its peer's copies and
+                                          returns, and mlora_sync_status() returns MLORA_ERR_TIMEOUT; that
+                                          call's outputs are undefined */
 #define MLORA_REUSE_STAGING 32u       /* mlora_backward skips rebuilding the bf16 adapter shadows and the
                                           staged s*H images when its workspace and H are the ones the last
                                           mlora_forward of this plan used and no AdamW step ran since (and,

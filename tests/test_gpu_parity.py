@@ -210,6 +210,29 @@ def test_device_wait_timeout_is_reported_and_context_survives():
     _run(wl)                                           # the context is still usable
 
 
+@pytest.mark.parametrize("window", ["pairs", "single"])
+def test_pair_kernel_wait_timeout_drains_and_context_survives(window):
+    """The same for the forward's CTA-pair kernels (test hook: the first pair's even CTA arms its
+    first slot for both CTAs' bytes but copies nothing).  With the shrink forced onto pairs both
+    the shrink and the base GEMM give up; otherwise only the base GEMM does.  Each kernel's MMA
+    wait runs out, its teardown waits (bounded) for the ring's outstanding copies, including the
+    odd CTA's, before either CTA's shared memory goes away; the status reads MLORA_ERR_TIMEOUT once,
+    and a normal plan afterwards computes correct results."""
+    wl = W.custom("timeout_pairs", 956, 512, 384, [8, 64, 130], [300, 100, 150], dtype="bf16")
+    T = W.materialise(wl)
+    flags = M.MLORA_DEBUG_SHORT_TIMEOUT | M.MLORA_DEBUG_DROP_COPY_PAIRS
+    flags |= M.MLORA_WINDOW_PAIRS if window == "pairs" else M.MLORA_WINDOW_SINGLE
+    bad = G.PackedLoRA(wl.d_in, wl.d_out, wl.ranks, wl.n_tokens, G.scales_of(wl), dtype="bf16", At=T.At, Bt=T.Bt,
+                       flags=flags)
+    try:
+        bad.forward(G.to_dev(T.X, "bf16"), G.to_dev(T.Wt, "bf16"))
+        assert bad.sync_status() == M.MLORA_ERR_TIMEOUT
+        assert bad.sync_status() == M.MLORA_OK
+    finally:
+        bad.close()
+    _run(wl)
+
+
 @pytest.mark.parametrize("grouped", [False, True], ids=["one_group", "qkv_groups"])
 def test_adamw_shadow_refresh_matches_repacking(grouped):
     """Three steps with MLORA_REUSE_STAGING and mlora_adamw_ws (the forward reuses the shadows the
