@@ -33,7 +33,7 @@ EXPORTS = ["mlora_plan", "mlora_plan_destroy", "mlora_forward", "mlora_backward"
            "mlora_last_error", "mlora_version", "mlora_profile_enable", "mlora_profile_read",
            "mlora_kernel_name", "mlora_launch_count", "mlora_forward_static_ws", "mlora_memory_estimate",
            "mlora_shard_jobs", "mlora_shard_jobs_multi", "mlora_forward_w4", "mlora_backward_w4",
-           "mlora_plan_grouped", "mlora_adamw_ws"]
+           "mlora_plan_grouped", "mlora_adamw_ws", "mlora_cost_estimate"]
 
 
 class mlora_segment(C.Structure):
@@ -44,7 +44,12 @@ class mlora_segment(C.Structure):
 
 class mlora_problem(C.Structure):
     _fields_ = [("n_tokens", C.c_int64), ("d_in", C.c_int32), ("d_out", C.c_int32), ("dtype", C.c_int32),
-                ("flags", C.c_uint32)]
+                ("flags", C.c_uint32), ("mem_budget_bytes", C.c_int64)]
+
+
+class mlora_cost_point(C.Structure):
+    _fields_ = [("d_in", C.c_int32), ("d_out", C.c_int32), ("n_tokens", C.c_int64), ("lora_work", C.c_double),
+                ("step_ms", C.c_double)]
 
 
 class mlora_group(C.Structure):
@@ -123,6 +128,9 @@ def lib() -> C.CDLL:
         L.mlora_shard_jobs_multi.argtypes = [C.POINTER(mlora_problem), i32, C.POINTER(mlora_segment), i32, i32,
                                              C.POINTER(i32), C.POINTER(C.c_double)]
         L.mlora_shard_jobs_multi.restype = i32
+        L.mlora_cost_estimate.argtypes = [vp, C.POINTER(mlora_cost_point), i32, C.POINTER(C.c_double),
+                                          C.POINTER(i32)]
+        L.mlora_cost_estimate.restype = i32
         _lib = L
     return _lib
 
@@ -262,3 +270,13 @@ def mlora_shard_jobs_multi(problems, segs, n_ranks: int):
     _check(lib().mlora_shard_jobs_multi(parr, len(problems), arr, len(segs), n_ranks, ranks, load),
            "mlora_shard_jobs_multi")
     return list(ranks), list(load)
+
+
+def mlora_cost_estimate(plan, points) -> tuple[float, int]:
+    """points: [(d_in, d_out, n_tokens, lora_work, step_ms), ...].  Returns (step ms, basis)."""
+    arr = (mlora_cost_point * len(points))(*[mlora_cost_point(int(a), int(b), int(n), float(w), float(t))
+                                             for a, b, n, w, t in points])
+    ms = C.c_double(0.0)
+    basis = C.c_int32(0)
+    _check(lib().mlora_cost_estimate(plan, arr, len(points), C.byref(ms), C.byref(basis)), "mlora_cost_estimate")
+    return ms.value, basis.value

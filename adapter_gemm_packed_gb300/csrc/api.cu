@@ -733,6 +733,17 @@ mlora_status mlora_plan_grouped(const mlora_problem* problem, const mlora_group*
   if ((problem->flags & MLORA_DEBUG_DROP_COPY_PAIRS) && (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT))
     P->debug_drop_pairs = true;
   build_tables(P);
+  if (problem->mem_budget_bytes > 0) {
+    mlora_memory m{};
+    mlora_memory_estimate(P, &m);
+    if (m.total > problem->mem_budget_bytes) {
+      char buf[200];
+      snprintf(buf, sizeof buf, "the pack needs %lld bytes of device memory, more than the budget of %lld",
+               static_cast<long long>(m.total), static_cast<long long>(problem->mem_budget_bytes));
+      mlora_plan_destroy(P);
+      return fail(MLORA_ERR_OOM, buf);
+    }
+  }
   if (!(problem->flags & MLORA_PLAN_HOST_ONLY)) {
     st = upload(P);
     if (st != MLORA_OK) {
@@ -1238,6 +1249,58 @@ mlora_status mlora_memory_estimate(const mlora_plan_t* P, mlora_memory* out) {
   m.total = m.base_weight + m.activations + m.lora_params + m.lora_grad_state + m.lora_act + m.workspace +
             m.plan_tables;
   *out = m;
+  return MLORA_OK;
+}
+
+mlora_status mlora_cost_estimate(const mlora_plan_t* P, const mlora_cost_point* table, int32_t n_points,
+                                 double* step_ms, int32_t* basis) {
+  if (!P || !table || !step_ms || n_points < 1) return fail(MLORA_ERR_INVALID, "null plan, table or output");
+  if (P->prob.dtype == MLORA_F32) return fail(MLORA_ERR_UNSUPPORTED, "the cost table covers bf16 packs");
+  for (int i = 0; i < n_points; ++i)
+    if (!(table[i].step_ms > 0.0) || table[i].n_tokens < 1 || table[i].d_in < 1 || table[i].d_out < 1)
+      return fail(MLORA_ERR_INVALID, "cost table point with a non-positive size or time");
+  auto work = [](double n, double din, double dout, double lora) { return 4.0 * n * din * dout + 6.0 * lora; };
+  double lora = 0.0;
+  for (const DevSub& sb : P->subs)
+    lora += static_cast<double>(P->segs[sb.job].n) * sb.r * (P->prob.d_in + (sb.o_hi - sb.o_lo));
+  const double F = work(static_cast<double>(P->prob.n_tokens), P->prob.d_in, P->prob.d_out, lora);
+  // the points of this shape, by work
+  std::vector<std::pair<double, double>> pts;   // (F, ms)
+  for (int i = 0; i < n_points; ++i)
+    if (table[i].d_in == P->prob.d_in && table[i].d_out == P->prob.d_out)
+      pts.push_back({work(static_cast<double>(table[i].n_tokens), table[i].d_in, table[i].d_out, table[i].lora_work),
+                     table[i].step_ms});
+  std::sort(pts.begin(), pts.end());
+  int b = 0;
+  double t;
+  if (pts.empty()) {
+    // another shape's rate: the point whose work is nearest in ratio
+    double best = 0.0, rate = 0.0;
+    for (int i = 0; i < n_points; ++i) {
+      const double f = work(static_cast<double>(table[i].n_tokens), table[i].d_in, table[i].d_out, table[i].lora_work);
+      const double d = std::fabs(std::log(f / F));
+      if (i == 0 || d < best) {
+        best = d;
+        rate = f / table[i].step_ms;
+      }
+    }
+    t = F / rate;
+    b = 2;
+  } else if (F <= pts.front().first) {
+    t = F / (pts.front().first / pts.front().second);
+    b = F == pts.front().first ? 0 : 1;
+  } else if (F >= pts.back().first) {
+    t = F / (pts.back().first / pts.back().second);
+    b = F == pts.back().first ? 0 : 1;
+  } else {
+    size_t k = 1;
+    while (pts[k].first < F) ++k;
+    const auto& lo = pts[k - 1];
+    const auto& hi = pts[k];
+    t = hi.first == lo.first ? lo.second : lo.second + (F - lo.first) * (hi.second - lo.second) / (hi.first - lo.first);
+  }
+  *step_ms = t;
+  if (basis) *basis = b;
   return MLORA_OK;
 }
 

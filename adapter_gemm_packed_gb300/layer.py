@@ -154,7 +154,7 @@ class PackedLoRA:
 
 
 def host_plan(d_in, d_out, ranks, n_tokens, dtype="bf16", scales=None, offsets=None, n_total=None,
-              with_moments=True, flags=0):
+              with_moments=True, flags=0, mem_budget=0):
     """Build a host-only plan (no CUDA call) over placeholder pointers, for inspecting the
     planner's tables.  Returns (handle, workspace_bytes); destroy with mlora_plan_destroy."""
     code = _DT[dtype][0]
@@ -169,7 +169,7 @@ def host_plan(d_in, d_out, ranks, n_tokens, dtype="bf16", scales=None, offsets=N
         segs.append(M.mlora_segment(o, n, r, s, *ptrs))
         off += n
     prob = M.mlora_problem(sum(n_tokens) if n_total is None else n_total, d_in, d_out, code,
-                           M.MLORA_PLAN_HOST_ONLY | flags)
+                           M.MLORA_PLAN_HOST_ONLY | flags, mem_budget)
     return M.mlora_plan(prob, segs)
 
 

@@ -872,6 +872,79 @@ def run_sweep(args):
             torch.cuda.empty_cache()
 
 
+# Cost-table calibration: the seven Llama-3-8B projections, the Qwen-2.5 shapes of the sweep and the
+# many-small-jobs down projection, each at several pack sizes of 1024-token jobs.
+CALIBRATE_SHAPES = [(4096, 4096), (4096, 1024), (4096, 14336), (14336, 4096), (2048, 2048), (2048, 11008),
+                    (3584, 3584), (3584, 18944), (28672, 8192)]
+CALIBRATE_TOKENS = [1024, 4096, 16384, 65536, 143360]
+CALIBRATE_RANKS = [8, 16, 32, 64, 128]
+
+
+def run_calibrate(args):
+    """Measure the step time (forward + backward + AdamW, back-to-back steps, inputs in device memory)
+    of packs of 1024-token jobs with ranks cycling through 8..128, for every shape and size above,
+    and write the cost table mlora_cost_estimate interpolates (adapter_gemm_packed_gb300/
+    cost_table_gb300.json, or --calibrate-out)."""
+    import torch
+    from adapter_gemm_packed_gb300 import _mlora as M
+    from adapter_gemm_packed_gb300 import cost
+    from adapter_gemm_packed_gb300.layer import PackedLoRA
+
+    torch.cuda.set_device(0)
+    gen = torch.Generator(device="cuda")
+    bf = torch.bfloat16
+    points = []
+    for d_in, d_out in CALIBRATE_SHAPES:
+        for N in CALIBRATE_TOKENS:
+            if N * (d_in + d_out) * 2 * 4 > 120e9:
+                continue
+            gen.manual_seed(11 * d_in + d_out + N)
+            J = max(1, N // 1024)
+            toks = [N // J] * J
+            toks[-1] += N - sum(toks)
+            ranks = [CALIBRATE_RANKS[j % len(CALIBRATE_RANKS)] for j in range(J)]
+            At = [torch.randn(r, d_in, device="cuda", generator=gen) * d_in ** -0.5 for r in ranks]
+            Bt = [torch.randn(d_out, r, device="cuda", generator=gen) * 0.02 for r in ranks]
+            layer = PackedLoRA(d_in, d_out, ranks, toks, [2.0] * J, At=At, Bt=Bt, flags=M.MLORA_REUSE_STAGING)
+            X = torch.randn(N, d_in, device="cuda", generator=gen).to(bf)
+            dY = torch.randn(N, d_out, device="cuda", generator=gen).to(bf)
+            Wt = (torch.randn(d_out, d_in, device="cuda", generator=gen) * 0.02).to(bf)
+            Y = torch.empty(N, d_out, dtype=bf, device="cuda")
+            dX = torch.empty(N, d_in, dtype=bf, device="cuda")
+            t = [0]
+
+            def step():
+                t[0] += 1
+                layer.forward(X, Wt, Y)
+                layer.backward(X, Wt, dY, dX)
+                layer.adamw(1e-3, 0.9, 0.999, 1e-8, 0.01, t[0])
+
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.calibrate_steps):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            if layer.sync_status() != M.MLORA_OK:
+                raise SystemExit("device status error in calibration")
+            ms = e0.elapsed_time(e1) / args.calibrate_steps
+            work = float(sum(n * r * (d_in + d_out) for n, r in zip(toks, ranks)))
+            points.append({"d_in": d_in, "d_out": d_out, "n_tokens": N, "jobs": J, "lora_work": work, "step_ms": ms})
+            print(json.dumps(points[-1]), flush=True)
+            layer.close()
+            del layer, X, dY, Wt, Y, dX, At, Bt
+            torch.cuda.empty_cache()
+    out = args.calibrate_out or cost.TABLE_PATH
+    with open(out, "w") as f:
+        json.dump({"what": "step time (forward + backward + AdamW) of packs of 1024-token jobs, ranks cycling "
+                           "8..128, bf16, back-to-back steps with inputs in device memory; one GB300",
+                   "command": "python bench.py --calibrate", "steps": args.calibrate_steps,
+                   "gpu": torch.cuda.get_device_name(0), "points": points}, f, indent=1)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -894,6 +967,10 @@ def main():
     ap.add_argument("--sweep-steps", type=int, default=10)
     ap.add_argument("--sweep-layers", default="", help="comma-separated subset of the sweep's layer names")
     ap.add_argument("--sweep-jobs", default="", help="comma-separated job counts (default 1,2,4,8,16,32)")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="measure the cost table of mlora_cost_estimate (one GPU) and write it")
+    ap.add_argument("--calibrate-steps", type=int, default=10)
+    ap.add_argument("--calibrate-out", default="")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
@@ -901,12 +978,12 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.sweep:
+    if args.sweep or args.calibrate:
         if world > 1:
-            raise SystemExit("--sweep runs on one GPU")
+            raise SystemExit("--sweep and --calibrate run on one GPU")
         import __graft_entry__
         __graft_entry__.build()
-        run_sweep(args)
+        run_sweep(args) if args.sweep else run_calibrate(args)
         return
     wl = workload(args.workload)
     if args.impl == "reference":

@@ -137,6 +137,10 @@ typedef struct mlora_problem {
     int32_t d_out;        /* multiple of 8 (bf16) or 4 (fp32) */
     int32_t dtype;        /* mlora_dtype */
     uint32_t flags;       /* MLORA_PLAN_* / MLORA_DEBUG_* bits */
+    int64_t mem_budget_bytes;  /* 0: no check.  Otherwise the device memory this layer may use: the
+                                  plan is refused with MLORA_ERR_OOM when mlora_memory_estimate's
+                                  total exceeds it (PLoRA §8: M_base + sum_k M_lora,k must stay
+                                  within c_load x M_gpu; the caller passes its share for this layer) */
 } mlora_problem;
 
 typedef struct mlora_plan_s mlora_plan_t;
@@ -310,6 +314,34 @@ typedef struct mlora_memory {
 
 /* Fill *out for the plan (host only; valid for host-only plans too). */
 mlora_status mlora_memory_estimate(const mlora_plan_t* plan, mlora_memory* out);
+
+/* Cost model of one training step of a pack on one GPU: T(H, 1) of "PLoRA: Efficient Concurrent
+ * LoRA Training for Large Language Models", §3.1-§3.2 (the planner's throughput objective divides
+ * by the step time T of a packed job; the page measures T from a job's first iterations).  Here T
+ * comes from a table of measured steps of this library (forward + backward + AdamW, inputs in
+ * device memory), one point per measured pack:
+ *   d_in, d_out  the layer's shape
+ *   n_tokens     N of the measured pack
+ *   lora_work    sum over its adapters of n_i r_i (d_in + w_i), w_i = the output width of B_i
+ *   step_ms      its measured step time
+ * A pack's algorithmic work is F = 4 N d_in d_out + 6 lora_work (the FLOP count of one step).
+ * Among the points with the plan's (d_in, d_out), sorted by F, T is interpolated linearly in F
+ * between the two points around the plan's F; below the smallest and above the largest point it
+ * is F divided by that point's rate F / step_ms.  With no point of that shape it is F divided by
+ * the rate of the point whose F is nearest (in ratio) to the plan's.  *step_ms receives T in
+ * milliseconds, *basis (may be NULL) 0 for an interpolation, 1 for a same-shape extrapolation, 2
+ * for another shape's rate.  bf16 and 4-bit-base plans; MLORA_ERR_UNSUPPORTED for fp32 plans,
+ * MLORA_ERR_INVALID for an empty table or a point with step_ms <= 0.  Host only. */
+typedef struct mlora_cost_point {
+    int32_t d_in;
+    int32_t d_out;
+    int64_t n_tokens;
+    double lora_work;
+    double step_ms;
+} mlora_cost_point;
+
+mlora_status mlora_cost_estimate(const mlora_plan_t* plan, const mlora_cost_point* table, int32_t n_points,
+                                 double* step_ms, int32_t* basis);
 
 /* Split whole jobs across n_ranks GPUs that each hold a replica of W (the layer shards by job
  * with no collective: every job's gradients and optimizer step stay on its GPU).  Jobs are
