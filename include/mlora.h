@@ -40,7 +40,8 @@
  * the plan's status word, read back by mlora_sync_status().
  * Threads: different plans may be used from different host threads at once (each call makes
  * the plan device's primary context current on its thread); calls on one plan must not overlap
- * on the host.  Every call can be captured into a CUDA graph.
+ * on the host.  mlora_forward, mlora_backward and mlora_adamw (and their _w4 / _ws forms) can be
+ * captured into a CUDA graph.
  */
 #ifndef MLORA_H
 #define MLORA_H
