@@ -152,10 +152,11 @@ struct mlora_plan_s {
   std::vector<WinItem> win;             // shrink / dH items of the single-CTA engine (tile, <= 2 chunks)
   std::vector<WinItem> win2;            // the same work on CTA pairs (tile = pair, 2 or 4 chunks)
   bool win_pairs = false;               // which of the two the shrink / dH launches run
+  int n_split = 0, split_parts = 1;     // win2 items cut along K (see build_tables) and their parts
   std::vector<WItem> da, db;
   std::vector<AdamItem> adam;
   bool can_backward = false, can_adamw = false;
-  size_t off_shadow = 0, off_himg = 0, off_dhimg = 0, off_wexp = 0, ws_bytes = 0;
+  size_t off_shadow = 0, off_partials = 0, off_himg = 0, off_dhimg = 0, off_wexp = 0, ws_bytes = 0;
   bool w4_fused = false;   // 4-bit base expanded inside the GEMMs instead of into the workspace
   int group_m = 8;
   // device
@@ -174,6 +175,7 @@ struct mlora_plan_s {
   WItem* d_db = nullptr;
   AdamItem* d_adam = nullptr;
   int* d_err = nullptr;
+  int* d_part_cnt = nullptr;            // arrival counters of the split pair items (zeroed at upload)
   unsigned long long timeout_ns = DEFAULT_TIMEOUT_NS;
   bool pdl = true;
   bool debug_drop = false;             // single-CTA shrink withholds one copy (test hook)
@@ -426,6 +428,7 @@ void build_tables(mlora_plan_t* P) {
       w.tile = t;
       w.q0 = m.q_lo + q;
       w.nq = std::min(MAX_ITEM_CHUNKS, m.nch - q);
+      w.nparts = 1;
       dh_range(w, w.q0, w.nq);
       P->win.push_back(w);
     }
@@ -441,6 +444,7 @@ void build_tables(mlora_plan_t* P) {
       w.q0 = m.q_lo + q;
       const int real = std::min(4, m.nch - q);
       w.nq = real + (real & 1);
+      w.nparts = 1;
       dh_range(w, w.q0, real);
       P->win2.push_back(w);
     }
@@ -452,6 +456,40 @@ void build_tables(mlora_plan_t* P) {
   if (pr.flags & MLORA_WINDOW_PAIRS) P->win_pairs = true;
   if (pr.flags & MLORA_WINDOW_SINGLE) P->win_pairs = false;
   if (P->debug_drop) P->win_pairs = false;   // the copy-withholding hook lives in the single-CTA shrink
+
+  // The persistent grid runs the pair items round-robin on num_sms / 2 pairs.  When the last wave
+  // would leave more than half of the pairs idle, its T items are cut along K into S parts each,
+  // one part per pair: the wave takes about 1/S of an item's time instead of a whole one, for the
+  // partial sums' extra bytes (each part's fp32 sums, up to 128 KB per CTA, written once and read
+  // once by the item's last part).  S = floor(pairs / T), at most MAX_WIN_PARTS, and small enough
+  // that every part keeps at least 16 K slices of both products (the shrink's d_in, and the d_out
+  // slices dH covers), so a part streams at least 256 KB per CTA against its 128 KB of sums.
+  P->n_split = 0;
+  P->split_parts = 1;
+  {
+    const int pairs = std::max(1, P->num_sms / 2);
+    const int I = static_cast<int>(P->win2.size());
+    const int T = I % pairs;
+    if (P->win_pairs && I > pairs && T > 0 && 2 * T <= pairs) {
+      int min_k = (pr.d_in + BK - 1) / BK;
+      for (int t = I - T; t < I; ++t) min_k = std::min(min_k, P->win2[t].dh_nkb);
+      const int S = std::min({MAX_WIN_PARTS, pairs / T, min_k / 16});
+      if (S >= 2) {
+        std::vector<WinItem> tail(P->win2.end() - T, P->win2.end());
+        P->win2.resize(I - T);
+        for (int t = 0; t < T; ++t)
+          for (int k = 0; k < S; ++k) {
+            WinItem w = tail[t];
+            w.part = k;
+            w.nparts = S;
+            w.slot = t;
+            P->win2.push_back(w);
+          }
+        P->n_split = T;
+        P->split_parts = S;
+      }
+    }
+  }
 
   // dA / dB work: (256-row block, job, <= MAX_ITEM_CHUNKS chunks), longest first.  A dB block
   // needs only the columns of the job's adapters whose output range meets it.
@@ -522,7 +560,10 @@ void build_tables(mlora_plan_t* P) {
     const size_t shadow = round_up(static_cast<size_t>(P->C_total) * pr.d_in * 2, 1024) +
                           round_up(static_cast<size_t>(P->C_total) * pr.d_out * 2, 1024);
     P->off_shadow = 0;
-    P->off_himg = round_up(shadow, 1024);
+    // fp32 partial sums of the split CTA-pair items: [slot][part][CTA of the pair][128 rows][256 columns]
+    P->off_partials = round_up(shadow, 1024);
+    const size_t partials = static_cast<size_t>(P->n_split) * P->split_parts * 2 * BM * 256 * 4;
+    P->off_himg = round_up(P->off_partials + partials, 1024);
     P->off_dhimg = P->off_himg + static_cast<size_t>(P->n_images) * IMG_BYTES;
     P->ws_bytes = P->off_dhimg + static_cast<size_t>(P->n_images) * IMG_BYTES;
     if (pr.dtype == MLORA_BF16_W4 && !P->w4_fused) {
@@ -550,8 +591,10 @@ mlora_status upload(mlora_plan_t* P) {
   const size_t b_segs = table_bytes(P->segs), b_mt = table_bytes(P->mtiles), b_it = table_bytes(P->img_tile),
                b_cs = table_bytes(P->col_sub), b_sc = table_bytes(P->col_scale), b_sub = table_bytes(P->subs),
                b_win = table_bytes(P->win), b_win2 = table_bytes(P->win2), b_da = table_bytes(P->da),
-               b_db = table_bytes(P->db), b_adam = table_bytes(P->adam), b_err = 256;
-  const size_t total = b_segs + b_mt + b_it + b_cs + b_sc + b_sub + b_win + b_win2 + b_da + b_db + b_adam + b_err;
+               b_db = table_bytes(P->db), b_adam = table_bytes(P->adam), b_err = 256,
+               b_cnt = round_up(static_cast<size_t>(P->n_split) * 8 * sizeof(int), 256);
+  const size_t total =
+      b_segs + b_mt + b_it + b_cs + b_sc + b_sub + b_win + b_win2 + b_da + b_db + b_adam + b_err + b_cnt;
   e = cudaMalloc(&P->dev_block, total);
   if (e != cudaSuccess) {
     P->dev_block = nullptr;
@@ -580,6 +623,12 @@ mlora_status upload(mlora_plan_t* P) {
   P->d_err = reinterpret_cast<int*>(b + o);
   e = cudaMemset(P->d_err, 0, sizeof(int));
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  o += b_err;
+  if (P->n_split > 0) {
+    P->d_part_cnt = reinterpret_cast<int*>(b + o);
+    e = cudaMemset(P->d_part_cnt, 0, static_cast<size_t>(P->n_split) * 8 * sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset");
+  }
   P->on_device = true;
   return MLORA_OK;
 }
@@ -732,6 +781,15 @@ mlora_status mlora_plan_grouped(const mlora_problem* problem, const mlora_group*
   if ((problem->flags & MLORA_DEBUG_DROP_COPY) && (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT)) P->debug_drop = true;
   if ((problem->flags & MLORA_DEBUG_DROP_COPY_PAIRS) && (problem->flags & MLORA_DEBUG_SHORT_TIMEOUT))
     P->debug_drop_pairs = true;
+  if (!(problem->flags & MLORA_PLAN_HOST_ONLY)) {
+    // the planner sizes the last wave of the CTA-pair work lists for this device's SM count
+    cudaError_t e = cudaGetDevice(&P->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
+    if (e != cudaSuccess) {
+      mlora_plan_destroy(P);
+      return cuda_fail(e, "querying the device");
+    }
+  }
   build_tables(P);
   if (problem->mem_budget_bytes > 0) {
     mlora_memory m{};
@@ -853,6 +911,8 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
     g.win = P->d_win2;
     g.n_items = static_cast<int>(P->win2.size());
     g.debug_drop = P->debug_drop_pairs ? 1 : 0;
+    g.partials = P->n_split ? reinterpret_cast<float*>(ws + P->off_partials) : nullptr;
+    g.part_cnt = P->d_part_cnt;
     e = timed(P, K_SHRINK, s, [&] {
       return launch_win_2sm<MODE_SHRINK>(mX, mAt, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
     });
@@ -987,6 +1047,8 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   if (P->win_pairs) {
     g.win = P->d_win2;
     g.n_items = static_cast<int>(P->win2.size());
+    g.partials = P->n_split ? reinterpret_cast<float*>(ws + P->off_partials) : nullptr;
+    g.part_cnt = P->d_part_cnt;
     e = timed(P, K_DH, s, [&] {
       return launch_win_2sm<MODE_DH>(mdY, mBt64, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
     });
@@ -1132,6 +1194,11 @@ mlora_status mlora_sync_status(const mlora_plan_t* P, void* stream) {
   if (v != 0) {
     e = cudaMemset(P->d_err, 0, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    // a launch that gave up may have left split items' arrival counts behind
+    if (P->d_part_cnt) {
+      e = cudaMemset(P->d_part_cnt, 0, static_cast<size_t>(P->n_split) * 8 * sizeof(int));
+      if (e != cudaSuccess) return cuda_fail(e, "clearing the split items' counters");
+    }
     char buf[96];
     snprintf(buf, sizeof buf, "a device-side wait gave up (code 0x%x)", v);
     return fail(MLORA_ERR_TIMEOUT, buf);
@@ -1164,7 +1231,7 @@ mlora_status mlora_plan_describe(const mlora_plan_t* P, int32_t what, int64_t* o
       break;
     case MLORA_Q_WINDOW_PAIRS:
       v.push_back(P->win_pairs ? 1 : 0);
-      for (const WinItem& w : P->win2) v.insert(v.end(), {w.tile, w.q0, w.nq, w.dh_kb0, w.dh_nkb});
+      for (const WinItem& w : P->win2) v.insert(v.end(), {w.tile, w.q0, w.nq, w.dh_kb0, w.dh_nkb, w.part, w.nparts});
       break;
     case MLORA_Q_ADAPTERS:
       for (const DevSub& sb : P->subs) v.insert(v.end(), {sb.job, sb.c0, sb.r, sb.o_lo, sb.o_hi});
@@ -1245,7 +1312,8 @@ mlora_status mlora_memory_estimate(const mlora_plan_t* P, mlora_memory* out) {
                                        table_bytes(P->col_sub) + table_bytes(P->col_scale) +
                                        table_bytes(P->subs) + table_bytes(P->win) + table_bytes(P->win2) +
                                        table_bytes(P->da) +
-                                       table_bytes(P->db) + table_bytes(P->adam) + 256);
+                                       table_bytes(P->db) + table_bytes(P->adam) + 256 +
+                                       round_up(static_cast<size_t>(P->n_split) * 8 * sizeof(int), 256));
   m.total = m.base_weight + m.activations + m.lora_params + m.lora_grad_state + m.lora_act + m.workspace +
             m.plan_tables;
   *out = m;

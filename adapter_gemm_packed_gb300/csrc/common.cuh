@@ -30,6 +30,7 @@ constexpr int IMG_BYTES = BM * CHUNK_COLS * 2;   // one staged [128 x 64] bf16 i
 constexpr int RANK_PAD = 16;         // each job's rank window is padded to a multiple of 16
 constexpr int GEMM_THREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int TMEM_COLS = 512;       // two 256-column fp32 accumulators
+constexpr int MAX_WIN_PARTS = 8;    // K parts of a CTA-pair shrink / dH item cut to fill a thin last wave
 constexpr int MAX_ITEM_CHUNKS = 2;  // rank chunks per shrink / dH / dA / dB work item (N <= 128)
 
 enum GemmMode : int {
@@ -86,8 +87,22 @@ struct WinItem {
   int tile, q0, nq;
   int dh_kb0, dh_nkb;   // dH: the 64-wide d_out slices its chunks' adapters cover (all of d_out
                         // unless the pack shares its input across projections)
-  int pad0, pad1, pad2;
+  // CTA-pair items of a last wave that would leave most pairs idle are cut along K: part `part` of
+  // `nparts` covers that share of the item's K slices, parks its fp32 partial sums in the
+  // workspace (partial set `slot`), and the last part to finish sums all parts in part order and
+  // writes the item's outputs.  nparts = 1: a whole item.
+  int part, nparts, slot;
 };
+
+// K slices [kb0, kb0 + nkb) of a CTA-pair rank-window item: the whole K range of its product
+// (d_in for the shrink, the covered d_out slices for dH) or its part's equal share of it.
+__host__ __device__ __forceinline__ void win_krange(const WinItem& w, bool dh, int kmain, int& kb0, int& nkb) {
+  const int b = dh ? w.dh_kb0 : 0, n = dh ? w.dh_nkb : kmain;
+  const int lo = static_cast<int>(static_cast<long long>(n) * w.part / w.nparts);
+  const int hi = static_cast<int>(static_cast<long long>(n) * (w.part + 1) / w.nparts);
+  kb0 = b + lo;
+  nkb = hi - lo;
+}
 
 // Weight-gradient work item (dA / dB): one 256-row block of d_in (dA) or d_out (dB), one
 // job, its 64-token half-tiles [ga, gb), chunks [q0, q0 + nq) of its rank window (nq <= MAX_ITEM_CHUNKS).
@@ -133,6 +148,8 @@ struct GemmArgs {
   unsigned long long timeout_ns;
   int pdl;                 // launched with programmatic dependent launch
   int debug_drop;          // test hook: CTA 0 arms its first slot but issues no copy into it
+  float* partials;         // CTA-pair shrink / dH: fp32 partial sums of split items (workspace)
+  int* part_cnt;           // ... and their arrival counters (slot, CTA of the pair, row quarter)
   // Shared-input packs (several adapters per job): per packed column, its adapter (-1 in the
   // padding) and scale.  Null for plans with one adapter per job, whose kernels read the job's.
   const DevSub* subs;      // job j's adapters are subs[j * n_groups .. j * n_groups + n_groups)

@@ -102,8 +102,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const int m0 = (2 * w.tile + static_cast<int>(rank)) * BM;
         const int nb = w.nq >> 1;                                   // chunks held by this CTA
         const int qb = w.q0 + static_cast<int>(rank) * nb;
-        const int nkb = (MODE == MODE_DH) ? w.dh_nkb : g.kmain;
-        const int kb0 = (MODE == MODE_DH) ? w.dh_kb0 : 0;
+        int kb0, nkb;                                               // the item's (or part's) K slices
+        win_krange(w, MODE == MODE_DH, g.kmain, kb0, nkb);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
             ok = false;
@@ -142,7 +142,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       bool ok = true;
       for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
         const WinItem w = g.win[item];
-        const int nkb = (MODE == MODE_DH) ? w.dh_nkb : g.kmain;
+        int kb0, nkb;
+        win_krange(w, MODE == MODE_DH, g.kmain, kb0, nkb);
         const uint32_t idesc = idesc_bf16(2 * BM, w.nq * CHUNK_COLS, false, MODE == MODE_DH);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
           ok = false;
@@ -195,6 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       tc_fence_after();
       const WinItem w = g.win[item];
       const int tile = 2 * w.tile + static_cast<int>(rank);
+      bool released = false;   // this warp has handed the accumulator back to the MMA
       if (tile < g.n_mtiles) {   // an odd last tile has no partner: its half computed zeros
         const MTile mt = g.mtiles[tile];
         const long long row = static_cast<long long>(tile) * BM + rit;
@@ -211,16 +213,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           hbase = sg.h_off + (row - sg.off) * sg.r - sg.c;
         }
         const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * 256;
-        // SHRINK: H = acc, image = s*acc.  DH: dH = s*acc, image = s*acc.
-#pragma unroll 1
-        for (int jq = 0; jq < w.nq; ++jq) {
+        // One chunk's 64 accumulated columns of this thread's row -> H (SHRINK: H = acc) or dH
+        // (DH: dH = s*acc), and the bf16 image s*acc, zero outside the row's job window.
+        auto emit_chunk = [&](int jq, const uint32_t* vv) {
           const int q = w.q0 + jq;
-          if (q >= mt.q_lo + mt.nch) break;   // padding chunk: no image slot, nothing to keep
           uint8_t* img = g.img_out + static_cast<size_t>(mt.img_off + q - mt.q_lo) * IMG_BYTES;
-          uint32_t vv[64];
-          tmem_ld32(t_acc + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&vv[0]));
-          tmem_ld32(t_acc + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&vv[32]));
-          tmem_ld_wait();
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const uint32_t* v = vv + half * 32;
@@ -261,11 +258,82 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             for (int k16 = 0; k16 < 4; ++k16)
               dst[k16] = make_uint4(pk[4 * k16], pk[4 * k16 + 1], pk[4 * k16 + 2], pk[4 * k16 + 3]);
           }
+        };
+        const int nreal = min(w.nq, mt.q_lo + mt.nch - w.q0);   // chunks past the window are padding
+        if (w.nparts == 1) {
+#pragma unroll 1
+          for (int jq = 0; jq < nreal; ++jq) {
+            uint32_t vv[64];
+            tmem_ld32(t_acc + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&vv[0]));
+            tmem_ld32(t_acc + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&vv[32]));
+            tmem_ld_wait();
+            emit_chunk(jq, vv);
+          }
+        } else {
+          // A part of an item cut along K: park this part's sums ([slot][part][CTA][256 columns]
+          // [128 rows], fp32, so that a warp's 32 rows of one column are one 128-byte line), hand
+          // the accumulator back, and count the arrival of this warp's 32 rows.  The last of the
+          // item's parts to arrive reads all parts' sums back in part order (a fixed order:
+          // results do not depend on timing) and writes the item's outputs.  Nothing waits for
+          // another CTA.
+          const size_t stride = static_cast<size_t>(BM) * 256;
+          float* mine = g.partials + (static_cast<size_t>(w.slot * w.nparts + w.part) * 2 + rank) * stride + rit;
+#pragma unroll 1
+          for (int jq = 0; jq < nreal; ++jq) {
+            uint32_t vv[64];
+            tmem_ld32(t_acc + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&vv[0]));
+            tmem_ld32(t_acc + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&vv[32]));
+            tmem_ld_wait();
+            float* col = mine + static_cast<size_t>(jq * CHUNK_COLS) * BM;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) col[c * BM] = __uint_as_float(vv[c]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(acc ? tempty_leader1 : tempty_leader0);
+          released = true;
+          __threadfence();   // this warp's sums are visible before its arrival is counted
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) {
+            int* cnt = g.part_cnt + (w.slot * 2 + static_cast<int>(rank)) * 4 + quarter;
+            if (atomicAdd(cnt, 1) == w.nparts - 1) {
+              *cnt = 0;       // every part has arrived: ready for the next launch
+              last = 1;
+            }
+          }
+          last = __shfl_sync(0xffffffffu, last, 0);
+          if (last) {
+            __threadfence();
+            const float* base = g.partials + (static_cast<size_t>(w.slot * w.nparts) * 2 + rank) * stride + rit;
+#pragma unroll 1
+            for (int jq = 0; jq < nreal; ++jq) {
+              const float* col = base + static_cast<size_t>(jq * CHUNK_COLS) * BM;
+              // part by part, all 64 columns' loads of a part in flight together; each column is
+              // summed in part order
+              float acc_v[64];
+#pragma unroll 1
+              for (int p = 0; p < w.nparts; ++p) {
+                const float* src = col + p * 2 * stride;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                  const float x = __ldcg(src + c * BM);
+                  acc_v[c] = p ? acc_v[c] + x : x;
+                }
+              }
+              uint32_t vv[64];
+#pragma unroll
+              for (int c = 0; c < 64; ++c) vv[c] = __float_as_uint(acc_v[c]);
+              emit_chunk(jq, vv);
+            }
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(acc ? tempty_leader1 : tempty_leader0);
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(acc ? tempty_leader1 : tempty_leader0);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }

@@ -88,12 +88,13 @@ def test_planner_tables_random(seed):
     plan, _ = host_plan(d_in, d_out, ranks, ns)
     try:
         mt = _describe(plan, M.MLORA_Q_MTILES).reshape(-1, 5)
-        items = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)[1:].reshape(-1, 5)
+        items = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)[1:].reshape(-1, 7)
     finally:
         M.mlora_plan_destroy(plan)
+    items = items[items[:, 5] == 0]          # one entry per item: its first part
     for p in range((len(mt) + 1) // 2):
         q_lo, nch = mt[2 * p, 2], mt[2 * p, 3]
-        got = [q for _, q0, nq, _, _ in items[items[:, 0] == p] for q in range(q0, q0 + nq)]
+        got = [q for _, q0, nq, _, _, _, _ in items[items[:, 0] == p] for q in range(q0, q0 + nq)]
         assert got[:nch] == list(range(q_lo, q_lo + nch)) and len(got) - nch in (0, 1)
 
 
@@ -101,6 +102,7 @@ def _check_tables(d_in, d_out, ranks, ns):
     plan, ws = host_plan(d_in, d_out, ranks, ns)
     try:
         summ, mt, cols, win, da, db = _tables(plan)
+        pw_items = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WINDOW_PAIRS)[1:]).reshape(-1, 7)
     finally:
         M.mlora_plan_destroy(plan)
     N = sum(ns)
@@ -157,9 +159,11 @@ def _check_tables(d_in, d_out, ranks, ns):
         assert set(cover) == want
         lens = [(gb - ga) * (16 + nq) for _, _, ga, gb, _, nq in items]
         assert lens == sorted(lens, reverse=True)       # longest first
-    # workspace = bf16 shadows + two image sets
+    # workspace = bf16 shadows + the split pair items' fp32 partial sums + two image sets
     shadow = -(-c * d_in * 2 // 1024) * 1024 + -(-c * d_out * 2 // 1024) * 1024
-    assert ws == shadow + 2 * img * 16384
+    split = pw_items[pw_items[:, 6] > 1]
+    partials = len(split) * 2 * 128 * 256 * 4
+    assert ws == shadow + -(-partials // 1024) * 1024 + 2 * img * 16384
 
 
 def _status_of(fn):
@@ -366,18 +370,56 @@ def test_pair_window_items(name):
         pw = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)
     finally:
         M.mlora_plan_destroy(plan)
-    items = pw[1:].reshape(-1, 5)
+    items = pw[1:].reshape(-1, 7)
+    items = items[items[:, 5] == 0]          # one entry per item: its first part
     n_pairs = (len(mt) + 1) // 2
     for p in range(n_pairs):
         q_lo, nch = mt[2 * p, 2], mt[2 * p, 3]
         mine = items[items[:, 0] == p]
         got = []
-        for _, q0, nq, kb0, nkb in mine:
+        for _, q0, nq, kb0, nkb, _, _ in mine:
             assert nq in (2, 4)
             assert (kb0, nkb) == (0, -(-d_out // 64))
             got.extend(range(q0, q0 + nq))
         real = list(range(q_lo, q_lo + nch))
         assert got[:nch] == real and len(got) - nch in (0, 1)
+
+
+@pytest.mark.parametrize("name", ["many_small", "mlp_up", "qproj"])
+def test_pair_items_of_a_thin_last_wave_are_cut_along_k(name):
+    """When the pair items' last wave would leave more than half of the pairs idle (host plans
+    assume 148 SMs: 74 pairs), each of its T items becomes S = min(8, 74 // T, shortest K / 16)
+    parts, one per pair, at the end of the list; the parts' K shares tile the item's K range
+    exactly once."""
+    d_in, d_out, ranks, ns = _case(name)
+    plan, _ = host_plan(d_in, d_out, ranks, ns, flags=M.MLORA_WINDOW_PAIRS)
+    try:
+        items = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)[1:].reshape(-1, 7)
+    finally:
+        M.mlora_plan_destroy(plan)
+    pairs = 74
+    whole = items[items[:, 6] == 1]
+    split = items[items[:, 6] > 1]
+    n_orig = len(whole) + (len(split) // split[0, 6] if len(split) else 0)
+    T = n_orig % pairs
+    tail = whole[len(whole) - T:] if len(split) == 0 else split[::max(1, split[0, 6])]
+    min_k = min([-(-d_in // 64)] + [int(x) for x in tail[:, 4]]) if T else 0
+    if n_orig > pairs and 0 < T and 2 * T <= pairs and min(8, pairs // T, min_k // 16) >= 2:
+        S = min(8, pairs // T, min_k // 16)
+        assert len(whole) == n_orig - T and len(split) == T * S <= pairs
+        assert (items[:len(whole), 6] == 1).all()        # whole items first, the parts last
+        for t in range(T):
+            grp = split[t * S:(t + 1) * S]
+            assert list(grp[:, 5]) == list(range(S)) and (grp[:, :5] == grp[0, :5]).all()
+            for kmain, dh in ((-(-d_in // 64), False), (grp[0, 4], True)):
+                base = grp[0, 3] if dh else 0
+                cover = []
+                for s in range(S):
+                    lo, hi = kmain * s // S, kmain * (s + 1) // S
+                    cover += list(range(base + lo, base + hi))
+                assert cover == list(range(base, base + kmain))
+    else:
+        assert len(split) == 0
 
 
 def test_window_engine_choice():
