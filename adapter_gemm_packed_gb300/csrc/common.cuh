@@ -106,9 +106,15 @@ __host__ __device__ __forceinline__ void win_krange(const WinItem& w, bool dh, i
 
 // Weight-gradient work item (dA / dB): one 256-row block of d_in (dA) or d_out (dB), one
 // job, its 64-token half-tiles [ga, gb), chunks [q0, q0 + nq) of its rank window (nq <= MAX_ITEM_CHUNKS).
+// An item whose tokens the schedule cuts across CTAs runs as `nparts` parts (token ranges in
+// order, `part` = this one's index): each part parks its fp32 sums in the workspace (nq units of
+// WG_UNIT floats from unit pbase + part * nq) and counts itself on counter set `cnt`; the last part
+// to arrive adds the parts in part order and writes the gradient.  nparts = 1: a whole item.
 struct WItem {
-  int row0, seg, ga, gb, q0, nq, pad0, pad1;
+  int row0, seg, ga, gb, q0, nq;
+  int part, nparts, pbase, cnt;
 };
+constexpr int WG_UNIT = 2 * BM * CHUNK_COLS;   // floats of one part's sums per chunk (256 rows x 64 columns)
 
 struct AdamItem {
   float* p;
@@ -148,8 +154,10 @@ struct GemmArgs {
   unsigned long long timeout_ns;
   int pdl;                 // launched with programmatic dependent launch
   int debug_drop;          // test hook: CTA 0 arms its first slot but issues no copy into it
-  float* partials;         // CTA-pair shrink / dH: fp32 partial sums of split items (workspace)
-  int* part_cnt;           // ... and their arrival counters (slot, CTA of the pair, row quarter)
+  float* partials;         // fp32 partial sums of items split across CTAs (workspace)
+  int* part_cnt;           // ... and their arrival counters (pair items: slot, CTA of the pair,
+                           // row quarter; dA / dB items: counter set, row quarter)
+  const int* cta_first;    // dA / dB: CTA c runs items [cta_first[c], cta_first[c + 1]) (null: round robin)
   // Shared-input packs (several adapters per job): per packed column, its adapter (-1 in the
   // padding) and scale.  Null for plans with one adapter per job, whose kernels read the job's.
   const DevSub* subs;      // job j's adapters are subs[j * n_groups .. j * n_groups + n_groups)

@@ -46,6 +46,11 @@ namespace {
 // reaches 6.6 TB/s with 4 x 16 KB per SM).
 // dA / dB items cover 256 rows of d_in / d_out (two M = 128 MMAs per K step sharing one staged
 // image operand), so their ring holds 32 KB of the streamed operand per stage.
+// dB's epilogue also stages each warp's 32 rows x 32 columns in shared memory (rows padded to 36
+// floats, so that both the row-wise writes and the 4-row reads run conflict-free) to store dB^T
+// rows with consecutive lanes on consecutive addresses.
+constexpr int DB_STAGE_LD = 36;
+constexpr int DB_STAGE_FLOATS = 32 * DB_STAGE_LD;
 template <int MODE>
 struct Ring {
   static constexpr bool kBase = MODE == MODE_FWD || MODE == MODE_BWD;
@@ -53,8 +58,20 @@ struct Ring {
   static constexpr int kStages = kBase ? 4 : (kWgrad ? 4 : 6);
   static constexpr int kABytes = kWgrad ? 2 * A_STAGE_BYTES : A_STAGE_BYTES;
   static constexpr int kBBytes = kBase ? B_STAGE_BYTES : MAX_ITEM_CHUNKS * CHUNK_COLS * BK * 2;
-  static constexpr int kSmem = kStages * (kABytes + kBBytes) + 1024 + 256;
+  static constexpr int kStageBytes = MODE == MODE_DB ? 4 * DB_STAGE_FLOATS * 4 : 0;
+  static constexpr int kSmem = kStages * (kABytes + kBBytes) + 1024 + 256 + kStageBytes;
 };
+static_assert(Ring<MODE_DB>::kSmem <= 232448, "dB ring + staging exceed the shared memory of a CTA");
+
+// The CTA's items: a contiguous run of the planner's per-CTA schedule (dA / dB), else every
+// gridDim.x-th item from blockIdx.x.
+struct ItemRange {
+  int first, end, step;
+};
+__device__ __forceinline__ ItemRange item_range(const GemmArgs& g) {
+  if (g.cta_first) return ItemRange{g.cta_first[blockIdx.x], g.cta_first[blockIdx.x + 1], 1};
+  return ItemRange{static_cast<int>(blockIdx.x), g.n_items, static_cast<int>(gridDim.x)};
+}
 
 __device__ __forceinline__ void decode_mn(const GemmArgs& g, int item, int& m, int& n) {
   const int per_group = g.group_m * g.n_tiles_n;
@@ -139,21 +156,23 @@ __device__ __forceinline__ void produce_kblock(const GemmArgs& g, const CUtensor
       else                                 // Bt_all [d_out, C] as MN-major (n = rank column, k = d_out)
         tma_load_2d_hint(sB + j * (CHUNK_COLS * BK * 2), tmB, full, (w.q0 + j) * CHUNK_COLS, k * BK, pol_keep);
     }
-  } else {
-    const WItem w = g.witems[item];
-    const int gh = w.ga + kb;            // 64-token half tile
-    const int t = gh >> 1, h = gh & 1;
-    const MTile mt = g.mtiles[t];
-    mbar_arrive_expect_tx(full, 2 * A_STAGE_BYTES + w.nq * (IMG_BYTES / 2));
-    // X (dA) or dY (dB) as an MN-major operand: 64 hidden columns x 64 tokens per box, four boxes
-    // for the item's 256 rows (two M = 128 operands, 16 KB each)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d_hint(sA + j * (64 * 64 * 2), tmA, full, w.row0 + 64 * j, gh * 64, pol_stream);
-    // staged images as an MN-major operand: 64 rank columns x 64 tokens per box
-    for (int j = 0; j < w.nq; ++j)
-      tma_load_2d_hint(sB + j * (IMG_BYTES / 2), tmI, full, 0, (mt.img_off + w.q0 + j - mt.q_lo) * BM + h * 64,
-                       pol_keep);
   }
+}
+
+// dA / dB: the K slice of 64-token half-tile gh of item w (mt: the descriptor of gh's 128-token tile).
+__device__ __forceinline__ void produce_wgrad(const CUtensorMap* tmA, const CUtensorMap* tmI, const WItem& w,
+                                              const MTile& mt, int gh, uint8_t* sA, uint8_t* sB, uint64_t* full,
+                                              uint64_t pol_stream, uint64_t pol_keep) {
+  const int h = gh & 1;
+  mbar_arrive_expect_tx(full, 2 * A_STAGE_BYTES + w.nq * (IMG_BYTES / 2));
+  // X (dA) or dY (dB) as an MN-major operand: 64 hidden columns x 64 tokens per box, four boxes
+  // for the item's 256 rows (two M = 128 operands, 16 KB each)
+#pragma unroll
+  for (int j = 0; j < 4; ++j) tma_load_2d_hint(sA + j * (64 * 64 * 2), tmA, full, w.row0 + 64 * j, gh * 64, pol_stream);
+  // staged images as an MN-major operand: 64 rank columns x 64 tokens per box
+  for (int j = 0; j < w.nq; ++j)
+    tma_load_2d_hint(sB + j * (IMG_BYTES / 2), tmI, full, 0, (mt.img_off + w.q0 + j - mt.q_lo) * BM + h * 64,
+                     pol_keep);
 }
 
 // ------------------------------------------------------------------- MMA (one thread)
@@ -197,8 +216,110 @@ __device__ __forceinline__ int find_seg(const DevSeg* segs, int first, int last,
   return j;
 }
 
+// Write columns [32 h, 32 h + 32) of chunk jq of a dA / dB item's row half mh: this thread's
+// row, values v.  All 32 lanes of the warp call it together (the dB store is warp-cooperative).
 template <int MODE>
-__device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint32_t t_acc, int quarter, int lane) {
+__device__ __forceinline__ void wgrad_emit(const GemmArgs& g, const WItem& w, const DevSeg& sg, int mh, int jq, int h,
+                                           const uint32_t (&v)[32], float* stage, int quarter, int lane) {
+  const int bound = (MODE == MODE_DA) ? g.d_in : g.d_out;
+  const int row = w.row0 + mh * BM + quarter * 32 + lane;   // d_in (DA) or d_out (DB) index
+  const int cfirst = (w.q0 + jq) * CHUNK_COLS + h * 32;      // packed column of v[0]
+  const int t0 = cfirst - sg.c;                              // rank index of v[0]
+  if (g.subs) {
+    // several adapters per job (one per projection): each adapter of this item's job takes
+    // its own run of the chunk's columns (dB only for the output rows its B covers).  A chunk
+    // can also hold other jobs' columns; this item reduced over its own job's tokens only,
+    // so those are left to the other jobs' items.
+    if (row >= bound) return;
+#pragma unroll 1
+    for (int a = w.seg * g.n_groups; a < (w.seg + 1) * g.n_groups; ++a) {
+      const DevSub sb = g.subs[a];
+      const int lo = max(sb.c0, cfirst), hi = min(sb.c0 + sb.r, cfirst + 32);
+      if (lo >= hi) continue;
+      if constexpr (MODE == MODE_DA) {
+        // dAt[t][row]: for a fixed t the 32 lanes write 32 consecutive rows (coalesced)
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const int c = cfirst + u;
+          if (c >= lo && c < hi) sb.dAt[static_cast<size_t>(c - sb.c0) * g.d_in + row] = __uint_as_float(v[u]);
+        }
+      } else {
+        if (row < sb.o_lo || row >= sb.o_hi) continue;
+        // dBt[row - o_lo][t]: one contiguous run per thread, 16-byte stores where aligned
+        float* dst = sb.dBt + static_cast<size_t>(row - sb.o_lo) * sb.r + (cfirst - sb.c0);   // + u
+        const bool al = ((static_cast<long long>(row - sb.o_lo) * sb.r + (cfirst - sb.c0)) & 3) == 0;
+#pragma unroll
+        for (int u = 0; u < 32; u += 4) {
+          const int c = cfirst + u;
+          if (al && c >= lo && c + 3 < hi) {
+            *reinterpret_cast<float4*>(dst + u) = make_float4(__uint_as_float(v[u]), __uint_as_float(v[u + 1]),
+                                                              __uint_as_float(v[u + 2]), __uint_as_float(v[u + 3]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (c + k >= lo && c + k < hi) dst[u + k] = __uint_as_float(v[u + k]);
+          }
+        }
+      }
+    }
+    return;
+  }
+  if constexpr (MODE == MODE_DA) {
+    // dAt_i[t][row]: for a fixed t the 32 lanes write 32 consecutive rows (coalesced)
+    if (row >= bound) return;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const int t = t0 + u;
+      if (t >= 0 && t < sg.r) sg.dAt[static_cast<size_t>(t) * g.d_in + row] = __uint_as_float(v[u]);
+    }
+  } else {
+    // dBt_i[row][t]: a thread holds one row, but a row's values are contiguous in memory, so the
+    // warp goes through shared memory and stores along the rows instead
+    const int r = sg.r;
+    const int lo = max(0, t0), hi = min(r, t0 + 32);
+    const int row_w = w.row0 + mh * BM + quarter * 32;   // the warp's first row
+    const int nrows = min(32, bound - row_w);            // its rows inside d_out
+    if (hi <= lo || nrows <= 0) return;                  // the same for the whole warp
+    float* buf = stage + quarter * DB_STAGE_FLOATS;
+    if (lo == 0 && hi == r && r < 32) {
+      // every row's r values lie in these 32 columns: the warp's rows are one contiguous run of
+      // 32 r floats, packed densely here and stored by consecutive lanes
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        if (t0 + u >= 0 && t0 + u < r) buf[lane * r + t0 + u] = __uint_as_float(v[u]);
+      __syncwarp();
+      float* dst = sg.dBt + static_cast<size_t>(row_w) * r;
+      for (int e = lane; e < nrows * r; e += 32) dst[e] = buf[e];
+    } else {
+      float4* b4 = reinterpret_cast<float4*>(buf + lane * DB_STAGE_LD);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        b4[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]), __uint_as_float(v[4 * k + 2]),
+                            __uint_as_float(v[4 * k + 3]));
+      __syncwarp();
+      if ((r & 3) == 0 && (reinterpret_cast<uintptr_t>(sg.dBt) & 15) == 0 && lo == t0 && hi == t0 + 32) {
+        // four rows of 32 columns per store instruction, 16 bytes per lane
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int rr = it * 4 + (lane >> 3), cc = (lane & 7) * 4;
+          if (rr < nrows)
+            *reinterpret_cast<float4*>(sg.dBt + static_cast<size_t>(row_w + rr) * r + t0 + cc) =
+                *reinterpret_cast<const float4*>(buf + rr * DB_STAGE_LD + cc);
+        }
+      } else {
+        // part of the 32 columns: one row per store instruction
+        const int t = lo + lane;
+        for (int rr = 0; rr < nrows; ++rr)
+          if (t < hi) sg.dBt[static_cast<size_t>(row_w + rr) * r + t] = buf[rr * DB_STAGE_LD + t - t0];
+      }
+    }
+    __syncwarp();   // the staging is reused by the next call
+  }
+}
+
+// Epilogue of a base-GEMM or rank-window item (the accumulator is handed back by the caller).
+template <int MODE>
+__device__ __forceinline__ bool epilogue_item(const GemmArgs& g, int item, uint32_t t_acc, int quarter, int lane) {
   const int rit = quarter * 32 + lane;   // accumulator row owned by this thread
   if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
     int m, n;
@@ -301,88 +422,84 @@ __device__ __forceinline__ void epilogue_item(const GemmArgs& g, int item, uint3
           dst[k16] = make_uint4(pk[4 * k16], pk[4 * k16 + 1], pk[4 * k16 + 2], pk[4 * k16 + 3]);
       }
     }
-  } else {
-    const WItem w = g.witems[item];
-    const DevSeg sg = g.segs[w.seg];
-    const int bound = (MODE == MODE_DA) ? g.d_in : g.d_out;
+  }
+  return false;
+}
+
+// dA / dB epilogue of item w (job record sg), both read ahead by the caller.  Returns true if it
+// already handed the accumulator back (arrived on tempty_bar).
+template <int MODE>
+__device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w, const DevSeg& sg, uint32_t t_acc,
+                                               int quarter, int lane, float* stage, uint64_t* tempty_bar) {
+  const int rit = quarter * 32 + lane;   // accumulator row owned by this thread
+  if (w.nparts == 1) {
 #pragma unroll 1
     for (int mh = 0; mh < 2; ++mh)
 #pragma unroll 1
+      for (int jq = 0; jq < w.nq; ++jq) {
+        // both 32-column halves of the chunk in flight before one wait
+        uint32_t v[64];
+        tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+        tmem_ld_wait();
+        wgrad_emit<MODE>(g, w, sg, mh, jq, 0, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]), stage, quarter, lane);
+        wgrad_emit<MODE>(g, w, sg, mh, jq, 1, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]), stage, quarter, lane);
+      }
+    return false;
+  }
+  // One part of an item cut across CTAs: park this part's sums (column-major per chunk, so a
+  // warp's 32 rows of one column are one 128-byte line), hand the accumulator back, count the
+  // arrival; the last part of the item to arrive sums all parts in part order and writes the
+  // gradient.  No CTA waits on another.
+  float* base = g.partials + static_cast<size_t>(w.pbase) * WG_UNIT;
+  float* mine = base + static_cast<size_t>(w.part) * w.nq * WG_UNIT;
+#pragma unroll 1
+  for (int mh = 0; mh < 2; ++mh)
+#pragma unroll 1
     for (int jq = 0; jq < w.nq; ++jq) {
-      const int row = w.row0 + mh * BM + rit;             // d_in (DA) or d_out (DB) index
-      // both 32-column halves of the chunk in flight before one wait
       uint32_t v[64];
       tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait();
-      const int cbase = (w.q0 + jq) * CHUNK_COLS - sg.c;   // rank index of v[0]
-      if (row >= bound) continue;
-      if (g.subs) {
-        // several adapters per job (one per projection): each adapter of this item's job takes
-        // its own run of the chunk's columns (dB only for the output rows its B covers).  A chunk
-        // can also hold other jobs' columns; this item reduced over its own job's tokens only,
-        // so those are left to the other jobs' items.
-        const int c_first = (w.q0 + jq) * CHUNK_COLS;
-#pragma unroll 1
-        for (int a = w.seg * g.n_groups; a < (w.seg + 1) * g.n_groups; ++a) {
-          const DevSub sb = g.subs[a];
-          const int lo = max(sb.c0, c_first), hi = min(sb.c0 + sb.r, c_first + CHUNK_COLS);
-          if (lo >= hi) continue;
-          if constexpr (MODE == MODE_DA) {
-            // dAt[t][row]: for a fixed t the 32 lanes write 32 consecutive rows (coalesced)
+      float* col = mine + static_cast<size_t>((mh * w.nq + jq) * CHUNK_COLS) * BM + rit;
 #pragma unroll
-            for (int u = 0; u < 64; ++u) {
-              const int c = c_first + u;
-              if (c >= lo && c < hi) sb.dAt[static_cast<size_t>(c - sb.c0) * g.d_in + row] = __uint_as_float(v[u]);
-            }
-          } else {
-            if (row < sb.o_lo || row >= sb.o_hi) continue;
-            // dBt[row - o_lo][t]: one contiguous run per thread, 16-byte stores where aligned
-            float* dst = sb.dBt + static_cast<size_t>(row - sb.o_lo) * sb.r + (c_first - sb.c0);   // + u
-            const bool al = ((static_cast<long long>(row - sb.o_lo) * sb.r + (c_first - sb.c0)) & 3) == 0;
-#pragma unroll
-            for (int u = 0; u < 64; u += 4) {
-              const int c = c_first + u;
-              if (al && c >= lo && c + 3 < hi) {
-                *reinterpret_cast<float4*>(dst + u) = make_float4(__uint_as_float(v[u]), __uint_as_float(v[u + 1]),
-                                                                  __uint_as_float(v[u + 2]), __uint_as_float(v[u + 3]));
-              } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  if (c + k >= lo && c + k < hi) dst[u + k] = __uint_as_float(v[u + k]);
-              }
-            }
-          }
-        }
-        continue;
-      }
-      if constexpr (MODE == MODE_DA) {
-        // dAt_i[t][row]: for a fixed t the 32 lanes write 32 consecutive rows (coalesced)
-#pragma unroll
-        for (int u = 0; u < 64; ++u) {
-          const int t = cbase + u;
-          if (t >= 0 && t < sg.r) sg.dAt[static_cast<size_t>(t) * g.d_in + row] = __uint_as_float(v[u]);
-        }
-      } else {
-        // dBt_i[row][t]: this thread's row segment is contiguous; 16-byte stores where aligned
-        // (the L2 merges the lanes' partial sectors).
-        float* dst = sg.dBt + static_cast<size_t>(row) * sg.r + cbase;   // + u
-        const bool al = ((static_cast<long long>(row) * sg.r + cbase) & 3) == 0;
-#pragma unroll
-        for (int u = 0; u < 64; u += 4) {
-          const int t = cbase + u;
-          if (al && t >= 0 && t + 3 < sg.r) {
-            *reinterpret_cast<float4*>(dst + u) = make_float4(__uint_as_float(v[u]), __uint_as_float(v[u + 1]),
-                                                              __uint_as_float(v[u + 2]), __uint_as_float(v[u + 3]));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (t + k >= 0 && t + k < sg.r) dst[u + k] = __uint_as_float(v[u + k]);
-          }
-        }
-      }
+      for (int u = 0; u < 64; ++u) col[u * BM] = __uint_as_float(v[u]);
     }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tempty_bar);
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) {
+    __threadfence();   // the warp's stores (ordered before this by the warp barrier) before the count
+    int* cnt = g.part_cnt + w.cnt * 4 + quarter;
+    last = atomicAdd(cnt, 1) == w.nparts - 1;
+    if (last) *cnt = 0;   // every part has arrived: the counter is ready for the next launch
   }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return true;
+  __threadfence();
+#pragma unroll 1
+  for (int mh = 0; mh < 2; ++mh)
+#pragma unroll 1
+    for (int jq = 0; jq < w.nq; ++jq)
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const float* src = base + static_cast<size_t>((mh * w.nq + jq) * CHUNK_COLS + h * 32) * BM + rit;
+        uint32_t v[32];
+#pragma unroll 1
+        for (int p = 0; p < w.nparts; ++p) {
+          const float* sp = src + static_cast<size_t>(p) * w.nq * WG_UNIT;
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float x = __ldcg(sp + u * BM);
+            v[u] = __float_as_uint(p ? __uint_as_float(v[u]) + x : x);
+          }
+        }
+        wgrad_emit<MODE>(g, w, sg, mh, jq, h, v, stage, quarter, lane);
+      }
+  return true;
 }
 
 }  // namespace
@@ -407,8 +524,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   uint64_t* done = tempty + 2;           // [1]       MMA drain at teardown
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* stage_buf = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);   // dB epilogue staging
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ItemRange items = item_range(g);
+  constexpr bool kWgrad = Ring<MODE>::kWgrad;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -444,8 +564,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < g.n_items; item += gridDim.x) {
-        const int nkb = item_kblocks<MODE>(g, item);
+      // dA / dB items are a few K slices long: the next item's descriptor is read one item ahead,
+      // and a tile's descriptor once per tile, so no dependent load sits between two copies
+      WItem w{};
+      if (kWgrad && items.first < items.end) w = g.witems[items.first];
+      for (int item = items.first; ok && item < items.end; item += items.step) {
+        WItem w_next{};
+        if (kWgrad && item + items.step < items.end) w_next = g.witems[item + items.step];
+        const int nkb = kWgrad ? w.gb - w.ga : item_kblocks<MODE>(g, item);
+        int t_have = -1;
+        MTile mt{};
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
             ok = false;
@@ -455,6 +583,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // Test hook for the timeout path: arm the slot, issue nothing.  The MMA warp's
             // bounded wait on it runs out and records a status code; nothing faults or hangs.
             mbar_arrive_expect_tx(&full[stage], A_BYTES);
+          } else if constexpr (kWgrad) {
+            const int gh = w.ga + kb;   // 64-token half-tile
+            if ((gh >> 1) != t_have) {
+              t_have = gh >> 1;
+              mt = g.mtiles[t_have];
+            }
+            produce_wgrad(&tmA, &tmI, w, mt, gh, sA + stage * A_BYTES, sB + stage * B_BYTES, &full[stage], pol_stream,
+                          pol_keep);
           } else {
             produce_kblock<MODE>(g, &tmA, &tmB, &tmE, &tmI, item, kb, sA + stage * A_BYTES, sB + stage * B_BYTES,
                                  &full[stage], pol_stream, pol_keep);
@@ -465,6 +601,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             phase ^= 1u;
           }
         }
+        w = w_next;
       }
       if (!ok || *abort_flag) {
         // Drain: wait (bounded) for the copies of the last STAGES issued slots to land so
@@ -486,15 +623,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < g.n_items; item += gridDim.x) {
+      WItem w{};
+      if (kWgrad && items.first < items.end) w = g.witems[items.first];
+      for (int item = items.first; ok && item < items.end; item += items.step) {
+        WItem w_next{};
+        if (kWgrad && item + items.step < items.end) w_next = g.witems[item + items.step];
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        const int nkb = item_kblocks<MODE>(g, item);
-        const int ncols = item_ncols<MODE>(g, item);
+        const int nkb = kWgrad ? w.gb - w.ga : item_kblocks<MODE>(g, item);
+        const int ncols = kWgrad ? CHUNK_COLS * w.nq : item_ncols<MODE>(g, item);
+        w = w_next;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
             ok = false;
@@ -523,7 +665,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int quarter = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int item = blockIdx.x; item < g.n_items; item += gridDim.x) {
+    // dA / dB: the next item's descriptor and its job's record are read as soon as this item's
+    // epilogue is done, while the MMA may still be working on the next accumulator
+    WItem w{};
+    DevSeg sg{};
+    if (kWgrad && items.first < items.end) {
+      w = g.witems[items.first];
+      sg = g.segs[w.seg];
+    }
+    for (int item = items.first; item < items.end; item += items.step) {
       // One lane waits; the warp follows its decision so the .sync.aligned TMEM loads below
       // are always executed by all 32 lanes together.
       int ok = 1;
@@ -532,10 +682,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
-      epilogue_item<MODE>(g, item, t_acc, quarter, lane);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
+      bool released;
+      if constexpr (kWgrad)
+        released = epilogue_wgrad<MODE>(g, w, sg, t_acc, quarter, lane, stage_buf, &tempty[acc]);
+      else
+        released = epilogue_item<MODE>(g, item, t_acc, quarter, lane);
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      }
+      if (kWgrad && item + items.step < items.end) {   // ahead of the next item's accumulator wait
+        w = g.witems[item + items.step];
+        sg = g.segs[w.seg];
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }

@@ -253,7 +253,9 @@ int64_t mlora_h_elems(const mlora_plan_t* plan);
  *                     n_items(shrink), n_items(dA), n_items(dB), workspace_bytes
  *   MLORA_Q_MTILES  : per 128-row tile: first job, last job, first chunk, chunk count, image offset
  *   MLORA_Q_COLUMNS : per job: first column of its rank window, padded width
- *   MLORA_Q_WGRAD_A : per dA work item: row block, job, first and end half-tile, first chunk, chunks
+ *   MLORA_Q_WGRAD_A : per dA work item, CTA by CTA: row block, job, first and end half-tile, first
+ *                     chunk, chunks, part, parts, CTA (an item whose tokens the schedule cuts
+ *                     across CTAs runs as `parts` items; parts = 1 for a whole item)
  *   MLORA_Q_WGRAD_B : per dB work item: same fields
  *   MLORA_Q_WINDOW  : per single-CTA shrink / dH work item: tile, first chunk, chunks, first dH K
  *                     slice, dH K slices

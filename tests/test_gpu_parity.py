@@ -413,6 +413,36 @@ def test_random_shapes_vs_oracle(seed):
         run.close()
 
 
+@pytest.mark.parametrize("grouped", [False, True], ids=["one_group", "qkv_groups"])
+def test_wgrad_items_cut_across_ctas_vs_oracle(grouped):
+    """dA / dB items whose tokens the schedule cuts across CTAs (each part parks fp32 sums, the
+    last part to arrive adds them in part order): long jobs next to short ones, so that items run
+    as 3 or more parts, in a plain pack and in a shared-input pack; every output against the oracle,
+    twice in a row bitwise (the partial sums' order does not depend on arrival order)."""
+    ns = [6000, 300, 4100, 64]
+    if grouped:
+        wl = W.custom_grouped("wgrad_cut_g", 962, 1024, [512, 128, 128], [[16, 8, 8], [64, 16, 16], [128, 32, 8],
+                                                                          [8, 8, 1]], ns, b_std=0.05)
+    else:
+        wl = W.custom("wgrad_cut", 961, 1024, 768, [16, 64, 128, 8], ns, b_std=0.05, w_std=0.05)
+    T = W.materialise(wl)
+    run = G.GpuRun(wl, T, step=False)
+    try:
+        assert run.status_after_backward == M.MLORA_OK
+        for what in (M.MLORA_Q_WGRAD_A, M.MLORA_Q_WGRAD_B):
+            items = np.array(run.layer.describe(what)).reshape(-1, 9)
+            assert items[:, 7].max() >= 3
+        G.compare(run.res, G.oracle_full(wl, T), G.TOL["bf16"], ["dAt", "dBt", "dX", "Y", "H", "dH"])
+        first = [a.clone() for a in run.layer.dAt] + [b.clone() for b in run.layer.dBt]
+        run.layer.backward(run.X, run.Wt, run.dY)
+        torch.cuda.synchronize()
+        assert run.layer.sync_status() == M.MLORA_OK
+        again = list(run.layer.dAt) + list(run.layer.dBt)
+        assert all(torch.equal(a, b) for a, b in zip(first, again))
+    finally:
+        run.close()
+
+
 @pytest.mark.parametrize("reuse", [False, True], ids=["repack", "reuse_staging"])
 def test_three_training_steps_vs_oracle(reuse):
     """Three steps of forward, backward and AdamW (t = 1, 2, 3) with fresh X and dY each step: the

@@ -39,8 +39,8 @@ def _tables(plan):
     mt = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_MTILES)).reshape(-1, 5)
     cols = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_COLUMNS)).reshape(-1, 2)
     win = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WINDOW)).reshape(-1, 5)
-    da = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WGRAD_A)).reshape(-1, 6)
-    db = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WGRAD_B)).reshape(-1, 6)
+    da = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WGRAD_A)).reshape(-1, 9)
+    db = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WGRAD_B)).reshape(-1, 9)
     return summ, mt, cols, win, da, db
 
 
@@ -142,28 +142,52 @@ def _check_tables(d_in, d_out, ranks, ns):
             seen[(t, q)] = 1
     want = {(t, q) for t in range(len(mt)) for q in range(mt[t, 2], mt[t, 2] + mt[t, 3])}
     assert set(seen) == want
-    # weight-gradient work: per job, its chunk span x row blocks exactly once, tokens covered
+    # weight-gradient work: per job, its chunk span x row blocks exactly once, its tokens covered
+    # exactly once by the parts of each item; the list runs CTA by CTA, each CTA's cut parts first
+    wg_units = []
     for items, rows_total in ((da, d_in), (db, d_out)):
-        cover = {}
-        for row0, j, ga, gb, q0, nq in items:
-            assert row0 % 256 == 0 and 0 <= row0 < rows_total and 1 <= nq <= 2
-            assert ga * 64 <= offs[j] and (offs[j] + ns[j]) <= gb * 64 and gb - ga <= -(-ns[j] // 64) + 1
-            for q in range(q0, q0 + nq):
-                key = (row0, j, q)
-                assert key not in cover
-                cover[key] = 1
-        want = set()
-        for j in range(len(ns)):
-            qa, qb = cols[j, 0] // 64, -(-(cols[j, 0] + cols[j, 1]) // 64)
-            want |= {(r0, j, q) for r0 in range(0, rows_total, 256) for q in range(qa, qb)}
-        assert set(cover) == want
-        lens = [(gb - ga) * (16 + nq) for _, _, ga, gb, _, nq in items]
-        assert lens == sorted(lens, reverse=True)       # longest first
-    # workspace = bf16 shadows + the split pair items' fp32 partial sums + two image sets
+        _check_wgrad(items, rows_total, ns, offs, cols)
+        wg_units.append(sum(nq for _, _, _, _, _, nq, part, parts, _ in items if parts > 1))
+    # workspace = bf16 shadows + the split items' fp32 partial sums (one region: the pair items'
+    # or dA's / dB's, whichever is larger) + two image sets
     shadow = -(-c * d_in * 2 // 1024) * 1024 + -(-c * d_out * 2 // 1024) * 1024
     split = pw_items[pw_items[:, 6] > 1]
-    partials = len(split) * 2 * 128 * 256 * 4
+    partials = max(len(split) * 2 * 128 * 256 * 4, max(wg_units) * 256 * 64 * 4)
     assert ws == shadow + -(-partials // 1024) * 1024 + 2 * img * 16384
+
+
+def _check_wgrad(items, rows_total, ns, offs, cols):
+    cover = {}
+    parts_of = {}
+    for row0, j, ga, gb, q0, nq, part, parts, cta in items:
+        assert row0 % 256 == 0 and 0 <= row0 < rows_total and 1 <= nq <= 2
+        assert 0 <= part < parts and ga < gb
+        parts_of.setdefault((row0, j, q0, nq), []).append((part, parts, ga, gb, cta))
+    for (row0, j, q0, nq), ps in parts_of.items():
+        ps.sort()
+        S = ps[0][1]
+        assert [p[0] for p in ps] == list(range(S)) and all(p[1] == S for p in ps)
+        # the parts' token ranges tile the job's half-tiles in order, each on its own CTA
+        assert ps[0][2] * 64 <= offs[j] < (ps[0][2] + 1) * 64
+        assert (ps[-1][3] - 1) * 64 < offs[j] + ns[j] <= ps[-1][3] * 64
+        assert all(ps[k][3] == ps[k + 1][2] for k in range(S - 1))
+        assert len({p[4] for p in ps}) == S
+        if S > 1:
+            assert all(p[3] - p[2] >= 4 for p in ps)   # no part shorter than 256 tokens
+        for q in range(q0, q0 + nq):
+            key = (row0, j, q)
+            assert key not in cover
+            cover[key] = 1
+    want = set()
+    for j in range(len(ns)):
+        qa, qb = cols[j, 0] // 64, -(-(cols[j, 0] + cols[j, 1]) // 64)
+        want |= {(r0, j, q) for r0 in range(0, rows_total, 256) for q in range(qa, qb)}
+    assert set(cover) == want
+    ctas = items[:, 8]
+    assert list(ctas) == sorted(ctas) and set(ctas) == set(range(ctas.max() + 1 if len(ctas) else 0))
+    for c in set(ctas):
+        split = items[ctas == c][:, 7] > 1
+        assert list(split) == sorted(split, reverse=True)   # cut parts first
 
 
 def _status_of(fn):
@@ -263,8 +287,8 @@ def test_grouped_plan_tables():
     try:
         ad = _describe(plan, M.MLORA_Q_ADAPTERS).reshape(-1, 5)
         cols = _describe(plan, M.MLORA_Q_COLUMNS).reshape(-1, 2)
-        wa = _describe(plan, M.MLORA_Q_WGRAD_A).reshape(-1, 6)
-        wb = _describe(plan, M.MLORA_Q_WGRAD_B).reshape(-1, 6)
+        wa = _describe(plan, M.MLORA_Q_WGRAD_A).reshape(-1, 9)
+        wb = _describe(plan, M.MLORA_Q_WGRAD_B).reshape(-1, 9)
         h = M.mlora_h_elems(plan)
     finally:
         M.mlora_plan_destroy(plan)
@@ -284,14 +308,16 @@ def test_grouped_plan_tables():
         sub = ad[ad[:, 0] == j]
         for r0 in range(0, d_out, 256):
             meets = sub[(sub[:, 3] < r0 + 256) & (sub[:, 4] > r0)]
-            got = sorted(q for row0, job, ga, gb, q0, nq in wb if job == j and row0 == r0 for q in range(q0, q0 + nq))
+            got = sorted(q for row0, job, ga, gb, q0, nq, part, *_ in wb if job == j and row0 == r0 and part == 0
+                         for q in range(q0, q0 + nq))
             if len(meets) == 0:
                 assert got == []
                 continue
             lo, hi = meets[:, 1].min(), (meets[:, 1] + meets[:, 2]).max()
             assert got == list(range(lo // 64, -(-hi // 64)))
         for r0 in range(0, d_in, 256):
-            got = sorted(q for row0, job, ga, gb, q0, nq in wa if job == j and row0 == r0 for q in range(q0, q0 + nq))
+            got = sorted(q for row0, job, ga, gb, q0, nq, part, *_ in wa if job == j and row0 == r0 and part == 0
+                         for q in range(q0, q0 + nq))
             lo, hi = cols[j][0], cols[j][0] + sum(rj)
             assert got == list(range(lo // 64, -(-hi // 64)))
 
@@ -483,3 +509,25 @@ def test_base_gemm_raster_keeps_the_weight_resident():
             assert (raster_n, group) == want
         finally:
             M.mlora_plan_destroy(plan)
+
+
+def test_wgrad_schedule_balances_mixed_job_lengths():
+    """dA / dB on the Llama-3-8B k projection's pack (32 jobs of 1-8 sequences of 1024 tokens, d_out
+    1024: four 256-row blocks, so a few long jobs' items would dominate a one-item-per-CTA
+    schedule): the wrap-around schedule cuts the long items into parts of at least 256 tokens and
+    no CTA's modelled load is more than 10 % above the mean (the planner's cost: 32 + 8 nq KB per
+    64-token half-tile, 64 nq + 32 per piece, 128 nq more for a piece of a cut item)."""
+    part = W.llama8b_layer_all().parts[1]
+    assert (part.d_in, part.d_out) == (4096, 1024)
+    plan, _ = host_plan(part.d_in, part.d_out, part.ranks, part.n_tokens)
+    try:
+        got = [_describe(plan, w).reshape(-1, 9) for w in (M.MLORA_Q_WGRAD_A, M.MLORA_Q_WGRAD_B)]
+    finally:
+        M.mlora_plan_destroy(plan)
+    for items in got:
+        load = np.zeros(items[:, 8].max() + 1)
+        for _, _, ga, gb, _, nq, _, parts, c in items:
+            load[c] += (gb - ga) * (32 + 8 * nq) + 64 * nq + 32 + (128 * nq if parts > 1 else 0)
+        assert len(load) == 148                      # a host plan models a 148-SM part
+        assert load.max() <= 1.10 * load.mean()
+    assert got[1][:, 7].max() >= 2                   # dB: long jobs' items were cut
