@@ -503,16 +503,17 @@ void build_tables(mlora_plan_t* P) {
   // run at the same time should read the same X / dY rows (the neighbouring 256-column blocks of
   // one job's tokens): those reads then cover whole rows of the row-major tensor instead of
   // scattered 512-byte pieces (a schedule that ran one job's blocks one after the other on the
-  // same CTA measured 1.3-1.5x slower).  Two schedules are built and the one whose modelled end is
-  // clearly sooner is kept:
+  // same CTA measured 1.3-1.5x slower).  Two schedules are built; the cut one is kept only where
+  // its modelled end is far sooner:
   //  - greedy list scheduling of the items in job order (longest jobs first, then block, then
   //    chunks), each to the CTA with the least modelled load: consecutive items (one job's
   //    blocks) start at about the same time on different CTAs, and longest-first keeps the ends
   //    even when the items are small against a CTA's share T of the total.
   //  - McNaughton's wrap-around rule over the items in block order (then job = token order, then
-  //    chunks), for few blocks and long jobs: CTA c ends at the cumulative boundary (c + 1) T, the
-  //    item at a boundary is cut there along its tokens (at a 64-token half-tile) and its rest
-  //    starts the next CTA, so every CTA ends near T whatever the mix of job lengths.  The CTAs of
+  //    chunks), for few blocks and long jobs: each CTA takes its even share of the work still
+  //    unassigned (T at first), the item at its end is cut there along its tokens (at a 64-token
+  //    half-tile) and its rest starts the next CTA, so every CTA ends near T whatever the mix of
+  //    job lengths.  The CTAs of
   //    the blocks' runs start at the same token offsets when the block count divides the CTA
   //    count (else at a few different offsets), so CTAs of different blocks still read the same
   //    rows together.  Pieces shorter than MIN_PART_HT half-tiles are not made.  A cut item's
@@ -521,10 +522,15 @@ void build_tables(mlora_plan_t* P) {
   auto wgrad = [&](int rows, bool by_output, std::vector<WItem>& items, std::vector<int>& first, int& sets,
                    int& units) {
     // modelled cost, in KB moved: per half-tile the streamed operand (32 KB) and the images (8 KB
-    // per chunk); per piece its epilogue (64 KB of fp32 sums per chunk) and a start-up
+    // per chunk); per piece its output (the gradient's 256 rows x 4 bytes, 1 KB, per column of the
+    // job inside the item's chunks) and a start-up
     auto per_ht = [](int nq) { return 32.0 + 8.0 * nq; };
-    auto fixed = [](int nq) { return 64.0 * nq + 32.0; };
-    auto cost = [&](const WItem& w) { return fixed(w.nq) + per_ht(w.nq) * (w.gb - w.ga); };
+    auto fixed = [&](const WItem& w) {
+      const DevSeg& d = P->segs[w.seg];
+      const int lo = std::max(d.c, w.q0 * CHUNK_COLS), hi = std::min(d.c + d.r, (w.q0 + w.nq) * CHUNK_COLS);
+      return 32.0 + std::max(0, hi - lo);
+    };
+    auto cost = [&](const WItem& w) { return fixed(w) + per_ht(w.nq) * (w.gb - w.ga); };
     // items of job i in row block r0
     auto block_items = [&](int i, int r0, std::vector<WItem>& out) {
       const DevSeg& d = P->segs[i];
@@ -570,20 +576,24 @@ void build_tables(mlora_plan_t* P) {
       g_span = *std::max_element(load.begin(), load.end());
     }
 
-    // McNaughton over the block order.  A piece of a cut item also writes its partial sums and
-    // the item's last part reads them all back: 128 KB per chunk per piece on top of its cost.
+    // McNaughton over the block order.  A piece of a cut item also writes its partial sums (all
+    // 64 columns of a chunk) and the item's last part reads them all back: 128 KB per chunk per
+    // piece on top of its cost.  Each CTA takes up to T; T is the smallest budget (to 0.1 %, by
+    // bisection) at which the last CTA's share stays within it as well.
     std::vector<std::vector<WItem>> m_cut, m_whole;
     double m_span = 0;
     int m_sets = 0, m_units = 0;
     {
-      auto piece_cost = [&](int nq, int nh, bool is_cut) { return fixed(nq) + per_ht(nq) * nh + (is_cut ? 128.0 * nq : 0.0); };
-      double T = total / n_cta;
-      for (int pass = 0; pass < 4; ++pass) {
+      auto piece_cost = [&](const WItem& w, int nh, bool is_cut) {
+        return fixed(w) + per_ht(w.nq) * nh + (is_cut ? 128.0 * w.nq : 0.0);
+      };
+      // lays the items out with budget T; returns the load of the last CTA (which takes whatever
+      // is left) and sets m_span to the largest load
+      auto lay_out = [&](double T) {
         m_cut.assign(n_cta, {});
         m_whole.assign(n_cta, {});
         std::vector<double> load(n_cta, 0.0);
         int c = 0;
-        double done = 0;   // cost assigned so far
         m_sets = 0;
         m_units = 0;
         for (const WItem& w : v) {
@@ -591,14 +601,14 @@ void build_tables(mlora_plan_t* P) {
           int a = w.ga;
           while (a < w.gb) {
             const int nh = w.gb - a;
-            const double room = (c + 1) * T - done - piece_cost(w.nq, 0, true);
+            const double room = T - load[c] - piece_cost(w, 0, true);
             int take = static_cast<int>(std::floor(room / per_ht(w.nq)));
             if (c == n_cta - 1 || take >= nh) {
               take = nh;   // the rest fits (or the last CTA takes it)
             } else {
               if (take < MIN_PART_HT) {
-                // a piece of MIN_PART_HT here overfills this CTA, none leaves its room to the next
-                // CTA: take the smaller of the two deviations
+                // a piece of MIN_PART_HT here overfills this CTA, none leaves its room empty: take
+                // the smaller of the two deviations
                 const bool empty = m_cut[c].empty() && m_whole[c].empty();
                 if (!empty && room < 0.5 * MIN_PART_HT * per_ht(w.nq)) {
                   ++c;
@@ -612,9 +622,7 @@ void build_tables(mlora_plan_t* P) {
             }
             pieces.push_back({c, a, a + take});
             (take == w.gb - w.ga ? m_whole : m_cut)[c].push_back(w);   // filled in below
-            const double pc = piece_cost(w.nq, take, take != w.gb - w.ga);
-            done += pc;
-            load[c] += pc;
+            load[c] += piece_cost(w, take, take != w.gb - w.ga);
             a += take;
             if (a < w.gb) ++c;
           }
@@ -634,13 +642,20 @@ void build_tables(mlora_plan_t* P) {
           }
         }
         m_span = *std::max_element(load.begin(), load.end());
-        const double T_next = done / n_cta;
-        if (T_next <= T * 1.001) break;
-        T = T_next;
+        return load[n_cta - 1];
+      };
+      double lo = total / n_cta, hi = 1.25 * lo;
+      while (lay_out(hi) > hi && hi < 64 * total) hi *= 1.25;
+      while (hi - lo > 0.001 * hi) {
+        const double mid = 0.5 * (lo + hi);
+        (lay_out(mid) > mid ? lo : hi) = mid;
       }
+      lay_out(hi);
     }
-    // the cut schedule only where it ends clearly sooner
-    const bool use_m = m_span < 0.95 * g_span;
+    // The cut schedule only where the greedy one is far off: its parts' partial sums and the last
+    // part's sum cost more than the model counts (measured: the cut schedule lost at a modelled
+    // 0.79 of the greedy end on a 16-block dA, and won at about 0.5 on a 4-block dB).
+    const bool use_m = m_span < 0.7 * g_span;
     std::vector<std::vector<WItem>> cut, whole;
     if (use_m) {
       cut = std::move(m_cut);

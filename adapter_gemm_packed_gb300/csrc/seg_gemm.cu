@@ -447,23 +447,37 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w
       }
     return false;
   }
-  // One part of an item cut across CTAs: park this part's sums (column-major per chunk, so a
-  // warp's 32 rows of one column are one 128-byte line), hand the accumulator back, count the
-  // arrival; the last part of the item to arrive sums all parts in part order and writes the
-  // gradient.  No CTA waits on another.
-  float* base = g.partials + static_cast<size_t>(w.pbase) * WG_UNIT;
-  float* mine = base + static_cast<size_t>(w.part) * w.nq * WG_UNIT;
+  // One part of an item cut across CTAs: park this part's sums, hand the accumulator back, count
+  // the arrival; the last part of the item to arrive sums all parts in part order and writes the
+  // gradient.  No CTA waits on another.  A part parks each 32-column group (row half mh, chunk jq,
+  // half h) that holds some of the job's columns as 8 runs of 4 columns, a run being [128 rows] of
+  // float4: a warp's 32 rows of a run are one 512-byte line, and the last part's sum has 8 loads
+  // in flight per part, two parts per round trip.
+  auto live = [&](int jq, int h) {
+    const int t0 = (w.q0 + jq) * CHUNK_COLS + h * 32 - sg.c;
+    return max(0, t0) < min(sg.r, t0 + 32);
+  };
+  float4* base = reinterpret_cast<float4*>(g.partials + static_cast<size_t>(w.pbase) * WG_UNIT);
+  const size_t part_f4 = static_cast<size_t>(w.nq) * (WG_UNIT / 4);   // float4s per part
+  float4* mine = base + static_cast<size_t>(w.part) * part_f4;
 #pragma unroll 1
   for (int mh = 0; mh < 2; ++mh)
 #pragma unroll 1
     for (int jq = 0; jq < w.nq; ++jq) {
+      if (!live(jq, 0) && !live(jq, 1)) continue;   // the same for the whole warp
       uint32_t v[64];
       tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait();
-      float* col = mine + static_cast<size_t>((mh * w.nq + jq) * CHUNK_COLS) * BM + rit;
 #pragma unroll
-      for (int u = 0; u < 64; ++u) col[u * BM] = __uint_as_float(v[u]);
+      for (int h = 0; h < 2; ++h) {
+        if (!live(jq, h)) continue;
+        float4* dst = mine + static_cast<size_t>(((mh * w.nq + jq) * 2 + h) * 8) * BM + rit;
+#pragma unroll
+        for (int u4 = 0; u4 < 8; ++u4)
+          dst[u4 * BM] = make_float4(__uint_as_float(v[h * 32 + 4 * u4]), __uint_as_float(v[h * 32 + 4 * u4 + 1]),
+                                     __uint_as_float(v[h * 32 + 4 * u4 + 2]), __uint_as_float(v[h * 32 + 4 * u4 + 3]));
+      }
     }
   tc_fence_before();
   __syncwarp();
@@ -480,22 +494,50 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return true;
   __threadfence();
+  const int S = w.nparts;
 #pragma unroll 1
   for (int mh = 0; mh < 2; ++mh)
 #pragma unroll 1
     for (int jq = 0; jq < w.nq; ++jq)
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        const float* src = base + static_cast<size_t>((mh * w.nq + jq) * CHUNK_COLS + h * 32) * BM + rit;
-        uint32_t v[32];
+        if (!live(jq, h)) continue;
+        const float4* src = base + static_cast<size_t>(((mh * w.nq + jq) * 2 + h) * 8) * BM + rit;
+        float4 acc[8];
 #pragma unroll 1
-        for (int p = 0; p < w.nparts; ++p) {
-          const float* sp = src + static_cast<size_t>(p) * w.nq * WG_UNIT;
+        for (int p = 0; p < S; p += 2) {
+          float4 a[8], b[8];
+          const bool two = p + 1 < S;
 #pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const float x = __ldcg(sp + u * BM);
-            v[u] = __float_as_uint(p ? __uint_as_float(v[u]) + x : x);
+          for (int u4 = 0; u4 < 8; ++u4) {
+            a[u4] = __ldcg(src + p * part_f4 + u4 * BM);
+            if (two) b[u4] = __ldcg(src + (p + 1) * part_f4 + u4 * BM);
           }
+#pragma unroll
+          for (int u4 = 0; u4 < 8; ++u4) {
+            if (p == 0) {
+              acc[u4] = a[u4];
+            } else {
+              acc[u4].x += a[u4].x;
+              acc[u4].y += a[u4].y;
+              acc[u4].z += a[u4].z;
+              acc[u4].w += a[u4].w;
+            }
+            if (two) {
+              acc[u4].x += b[u4].x;
+              acc[u4].y += b[u4].y;
+              acc[u4].z += b[u4].z;
+              acc[u4].w += b[u4].w;
+            }
+          }
+        }
+        uint32_t v[32];
+#pragma unroll
+        for (int u4 = 0; u4 < 8; ++u4) {
+          v[4 * u4] = __float_as_uint(acc[u4].x);
+          v[4 * u4 + 1] = __float_as_uint(acc[u4].y);
+          v[4 * u4 + 2] = __float_as_uint(acc[u4].z);
+          v[4 * u4 + 3] = __float_as_uint(acc[u4].w);
         }
         wgrad_emit<MODE>(g, w, sg, mh, jq, h, v, stage, quarter, lane);
       }

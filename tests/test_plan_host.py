@@ -516,18 +516,21 @@ def test_wgrad_schedule_balances_mixed_job_lengths():
     1024: four 256-row blocks, so a few long jobs' items would dominate a one-item-per-CTA
     schedule): the wrap-around schedule cuts the long items into parts of at least 256 tokens and
     no CTA's modelled load is more than 10 % above the mean (the planner's cost: 32 + 8 nq KB per
-    64-token half-tile, 64 nq + 32 per piece, 128 nq more for a piece of a cut item)."""
+    64-token half-tile; per piece 32 plus 1 per column of the job's rank window inside the piece's
+    chunks, and 128 nq more for a piece of a cut item)."""
     part = W.llama8b_layer_all().parts[1]
     assert (part.d_in, part.d_out) == (4096, 1024)
     plan, _ = host_plan(part.d_in, part.d_out, part.ranks, part.n_tokens)
     try:
         got = [_describe(plan, w).reshape(-1, 9) for w in (M.MLORA_Q_WGRAD_A, M.MLORA_Q_WGRAD_B)]
+        cols = _describe(plan, M.MLORA_Q_COLUMNS).reshape(-1, 2)
     finally:
         M.mlora_plan_destroy(plan)
     for items in got:
         load = np.zeros(items[:, 8].max() + 1)
-        for _, _, ga, gb, _, nq, _, parts, c in items:
-            load[c] += (gb - ga) * (32 + 8 * nq) + 64 * nq + 32 + (128 * nq if parts > 1 else 0)
+        for _, j, ga, gb, q0, nq, _, parts, c in items:
+            inside = max(0, min(cols[j, 0] + part.ranks[j], 64 * (q0 + nq)) - max(cols[j, 0], 64 * q0))
+            load[c] += (gb - ga) * (32 + 8 * nq) + 32 + inside + (128 * nq if parts > 1 else 0)
         assert len(load) == 148                      # a host plan models a 148-SM part
         assert load.max() <= 1.10 * load.mean()
     assert got[1][:, 7].max() >= 2                   # dB: long jobs' items were cut
