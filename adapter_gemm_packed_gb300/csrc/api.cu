@@ -24,6 +24,7 @@
 
 #include "common.cuh"
 #include "mlora.h"
+#include "raster.cuh"
 #include "pair.cuh"
 
 namespace mlora {
@@ -843,19 +844,6 @@ cudaError_t timed(const mlora_plan_t* Pc, int id, cudaStream_t s, F&& launch) {
   return e;
 }
 
-// Work list of the CTA-pair base GEMMs: 256x256 tiles, except that when the last wave would fill at
-// most half of the pairs its tiles are split into 256x128 halves, which finish that wave in half
-// the time (and give small problems twice the pairs).  Returns the number of pairs to launch.
-int pair_gemm_items(const mlora_plan_t* P, GemmArgs& g) {
-  const int n_tiles = ((P->n_mtiles + 1) / 2) * g.n_tiles_n;
-  const int pairs = std::max(1, P->num_sms / 2);
-  const int tail = n_tiles <= pairs ? n_tiles : n_tiles % pairs;
-  const bool split = tail > 0 && 2 * tail <= pairs;
-  g.n_full_items = split ? n_tiles - tail : n_tiles;
-  g.n_items = split ? n_tiles + tail : n_tiles;
-  return std::max(1, std::min(g.n_items, pairs));
-}
-
 GemmArgs base_args(const mlora_plan_t* P) {
   GemmArgs g{};
   g.N = static_cast<int>(P->prob.n_tokens);
@@ -879,35 +867,6 @@ GemmArgs base_args(const mlora_plan_t* P) {
 }
 
 int grid_of(const mlora_plan_t* P, int items) { return std::max(1, std::min(items, P->num_sms)); }
-
-// L2 room for the resident panel of a CTA-pair base GEMM's raster (see decode_pair).
-constexpr double RASTER_PANEL_BUDGET = 48.0 * (1 << 20);
-
-// Order and group size of a CTA-pair base GEMM's raster over its m_pairs x n_tiles full tiles
-// (K = the main product's reduction length).  Every 256-token pair reads a 256 x K panel of A and
-// every output tile a 256 x K panel of B (bf16).  A group of g tiles along one dimension keeps
-// its g panels in L2 while it sweeps the other dimension, so that dimension's panels are read
-// from HBM once per group: DRAM bytes ~ (resident side, once) + (swept side) x (groups).  The
-// resident panels must fit the L2 budget; groups are made equal.  Ties go to output-tile groups
-// (the weight stays resident).
-void set_raster(GemmArgs& g, int K) {
-  const double panel = 256.0 * K * 2.0;
-  const double budget = RASTER_PANEL_BUDGET;
-  const long long m_pairs = (g.n_mtiles + 1) / 2, n_tiles = g.n_tiles_n;
-  const long long gmax = std::max(1LL, static_cast<long long>(budget / panel));
-  double best = 0.0;
-  for (int by_n = 1; by_n >= 0; --by_n) {
-    const long long res = by_n ? n_tiles : m_pairs, swept = by_n ? m_pairs : n_tiles;
-    const long long groups = (res + std::min(res, gmax) - 1) / std::min(res, gmax);
-    const long long gsz = (res + groups - 1) / groups;
-    const double bytes = panel * (static_cast<double>(res) + static_cast<double>(swept) * groups);
-    if (by_n == 1 || bytes < best) {
-      best = bytes;
-      g.raster_n = by_n;
-      g.group_m = static_cast<int>(gsz);
-    }
-  }
-}
 
 mlora_status check_exec(const mlora_plan_t* P) {
   if (!P) return fail(MLORA_ERR_INVALID, "null plan");
@@ -1105,7 +1064,7 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
       return launch_gemm_2sm_w4<MODE_FWD>(mX, mQ, mS, mBt, mI, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
     });
   } else if (pairs) {
-    const int n_pairs = pair_gemm_items(P, g);
+    const int n_pairs = pair_gemm_items(P->n_mtiles, P->num_sms, g);
     g.debug_drop = P->debug_drop_pairs ? 1 : 0;
     e = timed(P, K_FWD_GEMM, s, [&] { return launch_gemm_2sm<MODE_FWD>(mX, mW, mBt, mI, mW64, mBt64, g, n_pairs, s); });
   } else {
@@ -1253,7 +1212,7 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
       return launch_gemm_2sm_w4<MODE_BWD>(mdY, mQ, mS, mAt64, mdHi, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
     });
   } else if (pairs) {
-    const int n_pairs = pair_gemm_items(P, g);
+    const int n_pairs = pair_gemm_items(P->n_mtiles, P->num_sms, g);
     e = timed(P, K_BWD_GEMM, s, [&] {
       return launch_gemm_2sm<MODE_BWD>(mdY, mWmn, mAt64, mdHi, mWmn, mAt64, g, n_pairs, s);
     });
@@ -1429,7 +1388,7 @@ mlora_status mlora_plan_describe(const mlora_plan_t* P, int32_t what, int64_t* o
       GemmArgs g = base_args(P);
       g.n_tiles_n = ((fwd ? P->prob.d_out : P->prob.d_in) + BN - 1) / BN;
       set_raster(g, fwd ? P->prob.d_in : P->prob.d_out);
-      const int n_pairs = pair_gemm_items(P, g);
+      const int n_pairs = pair_gemm_items(P->n_mtiles, P->num_sms, g);
       v = {g.raster_n, g.group_m, g.n_items, g.n_full_items, n_pairs};
       for (int it = 0; it < g.n_items; ++it) {
         int mp, col0, width;
