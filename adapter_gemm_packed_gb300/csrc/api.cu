@@ -746,10 +746,10 @@ size_t table_bytes(const std::vector<T>& v) {
 }
 
 // Arrival counters of split items: 8 per split CTA-pair item (CTA of the pair x row quarter), then
-// 4 per cut dA item and 4 per cut dB item (row quarters).
+// 8 per cut dA item and 8 per cut dB item (row quarter x 128-row half: one per epilogue warp).
 size_t counter_ints(const mlora_plan_t* P) {
-  return static_cast<size_t>(P->n_split) * 8 + static_cast<size_t>(P->da_sets) * 4 +
-         static_cast<size_t>(P->db_sets) * 4;
+  return static_cast<size_t>(P->n_split) * 8 + static_cast<size_t>(P->da_sets) * 8 +
+         static_cast<size_t>(P->db_sets) * 8;
 }
 
 mlora_status upload(mlora_plan_t* P) {
@@ -1193,7 +1193,7 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   g.n_items = static_cast<int>(P->db.size());
   g.cta_first = P->d_db_first;
   g.partials = reinterpret_cast<float*>(ws + P->off_partials);
-  g.part_cnt = P->d_part_cnt ? P->d_part_cnt + static_cast<size_t>(P->n_split) * 8 + static_cast<size_t>(P->da_sets) * 4
+  g.part_cnt = P->d_part_cnt ? P->d_part_cnt + static_cast<size_t>(P->n_split) * 8 + static_cast<size_t>(P->da_sets) * 8
                              : nullptr;
   const int db_ctas = static_cast<int>(P->db_first.size()) - 1;
   e = timed(P, K_DB, s, [&] { return launch_seg_gemm<MODE_DB>(mdYt, mdYt, mdYt, mHi, g, db_ctas, s); });

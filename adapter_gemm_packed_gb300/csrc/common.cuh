@@ -156,7 +156,7 @@ struct GemmArgs {
   int debug_drop;          // test hook: CTA 0 arms its first slot but issues no copy into it
   float* partials;         // fp32 partial sums of items split across CTAs (workspace)
   int* part_cnt;           // ... and their arrival counters (pair items: slot, CTA of the pair,
-                           // row quarter; dA / dB items: counter set, row quarter)
+                           // row quarter; dA / dB items: counter set, row quarter, row half)
   const int* cta_first;    // dA / dB: CTA c runs items [cta_first[c], cta_first[c + 1]) (null: round robin)
   // Shared-input packs (several adapters per job): per packed column, its adapter (-1 in the
   // padding) and scale.  Null for plans with one adapter per job, whose kernels read the job's.

@@ -26,10 +26,11 @@
 // per job without masks in the main loop (tLoRA's "adaptively reconstructed low-rank tiles",
 // read as tiles assembled from the jobs a token tile happens to cover).
 //
-// Roles (192 threads, one CTA per SM, persistent over a static work list):
+// Roles (192 threads, 320 for dA / dB; one CTA per SM, persistent over a static work list):
 //   warp 0     TMA producer (one lane) into a STAGES-deep smem ring
 //   warp 1     TMEM allocator and MMA issuer (one lane), two 256-column accumulators
-//   warps 2-5  epilogue: TMEM -> registers -> global (lane quarter = warp id % 4)
+//   warps 2-5  epilogue: TMEM -> registers -> global (lane quarter = warp id % 4); dA / dB have
+//              warps 2-9, two per lane quarter (one per 128-row half of the item)
 // Every wait is bounded (see mbar_wait): on expiry the CTA records a status code, drains
 // what it issued, frees TMEM and returns.
 #include "common.cuh"
@@ -46,11 +47,16 @@ namespace {
 // reaches 6.6 TB/s with 4 x 16 KB per SM).
 // dA / dB items cover 256 rows of d_in / d_out (two M = 128 MMAs per K step sharing one staged
 // image operand), so their ring holds 32 KB of the streamed operand per stage.
-// dB's epilogue also stages each warp's 32 rows x 32 columns in shared memory (rows padded to 36
-// floats, so that both the row-wise writes and the 4-row reads run conflict-free) to store dB^T
-// rows with consecutive lanes on consecutive addresses.
-constexpr int DB_STAGE_LD = 36;
-constexpr int DB_STAGE_FLOATS = 32 * DB_STAGE_LD;
+// dB's epilogue also stages each warp's 32 rows x 16 columns in shared memory to store dB^T rows
+// with consecutive lanes on consecutive addresses: a row's four float4 sit at slots k ^ ((row >> 1)
+// & 3), so that both the row-wise writes (one row per lane) and the reads (eight rows of 16
+// columns per instruction) touch every bank once per 128 bytes.
+constexpr int DB_STAGE_FLOATS = 32 * 16;
+__device__ __forceinline__ int db_slot(int row, int k) { return row * 4 + (k ^ ((row >> 1) & 3)); }
+
+// dA / dB run two epilogue warps per TMEM lane quarter (one per 128-row half of the item): their
+// items are a few K slices long and their epilogue writes as many bytes as the item reads, so its
+// latency chain (TMEM load, staging, store) would otherwise set the pace.
 template <int MODE>
 struct Ring {
   static constexpr bool kBase = MODE == MODE_FWD || MODE == MODE_BWD;
@@ -58,7 +64,9 @@ struct Ring {
   static constexpr int kStages = kBase ? 4 : (kWgrad ? 4 : 6);
   static constexpr int kABytes = kWgrad ? 2 * A_STAGE_BYTES : A_STAGE_BYTES;
   static constexpr int kBBytes = kBase ? B_STAGE_BYTES : MAX_ITEM_CHUNKS * CHUNK_COLS * BK * 2;
-  static constexpr int kStageBytes = MODE == MODE_DB ? 4 * DB_STAGE_FLOATS * 4 : 0;
+  static constexpr int kEpiWarps = kWgrad ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kStageBytes = MODE == MODE_DB ? kEpiWarps * DB_STAGE_FLOATS * 4 : 0;
   static constexpr int kSmem = kStages * (kABytes + kBBytes) + 1024 + 256 + kStageBytes;
 };
 static_assert(Ring<MODE_DB>::kSmem <= 232448, "dB ring + staging exceed the shared memory of a CTA");
@@ -274,46 +282,55 @@ __device__ __forceinline__ void wgrad_emit(const GemmArgs& g, const WItem& w, co
     }
   } else {
     // dBt_i[row][t]: a thread holds one row, but a row's values are contiguous in memory, so the
-    // warp goes through shared memory and stores along the rows instead
+    // warp goes through shared memory and stores along the rows instead, 16 columns at a time
     const int r = sg.r;
-    const int lo = max(0, t0), hi = min(r, t0 + 32);
     const int row_w = w.row0 + mh * BM + quarter * 32;   // the warp's first row
     const int nrows = min(32, bound - row_w);            // its rows inside d_out
-    if (hi <= lo || nrows <= 0) return;                  // the same for the whole warp
-    float* buf = stage + quarter * DB_STAGE_FLOATS;
-    if (lo == 0 && hi == r && r < 32) {
-      // every row's r values lie in these 32 columns: the warp's rows are one contiguous run of
-      // 32 r floats, packed densely here and stored by consecutive lanes
+    if (nrows <= 0) return;                              // the same for the whole warp
+    float* buf = stage;
+    float4* buf4 = reinterpret_cast<float4*>(stage);
+    const bool al4 = (r & 3) == 0 && (reinterpret_cast<uintptr_t>(sg.dBt) & 15) == 0;
 #pragma unroll
-      for (int u = 0; u < 32; ++u)
-        if (t0 + u >= 0 && t0 + u < r) buf[lane * r + t0 + u] = __uint_as_float(v[u]);
-      __syncwarp();
-      float* dst = sg.dBt + static_cast<size_t>(row_w) * r;
-      for (int e = lane; e < nrows * r; e += 32) dst[e] = buf[e];
-    } else {
-      float4* b4 = reinterpret_cast<float4*>(buf + lane * DB_STAGE_LD);
+    for (int qq = 0; qq < 2; ++qq) {
+      const int tq = t0 + qq * 16;   // rank index of this quarter's first column
+      const int lo = max(0, tq), hi = min(r, tq + 16);
+      if (hi <= lo) continue;        // the same for the whole warp
+      if (lo == 0 && hi == r && r < 16) {
+        // every row's r values lie in these 16 columns: the warp's rows are one contiguous run of
+        // 32 r floats, packed densely here and stored by consecutive lanes
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        b4[k] = make_float4(__uint_as_float(v[4 * k]), __uint_as_float(v[4 * k + 1]), __uint_as_float(v[4 * k + 2]),
-                            __uint_as_float(v[4 * k + 3]));
-      __syncwarp();
-      if ((r & 3) == 0 && (reinterpret_cast<uintptr_t>(sg.dBt) & 15) == 0 && lo == t0 && hi == t0 + 32) {
-        // four rows of 32 columns per store instruction, 16 bytes per lane
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int rr = it * 4 + (lane >> 3), cc = (lane & 7) * 4;
-          if (rr < nrows)
-            *reinterpret_cast<float4*>(sg.dBt + static_cast<size_t>(row_w + rr) * r + t0 + cc) =
-                *reinterpret_cast<const float4*>(buf + rr * DB_STAGE_LD + cc);
-        }
+        for (int u = 0; u < 16; ++u)
+          if (tq + u >= 0 && tq + u < r) buf[lane * r + tq + u] = __uint_as_float(v[qq * 16 + u]);
+        __syncwarp();
+        float* dst = sg.dBt + static_cast<size_t>(row_w) * r;
+        for (int e = lane; e < nrows * r; e += 32) dst[e] = buf[e];
       } else {
-        // part of the 32 columns: one row per store instruction
-        const int t = lo + lane;
-        for (int rr = 0; rr < nrows; ++rr)
-          if (t < hi) sg.dBt[static_cast<size_t>(row_w + rr) * r + t] = buf[rr * DB_STAGE_LD + t - t0];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          buf4[db_slot(lane, k)] = make_float4(__uint_as_float(v[qq * 16 + 4 * k]), __uint_as_float(v[qq * 16 + 4 * k + 1]),
+                                               __uint_as_float(v[qq * 16 + 4 * k + 2]),
+                                               __uint_as_float(v[qq * 16 + 4 * k + 3]));
+        __syncwarp();
+        if (al4 && lo == tq && hi == tq + 16) {
+          // eight rows of 16 columns per store instruction, 16 bytes per lane
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int rr = it * 8 + (lane >> 2), k = lane & 3;
+            if (rr < nrows)
+              *reinterpret_cast<float4*>(sg.dBt + static_cast<size_t>(row_w + rr) * r + tq + 4 * k) = buf4[db_slot(rr, k)];
+          }
+        } else {
+          // part of the 16 columns: one row per store instruction
+          const int t = lo + lane;
+          if (lane < 16) {
+            const int c = t - tq;
+            for (int rr = 0; rr < nrows; ++rr)
+              if (t < hi) sg.dBt[static_cast<size_t>(row_w + rr) * r + t] = buf[db_slot(rr, c >> 2) * 4 + (c & 3)];
+          }
+        }
       }
+      __syncwarp();   // the staging is reused next
     }
-    __syncwarp();   // the staging is reused by the next call
   }
 }
 
@@ -429,22 +446,21 @@ __device__ __forceinline__ bool epilogue_item(const GemmArgs& g, int item, uint3
 // dA / dB epilogue of item w (job record sg), both read ahead by the caller.  Returns true if it
 // already handed the accumulator back (arrived on tempty_bar).
 template <int MODE>
+// This warp handles row half mh of the item (lanes of its quarter); `stage` is its own staging.
 __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w, const DevSeg& sg, uint32_t t_acc,
-                                               int quarter, int lane, float* stage, uint64_t* tempty_bar) {
+                                               int quarter, int mh, int lane, float* stage, uint64_t* tempty_bar) {
   const int rit = quarter * 32 + lane;   // accumulator row owned by this thread
   if (w.nparts == 1) {
 #pragma unroll 1
-    for (int mh = 0; mh < 2; ++mh)
-#pragma unroll 1
-      for (int jq = 0; jq < w.nq; ++jq) {
-        // both 32-column halves of the chunk in flight before one wait
-        uint32_t v[64];
-        tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-        tmem_ld_wait();
-        wgrad_emit<MODE>(g, w, sg, mh, jq, 0, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]), stage, quarter, lane);
-        wgrad_emit<MODE>(g, w, sg, mh, jq, 1, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]), stage, quarter, lane);
-      }
+    for (int jq = 0; jq < w.nq; ++jq) {
+      // both 32-column halves of the chunk in flight before one wait
+      uint32_t v[64];
+      tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld_wait();
+      wgrad_emit<MODE>(g, w, sg, mh, jq, 0, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]), stage, quarter, lane);
+      wgrad_emit<MODE>(g, w, sg, mh, jq, 1, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]), stage, quarter, lane);
+    }
     return false;
   }
   // One part of an item cut across CTAs: park this part's sums, hand the accumulator back, count
@@ -461,24 +477,22 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w
   const size_t part_f4 = static_cast<size_t>(w.nq) * (WG_UNIT / 4);   // float4s per part
   float4* mine = base + static_cast<size_t>(w.part) * part_f4;
 #pragma unroll 1
-  for (int mh = 0; mh < 2; ++mh)
-#pragma unroll 1
-    for (int jq = 0; jq < w.nq; ++jq) {
-      if (!live(jq, 0) && !live(jq, 1)) continue;   // the same for the whole warp
-      uint32_t v[64];
-      tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-      tmem_ld_wait();
+  for (int jq = 0; jq < w.nq; ++jq) {
+    if (!live(jq, 0) && !live(jq, 1)) continue;   // the same for the whole warp
+    uint32_t v[64];
+    tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+    tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+    tmem_ld_wait();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (!live(jq, h)) continue;
-        float4* dst = mine + static_cast<size_t>(((mh * w.nq + jq) * 2 + h) * 8) * BM + rit;
+    for (int h = 0; h < 2; ++h) {
+      if (!live(jq, h)) continue;
+      float4* dst = mine + static_cast<size_t>(((mh * w.nq + jq) * 2 + h) * 8) * BM + rit;
 #pragma unroll
-        for (int u4 = 0; u4 < 8; ++u4)
-          dst[u4 * BM] = make_float4(__uint_as_float(v[h * 32 + 4 * u4]), __uint_as_float(v[h * 32 + 4 * u4 + 1]),
-                                     __uint_as_float(v[h * 32 + 4 * u4 + 2]), __uint_as_float(v[h * 32 + 4 * u4 + 3]));
-      }
+      for (int u4 = 0; u4 < 8; ++u4)
+        dst[u4 * BM] = make_float4(__uint_as_float(v[h * 32 + 4 * u4]), __uint_as_float(v[h * 32 + 4 * u4 + 1]),
+                                   __uint_as_float(v[h * 32 + 4 * u4 + 2]), __uint_as_float(v[h * 32 + 4 * u4 + 3]));
     }
+  }
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(tempty_bar);
@@ -487,7 +501,7 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w
   int last = 0;
   if (lane == 0) {
     __threadfence();   // the warp's stores (ordered before this by the warp barrier) before the count
-    int* cnt = g.part_cnt + w.cnt * 4 + quarter;
+    int* cnt = g.part_cnt + w.cnt * 8 + quarter * 2 + mh;
     last = atomicAdd(cnt, 1) == w.nparts - 1;
     if (last) *cnt = 0;   // every part has arrived: the counter is ready for the next launch
   }
@@ -496,58 +510,56 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w
   __threadfence();
   const int S = w.nparts;
 #pragma unroll 1
-  for (int mh = 0; mh < 2; ++mh)
+  for (int jq = 0; jq < w.nq; ++jq)
 #pragma unroll 1
-    for (int jq = 0; jq < w.nq; ++jq)
+    for (int h = 0; h < 2; ++h) {
+      if (!live(jq, h)) continue;
+      const float4* src = base + static_cast<size_t>(((mh * w.nq + jq) * 2 + h) * 8) * BM + rit;
+      float4 acc[8];
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        if (!live(jq, h)) continue;
-        const float4* src = base + static_cast<size_t>(((mh * w.nq + jq) * 2 + h) * 8) * BM + rit;
-        float4 acc[8];
-#pragma unroll 1
-        for (int p = 0; p < S; p += 2) {
-          float4 a[8], b[8];
-          const bool two = p + 1 < S;
-#pragma unroll
-          for (int u4 = 0; u4 < 8; ++u4) {
-            a[u4] = __ldcg(src + p * part_f4 + u4 * BM);
-            if (two) b[u4] = __ldcg(src + (p + 1) * part_f4 + u4 * BM);
-          }
-#pragma unroll
-          for (int u4 = 0; u4 < 8; ++u4) {
-            if (p == 0) {
-              acc[u4] = a[u4];
-            } else {
-              acc[u4].x += a[u4].x;
-              acc[u4].y += a[u4].y;
-              acc[u4].z += a[u4].z;
-              acc[u4].w += a[u4].w;
-            }
-            if (two) {
-              acc[u4].x += b[u4].x;
-              acc[u4].y += b[u4].y;
-              acc[u4].z += b[u4].z;
-              acc[u4].w += b[u4].w;
-            }
-          }
-        }
-        uint32_t v[32];
+      for (int p = 0; p < S; p += 2) {
+        float4 a[8], b[8];
+        const bool two = p + 1 < S;
 #pragma unroll
         for (int u4 = 0; u4 < 8; ++u4) {
-          v[4 * u4] = __float_as_uint(acc[u4].x);
-          v[4 * u4 + 1] = __float_as_uint(acc[u4].y);
-          v[4 * u4 + 2] = __float_as_uint(acc[u4].z);
-          v[4 * u4 + 3] = __float_as_uint(acc[u4].w);
+          a[u4] = __ldcg(src + p * part_f4 + u4 * BM);
+          if (two) b[u4] = __ldcg(src + (p + 1) * part_f4 + u4 * BM);
         }
-        wgrad_emit<MODE>(g, w, sg, mh, jq, h, v, stage, quarter, lane);
+#pragma unroll
+        for (int u4 = 0; u4 < 8; ++u4) {
+          if (p == 0) {
+            acc[u4] = a[u4];
+          } else {
+            acc[u4].x += a[u4].x;
+            acc[u4].y += a[u4].y;
+            acc[u4].z += a[u4].z;
+            acc[u4].w += a[u4].w;
+          }
+          if (two) {
+            acc[u4].x += b[u4].x;
+            acc[u4].y += b[u4].y;
+            acc[u4].z += b[u4].z;
+            acc[u4].w += b[u4].w;
+          }
+        }
       }
+      uint32_t v[32];
+#pragma unroll
+      for (int u4 = 0; u4 < 8; ++u4) {
+        v[4 * u4] = __float_as_uint(acc[u4].x);
+        v[4 * u4 + 1] = __float_as_uint(acc[u4].y);
+        v[4 * u4 + 2] = __float_as_uint(acc[u4].z);
+        v[4 * u4 + 3] = __float_as_uint(acc[u4].w);
+      }
+      wgrad_emit<MODE>(g, w, sg, mh, jq, h, v, stage, quarter, lane);
+    }
   return true;
 }
 
 }  // namespace
 
 template <int MODE>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(Ring<MODE>::kThreads, 1)
     k_seg_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmI,
                const __grid_constant__ GemmArgs g) {
@@ -579,7 +591,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], Ring<MODE>::kEpiWarps);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -705,6 +717,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else {
     const int quarter = warp & 3;
+    const int mh = (warp - 2) >> 2;   // dA / dB: the item's row half this warp writes
+    float* my_stage = stage_buf + (warp - 2) * DB_STAGE_FLOATS;
     int acc = 0;
     uint32_t acc_phase = 0;
     // dA / dB: the next item's descriptor and its job's record are read as soon as this item's
@@ -726,7 +740,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       bool released;
       if constexpr (kWgrad)
-        released = epilogue_wgrad<MODE>(g, w, sg, t_acc, quarter, lane, stage_buf, &tempty[acc]);
+        released = epilogue_wgrad<MODE>(g, w, sg, t_acc, quarter, mh, lane, my_stage, &tempty[acc]);
       else
         released = epilogue_item<MODE>(g, item, t_acc, quarter, lane);
       if (!released) {
@@ -759,7 +773,7 @@ cudaError_t launch_seg_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, cons
   cudaError_t e = ensure_smem_attr(k_seg_gemm<MODE>, Ring<MODE>::kSmem, attr_done);
   if (e != cudaSuccess) return e;
   if (g.n_items <= 0) return cudaSuccess;
-  return launch_k(k_seg_gemm<MODE>, dim3(grid), dim3(GEMM_THREADS), Ring<MODE>::kSmem, stream, g.pdl != 0, tmA, tmB,
+  return launch_k(k_seg_gemm<MODE>, dim3(grid), dim3(Ring<MODE>::kThreads), Ring<MODE>::kSmem, stream, g.pdl != 0, tmA, tmB,
                   tmE, tmI, g);
 }
 
