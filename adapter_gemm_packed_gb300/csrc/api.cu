@@ -33,7 +33,8 @@ cudaError_t launch_seg_gemm(const CUtensorMap&, const CUtensorMap&, const CUtens
                             const GemmArgs&, int, cudaStream_t);
 template <int MODE>
 cudaError_t launch_gemm_2sm(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                            const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
+                            const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const GemmArgs&, int,
+                            cudaStream_t);
 template <int MODE>
 cudaError_t launch_gemm_2sm_w4(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
@@ -1066,7 +1067,9 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
   } else if (pairs) {
     const int n_pairs = pair_gemm_items(P->n_mtiles, P->num_sms, g);
     g.debug_drop = P->debug_drop_pairs ? 1 : 0;
-    e = timed(P, K_FWD_GEMM, s, [&] { return launch_gemm_2sm<MODE_FWD>(mX, mW, mBt, mI, mW64, mBt64, g, n_pairs, s); });
+    CUtensorMap mY;
+    if ((st = make_map(&mY, Y, pr.d_out, pr.n_tokens, pr.d_out, 64, 128)) != MLORA_OK) return st;
+    e = timed(P, K_FWD_GEMM, s, [&] { return launch_gemm_2sm<MODE_FWD>(mX, mW, mBt, mI, mW64, mBt64, mY, g, n_pairs, s); });
   } else {
     g.n_items = P->n_mtiles * g.n_tiles_n;
     e = timed(P, K_FWD_GEMM, s, [&] { return launch_seg_gemm<MODE_FWD>(mX, mW, mBt, mI, g, grid_of(P, g.n_items), s); });
@@ -1213,8 +1216,10 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
     });
   } else if (pairs) {
     const int n_pairs = pair_gemm_items(P->n_mtiles, P->num_sms, g);
+    CUtensorMap mdX;
+    if ((st = make_map(&mdX, dX, pr.d_in, pr.n_tokens, pr.d_in, 64, 128)) != MLORA_OK) return st;
     e = timed(P, K_BWD_GEMM, s, [&] {
-      return launch_gemm_2sm<MODE_BWD>(mdY, mWmn, mAt64, mdHi, mWmn, mAt64, g, n_pairs, s);
+      return launch_gemm_2sm<MODE_BWD>(mdY, mWmn, mAt64, mdHi, mWmn, mAt64, mdX, g, n_pairs, s);
     });
   } else {
     g.n_items = P->n_mtiles * g.n_tiles_n;

@@ -33,18 +33,24 @@ namespace {
 constexpr int S2 = 6;                         // pipeline stages
 constexpr int A2_BYTES = 128 * BK * 2;        // this CTA's 128 rows of A per stage
 constexpr int B2_BYTES = 128 * BK * 2;        // this CTA's 128-row half of B per stage
-constexpr int SMEM_2SM = S2 * (A2_BYTES + B2_BYTES) + 1024 + 256;
+constexpr int Y_CHUNK_BYTES = BM * 64 * 2;    // one staged 128-row x 64-column bf16 output box
+// ring, then barriers (a 1 KB slot, so the staging that follows stays 1 KB aligned for its
+// 128-byte swizzle), two output boxes, and slack to align the dynamic base
+constexpr int SMEM_2SM = S2 * (A2_BYTES + B2_BYTES) + 1024 + 2 * Y_CHUNK_BYTES + 1024;
+constexpr int EPI_BAR = 1;                    // named barrier of the four epilogue warps
+constexpr int EPI_ISSUER = 64;                // thread that issues the epilogue's TMA stores
 
 }  // namespace
 
 // tmB / tmE: 128-row boxes for the forward's K-major B halves; tmB64 / tmE64: the same tensors
 // with 64-row boxes (half tiles).  The backward's MN-major B uses 64-wide boxes throughout.
+// tmY: the output (Y or dX), 64-column x 128-row boxes, 128-byte swizzle.
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_2sm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmE, const __grid_constant__ CUtensorMap tmI,
                const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmE64,
-               const __grid_constant__ GemmArgs g) {
+               const __grid_constant__ CUtensorMap tmY, const __grid_constant__ GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -58,6 +64,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* ring_hi = tmem_slot + 2;   // (even CTA) ring positions filled, max over both producers
+  uint8_t* ystage = reinterpret_cast<uint8_t*>(bars) + 1024;   // [2] staged output boxes
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
@@ -81,6 +88,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmE);
     prefetch_tmap(&tmI);
+    prefetch_tmap(&tmY);
     if (MODE == MODE_FWD && g.n_full_items < g.n_items) {
       prefetch_tmap(&tmB64);
       prefetch_tmap(&tmE64);
@@ -199,56 +207,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       mbar_wait(done, 0, &no_abort, g.err, DEV_ERR_TIMEOUT_TEARDOWN, tmo);
     }
   } else {
+    // Epilogue: per 64-column chunk of the tile, TMEM -> registers -> bf16 -> a staged box in
+    // shared memory (128-byte swizzle: row r's 16-byte piece j at slot j ^ (r & 7)) -> one TMA
+    // store of 128 rows x 64 columns.  Whole 128-byte rows reach the L2 instead of 16-byte pieces of
+    // 32 rows per store instruction.  Two staged boxes alternate; a box is rewritten only after the
+    // store that read it two chunks earlier has finished reading.  The four warps take every
+    // decision together (named barrier EPI_BAR), so none can leave the others waiting at it.
     const int quarter = warp & 3;
     const int rit = quarter * 32 + lane;
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&tempty[0]), 0);
     const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
+    const bool issuer = threadIdx.x == EPI_ISSUER;
     int acc = 0;
     uint32_t acc_phase = 0;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
+    uint32_t chunk_no = 0;
     const int ld = g.ld_out;
     for (int item = pair; item < g.n_items; item += n_pairs_grid) {
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, g.err, DEV_ERR_TIMEOUT_EPILOGUE, tmo);
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!named_bar_and(EPI_BAR, 128, ok)) break;
       tc_fence_after();
       int mp, col0, width;
       decode_item(g, item, mp, col0, width);
-      const long long row = static_cast<long long>(2 * mp + static_cast<int>(rank)) * BM + rit;
+      const int m0 = (2 * mp + static_cast<int>(rank)) * BM;   // this CTA's first output row
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      const int n_chunks = width / 64;
 #pragma unroll 1
-      for (int cb = 0; cb < width; cb += 32) {
-        uint32_t v[32];
-        tmem_ld32(t_acc + cb, v);
+      for (int c = 0; c < n_chunks; ++c, ++chunk_no) {
+        uint32_t v[64];
+        tmem_ld32(t_acc + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(t_acc + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         tmem_ld_wait();
-        const int col = col0 + cb;
-        if (row < g.N && col < ld) {
-          __nv_bfloat16* dst = out + row * ld + col;
-          if (col + 32 <= ld) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+        if (c == n_chunks - 1) {   // the accumulator is read: hand it back to the MMA
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(acc ? tempty_leader1 : tempty_leader0);
+        }
+        uint4 u[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
-              u.y = pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
-              u.z = pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
-              u.w = pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-              d4[q] = u;
-            }
-          } else {
+        for (int j = 0; j < 8; ++j) {
+          u[j].x = pack_bf16x2(__uint_as_float(v[8 * j + 0]), __uint_as_float(v[8 * j + 1]));
+          u[j].y = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+          u[j].z = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+          u[j].w = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+        }
+        uint8_t* box = ystage + (chunk_no & 1u) * Y_CHUNK_BYTES;
+        if (issuer) bulk_wait_group_read<1>();   // the store of two chunks ago has read this box
+        named_bar_sync(EPI_BAR, 128);
+        uint8_t* row_base = box + rit * 128;
 #pragma unroll
-            for (int u = 0; u < 32; ++u)
-              if (col + u < ld) dst[u] = __float2bfloat16_rn(__uint_as_float(v[u]));
-          }
+        for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(row_base + ((j ^ (rit & 7)) << 4)) = u[j];
+        fence_proxy_async_smem();
+        named_bar_sync(EPI_BAR, 128);
+        if (issuer) {
+          const int col = col0 + c * 64;
+          if (m0 < g.N && col < ld) tma_store_2d(&tmY, box, col, m0);
+          bulk_commit_group();   // one group per chunk, empty when nothing was stored
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(acc ? tempty_leader1 : tempty_leader0);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (issuer) bulk_wait_group<0>();   // every store written before the CTA leaves
   }
 
   // No copy is issued after this barrier; the even CTA then waits for the last ring positions'
@@ -267,20 +288,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
 template <int MODE>
 cudaError_t launch_gemm_2sm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmE,
                             const CUtensorMap& tmI, const CUtensorMap& tmB64, const CUtensorMap& tmE64,
-                            const GemmArgs& g, int n_pairs, cudaStream_t stream) {
+                            const CUtensorMap& tmY, const GemmArgs& g, int n_pairs, cudaStream_t stream) {
   static std::atomic<unsigned long long> attr_done{0};
   cudaError_t e = ensure_smem_attr(k_gemm_2sm<MODE>, SMEM_2SM, attr_done);
   if (e != cudaSuccess) return e;
   if (g.n_items <= 0) return cudaSuccess;
   return launch_k(k_gemm_2sm<MODE>, dim3(2 * n_pairs), dim3(GEMM_THREADS), SMEM_2SM, stream, g.pdl != 0, tmA, tmB,
-                  tmE, tmI, tmB64, tmE64, g);
+                  tmE, tmI, tmB64, tmE64, tmY, g);
 }
 
 template cudaError_t launch_gemm_2sm<MODE_FWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                                const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                               const GemmArgs&, int, cudaStream_t);
+                                               const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 template cudaError_t launch_gemm_2sm<MODE_BWD>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                                const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                               const GemmArgs&, int, cudaStream_t);
+                                               const CUtensorMap&, const GemmArgs&, int, cudaStream_t);
 
 }  // namespace mlora

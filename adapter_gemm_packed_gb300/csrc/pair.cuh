@@ -90,6 +90,56 @@ __device__ __forceinline__ void bulk_signal_remote(uint32_t dst_cluster, const v
                : "memory");
 }
 
+// TMA tile store of a box from this CTA's shared memory into global memory (a bulk async-group
+// of the issuing thread; the box's swizzle is the tensor map's).  Parts of the box outside the
+// tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
+// Close the issuing thread's bulk async operations into a group (an empty group if there are none).
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of the issuing thread's most recent bulk groups are still reading their
+// shared-memory source (the older ones' sources may be overwritten).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until at most N of the issuing thread's most recent bulk groups are incomplete (their
+// writes performed).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Order this thread's generic-proxy writes to shared memory before later async-proxy reads of it
+// (a TMA store issued after a barrier).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Named barrier `id` over `n` threads (a multiple of 32) that also returns the AND of `pred`
+// over them: every participant gets the same decision.
+__device__ __forceinline__ int named_bar_and(int id, int n, int pred) {
+  int out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"(pred), "r"(id), "r"(n)
+      : "memory");
+  return out;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // Teardown of a CTA pair's main ring.  Every copy into a ring slot, whichever CTA issues it,
 // counts on the even CTA's full barrier of that slot, and every issuer fills ring position p only
 // after the MMA released position p - S.  So once no thread can issue any more (a cluster barrier
