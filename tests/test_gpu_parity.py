@@ -64,6 +64,8 @@ SMALL_BF16 = {
     "single_token_job": dict(d_in=128, d_out=136, ranks=[5], n_tokens=[1]),
     "one_job_many_tiles": dict(d_in=1024, d_out=512, ranks=[32], n_tokens=[1000]),
     "wide_hidden": dict(d_in=2048, d_out=1536, ranks=[16, 128, 8], n_tokens=[256, 384, 130]),
+    # d_in and d_out not multiples of 64: the base GEMMs' TMA stores clip a partial 64-column box
+    "ragged_columns": dict(d_in=264, d_out=200, ranks=[8, 33, 128], n_tokens=[300, 45, 170]),
 }
 
 
