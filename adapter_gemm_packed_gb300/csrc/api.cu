@@ -7,10 +7,12 @@
 // tokens / hidden dims, never along the rank).  It lays every job's rank window side by side in
 // one packed rank space (windows padded to 16 columns, cut into 64-column chunks), maps each
 // 128-token tile to the jobs and chunks it covers, and builds one static work list per kernel:
-//   * base GEMMs: (token tile x 256 output columns), rastered in groups of M tiles for L2 reuse;
-//   * shrink / dH: (token tile, <= 2 64-column chunks of its window);
-//   * dA / dB: (256-row block of d_in / d_out, job, <= 2 chunks), sorted longest-first so the
-//     persistent grid's round-robin assignment balances uneven jobs.
+//   * base GEMMs: (256-token pair x 256 output columns) on CTA pairs, rastered in groups whose
+//     resident panels fit the L2 (raster.cuh);
+//   * shrink / dH: (token tile, <= 2 64-column chunks of its window), or on CTA pairs (256-token
+//     pair, <= 4 chunks), a thin last wave cut along K;
+//   * dA / dB: (256-row block of d_in / d_out, job, <= 2 chunks) laid out per CTA, by greedy list
+//     scheduling in job order or by McNaughton's wrap-around rule with items cut along their tokens.
 #include <algorithm>
 #include <array>
 #include <cmath>

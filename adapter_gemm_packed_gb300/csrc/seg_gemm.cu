@@ -31,6 +31,8 @@
 //   warp 1     TMEM allocator and MMA issuer (one lane), two 256-column accumulators
 //   warps 2-5  epilogue: TMEM -> registers -> global (lane quarter = warp id % 4); dA / dB have
 //              warps 2-9, two per lane quarter (one per 128-row half of the item)
+// The CTA-pair base GEMMs (gemm_2sm.cu) write Y / dX through shared memory and TMA stores; this
+// engine's single-CTA base GEMMs (kept for comparison) store from registers.
 // Every wait is bounded (see mbar_wait): on expiry the CTA records a status code, drains
 // what it issued, frees TMEM and returns.
 #include "common.cuh"
