@@ -40,8 +40,10 @@
  * the plan's status word, read back by mlora_sync_status().
  * Threads: different plans may be used from different host threads at once (each call makes
  * the plan device's primary context current on its thread); calls on one plan must not overlap
- * on the host.  mlora_forward, mlora_backward and mlora_adamw (and their _w4 / _ws forms) can be
- * captured into a CUDA graph.
+ * on the host, and their launches must not run at the same time on the device either (one
+ * stream, or streams ordered by events): a plan's status word and the arrival counters of its
+ * work items that are cut across CTAs belong to the plan.  mlora_forward, mlora_backward and
+ * mlora_adamw (and their _w4 / _ws forms) can be captured into a CUDA graph.
  */
 #ifndef MLORA_H
 #define MLORA_H
