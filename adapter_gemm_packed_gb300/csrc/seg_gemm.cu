@@ -93,6 +93,8 @@ __device__ __forceinline__ void decode_mn(const GemmArgs& g, int item, int& m, i
   n = in_group / gm;
 }
 
+// K slices and accumulator columns (MMA N) of a base-GEMM or rank-window item (dA / dB items
+// carry both in their descriptor, which the roles read one item ahead).
 template <int MODE>
 __device__ __forceinline__ int item_kblocks(const GemmArgs& g, int item) {
   if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
@@ -101,23 +103,17 @@ __device__ __forceinline__ int item_kblocks(const GemmArgs& g, int item) {
     return g.kmain + g.mtiles[m].nch;
   } else if constexpr (MODE == MODE_SHRINK) {
     return g.kmain;
-  } else if constexpr (MODE == MODE_DH) {
-    return g.win[item].dh_nkb;
   } else {
-    const WItem w = g.witems[item];
-    return w.gb - w.ga;
+    return g.win[item].dh_nkb;
   }
 }
 
-// Number of accumulator columns (MMA N) of an item.
 template <int MODE>
 __device__ __forceinline__ int item_ncols(const GemmArgs& g, int item) {
   if constexpr (MODE == MODE_FWD || MODE == MODE_BWD) {
     return BN;
-  } else if constexpr (MODE == MODE_SHRINK || MODE == MODE_DH) {
-    return CHUNK_COLS * g.win[item].nq;
   } else {
-    return CHUNK_COLS * g.witems[item].nq;
+    return CHUNK_COLS * g.win[item].nq;
   }
 }
 
@@ -627,7 +623,9 @@ __global__ void __launch_bounds__(Ring<MODE>::kThreads, 1)
       for (int item = items.first; ok && item < items.end; item += items.step) {
         WItem w_next{};
         if (kWgrad && item + items.step < items.end) w_next = g.witems[item + items.step];
-        const int nkb = kWgrad ? w.gb - w.ga : item_kblocks<MODE>(g, item);
+        int nkb;
+        if constexpr (kWgrad) nkb = w.gb - w.ga;
+        else nkb = item_kblocks<MODE>(g, item);
         int t_have = -1;
         MTile mt{};
         for (int kb = 0; kb < nkb; ++kb) {
@@ -690,8 +688,14 @@ __global__ void __launch_bounds__(Ring<MODE>::kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        const int nkb = kWgrad ? w.gb - w.ga : item_kblocks<MODE>(g, item);
-        const int ncols = kWgrad ? CHUNK_COLS * w.nq : item_ncols<MODE>(g, item);
+        int nkb, ncols;
+        if constexpr (kWgrad) {
+          nkb = w.gb - w.ga;
+          ncols = CHUNK_COLS * w.nq;
+        } else {
+          nkb = item_kblocks<MODE>(g, item);
+          ncols = item_ncols<MODE>(g, item);
+        }
         w = w_next;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
