@@ -5,12 +5,14 @@
 //                                         Wt and At_all)
 //
 // A pair of CTAs on the two SMs of a TPC computes one 256-token x 256-column tile: each CTA
-// stages its own 128 rows of A and its own 128-row half of B per 64-wide K slice (32 KB) in a
-// 6-deep ring, and the even CTA issues one M=256, N=256 tcgen05.mma per 16-wide K step that
-// reads both CTAs' shared memory and writes each CTA's 128 accumulator lanes.  Against the
-// single-CTA 128x256 tile this halves the B bytes each SM pulls from L2 per FLOP and buys two
-// more pipeline stages (the single-CTA kernel's profile showed the tensor pipe waiting on
-// operands at ~60 % activity with L2 and DRAM far from saturated).
+// stages its own 128 rows of A and its own 128-row half of B per 64-wide K slice (32 KB); a ring
+// slot holds two such slices (64 KB per CTA, three slots), and the even CTA issues one M=256,
+// N=256 tcgen05.mma per 16-wide K step that reads both CTAs' shared memory and writes each CTA's
+// 128 accumulator lanes.  Against the single-CTA 128x256 tile this halves the B bytes each SM
+// pulls from L2 per FLOP (the single-CTA kernel's profile showed the tensor pipe waiting on
+// operands at ~60 % activity with L2 and DRAM far from saturated).  Two slices per slot halve
+// the barrier waits, slot releases and copy arms per MMA against one slice per slot (six slots
+// of 32 KB): the layer's GEMMs measured 3-6 % faster with the same bytes in flight.
 //
 // Synchronisation: the even CTA's full[s] barrier collects the TMA bytes of both CTAs (the odd
 // CTA's copies signal it through .cta_group::2); the MMA warp's commits are multicast to both
@@ -30,13 +32,14 @@ using namespace pair;
 
 namespace {
 
-constexpr int S2 = 6;                         // pipeline stages
-constexpr int A2_BYTES = 128 * BK * 2;        // this CTA's 128 rows of A per stage
-constexpr int B2_BYTES = 128 * BK * 2;        // this CTA's 128-row half of B per stage
+constexpr int S2 = 3;                         // pipeline stages, two 64-wide K slices each
+constexpr int A2_BYTES = 128 * BK * 2;        // this CTA's 128 rows of A per K slice
+constexpr int B2_BYTES = 128 * BK * 2;        // this CTA's 128-row half of B per K slice
+constexpr int STAGE_A = 2 * A2_BYTES, STAGE_B = 2 * B2_BYTES;
 constexpr int Y_CHUNK_BYTES = BM * 64 * 2;    // one staged 128-row x 64-column bf16 output box
 // ring, then barriers (a 1 KB slot, so the staging that follows stays 1 KB aligned for its
 // 128-byte swizzle), two output boxes, and slack to align the dynamic base
-constexpr int SMEM_2SM = S2 * (A2_BYTES + B2_BYTES) + 1024 + 2 * Y_CHUNK_BYTES + 1024;
+constexpr int SMEM_2SM = S2 * (STAGE_A + STAGE_B) + 1024 + 2 * Y_CHUNK_BYTES + 1024;
 constexpr int EPI_BAR = 1;                    // named barrier of the four epilogue warps
 constexpr int EPI_ISSUER = 64;                // thread that issues the epilogue's TMA stores
 
@@ -54,8 +57,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + S2 * A2_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S2 * B2_BYTES);
+  uint8_t* sB = smem + S2 * STAGE_A;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + S2 * STAGE_B);
   uint64_t* full = bars;               // [S2]  (even CTA) TMA bytes of both CTAs -> MMA
   uint64_t* empty = bars + S2;         // [S2]  MMA -> each CTA's producer
   uint64_t* tfull = bars + 2 * S2;     // [2]   MMA -> each CTA's epilogue
@@ -118,36 +121,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         const int m0 = tile * BM;
         const int nh0 = col0 + static_cast<int>(rank) * (width / 2);   // this CTA's half of the item's columns
         const int nkb = g.kmain + mt.nch;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb0 = 0; kb0 < nkb; kb0 += 2) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
             ok = false;
             break;
           }
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (A2_BYTES + width * BK));
+          const int nsub = nkb - kb0 < 2 ? nkb - kb0 : 2;
+          if (leader) mbar_arrive_expect_tx(&full[stage], nsub * 2 * (A2_BYTES + width * BK));
           const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
-          uint8_t* a = sA + stage * A2_BYTES;
-          uint8_t* b = sB + stage * B2_BYTES;
           ++filled;
-          if (g.debug_drop && leader && pair == 0 && filled == 1) {
-            // Test hook for the timeout path: the slot is armed for both CTAs' bytes but this CTA
-            // copies nothing into it, so the MMA's bounded wait runs out and records a status
-            // code; the teardown drain then waits out the peer's copies.  Nothing faults or hangs.
-          } else if (kb < g.kmain) {
-            tma_load_2d_pair(a, &tmA, bar, kb * BK, m0);
-            if constexpr (MODE == MODE_FWD) {
-              tma_load_2d_pair(b, half ? &tmB64 : &tmB, bar, kb * BK, nh0);
+          for (int h = 0; h < nsub; ++h) {
+            const int kb = kb0 + h;
+            uint8_t* a = sA + stage * STAGE_A + h * A2_BYTES;
+            uint8_t* b = sB + stage * STAGE_B + h * B2_BYTES;
+            if (g.debug_drop && leader && pair == 0 && filled == 1) {
+              // Test hook for the timeout path: the slot is armed for both CTAs' bytes but this
+              // CTA copies nothing into it, so the MMA's bounded wait runs out and records a status
+              // code; the teardown drain then waits out the peer's copies.  Nothing faults or hangs.
+            } else if (kb < g.kmain) {
+              tma_load_2d_pair(a, &tmA, bar, kb * BK, m0);
+              if constexpr (MODE == MODE_FWD) {
+                tma_load_2d_pair(b, half ? &tmB64 : &tmB, bar, kb * BK, nh0);
+              } else {
+                tma_load_2d_pair(b, &tmB, bar, nh0, kb * BK);
+                if (!half) tma_load_2d_pair(b + 64 * 64 * 2, &tmB, bar, nh0 + 64, kb * BK);
+              }
             } else {
-              tma_load_2d_pair(b, &tmB, bar, nh0, kb * BK);
-              if (!half) tma_load_2d_pair(b + 64 * 64 * 2, &tmB, bar, nh0 + 64, kb * BK);
-            }
-          } else {
-            const int e = kb - g.kmain;
-            tma_load_2d_pair(a, &tmI, bar, 0, (mt.img_off + e) * BM);
-            if constexpr (MODE == MODE_FWD) {   // Bt_all rows, K-major
-              tma_load_2d_pair(b, half ? &tmE64 : &tmE, bar, (mt.q_lo + e) * CHUNK_COLS, nh0);
-            } else {   // At_all [C, d_in] as MN-major B (n = d_in index, k = rank column)
-              tma_load_2d_pair(b, &tmE, bar, nh0, (mt.q_lo + e) * CHUNK_COLS);
-              if (!half) tma_load_2d_pair(b + 64 * 64 * 2, &tmE, bar, nh0 + 64, (mt.q_lo + e) * CHUNK_COLS);
+              const int e = kb - g.kmain;
+              tma_load_2d_pair(a, &tmI, bar, 0, (mt.img_off + e) * BM);
+              if constexpr (MODE == MODE_FWD) {
+                tma_load_2d_pair(b, half ? &tmE64 : &tmE, bar, (mt.q_lo + e) * CHUNK_COLS, nh0);
+              } else {
+                tma_load_2d_pair(b, &tmE, bar, nh0, (mt.q_lo + e) * CHUNK_COLS);
+                if (!half) tma_load_2d_pair(b + 64 * 64 * 2, &tmE, bar, nh0 + 64, (mt.q_lo + e) * CHUNK_COLS);
+              }
             }
           }
           if (++stage == S2) {
@@ -176,20 +183,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb0 = 0; kb0 < nkb; kb0 += 2) {
           if (!mbar_wait(&full[stage], phase, abort_flag, g.err, DEV_ERR_TIMEOUT_MMA, tmo)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = smem_u32(sA + stage * A2_BYTES);
-          const uint32_t b = smem_u32(sB + stage * B2_BYTES);
+          const int nsub = nkb - kb0 < 2 ? nkb - kb0 : 2;
           constexpr bool b_mn = MODE == MODE_BWD;   // W and At_all are both read MN-major
+          for (int h = 0; h < nsub; ++h) {
+            const uint32_t a = smem_u32(sA + stage * STAGE_A + h * A2_BYTES);
+            const uint32_t b = smem_u32(sB + stage * STAGE_B + h * B2_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = smem_desc(a + k * 32, 16, 1024);
-            const uint64_t bd = b_mn ? smem_desc(b + k * 2048, 64 * 64 * 2, 1024) : smem_desc(b + k * 32, 16, 1024);
-            umma_pair_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint64_t ad = smem_desc(a + k * 32, 16, 1024);
+              const uint64_t bd = b_mn ? smem_desc(b + k * 2048, 64 * 64 * 2, 1024) : smem_desc(b + k * 32, 16, 1024);
+              umma_pair_bf16(d_tmem, ad, bd, idesc, (kb0 + h > 0 || k > 0) ? 1u : 0u);
+            }
           }
           umma_pair_commit_mc(&empty[stage], 0x3);
           if (++stage == S2) {
