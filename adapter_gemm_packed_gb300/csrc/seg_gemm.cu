@@ -318,12 +318,21 @@ __device__ __forceinline__ void wgrad_emit(const GemmArgs& g, const WItem& w, co
               *reinterpret_cast<float4*>(sg.dBt + static_cast<size_t>(row_w + rr) * r + tq + 4 * k) = buf4[db_slot(rr, k)];
           }
         } else {
-          // part of the 16 columns: one row per store instruction
-          const int t = lo + lane;
-          if (lane < 16) {
-            const int c = t - tq;
-            for (int rr = 0; rr < nrows; ++rr)
-              if (t < hi) sg.dBt[static_cast<size_t>(row_w + rr) * r + t] = buf[db_slot(rr, c >> 2) * 4 + (c & 3)];
+          // rows not 16-byte aligned (r not a multiple of 4) or part of the 16 columns: the wq valid
+          // columns of the warp's rows taken in row order, element e at row e / wq and column
+          // lo + e % wq, 32 consecutive elements per store instruction (one run of wq floats per row)
+          const int wq = hi - lo, n_el = nrows * wq;
+          const int step_r = 32 / wq, step_c = 32 - step_r * wq;
+          int rr = lane / wq, c = lane - rr * wq;
+          for (int e = lane; e < n_el; e += 32) {
+            const int cq = lo - tq + c;   // column within the staged 16
+            sg.dBt[static_cast<size_t>(row_w + rr) * r + lo + c] = buf[db_slot(rr, cq >> 2) * 4 + (cq & 3)];
+            rr += step_r;
+            c += step_c;
+            if (c >= wq) {
+              c -= wq;
+              ++rr;
+            }
           }
         }
       }
