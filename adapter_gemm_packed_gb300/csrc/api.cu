@@ -18,6 +18,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <limits>
 #include <new>
 #include <string>
 #include <vector>
@@ -155,9 +156,13 @@ struct mlora_plan_s {
   std::vector<int> img_tile;
   std::vector<int> col_sub;             // per packed column (chunk-padded), -1 in padding
   std::vector<WinItem> win;             // shrink / dH items of the single-CTA engine (tile, <= 2 chunks)
-  std::vector<WinItem> win2;            // the same work on CTA pairs (tile = pair, 2 or 4 chunks)
+  std::vector<WinItem> win2;            // the shrink on CTA pairs (tile = pair, 2 or 4 chunks), per-pair lists
   bool win_pairs = false;               // which of the two the shrink / dH launches run
-  int n_split = 0, split_parts = 1;     // win2 items cut along K (see build_tables) and their parts
+  std::vector<int> win2_first;          // shrink: pair p runs win2[win2_first[p] .. win2_first[p + 1])
+  std::vector<WinItem> win2d;           // dH on CTA pairs: the same items laid out for dH's K range
+  std::vector<int> win2d_first;
+  int n_split = 0, win_units = 0;       // pair items cut along K (see build_tables), and their pieces
+                                        // (the larger of the two products')
   std::vector<WItem> da, db;             // dA / dB items, CTA by CTA (see build_tables)
   std::vector<int> da_first, db_first;   // CTA c runs items [first[c], first[c + 1])
   int da_sets = 0, db_sets = 0;          // items cut across CTAs (one arrival-counter set each)
@@ -183,6 +188,9 @@ struct mlora_plan_s {
   WItem* d_db = nullptr;
   int* d_da_first = nullptr;
   int* d_db_first = nullptr;
+  int* d_win2_first = nullptr;
+  WinItem* d_win2d = nullptr;
+  int* d_win2d_first = nullptr;
   AdamItem* d_adam = nullptr;
   int* d_err = nullptr;
   int* d_part_cnt = nullptr;            // arrival counters of the split items: pair items, then dA's,
@@ -440,6 +448,7 @@ void build_tables(mlora_plan_t* P) {
       w.q0 = m.q_lo + q;
       w.nq = std::min(MAX_ITEM_CHUNKS, m.nch - q);
       w.nparts = 1;
+      w.f1 = WIN_FRAC;
       dh_range(w, w.q0, w.nq);
       P->win.push_back(w);
     }
@@ -456,6 +465,7 @@ void build_tables(mlora_plan_t* P) {
       const int real = std::min(4, m.nch - q);
       w.nq = real + (real & 1);
       w.nparts = 1;
+      w.f1 = WIN_FRAC;
       dh_range(w, w.q0, real);
       P->win2.push_back(w);
     }
@@ -468,38 +478,156 @@ void build_tables(mlora_plan_t* P) {
   if (pr.flags & MLORA_WINDOW_SINGLE) P->win_pairs = false;
   if (P->debug_drop) P->win_pairs = false;   // the copy-withholding hook lives in the single-CTA shrink
 
-  // The persistent grid runs the pair items round-robin on num_sms / 2 pairs.  When the last wave
-  // would leave more than half of the pairs idle, its T items are cut along K into S parts each,
-  // one part per pair: the wave takes about 1/S of an item's time instead of a whole one, for the
-  // partial sums' extra bytes (each part's fp32 sums, up to 128 KB per CTA, written once and read
-  // once by the item's last part).  S = floor(pairs / T), at most MAX_WIN_PARTS, and small enough
-  // that every part keeps at least 16 K slices of both products (the shrink's d_in, and the d_out
-  // slices dH covers), so a part streams at least 256 KB per CTA against its 128 KB of sums.
-  P->n_split = 0;
-  P->split_parts = 1;
-  {
-    const int pairs = std::max(1, P->num_sms / 2);
-    const int I = static_cast<int>(P->win2.size());
-    const int T = I % pairs;
-    if (P->win_pairs && I > pairs && T > 0 && 2 * T <= pairs) {
-      int min_k = (pr.d_in + BK - 1) / BK;
-      for (int t = I - T; t < I; ++t) min_k = std::min(min_k, P->win2[t].dh_nkb);
-      const int S = std::min({MAX_WIN_PARTS, pairs / T, min_k / 16});
-      if (S >= 2) {
-        std::vector<WinItem> tail(P->win2.end() - T, P->win2.end());
-        P->win2.resize(I - T);
-        for (int t = 0; t < T; ++t)
-          for (int k = 0; k < S; ++k) {
-            WinItem w = tail[t];
-            w.part = k;
-            w.nparts = S;
-            w.slot = t;
-            P->win2.push_back(w);
-          }
-        P->n_split = T;
-        P->split_parts = S;
+  // CTA-pair schedules of the shrink and of dH: for each product a list per pair.  The modelled
+  // cost of an item, in KB per CTA, is what it streams (per 64-wide K slice of the product, 16 KB
+  // of X or dY and 8 KB per rank-operand chunk the CTA holds), its images (16 KB per chunk) and a
+  // start-up.  First the items go whole, in tile order, each to the least-loaded pair, while that
+  // pair then stays within an eighth of the item above the average load: the first waves run like
+  // a round robin (a tile's items, which read the same X / dY rows, side by side).  The rest are
+  // laid out by McNaughton's wrap-around rule over the pairs in ascending order of load: each pair
+  // is filled up to a level T, the item at its end is cut there along K (at least 16 K slices per
+  // piece) and its rest starts the next pair; T is the level whose layout has the smallest largest
+  // load (scanned below).  A cut piece also parks its fp32 sums and the item's
+  // last piece reads all of them back: 64 KB per chunk per piece in the model.  Against a round
+  // robin this fills the last wave's idle pairs (one item of a wave's time left to a few pairs)
+  // and the pairs a pack with fewer items than pairs leaves idle.  The two products' K ranges
+  // differ (d_in against the d_out slices dH covers), so each gets its own layout; the launches
+  // run one after the other and share the partial sums and counters.
+  auto pair_schedule = [&](const std::vector<WinItem>& v, bool dh, std::vector<WinItem>& out,
+                           std::vector<int>& first, int& sets, int& units) {
+    out.clear();
+    first.clear();
+    sets = units = 0;
+    const int NP = std::max(1, P->num_sms / 2);
+    const int kin = (pr.d_in + BK - 1) / BK;
+    auto ks = [&](const WinItem& w) { return dh ? w.dh_nkb : kin; };
+    auto var = [&](const WinItem& w) { return ks(w) * (16.0 + 8.0 * (w.nq / 2)); };
+    auto fix = [&](const WinItem& w) { return 32.0 + 16.0 * w.nq; };
+    auto cutc = [&](const WinItem& w) { return 64.0 * w.nq; };
+    // the smallest share of a piece: 16 K slices (an item shorter than 32 slices is never cut)
+    auto fmin = [&](const WinItem& w) {
+      const int mk = std::max(1, ks(w));
+      return static_cast<int>((16LL * WIN_FRAC + mk - 1) / mk);
+    };
+    std::vector<std::vector<WinItem>> lists(NP);
+    std::vector<double> load(NP, 0.0);
+    size_t i = 0;
+    if (P->win_pairs) {
+      double total = 0;
+      for (const WinItem& w : v) total += var(w) + fix(w);
+      const double avg = total / NP;
+      for (; i < v.size(); ++i) {
+        int p = 0;   // the least-loaded pair (lowest index among equals)
+        for (int k = 1; k < NP; ++k)
+          if (load[k] < load[p]) p = k;
+        const double c = var(v[i]) + fix(v[i]);
+        if (load[p] + c > avg + c / 8) break;
+        lists[p].push_back(v[i]);
+        load[p] += c;
       }
+    } else {
+      for (; i < v.size(); ++i) lists[i % NP].push_back(v[i]);   // not launched: whole items
     }
+    if (i < v.size()) {
+      std::vector<int> order(NP);
+      for (int k = 0; k < NP; ++k) order[k] = k;
+      std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return load[x] < load[y]; });
+      std::vector<std::vector<WinItem>> add;
+      // lays out items i.. at level T (the last pair in the order takes whatever is left, if the
+      // layout reaches it); returns the largest load and leaves the per-pair pieces in `add`
+      auto lay_out = [&](double T) {
+        add.assign(NP, {});
+        std::vector<double> ld = load;
+        sets = units = 0;
+        int oi = 0;
+        for (size_t k = i; k < v.size(); ++k) {
+          const WinItem& w = v[k];
+          const int fm = fmin(w);
+          std::vector<std::array<int, 3>> pieces;   // (pair, f0, f1)
+          int f = 0;
+          while (f < WIN_FRAC) {
+            const int p = order[oi];
+            const int rest = WIN_FRAC - f;
+            int take;
+            if (oi == NP - 1) {
+              take = rest;   // the last pair takes whatever is left
+            } else {
+              const double room = T - ld[p] - fix(w) - cutc(w);
+              take = room <= 0 ? 0 : static_cast<int>(std::min<double>(rest, std::floor(room / var(w) * WIN_FRAC)));
+              if (take < rest) {
+                if (take < fm) {
+                  // a piece of the smallest share here overfills this pair, none leaves its room
+                  // empty: take the smaller of the two deviations (an empty pair always takes one)
+                  const bool empty = lists[p].empty() && add[p].empty();
+                  if (!empty && room < 0.5 * fm / WIN_FRAC * var(w)) {
+                    ++oi;
+                    continue;
+                  }
+                  take = std::min(rest, fm);
+                }
+                const int r2 = rest - take;
+                if (r2 > 0 && r2 < fm)   // no stub: take it all, or leave the smallest share
+                  take = (2 * r2 < fm || rest < 2 * fm) ? rest : rest - fm;
+              }
+            }
+            pieces.push_back({p, f, f + take});
+            ld[p] += fix(w) + var(w) * take / WIN_FRAC + (take == WIN_FRAC ? 0.0 : cutc(w));
+            add[p].push_back(w);   // filled in below
+            f += take;
+            if (f < WIN_FRAC) ++oi;
+          }
+          const int S = static_cast<int>(pieces.size());
+          for (int q = 0; q < S; ++q) {
+            WinItem& x = add[pieces[q][0]].back();
+            x.part = q;
+            x.nparts = S;
+            x.f0 = pieces[q][1];
+            x.f1 = pieces[q][2];
+            x.slot = S > 1 ? sets : 0;
+            x.pbase = S > 1 ? units : 0;
+          }
+          if (S > 1) {
+            ++sets;
+            units += S;
+          }
+        }
+        return *std::max_element(ld.begin(), ld.end());
+      };
+      // The level: pieces of at least 16 slices make the largest load jump with T (a piece that
+      // would fit only in part overfills a pair, or moves on and leaves its room empty), so T is
+      // scanned from the average load up to 1.5x (and a few larger values) in steps of 0.2 %, and
+      // the layout with the smallest largest load is kept (the lowest T among equals).
+      double avg = 0;
+      for (size_t k = i; k < v.size(); ++k) avg += var(v[k]) + fix(v[k]);
+      for (int k = 0; k < NP; ++k) avg += load[k];
+      avg /= NP;
+      double best_T = avg, best = std::numeric_limits<double>::infinity();
+      for (int step = 0; step <= 253; ++step) {
+        const double T = avg * (step <= 250 ? 1.0 + 0.002 * step : 1.0 + (step - 249));
+        const double span = lay_out(T);
+        if (span < best) {
+          best = span;
+          best_T = T;
+        }
+      }
+      lay_out(best_T);
+      for (int k = 0; k < NP; ++k) lists[k].insert(lists[k].end(), add[k].begin(), add[k].end());
+    }
+    int used = NP;
+    while (used > 1 && lists[used - 1].empty()) --used;
+    for (int k = 0; k < used; ++k) {
+      first.push_back(static_cast<int>(out.size()));
+      out.insert(out.end(), lists[k].begin(), lists[k].end());
+    }
+    first.push_back(static_cast<int>(out.size()));
+  };
+  {
+    const std::vector<WinItem> v = std::move(P->win2);
+    int s_sets, s_units, d_sets, d_units;
+    pair_schedule(v, false, P->win2, P->win2_first, s_sets, s_units);
+    pair_schedule(v, true, P->win2d, P->win2d_first, d_sets, d_units);
+    P->n_split = std::max(s_sets, d_sets);
+    P->win_units = std::max(s_units, d_units);
   }
 
   // dA / dB work: (256-row block, job, <= MAX_ITEM_CHUNKS chunks) over the job's tokens.  A dB
@@ -723,10 +851,10 @@ void build_tables(mlora_plan_t* P) {
                           round_up(static_cast<size_t>(P->C_total) * pr.d_out * 2, 1024);
     P->off_shadow = 0;
     // fp32 partial sums of split items, one region shared by the launches that use it in turn:
-    // the CTA-pair shrink / dH ([slot][part][CTA of the pair][128 rows][256 columns]) and dB / dA
+    // the CTA-pair shrink / dH ([piece][CTA of the pair][256 columns][128 rows]) and dB / dA
     // (per cut item: [part][chunk][256 rows x 64 columns])
     P->off_partials = round_up(shadow, 1024);
-    const size_t partials = std::max(static_cast<size_t>(P->n_split) * P->split_parts * 2 * BM * 256 * 4,
+    const size_t partials = std::max(static_cast<size_t>(P->win_units) * 2 * BM * 256 * 4,
                                      static_cast<size_t>(std::max(P->da_units, P->db_units)) * WG_UNIT * 4);
     P->off_himg = round_up(P->off_partials + partials, 1024);
     P->off_dhimg = P->off_himg + static_cast<size_t>(P->n_images) * IMG_BYTES;
@@ -764,9 +892,11 @@ mlora_status upload(mlora_plan_t* P) {
                b_cs = table_bytes(P->col_sub), b_sc = table_bytes(P->col_scale), b_sub = table_bytes(P->subs),
                b_win = table_bytes(P->win), b_win2 = table_bytes(P->win2), b_da = table_bytes(P->da),
                b_db = table_bytes(P->db), b_daf = table_bytes(P->da_first), b_dbf = table_bytes(P->db_first),
-               b_adam = table_bytes(P->adam), b_err = 256, b_cnt = round_up(counter_ints(P) * sizeof(int), 256);
+               b_w2f = table_bytes(P->win2_first), b_w2d = table_bytes(P->win2d),
+               b_w2df = table_bytes(P->win2d_first), b_adam = table_bytes(P->adam), b_err = 256,
+               b_cnt = round_up(counter_ints(P) * sizeof(int), 256);
   const size_t total = b_segs + b_mt + b_it + b_cs + b_sc + b_sub + b_win + b_win2 + b_da + b_db + b_daf + b_dbf +
-                       b_adam + b_err + b_cnt;
+                       b_w2f + b_w2d + b_w2df + b_adam + b_err + b_cnt;
   e = cudaMalloc(&P->dev_block, total);
   if (e != cudaSuccess) {
     P->dev_block = nullptr;
@@ -792,6 +922,9 @@ mlora_status upload(mlora_plan_t* P) {
       (e = place(P->d_da, P->da, b_da)) != cudaSuccess || (e = place(P->d_db, P->db, b_db)) != cudaSuccess ||
       (e = place(P->d_da_first, P->da_first, b_daf)) != cudaSuccess ||
       (e = place(P->d_db_first, P->db_first, b_dbf)) != cudaSuccess ||
+      (e = place(P->d_win2_first, P->win2_first, b_w2f)) != cudaSuccess ||
+      (e = place(P->d_win2d, P->win2d, b_w2d)) != cudaSuccess ||
+      (e = place(P->d_win2d_first, P->win2d_first, b_w2df)) != cudaSuccess ||
       (e = place(P->d_adam, P->adam, b_adam)) != cudaSuccess)
     return cuda_fail(e, "uploading the plan tables");
   P->d_err = reinterpret_cast<int*>(b + o);
@@ -1043,11 +1176,11 @@ mlora_status forward_impl(const mlora_plan_t* P, const void* X, const void* Wt, 
     g.win = P->d_win2;
     g.n_items = static_cast<int>(P->win2.size());
     g.debug_drop = P->debug_drop_pairs ? 1 : 0;
+    g.cta_first = P->d_win2_first;
     g.partials = P->n_split ? reinterpret_cast<float*>(ws + P->off_partials) : nullptr;
     g.part_cnt = P->d_part_cnt;
-    e = timed(P, K_SHRINK, s, [&] {
-      return launch_win_2sm<MODE_SHRINK>(mX, mAt, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
-    });
+    const int n_pairs = static_cast<int>(P->win2_first.size()) - 1;
+    e = timed(P, K_SHRINK, s, [&] { return launch_win_2sm<MODE_SHRINK>(mX, mAt, g, n_pairs, s); });
   } else {
     g.n_items = static_cast<int>(P->win.size());
     g.debug_drop = P->debug_drop ? 1 : 0;
@@ -1179,13 +1312,13 @@ mlora_status backward_impl(const mlora_plan_t* P, const void* X, const void* Wt,
   g.img_out = dhimg;
   g.hout = dH;
   if (P->win_pairs) {
-    g.win = P->d_win2;
-    g.n_items = static_cast<int>(P->win2.size());
+    g.win = P->d_win2d;
+    g.n_items = static_cast<int>(P->win2d.size());
+    g.cta_first = P->d_win2d_first;
     g.partials = P->n_split ? reinterpret_cast<float*>(ws + P->off_partials) : nullptr;
     g.part_cnt = P->d_part_cnt;
-    e = timed(P, K_DH, s, [&] {
-      return launch_win_2sm<MODE_DH>(mdY, mBt64, g, std::max(1, std::min(g.n_items, P->num_sms / 2)), s);
-    });
+    const int n_pairs = static_cast<int>(P->win2d_first.size()) - 1;
+    e = timed(P, K_DH, s, [&] { return launch_win_2sm<MODE_DH>(mdY, mBt64, g, n_pairs, s); });
   } else {
     g.n_items = static_cast<int>(P->win.size());
     e = timed(P, K_DH, s, [&] { return launch_seg_gemm<MODE_DH>(mdY, mBt64, mBt64, mdY, g, grid_of(P, g.n_items), s); });
@@ -1381,10 +1514,22 @@ mlora_status mlora_plan_describe(const mlora_plan_t* P, int32_t what, int64_t* o
     case MLORA_Q_WINDOW:
       for (const WinItem& w : P->win) v.insert(v.end(), {w.tile, w.q0, w.nq, w.dh_kb0, w.dh_nkb});
       break;
-    case MLORA_Q_WINDOW_PAIRS:
+    case MLORA_Q_WINDOW_PAIRS: {
       v.push_back(P->win_pairs ? 1 : 0);
-      for (const WinItem& w : P->win2) v.insert(v.end(), {w.tile, w.q0, w.nq, w.dh_kb0, w.dh_nkb, w.part, w.nparts});
+      const int kin = (P->prob.d_in + BK - 1) / BK;
+      for (int prod = 0; prod < 2; ++prod) {
+        const std::vector<WinItem>& it = prod ? P->win2d : P->win2;
+        const std::vector<int>& first = prod ? P->win2d_first : P->win2_first;
+        for (size_t p = 0; p + 1 < first.size(); ++p)
+          for (int k = first[p]; k < first[p + 1]; ++k) {
+            const WinItem& w = it[k];
+            int k0, nk;
+            win_krange(w, prod == 1, kin, k0, nk);
+            v.insert(v.end(), {prod, static_cast<int64_t>(p), w.tile, w.q0, w.nq, k0, nk, w.part, w.nparts});
+          }
+      }
       break;
+    }
     case MLORA_Q_ADAPTERS:
       for (const DevSub& sb : P->subs) v.insert(v.end(), {sb.job, sb.c0, sb.r, sb.o_lo, sb.o_hi});
       break;
@@ -1464,7 +1609,9 @@ mlora_status mlora_memory_estimate(const mlora_plan_t* P, mlora_memory* out) {
                                        table_bytes(P->col_sub) + table_bytes(P->col_scale) +
                                        table_bytes(P->subs) + table_bytes(P->win) + table_bytes(P->win2) +
                                        table_bytes(P->da) + table_bytes(P->db) + table_bytes(P->da_first) +
-                                       table_bytes(P->db_first) + table_bytes(P->adam) + 256 +
+                                       table_bytes(P->db_first) + table_bytes(P->win2_first) +
+                                       table_bytes(P->win2d) + table_bytes(P->win2d_first) +
+                                       table_bytes(P->adam) + 256 +
                                        round_up(counter_ints(P) * sizeof(int), 256));
   m.total = m.base_weight + m.activations + m.lora_params + m.lora_grad_state + m.lora_act + m.workspace +
             m.plan_tables;

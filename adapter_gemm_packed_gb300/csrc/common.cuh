@@ -30,7 +30,6 @@ constexpr int IMG_BYTES = BM * CHUNK_COLS * 2;   // one staged [128 x 64] bf16 i
 constexpr int RANK_PAD = 16;         // each job's rank window is padded to a multiple of 16
 constexpr int GEMM_THREADS = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int TMEM_COLS = 512;       // two 256-column fp32 accumulators
-constexpr int MAX_WIN_PARTS = 8;    // K parts of a CTA-pair shrink / dH item cut to fill a thin last wave
 constexpr int MAX_ITEM_CHUNKS = 2;  // rank chunks per shrink / dH / dA / dB work item (N <= 128)
 
 enum GemmMode : int {
@@ -87,19 +86,23 @@ struct WinItem {
   int tile, q0, nq;
   int dh_kb0, dh_nkb;   // dH: the 64-wide d_out slices its chunks' adapters cover (all of d_out
                         // unless the pack shares its input across projections)
-  // CTA-pair items of a last wave that would leave most pairs idle are cut along K: part `part` of
-  // `nparts` covers that share of the item's K slices, parks its fp32 partial sums in the
-  // workspace (partial set `slot`), and the last part to finish sums all parts in part order and
-  // writes the item's outputs.  nparts = 1: a whole item.
+  // The CTA-pair schedule can cut an item along K into `nparts` pieces on different pairs: piece
+  // `part` covers the share [f0, f1) / WIN_FRAC of each product's K slices, parks its fp32
+  // partial sums in the workspace (partial set pbase + part), counts itself on counter set
+  // `slot`, and the last piece to finish sums all pieces in part order and writes the item's
+  // outputs.  nparts = 1: a whole item (f0 = 0, f1 = WIN_FRAC).
   int part, nparts, slot;
+  int f0, f1, pbase;
 };
+constexpr int WIN_FRAC = 1 << 16;
 
-// K slices [kb0, kb0 + nkb) of a CTA-pair rank-window item: the whole K range of its product
-// (d_in for the shrink, the covered d_out slices for dH) or its part's equal share of it.
+// K slices [kb0, kb0 + nkb) of a CTA-pair rank-window item: its share of the whole K range of the
+// product (d_in for the shrink, the covered d_out slices for dH).  The pieces of one item take
+// consecutive shares, so their slice ranges tile the product's range exactly once.
 __host__ __device__ __forceinline__ void win_krange(const WinItem& w, bool dh, int kmain, int& kb0, int& nkb) {
   const int b = dh ? w.dh_kb0 : 0, n = dh ? w.dh_nkb : kmain;
-  const int lo = static_cast<int>(static_cast<long long>(n) * w.part / w.nparts);
-  const int hi = static_cast<int>(static_cast<long long>(n) * (w.part + 1) / w.nparts);
+  const int lo = static_cast<int>(static_cast<long long>(n) * w.f0 / WIN_FRAC);
+  const int hi = static_cast<int>(static_cast<long long>(n) * w.f1 / WIN_FRAC);
   kb0 = b + lo;
   nkb = hi - lo;
 }
@@ -157,7 +160,8 @@ struct GemmArgs {
   float* partials;         // fp32 partial sums of items split across CTAs (workspace)
   int* part_cnt;           // ... and their arrival counters (pair items: slot, CTA of the pair,
                            // row quarter; dA / dB items: counter set, row quarter, row half)
-  const int* cta_first;    // dA / dB: CTA c runs items [cta_first[c], cta_first[c + 1]) (null: round robin)
+  const int* cta_first;    // dA / dB: CTA c runs items [cta_first[c], cta_first[c + 1]); CTA-pair shrink /
+                           // dH: pair p runs [cta_first[p], cta_first[p + 1]) (null: round robin)
   // Shared-input packs (several adapters per job): per packed column, its adapter (-1 in the
   // padding) and scale.  Null for plans with one adapter per job, whose kernels read the job's.
   const DevSub* subs;      // job j's adapters are subs[j * n_groups .. j * n_groups + n_groups)

@@ -12,7 +12,10 @@
 // many bytes of the rank operand from L2, and a tile's X (or dY) is re-read once per four
 // chunks instead of once per two: what limits wide windows (jobs with large or several ranks
 // sharing a tile).  Items carry an even chunk count (a window of one chunk is padded to two),
-// so both CTAs always load whole chunks; a padding chunk is computed and discarded.
+// so both CTAs always load whole chunks; a padding chunk is computed and discarded.  Each pair
+// runs its own list of items (the planner's per-pair schedule); an item the schedule cuts along
+// K runs as pieces on several pairs, each parking fp32 partial sums, and the last piece to
+// finish adds them in piece order before writing the outputs.
 //
 // The epilogue of each CTA writes its own tile: H (SHRINK, fp32) or dH (scaled), and the bf16
 // images of s*H / dH per (tile, chunk), zero outside each row's job window, exactly as the
@@ -88,6 +91,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   const unsigned long long tmo = g.timeout_ns;
   griddep_wait();
   griddep_launch_dependents();
+  // this pair's items: its run of the planner's per-pair list, else every n_pairs_grid-th item
+  const int it_first = g.cta_first ? g.cta_first[pair_id] : pair_id;
+  const int it_end = g.cta_first ? g.cta_first[pair_id + 1] : g.n_items;
+  const int it_step = g.cta_first ? 1 : n_pairs_grid;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -97,7 +104,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       uint32_t phase = 0;
       uint32_t filled = 0;
       bool ok = true;
-      for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
+      for (int item = it_first; ok && item < it_end; item += it_step) {
         const WinItem w = g.win[item];
         const int m0 = (2 * w.tile + static_cast<int>(rank)) * BM;
         const int nb = w.nq >> 1;                                   // chunks held by this CTA
@@ -140,7 +147,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int item = pair_id; ok && item < g.n_items; item += n_pairs_grid) {
+      for (int item = it_first; ok && item < it_end; item += it_step) {
         const WinItem w = g.win[item];
         int kb0, nkb;
         win_krange(w, MODE == MODE_DH, g.kmain, kb0, nkb);
@@ -188,7 +195,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     const uint32_t tempty_leader1 = mapa_shared(smem_u32(&tempty[1]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int item = pair_id; item < g.n_items; item += n_pairs_grid) {
+    for (int item = it_first; item < it_end; item += it_step) {
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, g.err, DEV_ERR_TIMEOUT_EPILOGUE, tmo);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -270,14 +277,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
             emit_chunk(jq, vv);
           }
         } else {
-          // A part of an item cut along K: park this part's sums ([slot][part][CTA][256 columns]
+          // A part of an item cut along K: park this part's sums ([pbase + part][CTA][256 columns]
           // [128 rows], fp32, so that a warp's 32 rows of one column are one 128-byte line), hand
           // the accumulator back, and count the arrival of this warp's 32 rows.  The last of the
           // item's parts to arrive reads all parts' sums back in part order (a fixed order:
           // results do not depend on timing) and writes the item's outputs.  Nothing waits for
           // another CTA.
           const size_t stride = static_cast<size_t>(BM) * 256;
-          float* mine = g.partials + (static_cast<size_t>(w.slot * w.nparts + w.part) * 2 + rank) * stride + rit;
+          float* mine = g.partials + (static_cast<size_t>(w.pbase + w.part) * 2 + rank) * stride + rit;
 #pragma unroll 1
           for (int jq = 0; jq < nreal; ++jq) {
             uint32_t vv[64];
@@ -305,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
           last = __shfl_sync(0xffffffffu, last, 0);
           if (last) {
             __threadfence();
-            const float* base = g.partials + (static_cast<size_t>(w.slot * w.nparts) * 2 + rank) * stride + rit;
+            const float* base = g.partials + (static_cast<size_t>(w.pbase) * 2 + rank) * stride + rit;
 #pragma unroll 1
             for (int jq = 0; jq < nreal; ++jq) {
               const float* col = base + static_cast<size_t>(jq * CHUNK_COLS) * BM;

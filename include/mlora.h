@@ -263,10 +263,11 @@ int64_t mlora_h_elems(const mlora_plan_t* plan);
  *                     slice, dH K slices
  *   MLORA_Q_ADAPTERS: per segment-table entry: job, first packed column, rank, first and end
  *                     output column of its B
- *   MLORA_Q_WINDOW_PAIRS: 1 if the shrink / dH run on CTA pairs, else 0; then per pair item:
- *                     pair, first chunk, chunks (even), first dH K slice, dH K slices, part, parts
- *                     (an item of a last wave that would leave most pairs idle is cut along K into
- *                     `parts` items, one per pair; parts = 1 for a whole item)
+ *   MLORA_Q_WINDOW_PAIRS: 1 if the shrink / dH run on CTA pairs, else 0; then the CTA pairs'
+ *                     work lists, pair by pair, one entry per item or piece: CTA pair, 256-token
+ *                     pair of tiles, first chunk, chunks (even), first shrink K slice, shrink K
+ *                     slices, first dH K slice, dH K slices, piece, pieces (an item the schedule
+ *                     cuts along K runs as `pieces` entries on different pairs; 1 = whole item)
  *   MLORA_Q_GEMM_FWD / MLORA_Q_GEMM_BWD: the CTA-pair base GEMM's work list in launch order:
  *                     raster order (1 = groups of output tiles sweep the token pairs, 0 = groups
  *                     of token pairs sweep the output tiles), group size, items, full-width

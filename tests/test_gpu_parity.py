@@ -445,6 +445,49 @@ def test_wgrad_items_cut_across_ctas_vs_oracle(grouped):
         run.close()
 
 
+PAIR_CUT_CASES = {
+    # three one-job pair tiles of two chunks, 64 K slices each way: every item in four pieces
+    "even": lambda: W.custom("pair_cut", 963, 4096, 4096, [128, 128, 128], [256, 256, 256], b_std=0.05, w_std=0.05),
+    # several jobs per pair tile (items of four chunks and a padded pair), ragged ranks and
+    # tokens, dH 32 slices against the shrink's 64
+    "ragged": lambda: W.custom("pair_cut_r", 964, 4096, 2048, [3, 64, 200, 17, 128], [100, 300, 57, 250, 40],
+                               b_std=0.05, w_std=0.05),
+    # a shared-input pack: the first job's window is six chunks, so its second item holds only the
+    # k / v adapters' columns and its dH reads (and is cut within) their d_out slices 32..63
+    "qkv_groups": lambda: W.custom_grouped("pair_cut_g", 965, 4096, [2048, 1024, 1024],
+                                           [[256, 64, 64], [32, 16, 16], [16, 8, 8]], [256, 200, 250],
+                                           b_std=0.05),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PAIR_CUT_CASES))
+def test_pair_items_cut_along_k_vs_oracle(name):
+    """CTA-pair shrink / dH items that the per-pair schedule cuts along K (few items for the pairs:
+    every item in several pieces, each parking fp32 sums; the last piece to arrive adds them in
+    piece order and writes H / dH and the images): every output against the oracle, and a second
+    forward + backward bitwise equal to the first."""
+    wl = PAIR_CUT_CASES[name]()
+    T = W.materialise(wl)
+    run = G.GpuRun(wl, T, step=False, flags=M.MLORA_WINDOW_PAIRS)
+    try:
+        assert run.status_after_backward == M.MLORA_OK
+        # entries: product (0 shrink, 1 dH), pair, tile pair, first chunk, chunks, first K slice,
+        # K slices, piece, pieces
+        items = np.array(run.layer.describe(M.MLORA_Q_WINDOW_PAIRS))[1:].reshape(-1, 9)
+        assert items[:, 8].min() >= 2          # every item cut, in both products
+        if name == "qkv_groups":
+            assert ((items[:, 0] == 1) & (items[:, 5] >= 32)).any()   # a dH piece inside the k / v slices
+        G.compare(run.res, G.oracle_full(wl, T), G.TOL["bf16"], ["Y", "dX", "H", "dH", "dAt", "dBt"])
+        first = [t.clone() for t in (run.layer.H, run.layer.dH)]
+        run.layer.forward(run.X, run.Wt)
+        run.layer.backward(run.X, run.Wt, run.dY)
+        torch.cuda.synchronize()
+        assert run.layer.sync_status() == M.MLORA_OK
+        assert all(torch.equal(a, b) for a, b in zip(first, (run.layer.H, run.layer.dH)))
+    finally:
+        run.close()
+
+
 @pytest.mark.parametrize("reuse", [False, True], ids=["repack", "reuse_staging"])
 def test_three_training_steps_vs_oracle(reuse):
     """Three steps of forward, backward and AdamW (t = 1, 2, 3) with fresh X and dY each step: the

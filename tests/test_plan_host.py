@@ -88,21 +88,54 @@ def test_planner_tables_random(seed):
     plan, _ = host_plan(d_in, d_out, ranks, ns)
     try:
         mt = _describe(plan, M.MLORA_Q_MTILES).reshape(-1, 5)
-        items = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)[1:].reshape(-1, 7)
+        shrink, dh = _pair_entries(plan)
     finally:
         M.mlora_plan_destroy(plan)
-    items = items[items[:, 5] == 0]          # one entry per item: its first part
-    for p in range((len(mt) + 1) // 2):
-        q_lo, nch = mt[2 * p, 2], mt[2 * p, 3]
-        got = [q for _, q0, nq, _, _, _, _ in items[items[:, 0] == p] for q in range(q0, q0 + nq)]
-        assert got[:nch] == list(range(q_lo, q_lo + nch)) and len(got) - nch in (0, 1)
+    _check_pair_pieces(shrink, lambda t, q: (0, -(-d_in // 64)))
+    _check_pair_pieces(dh, lambda t, q: (0, -(-d_out // 64)))
+    for items in (shrink, dh):
+        items = items[items[:, 6] == 0]          # one entry per item: its first piece
+        items = items[np.lexsort((items[:, 2], items[:, 1]))]
+        for p in range((len(mt) + 1) // 2):
+            q_lo, nch = mt[2 * p, 2], mt[2 * p, 3]
+            got = [q for row in items[items[:, 1] == p] for q in range(row[2], row[2] + row[3])]
+            assert got[:nch] == list(range(q_lo, q_lo + nch)) and len(got) - nch in (0, 1)
+
+
+def _pair_entries(plan):
+    """The CTA-pair schedules as (shrink entries, dH entries), each row: pair, 256-token pair of
+    tiles, first chunk, chunks, first K slice, K slices, piece, pieces."""
+    d = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)[1:].reshape(-1, 9)
+    return d[d[:, 0] == 0][:, 1:], d[d[:, 0] == 1][:, 1:]
+
+
+def _check_pair_pieces(items, kslices):
+    """One product's CTA-pair schedule: the list runs pair by pair; the pieces of an item sit on
+    distinct pairs, numbered 0..S-1, and in that order tile the item's K range exactly once (all
+    of it: kslices(first chunk) gives its first slice and count), each piece of a cut item keeping
+    at least 16 slices (the planner cuts at shares of 16 slices, rounded down: 15 or more)."""
+    assert (np.diff(items[:, 0]) >= 0).all()
+    groups = {}
+    for row in items:
+        groups.setdefault((row[1], row[2]), []).append(row)
+    for (tile, q0), rows in groups.items():
+        rows.sort(key=lambda r: r[6])
+        S = rows[0][7]
+        assert [r[6] for r in rows] == list(range(S)) and all(r[7] == S for r in rows)
+        assert len({r[0] for r in rows}) == S and len({r[3] for r in rows}) == 1
+        k0, n = kslices(tile, q0)
+        for r in rows:
+            assert r[4] == k0 and r[5] >= (15 if S > 1 else 1)
+            k0 += r[5]
+        assert k0 == kslices(tile, q0)[0] + n
+    return groups
 
 
 def _check_tables(d_in, d_out, ranks, ns):
     plan, ws = host_plan(d_in, d_out, ranks, ns)
     try:
         summ, mt, cols, win, da, db = _tables(plan)
-        pw_items = np.array(M.mlora_plan_describe(plan, M.MLORA_Q_WINDOW_PAIRS)[1:]).reshape(-1, 7)
+        pw_shrink, pw_dh = _pair_entries(plan)
     finally:
         M.mlora_plan_destroy(plan)
     N = sum(ns)
@@ -151,8 +184,9 @@ def _check_tables(d_in, d_out, ranks, ns):
     # workspace = bf16 shadows + the split items' fp32 partial sums (one region: the pair items'
     # or dA's / dB's, whichever is larger) + two image sets
     shadow = -(-c * d_in * 2 // 1024) * 1024 + -(-c * d_out * 2 // 1024) * 1024
-    split = pw_items[pw_items[:, 6] > 1]
-    partials = max(len(split) * 2 * 128 * 256 * 4, max(wg_units) * 256 * 64 * 4)
+    # the pieces of cut pair items, one partial set each (shrink and dH share the region)
+    split = max((pw_shrink[:, 7] > 1).sum(), (pw_dh[:, 7] > 1).sum())
+    partials = max(split * 2 * 128 * 256 * 4, max(wg_units) * 256 * 64 * 4)
     assert ws == shadow + -(-partials // 1024) * 1024 + 2 * img * 16384
 
 
@@ -360,6 +394,24 @@ def test_grouped_plan_rejects(bad, status):
     assert _status_of(lambda: M.mlora_plan_destroy(M.mlora_plan_grouped(prob, groups, segs)[0])) == status
 
 
+def test_grouped_pair_dh_pieces_stay_in_their_slices():
+    """A shared-input pack on CTA pairs: job 0's window (ranks 256, 64, 64: six chunks) makes a pair
+    item of chunks 0-3 that holds only q columns and one of chunks 4-5 with only k / v columns;
+    their dH K ranges are those projections' d_out slices (0..31 and 32..63), and each item's
+    pieces tile exactly its range."""
+    from adapter_gemm_packed_gb300.layer import host_plan_grouped
+    plan, _ = host_plan_grouped(4096, [2048, 1024, 1024], [[256, 64, 64], [32, 16, 16], [16, 8, 8]],
+                                [256, 200, 250], flags=M.MLORA_WINDOW_PAIRS)
+    try:
+        shrink, dh = _pair_entries(plan)
+    finally:
+        M.mlora_plan_destroy(plan)
+    whole = {(0, 0): (0, 32), (0, 4): (32, 32), (1, 6): (0, 64), (2, 7): (0, 64)}
+    _check_pair_pieces(shrink, lambda t, q: (0, 64))
+    groups = _check_pair_pieces(dh, lambda t, q: whole[(t, q)])
+    assert set(groups) == set(whole) and all(rows[0][7] >= 2 for rows in groups.values())
+
+
 def test_grouped_dh_items_read_only_their_projections_slices():
     """A dH item of a shared-input pack streams only the d_out slices covered by the adapters
     that own its chunks' columns: chunks holding only k columns read only k's slice of dY."""
@@ -388,64 +440,83 @@ def test_grouped_dh_items_read_only_their_projections_slices():
 @pytest.mark.parametrize("name", ["ragged", "tiny_segments", "one_token", "qproj", "many_small"])
 def test_pair_window_items(name):
     """Pair items cover each 256-token pair's shared chunk range exactly once, in groups of at most
-    four chunks padded to an even count (the padding chunk sits right after the range)."""
+    four chunks padded to an even count (the padding chunk sits right after the range), in both
+    products' schedules; the shrink reads all of d_in and dH all of d_out (one projection)."""
     d_in, d_out, ranks, ns = _case(name)
     plan, _ = host_plan(d_in, d_out, ranks, ns)
     try:
         mt = _describe(plan, M.MLORA_Q_MTILES).reshape(-1, 5)
-        pw = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)
+        shrink, dh = _pair_entries(plan)
     finally:
         M.mlora_plan_destroy(plan)
-    items = pw[1:].reshape(-1, 7)
-    items = items[items[:, 5] == 0]          # one entry per item: its first part
-    n_pairs = (len(mt) + 1) // 2
-    for p in range(n_pairs):
-        q_lo, nch = mt[2 * p, 2], mt[2 * p, 3]
-        mine = items[items[:, 0] == p]
-        got = []
-        for _, q0, nq, kb0, nkb, _, _ in mine:
-            assert nq in (2, 4)
-            assert (kb0, nkb) == (0, -(-d_out // 64))
-            got.extend(range(q0, q0 + nq))
-        real = list(range(q_lo, q_lo + nch))
-        assert got[:nch] == real and len(got) - nch in (0, 1)
+    for items, K in ((shrink, -(-d_in // 64)), (dh, -(-d_out // 64))):
+        groups = _check_pair_pieces(items, lambda t, q: (0, K))
+        for p in range((len(mt) + 1) // 2):
+            q_lo, nch = mt[2 * p, 2], mt[2 * p, 3]
+            got = []
+            for (tile, q0), rows in sorted(groups.items()):
+                if tile == p:
+                    assert rows[0][3] in (2, 4)
+                    got.extend(range(q0, q0 + rows[0][3]))
+            assert got[:nch] == list(range(q_lo, q_lo + nch)) and len(got) - nch in (0, 1)
 
 
-@pytest.mark.parametrize("name", ["many_small", "mlp_up", "qproj"])
-def test_pair_items_of_a_thin_last_wave_are_cut_along_k(name):
-    """When the pair items' last wave would leave more than half of the pairs idle (host plans
-    assume 148 SMs: 74 pairs), each of its T items becomes S = min(8, 74 // T, shortest K / 16)
-    parts, one per pair, at the end of the list; the parts' K shares tile the item's K range
-    exactly once."""
-    d_in, d_out, ranks, ns = _case(name)
+def _pair_loads(items):
+    """Modelled per-pair load of one product's CTA-pair schedule, as the planner counts it (KB
+    per CTA)."""
+    loads = np.zeros(items[:, 0].max() + 1)
+    for row in items:
+        nq, S = row[3], row[7]
+        loads[row[0]] += row[5] * (16 + 8 * (nq // 2)) + 32 + 16 * nq + (64 * nq if S > 1 else 0)
+    return loads
+
+
+@pytest.mark.parametrize("name, bound", [("many_small", 1.12), ("mlp_up", 1.12), ("qproj", 1.0),
+                                         ("layer_q", 1.05), ("layer_gate", 1.05), ("layer_down", 1.05)])
+def test_pair_schedule_balances_the_pairs(name, bound):
+    """Each product's per-pair lists (host plans assume 148 SMs: 74 pairs) keep every pair near the
+    average modelled load: whole items first while they fit, then the rest cut along K across the
+    least loaded pairs.  A round robin left these packs at 1.10-1.41x the average (the
+    many-small-jobs pack 1.37, mlp_up 1.41, q_proj's 64 items on 64 of 74 pairs).  q_proj stays
+    whole: cutting its 64 items over 74 pairs would save less than the pieces' partial sums cost."""
+    if name.startswith("layer_"):
+        wl = W.llama8b_layer(["q", "k", "v", "o", "gate", "up", "down"].index(name[6:]))
+        d_in, d_out, ranks, ns = wl.d_in, wl.d_out, wl.ranks, wl.n_tokens
+    else:
+        d_in, d_out, ranks, ns = _case(name)
     plan, _ = host_plan(d_in, d_out, ranks, ns, flags=M.MLORA_WINDOW_PAIRS)
     try:
-        items = _describe(plan, M.MLORA_Q_WINDOW_PAIRS)[1:].reshape(-1, 7)
+        shrink, dh = _pair_entries(plan)
     finally:
         M.mlora_plan_destroy(plan)
-    pairs = 74
-    whole = items[items[:, 6] == 1]
-    split = items[items[:, 6] > 1]
-    n_orig = len(whole) + (len(split) // split[0, 6] if len(split) else 0)
-    T = n_orig % pairs
-    tail = whole[len(whole) - T:] if len(split) == 0 else split[::max(1, split[0, 6])]
-    min_k = min([-(-d_in // 64)] + [int(x) for x in tail[:, 4]]) if T else 0
-    if n_orig > pairs and 0 < T and 2 * T <= pairs and min(8, pairs // T, min_k // 16) >= 2:
-        S = min(8, pairs // T, min_k // 16)
-        assert len(whole) == n_orig - T and len(split) == T * S <= pairs
-        assert (items[:len(whole), 6] == 1).all()        # whole items first, the parts last
-        for t in range(T):
-            grp = split[t * S:(t + 1) * S]
-            assert list(grp[:, 5]) == list(range(S)) and (grp[:, :5] == grp[0, :5]).all()
-            for kmain, dh in ((-(-d_in // 64), False), (grp[0, 4], True)):
-                base = grp[0, 3] if dh else 0
-                cover = []
-                for s in range(S):
-                    lo, hi = kmain * s // S, kmain * (s + 1) // S
-                    cover += list(range(base + lo, base + hi))
-                assert cover == list(range(base, base + kmain))
-    else:
-        assert len(split) == 0
+    for items, K in ((shrink, -(-d_in // 64)), (dh, -(-d_out // 64))):
+        _check_pair_pieces(items, lambda t, q: (0, K))
+        loads = _pair_loads(items)
+        assert len(loads) <= 74
+        if name == "qproj":
+            assert (items[:, 7] == 1).all() and len(loads) == len(items) == 64
+        else:
+            assert len(loads) == 74 and (items[:, 7] > 1).any()
+            assert loads.max() <= bound * loads.sum() / 74
+
+
+def test_pair_schedule_hand_worked():
+    """Three items of 64 K slices each way (d_in = d_out = 4096, one 256-token pair per job, two
+    chunks) on 74 pairs: an item costs 64 x 24 + 32 + 32 = 1600 KB per CTA and the average over 74
+    pairs is far below one item, so the greedy phase takes none and McNaughton's rule cuts every
+    item into pieces of the smallest share, 16 of its 64 slices: four pieces each, on 12 distinct
+    pairs, in both products."""
+    plan, _ = host_plan(4096, 4096, [128, 128, 128], [256, 256, 256], flags=M.MLORA_WINDOW_PAIRS)
+    try:
+        shrink, dh = _pair_entries(plan)
+    finally:
+        M.mlora_plan_destroy(plan)
+    for items in (shrink, dh):
+        groups = _check_pair_pieces(items, lambda t, q: (0, 64))
+        assert len(groups) == 3
+        for rows in groups.values():
+            assert [(r[4], r[5]) for r in rows] == [(0, 16), (16, 16), (32, 16), (48, 16)]
+        assert sorted(items[:, 0]) == list(range(12))
 
 
 def test_window_engine_choice():
