@@ -395,6 +395,8 @@ def options_of(wl, args):
         opts.append("MLORA_REUSE_STAGING (backward reuses the forward's bf16 shadows and staged H)")
     if args.window != "auto":
         opts.append({"pairs": "MLORA_WINDOW_PAIRS", "single": "MLORA_WINDOW_SINGLE"}[args.window])
+    if args.no_overlap:
+        opts.append("MLORA_NO_OVERLAP (each kernel launched after the previous one ends)")
     if parts_of(wl)[0].dtype == "bf16_w4":
         opts.append("MLORA_W4_FUSED (codes expanded inside the base GEMMs)" if args.w4_fused else
                     "4-bit base expanded to bf16 once per call, then the bf16 GEMMs")
@@ -518,6 +520,7 @@ def run_ours(args, wl, rank, world, local_rank):
     layered = hasattr(wl, "parts")
     flags = (0 if args.no_reuse else M.MLORA_REUSE_STAGING) | (M.MLORA_W4_FUSED if args.w4_fused else 0)
     flags |= {"auto": 0, "pairs": M.MLORA_WINDOW_PAIRS, "single": M.MLORA_WINDOW_SINGLE}[args.window]
+    flags |= M.MLORA_NO_OVERLAP if args.no_overlap else 0
     # this rank's jobs (all of them on one GPU)
     rank_of_job, load = shard(wl, world)
     mine = jobs_of_rank(rank_of_job, rank)
@@ -958,6 +961,8 @@ def main():
     ap.add_argument("--w4-fused", action="store_true", help="4-bit base: expand inside the GEMMs (MLORA_W4_FUSED)")
     ap.add_argument("--window", choices=["auto", "pairs", "single"], default="auto",
                     help="engine of the shrink / dH products (default: the planner's choice)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch every kernel after the previous one ends (MLORA_NO_OVERLAP)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens-per-job", type=int, default=64)
