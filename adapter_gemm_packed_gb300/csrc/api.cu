@@ -10,7 +10,8 @@
 //   * base GEMMs: (256-token pair x 256 output columns) on CTA pairs, rastered in groups whose
 //     resident panels fit the L2 (raster.cuh);
 //   * shrink / dH: (token tile, <= 2 64-column chunks of its window), or on CTA pairs (256-token
-//     pair, <= 4 chunks), a thin last wave cut along K;
+//     pair, <= 4 chunks) laid out per pair and per product, the items past the even share cut
+//     along K;
 //   * dA / dB: (256-row block of d_in / d_out, job, <= 2 chunks) laid out per CTA, by greedy list
 //     scheduling in job order or by McNaughton's wrap-around rule with items cut along their tokens.
 #include <algorithm>
