@@ -377,7 +377,7 @@ mlora_status mlora_shard_jobs_multi(const mlora_problem* problems, int32_t n_pro
  * device array of 64 MiB that the library holds on every GPU it is loaded on until the
  * process exits.  This call allocates nothing (no cudaMalloc, cudaFree or allocating library
  * routine).  Its first call on a device looks up that array's device address on the current
- * device (a one-time set-up per device); make that first call before any stream capture.
+ * device (a one-time set-up per device).
  * Plans whose forward needs more scratch than 64 MiB, and plans with a 4-bit base
  * (MLORA_BF16_W4), are rejected with MLORA_ERR_UNSUPPORTED and a message in
  * mlora_last_error(); use mlora_forward / mlora_forward_w4 for them.  All calls on a device
