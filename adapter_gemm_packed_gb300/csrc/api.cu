@@ -679,7 +679,8 @@ void build_tables(mlora_plan_t* P) {
       if (c_hi <= c_lo) return;
       const int qa = c_lo / CHUNK_COLS, qb = (c_hi + CHUNK_COLS - 1) / CHUNK_COLS;
       for (int q = qa; q < qb; q += MAX_ITEM_CHUNKS)
-        out.push_back(WItem{r0, i, ga, gb, q, std::min(MAX_ITEM_CHUNKS, qb - q), 0, 1, 0, 0});
+        out.push_back(WItem{r0, i, ga, gb, q, std::min(MAX_ITEM_CHUNKS, qb - q), 0, 1, 0, 0, d.c, d.r,
+                            by_output ? d.dBt : d.dAt});
     };
     std::vector<WItem> v;   // block order
     for (int r0 = 0; r0 < rows; r0 += 2 * BM)

@@ -116,6 +116,8 @@ __host__ __device__ __forceinline__ void win_krange(const WinItem& w, bool dh, i
 struct WItem {
   int row0, seg, ga, gb, q0, nq;
   int part, nparts, pbase, cnt;
+  int c0, r;    // the job's window start and rank, and its gradient (dAt for dA, dBt for dB; null in
+  float* out;   // a shared-input pack, whose adapters the epilogue reads from the adapter table)
 };
 constexpr int WG_UNIT = 2 * BM * CHUNK_COLS;   // floats of one part's sums per chunk (256 rows x 64 columns)
 

@@ -225,12 +225,12 @@ __device__ __forceinline__ int find_seg(const DevSeg* segs, int first, int last,
 // Write columns [32 h, 32 h + 32) of chunk jq of a dA / dB item's row half mh: this thread's
 // row, values v.  All 32 lanes of the warp call it together (the dB store is warp-cooperative).
 template <int MODE>
-__device__ __forceinline__ void wgrad_emit(const GemmArgs& g, const WItem& w, const DevSeg& sg, int mh, int jq, int h,
+__device__ __forceinline__ void wgrad_emit(const GemmArgs& g, const WItem& w, int mh, int jq, int h,
                                            const uint32_t (&v)[32], float* stage, int quarter, int lane) {
   const int bound = (MODE == MODE_DA) ? g.d_in : g.d_out;
   const int row = w.row0 + mh * BM + quarter * 32 + lane;   // d_in (DA) or d_out (DB) index
   const int cfirst = (w.q0 + jq) * CHUNK_COLS + h * 32;      // packed column of v[0]
-  const int t0 = cfirst - sg.c;                              // rank index of v[0]
+  const int t0 = cfirst - w.c0;                              // rank index of v[0]
   if (g.subs) {
     // several adapters per job (one per projection): each adapter of this item's job takes
     // its own run of the chunk's columns (dB only for the output rows its B covers).  A chunk
@@ -276,18 +276,18 @@ __device__ __forceinline__ void wgrad_emit(const GemmArgs& g, const WItem& w, co
 #pragma unroll
     for (int u = 0; u < 32; ++u) {
       const int t = t0 + u;
-      if (t >= 0 && t < sg.r) sg.dAt[static_cast<size_t>(t) * g.d_in + row] = __uint_as_float(v[u]);
+      if (t >= 0 && t < w.r) w.out[static_cast<size_t>(t) * g.d_in + row] = __uint_as_float(v[u]);
     }
   } else {
     // dBt_i[row][t]: a thread holds one row, but a row's values are contiguous in memory, so the
     // warp goes through shared memory and stores along the rows instead, 16 columns at a time
-    const int r = sg.r;
+    const int r = w.r;
     const int row_w = w.row0 + mh * BM + quarter * 32;   // the warp's first row
     const int nrows = min(32, bound - row_w);            // its rows inside d_out
     if (nrows <= 0) return;                              // the same for the whole warp
     float* buf = stage;
     float4* buf4 = reinterpret_cast<float4*>(stage);
-    const bool al4 = (r & 3) == 0 && (reinterpret_cast<uintptr_t>(sg.dBt) & 15) == 0;
+    const bool al4 = (r & 3) == 0 && (reinterpret_cast<uintptr_t>(w.out) & 15) == 0;
 #pragma unroll
     for (int qq = 0; qq < 2; ++qq) {
       const int tq = t0 + qq * 16;   // rank index of this quarter's first column
@@ -300,7 +300,7 @@ __device__ __forceinline__ void wgrad_emit(const GemmArgs& g, const WItem& w, co
         for (int u = 0; u < 16; ++u)
           if (tq + u >= 0 && tq + u < r) buf[lane * r + tq + u] = __uint_as_float(v[qq * 16 + u]);
         __syncwarp();
-        float* dst = sg.dBt + static_cast<size_t>(row_w) * r;
+        float* dst = w.out + static_cast<size_t>(row_w) * r;
         for (int e = lane; e < nrows * r; e += 32) dst[e] = buf[e];
       } else {
 #pragma unroll
@@ -315,7 +315,7 @@ __device__ __forceinline__ void wgrad_emit(const GemmArgs& g, const WItem& w, co
           for (int it = 0; it < 4; ++it) {
             const int rr = it * 8 + (lane >> 2), k = lane & 3;
             if (rr < nrows)
-              *reinterpret_cast<float4*>(sg.dBt + static_cast<size_t>(row_w + rr) * r + tq + 4 * k) = buf4[db_slot(rr, k)];
+              *reinterpret_cast<float4*>(w.out + static_cast<size_t>(row_w + rr) * r + tq + 4 * k) = buf4[db_slot(rr, k)];
           }
         } else {
           // rows not 16-byte aligned (r not a multiple of 4) or part of the 16 columns: the wq valid
@@ -326,7 +326,7 @@ __device__ __forceinline__ void wgrad_emit(const GemmArgs& g, const WItem& w, co
           int rr = lane / wq, c = lane - rr * wq;
           for (int e = lane; e < n_el; e += 32) {
             const int cq = lo - tq + c;   // column within the staged 16
-            sg.dBt[static_cast<size_t>(row_w + rr) * r + lo + c] = buf[db_slot(rr, cq >> 2) * 4 + (cq & 3)];
+            w.out[static_cast<size_t>(row_w + rr) * r + lo + c] = buf[db_slot(rr, cq >> 2) * 4 + (cq & 3)];
             rr += step_r;
             c += step_c;
             if (c >= wq) {
@@ -450,11 +450,12 @@ __device__ __forceinline__ bool epilogue_item(const GemmArgs& g, int item, uint3
   return false;
 }
 
-// dA / dB epilogue of item w (job record sg), both read ahead by the caller.  Returns true if it
-// already handed the accumulator back (arrived on tempty_bar).
+// dA / dB epilogue of item w (read ahead by the caller; it carries its job's window and output, so
+// no dependent load sits between two items).  Returns true if it already handed the accumulator
+// back (arrived on tempty_bar).
 template <int MODE>
 // This warp handles row half mh of the item (lanes of its quarter); `stage` is its own staging.
-__device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w, const DevSeg& sg, uint32_t t_acc,
+__device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w, uint32_t t_acc,
                                                int quarter, int mh, int lane, float* stage, uint64_t* tempty_bar) {
   const int rit = quarter * 32 + lane;   // accumulator row owned by this thread
   if (w.nparts == 1) {
@@ -465,8 +466,8 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w
       tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       tmem_ld32(t_acc + mh * 128 + jq * CHUNK_COLS + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait();
-      wgrad_emit<MODE>(g, w, sg, mh, jq, 0, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]), stage, quarter, lane);
-      wgrad_emit<MODE>(g, w, sg, mh, jq, 1, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]), stage, quarter, lane);
+      wgrad_emit<MODE>(g, w, mh, jq, 0, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]), stage, quarter, lane);
+      wgrad_emit<MODE>(g, w, mh, jq, 1, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]), stage, quarter, lane);
     }
     return false;
   }
@@ -477,8 +478,8 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w
   // float4: a warp's 32 rows of a run are one 512-byte line, and the last part's sum has 8 loads
   // in flight per part, two parts per round trip.
   auto live = [&](int jq, int h) {
-    const int t0 = (w.q0 + jq) * CHUNK_COLS + h * 32 - sg.c;
-    return max(0, t0) < min(sg.r, t0 + 32);
+    const int t0 = (w.q0 + jq) * CHUNK_COLS + h * 32 - w.c0;
+    return max(0, t0) < min(w.r, t0 + 32);
   };
   float4* base = reinterpret_cast<float4*>(g.partials + static_cast<size_t>(w.pbase) * WG_UNIT);
   const size_t part_f4 = static_cast<size_t>(w.nq) * (WG_UNIT / 4);   // float4s per part
@@ -558,7 +559,7 @@ __device__ __forceinline__ bool epilogue_wgrad(const GemmArgs& g, const WItem& w
         v[4 * u4 + 2] = __float_as_uint(acc[u4].z);
         v[4 * u4 + 3] = __float_as_uint(acc[u4].w);
       }
-      wgrad_emit<MODE>(g, w, sg, mh, jq, h, v, stage, quarter, lane);
+      wgrad_emit<MODE>(g, w, mh, jq, h, v, stage, quarter, lane);
     }
   return true;
 }
@@ -625,18 +626,24 @@ __global__ void __launch_bounds__(Ring<MODE>::kThreads, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      // dA / dB items are a few K slices long: the next item's descriptor is read one item ahead,
-      // and a tile's descriptor once per tile, so no dependent load sits between two copies
+      // dA / dB items are a few K slices long: the next item's descriptor and its first tile's
+      // record are read one item ahead, and each further tile's record one tile ahead, so no
+      // dependent load sits between two copies
       WItem w{};
-      if (kWgrad && items.first < items.end) w = g.witems[items.first];
+      MTile mt_first{};
+      if (kWgrad && items.first < items.end) {
+        w = g.witems[items.first];
+        mt_first = g.mtiles[w.ga >> 1];
+      }
       for (int item = items.first; ok && item < items.end; item += items.step) {
         WItem w_next{};
         if (kWgrad && item + items.step < items.end) w_next = g.witems[item + items.step];
         int nkb;
         if constexpr (kWgrad) nkb = w.gb - w.ga;
         else nkb = item_kblocks<MODE>(g, item);
-        int t_have = -1;
-        MTile mt{};
+        int t_have = w.ga >> 1;
+        MTile mt = mt_first, mt_ahead{};
+        if (kWgrad && ((w.gb - 1) >> 1) > t_have) mt_ahead = g.mtiles[t_have + 1];
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, g.err, DEV_ERR_TIMEOUT_PRODUCER, tmo)) {
             ok = false;
@@ -648,9 +655,10 @@ __global__ void __launch_bounds__(Ring<MODE>::kThreads, 1)
             mbar_arrive_expect_tx(&full[stage], A_BYTES);
           } else if constexpr (kWgrad) {
             const int gh = w.ga + kb;   // 64-token half-tile
-            if ((gh >> 1) != t_have) {
+            if ((gh >> 1) != t_have) {  // the next tile (half-tiles run in order)
               t_have = gh >> 1;
-              mt = g.mtiles[t_have];
+              mt = mt_ahead;
+              if (((w.gb - 1) >> 1) > t_have) mt_ahead = g.mtiles[t_have + 1];
             }
             produce_wgrad(&tmA, &tmI, w, mt, gh, sA + stage * A_BYTES, sB + stage * B_BYTES, &full[stage], pol_stream,
                           pol_keep);
@@ -664,6 +672,7 @@ __global__ void __launch_bounds__(Ring<MODE>::kThreads, 1)
             phase ^= 1u;
           }
         }
+        if (kWgrad && item + items.step < items.end) mt_first = g.mtiles[w_next.ga >> 1];
         w = w_next;
       }
       if (!ok || *abort_flag) {
@@ -736,14 +745,11 @@ __global__ void __launch_bounds__(Ring<MODE>::kThreads, 1)
     float* my_stage = stage_buf + (warp - 2) * DB_STAGE_FLOATS;
     int acc = 0;
     uint32_t acc_phase = 0;
-    // dA / dB: the next item's descriptor and its job's record are read as soon as this item's
-    // epilogue is done, while the MMA may still be working on the next accumulator
+    // dA / dB: the next item's descriptor (which carries its job's window and output) is read as
+    // soon as this item's epilogue is done, while the MMA may still be working on the next
+    // accumulator
     WItem w{};
-    DevSeg sg{};
-    if (kWgrad && items.first < items.end) {
-      w = g.witems[items.first];
-      sg = g.segs[w.seg];
-    }
+    if (kWgrad && items.first < items.end) w = g.witems[items.first];
     for (int item = items.first; item < items.end; item += items.step) {
       // One lane waits; the warp follows its decision so the .sync.aligned TMEM loads below
       // are always executed by all 32 lanes together.
@@ -755,7 +761,7 @@ __global__ void __launch_bounds__(Ring<MODE>::kThreads, 1)
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       bool released;
       if constexpr (kWgrad)
-        released = epilogue_wgrad<MODE>(g, w, sg, t_acc, quarter, mh, lane, my_stage, &tempty[acc]);
+        released = epilogue_wgrad<MODE>(g, w, t_acc, quarter, mh, lane, my_stage, &tempty[acc]);
       else
         released = epilogue_item<MODE>(g, item, t_acc, quarter, lane);
       if (!released) {
@@ -763,10 +769,7 @@ __global__ void __launch_bounds__(Ring<MODE>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
       }
-      if (kWgrad && item + items.step < items.end) {   // ahead of the next item's accumulator wait
-        w = g.witems[item + items.step];
-        sg = g.segs[w.seg];
-      }
+      if (kWgrad && item + items.step < items.end) w = g.witems[item + items.step];   // ahead of the next wait
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
