@@ -247,6 +247,12 @@ def test_plan_rejects_bad_tables(bad, status):
     assert _status_of(lambda: M.mlora_plan_destroy(host_plan(**args)[0])) == status
 
 
+def test_plan_rejects_an_empty_pack():
+    """A pack with no jobs (and no tokens) is an invalid table, reported with a message."""
+    assert _status_of(lambda: host_plan(64, 64, [], [])) == M.MLORA_ERR_INVALID
+    assert b"n_segs" in M.lib().mlora_last_error()
+
+
 def test_plan_rejects_null_and_misaligned_adapters():
     ok = M.mlora_segment(0, 4, 2, 1.0, 0x1000, 0x2000, 0, 0, 0, 0, 0, 0)
     prob = M.mlora_problem(4, 64, 64, M.MLORA_BF16, M.MLORA_PLAN_HOST_ONLY)
