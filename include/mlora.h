@@ -99,7 +99,9 @@ typedef enum mlora_dtype {
                                           these calls (results are then identical to the full passes) */
 #define MLORA_NO_OVERLAP 8u            /* launch every kernel strictly after the previous one (no programmatic
                                           dependent launch overlapping a kernel's prologue with the tail of
-                                          the one before); results are identical either way */
+                                          the one before); results are identical either way.  Plans whose
+                                          base product n_tokens * d_in * d_out exceeds 4e11 launch this way
+                                          by default (measured faster there) */
 #define MLORA_GEMM_SINGLE_CTA 4u       /* run the two base GEMMs on single-CTA 128x256 tiles instead of
                                           CTA pairs (256x256 tiles); same results up to rounding order */
 #define MLORA_WINDOW_PAIRS 128u        /* run the shrink and dH products on CTA pairs (256-token tiles sharing

@@ -117,7 +117,7 @@ def test_repeat_calls_are_deterministic():
 
 
 def test_launch_overlap_does_not_change_results():
-    """Programmatic dependent launch (the default) and strictly serial launches give bitwise
+    """Programmatic dependent launch (the default for packs of this size) and strictly serial launches give bitwise
     identical outputs: every kernel waits for its predecessor before touching memory."""
     wl = W.custom("overlap", 954, 512, 384, [4, 64, 130], [300, 100, 150], dtype="bf16")
     T = W.materialise(wl)
