@@ -18,6 +18,7 @@ MLORA_PLAN_HOST_ONLY = 1
 MLORA_DEBUG_SHORT_TIMEOUT = 2
 MLORA_GEMM_SINGLE_CTA = 4
 MLORA_NO_OVERLAP = 8
+MLORA_OVERLAP = 1024
 MLORA_REUSE_STAGING = 32
 MLORA_W4_FUSED = 64
 MLORA_WINDOW_PAIRS = 128

@@ -1048,6 +1048,7 @@ mlora_status mlora_plan_grouped(const mlora_problem* problem, const mlora_group*
   // 2.7e11 multiply-adds per base product, 0.738-0.740 against 0.751-0.755 ms).  It is kept for
   // plans whose base product N d_in d_out is at most 4e11.
   if (static_cast<double>(problem->n_tokens) * problem->d_in * problem->d_out > 4e11) P->pdl = false;
+  if (problem->flags & MLORA_OVERLAP) P->pdl = true;
   if (problem->flags & MLORA_NO_OVERLAP) P->pdl = false;
   if (problem->flags & MLORA_REUSE_STAGING) P->reuse_staging = true;
   if (problem->flags & MLORA_W4_FUSED) P->w4_fused = true;

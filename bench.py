@@ -397,6 +397,8 @@ def options_of(wl, args):
         opts.append({"pairs": "MLORA_WINDOW_PAIRS", "single": "MLORA_WINDOW_SINGLE"}[args.window])
     if args.no_overlap:
         opts.append("MLORA_NO_OVERLAP (each kernel launched after the previous one ends)")
+    if args.overlap:
+        opts.append("MLORA_OVERLAP (programmatic overlap whatever the plan's size)")
     if parts_of(wl)[0].dtype == "bf16_w4":
         opts.append("MLORA_W4_FUSED (codes expanded inside the base GEMMs)" if args.w4_fused else
                     "4-bit base expanded to bf16 once per call, then the bf16 GEMMs")
@@ -521,6 +523,7 @@ def run_ours(args, wl, rank, world, local_rank):
     flags = (0 if args.no_reuse else M.MLORA_REUSE_STAGING) | (M.MLORA_W4_FUSED if args.w4_fused else 0)
     flags |= {"auto": 0, "pairs": M.MLORA_WINDOW_PAIRS, "single": M.MLORA_WINDOW_SINGLE}[args.window]
     flags |= M.MLORA_NO_OVERLAP if args.no_overlap else 0
+    flags |= M.MLORA_OVERLAP if args.overlap else 0
     # this rank's jobs (all of them on one GPU)
     rank_of_job, load = shard(wl, world)
     mine = jobs_of_rank(rank_of_job, rank)
@@ -963,6 +966,8 @@ def main():
                     help="engine of the shrink / dH products (default: the planner's choice)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch every kernel after the previous one ends (MLORA_NO_OVERLAP)")
+    ap.add_argument("--overlap", action="store_true",
+                    help="keep the programmatic overlap whatever the plan's size (MLORA_OVERLAP)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens-per-job", type=int, default=64)

@@ -102,6 +102,8 @@ typedef enum mlora_dtype {
                                           the one before); results are identical either way.  Plans whose
                                           base product n_tokens * d_in * d_out exceeds 4e11 launch this way
                                           by default (measured faster there) */
+#define MLORA_OVERLAP 1024u           /* keep the programmatic overlap whatever the plan's size (MLORA_NO_OVERLAP
+                                          wins if both are given) */
 #define MLORA_GEMM_SINGLE_CTA 4u       /* run the two base GEMMs on single-CTA 128x256 tiles instead of
                                           CTA pairs (256x256 tiles); same results up to rounding order */
 #define MLORA_WINDOW_PAIRS 128u        /* run the shrink and dH products on CTA pairs (256-token tiles sharing
